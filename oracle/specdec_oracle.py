@@ -1,0 +1,460 @@
+"""Reference oracle for speculative-decoding verification -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, fp64 CPU statement of what the verification step computes.  Only the
+test suite (``tests/``), ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import or call it.  The product path (the CUDA library and its
+Python binding) never does, and this module imports nothing from the product.
+
+Sources (cited by page title and section throughout):
+
+* "Speculative decoding" (zerotofrontier.app, Chapter 20, Section 20.5) -- below "SD 20.5".
+* "Speculative-Decoding / Medusa" (s1mplewind.github.io) -- below "Medusa notes".
+* "Speculative Decoding: The Art of Guessing Well" (astralord.github.io) -- below "Art of Guessing".
+
+Every floating-point input is widened exactly to float64 (bf16 and fp32 values are
+exactly representable) and all arithmetic is float64.  Readings taken where the pages
+are silent or disagree are marked READING and listed in the design doc.
+
+Parity status: every public function here is pinned by ``tests/test_oracle_pins.py``
+(worked examples, closed forms, identities and exact integration over the uniforms);
+none is "parity unpinned".
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+import itertools
+
+import numpy as np
+
+# READING: a temperature below this threshold selects greedy (argmax) verification for
+# that sequence; the pages treat tau = 0 as greedy decoding (SD 20.5, "Acceptance rate
+# and temperature" exercise) and the workloads also use T < 1e-3.
+GREEDY_T = 1e-3
+
+# Per-sequence status bits.  These values are the interface documented for the
+# library's status output; the oracle states them independently.
+STATUS_BAD_LOGIT = 1        # a NaN or +inf logit in a row the verifier reads (error)
+STATUS_EMPTY_ROW = 2        # a row with no finite logit, i.e. all -inf (error)
+STATUS_BAD_TOKEN = 4        # a draft / node token outside [0, V) (error)
+STATUS_BAD_PROB = 8         # a draft probability that is NaN, inf or negative (error)
+STATUS_BAD_UNIFORM = 16     # a uniform outside [0, 1) on a sampled sequence (error)
+STATUS_BAD_TREE = 32        # parent not in [-1, i) or a tree deeper than max_depth (error)
+STATUS_ZERO_Q = 256         # q_i(x_i) == 0 for a drafted token (warning)
+STATUS_ZERO_RESIDUAL = 512  # residual mass was 0; the draw fell back to p (warning)
+STATUS_ERROR_MASK = 0xFF
+
+
+def widen(a) -> np.ndarray:
+    """Exact widening of bf16 / fp32 / int inputs to float64."""
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------------------
+# Distributions and their elementary statistics
+# ---------------------------------------------------------------------------------------
+
+def target_distribution(logits_row, T: float) -> np.ndarray:
+    """p = softmax(l / T) over the vocabulary, in float64.
+
+    SD 20.5, "When the target samples, keep a guess with probability p over q": p is the
+    distribution the target really samples from, after temperature.  The maximum is
+    subtracted first (a shift that leaves the softmax unchanged); a -inf logit gets
+    probability exactly 0.
+    """
+    l = widen(logits_row)
+    m = l.max()
+    e = np.exp((l - m) / np.float64(T))
+    return e / e.sum()
+
+
+def lowest_argmax(logits_row) -> int:
+    """Greedy choice z = argmax_x l(x), the smallest index among equal maxima.
+
+    SD 20.5, "A round of greedy speculative decoding" (the target's own choice z_i).
+    READING: ties resolve to the lowest token id.
+    """
+    l = widen(logits_row)
+    return int(np.flatnonzero(l == l.max())[0])
+
+
+def total_variation(p, q) -> float:
+    """TV(p, q) = 1/2 sum_x |p(x) - q(x)|  (SD 20.5, "Acceptance rate and temperature")."""
+    return 0.5 * float(np.abs(widen(p) - widen(q)).sum())
+
+
+def acceptance_rate(p, q) -> float:
+    """alpha = sum_x min(p(x), q(x)), the probability one draft is kept.
+
+    SD 20.5, "The speculative sampling rule"; Art of Guessing, "Speculative sampling".
+    """
+    return float(np.minimum(widen(p), widen(q)).sum())
+
+
+def residual_distribution(p, q) -> np.ndarray:
+    """Unnormalised residual (p - q)+ (SD 20.5, "The speculative sampling rule")."""
+    return np.maximum(0.0, widen(p) - widen(q))
+
+
+def expected_tokens_iid(alpha: float, gamma: int) -> float:
+    """E[J + 1] = (1 - alpha^(gamma+1)) / (1 - alpha) under i.i.d. acceptance.
+
+    SD 20.5, "Expected tokens per round"; Art of Guessing, "How many tokens do we get?".
+    """
+    if alpha == 1.0:
+        return float(gamma + 1)
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+def inverse_cdf(weights, u: float):
+    """Smallest k with C_k > u * S, C the running sum of the weights and S their total.
+
+    The extra token of a round is one categorical draw (SD 20.5, "Verify one round of
+    speculative sampling" uses one rng.choice); READING: the draw is the inverse CDF of
+    the caller's uniform.  Zero-weight entries are never chosen.  If rounding leaves no
+    qualifying k, the last entry with positive weight is taken.  Returns (k, C, S).
+    """
+    w = widen(weights)
+    C = np.cumsum(w)
+    S = C[-1]
+    hits = np.flatnonzero(C > u * S)
+    if hits.size:
+        k = int(hits[0])
+    else:
+        k = int(np.flatnonzero(w > 0)[-1])
+    return k, C, S
+
+
+def _row_status(logits_row) -> int:
+    l = widen(logits_row)
+    if np.isnan(l).any() or np.isposinf(l).any():
+        return STATUS_BAD_LOGIT
+    if not np.isfinite(l).any():
+        return STATUS_EMPTY_ROW
+    return 0
+
+
+# ---------------------------------------------------------------------------------------
+# Chain verification (one round, one sequence)
+# ---------------------------------------------------------------------------------------
+
+def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False) -> dict:
+    """One round of speculative-sampling verification for one sequence.
+
+    Follows SD 20.5, "A round of speculative sampling" (Leviathan et al. Alg. 1 /
+    Chen et al. Alg. 2) and the exercise "Verify one round of speculative sampling",
+    cross-read with Art of Guessing, "Speculative sampling" (the JAX verify):
+
+      p_i = softmax(l_i / T) for i = 0..gamma        (rows are the target's distributions)
+      accept draft i  iff  u_i < p_i(x_i) / q_i(x_i), evaluated as u_i * q_i(x_i) < p_i(x_i)
+      J = number of leading accepted drafts
+      extra token y ~ (p_J - q_J)+ normalised, with q_gamma == 0 (bonus from p_gamma)
+      emit x_0 .. x_{J-1}, y
+
+    A sequence with T < GREEDY_T is verified greedily (SD 20.5, "A round of greedy
+    speculative decoding", and the special case "A greedy target" of the rule):
+    accept while x_i == z_i = lowest argmax of row i, then emit z_J; q and u are unused.
+
+    Arguments: logits [gamma+1, V]; q [gamma, V] (used as given, READING: no
+    renormalisation); drafts [gamma] ints; T scalar; u [gamma+1] with u[i] the test
+    uniform of position i and u[gamma] the uniform of the extra token (READING).
+
+    Returns a dict: tokens [gamma+1] (-1 padded), J, status, p_draft [gamma] (p_i(x_i),
+    NaN where unevaluated), q_draft [gamma], margins [gamma] (|u_i - p_i(x_i)/q_i(x_i)|,
+    the distance of the test to its decision boundary), and for a sampled draw 'y_u'
+    (u * S) plus, when want_cdf, 'cdf' and 'S' of the weights the draw used.
+    """
+    logits = np.asarray(logits)
+    g1, V = logits.shape
+    gamma = g1 - 1
+    drafts = [int(x) for x in np.asarray(drafts).reshape(-1)]
+    assert len(drafts) == gamma
+    u = widen(u).reshape(-1)
+    greedy = bool(T < GREEDY_T)
+    out = {
+        "tokens": np.full(gamma + 1, -1, dtype=np.int64),
+        "J": -1,
+        "status": 0,
+        "p_draft": np.full(gamma, np.nan),
+        "q_draft": np.full(gamma, np.nan),
+        "margins": np.full(gamma, np.inf),
+        "greedy": greedy,
+    }
+    status = 0
+    for i in range(g1):
+        status |= _row_status(logits[i])
+    for x in drafts:
+        if not (0 <= x < V):
+            status |= STATUS_BAD_TOKEN
+    if not greedy:
+        if not np.all((u >= 0.0) & (u < 1.0)):
+            status |= STATUS_BAD_UNIFORM
+        if not (status & STATUS_BAD_TOKEN):
+            for i, x in enumerate(drafts):
+                qx = float(widen(q[i][x]))
+                if not np.isfinite(qx) or qx < 0.0:
+                    status |= STATUS_BAD_PROB
+    if status & STATUS_ERROR_MASK:
+        out["status"] = status
+        return out
+
+    if greedy:
+        z = [lowest_argmax(logits[i]) for i in range(g1)]
+        J = 0
+        while J < gamma and drafts[J] == z[J]:
+            J += 1
+        out["tokens"][:J] = drafts[:J]
+        out["tokens"][J] = z[J]
+        out["J"] = J
+        out["status"] = status
+        return out
+
+    # Sampled: every row's probabilities are evaluated (the library reads every row).
+    p = [target_distribution(logits[i], T) for i in range(g1)]
+    accepted = []
+    for i, x in enumerate(drafts):
+        px = p[i][x]
+        qx = float(widen(q[i][x]))
+        out["p_draft"][i] = px
+        out["q_draft"][i] = qx
+        if qx == 0.0:
+            # READING: a draft the drafter could not have produced; SD 20.5 notes the
+            # ratio is then never needed.  Accept iff p(x) > 0 and warn.
+            status |= STATUS_ZERO_Q
+            ok = px > 0.0
+        else:
+            ok = u[i] * qx < px
+            out["margins"][i] = abs(u[i] - px / qx)
+        accepted.append(ok)
+    J = 0
+    while J < gamma and accepted[J]:
+        J += 1
+
+    if J < gamma:
+        qJ = widen(q[J])
+        if np.isnan(qJ).any() or np.isinf(qJ).any() or (qJ < 0).any():
+            out["status"] = status | STATUS_BAD_PROB
+            return out
+        w = residual_distribution(p[J], qJ)
+    else:
+        # q_{gamma+1} == 0: the residual of the bonus row is p itself
+        # (SD 20.5, "Speculative verification in PyTorch"; Art of Guessing, JAX verify).
+        w = p[gamma].copy()
+    if not (w.sum() > 0.0):
+        # READING: possible only through rounding (p == q is always accepted); draw from p.
+        status |= STATUS_ZERO_RESIDUAL
+        w = p[J].copy()
+    y, C, S = inverse_cdf(w, u[gamma])
+    out["tokens"][:J] = drafts[:J]
+    out["tokens"][J] = y
+    out["J"] = J
+    out["status"] = status
+    out["y_u"] = u[gamma] * S
+    if want_cdf:
+        out["cdf"] = C
+        out["S"] = S
+    return out
+
+
+def verify_chain(logits, q, drafts, T, u) -> dict:
+    """Batched chain verification: a Python loop of verify_chain_sequence over B.
+
+    Shapes: logits [B, gamma+1, V], q [B, gamma, V], drafts [B, gamma], T [B],
+    u [B, gamma+1].  Returns stacked tokens [B, gamma+1], J [B], status [B],
+    p_draft [B, gamma].
+    """
+    B = np.asarray(logits).shape[0]
+    res = [verify_chain_sequence(logits[b], q[b], drafts[b], float(T[b]), u[b]) for b in range(B)]
+    return {
+        "tokens": np.stack([r["tokens"] for r in res]),
+        "J": np.array([r["J"] for r in res]),
+        "status": np.array([r["status"] for r in res]),
+        "p_draft": np.stack([r["p_draft"] for r in res]),
+        "per_seq": res,
+    }
+
+
+def verify_greedy_sequence(logits, drafts) -> dict:
+    """Greedy verification only (SD 20.5, "A round of greedy speculative decoding";
+    Art of Guessing, "Draft and verify"): J = longest prefix with x_i == z_i, emit z_J."""
+    g1 = np.asarray(logits).shape[0]
+    return verify_chain_sequence(logits, None, drafts, 0.0, np.zeros(g1))
+
+
+# ---------------------------------------------------------------------------------------
+# Token trees
+# ---------------------------------------------------------------------------------------
+
+def tree_depths(parents) -> np.ndarray:
+    """depth(i) = number of ancestors of node i; children of the prefix have depth 0.
+
+    SD 20.5, "Token tree and tree attention".  Parents must satisfy par(i) in [-1, i).
+    """
+    parents = [int(x) for x in parents]
+    depth = np.zeros(len(parents), dtype=np.int64)
+    for i, a in enumerate(parents):
+        if not (-1 <= a < i):
+            raise ValueError(f"parent of node {i} is {a}, not in [-1, {i})")
+        depth[i] = 0 if a == -1 else depth[a] + 1
+    return depth
+
+
+def build_tree_mask(parents, prefix_len: int):
+    """Tree-attention mask M [n, P+n] (bool) and position ids P + depth (int64).
+
+    SD 20.5, "Token tree and tree attention": node i sees every prefix position, itself
+    and its ancestors, nothing else; its position id is P + depth(i).  Plain ancestor
+    walk.  Returns (mask, position_ids, depth).
+    """
+    parents = [int(x) for x in parents]
+    n = len(parents)
+    depth = tree_depths(parents)
+    mask = np.zeros((n, prefix_len + n), dtype=bool)
+    mask[:, :prefix_len] = True
+    for i in range(n):
+        a = i
+        while a != -1:
+            mask[i, prefix_len + a] = True
+            a = parents[a]
+    return mask, prefix_len + depth, depth
+
+
+def verify_tree_sequence(logits, node_tokens, parents, T: float, u, max_depth: int) -> dict:
+    """Medusa-style walk of a candidate tree for one sequence.
+
+    Medusa notes, section "Attention Tree" (the target samples a token at the current
+    node -- argmax when greedy -- and verification descends into the child carrying
+    that token, stopping when none does); SD 20.5 states the greedy walk after the
+    exercise "The tree attention mask".
+
+    Row 0 of logits is the root (the distribution after the committed prefix); row
+    1 + i is the distribution after node i.  The draw at depth d uses uniform u[d]
+    (inverse CDF of softmax(l / T)).  READING: among children with equal tokens the
+    lowest node index is taken.  Returns tokens [max_depth+1] (-1 padded), path
+    [max_depth] (node ids, -1 padded), n_accepted and status.
+    """
+    logits = np.asarray(logits)
+    n1, V = logits.shape
+    n = n1 - 1
+    parents = [int(x) for x in parents]
+    node_tokens = [int(x) for x in node_tokens]
+    u = widen(u).reshape(-1)
+    greedy = bool(T < GREEDY_T)
+    out = {
+        "tokens": np.full(max_depth + 1, -1, dtype=np.int64),
+        "path": np.full(max_depth, -1, dtype=np.int64),
+        "n_accepted": -1,
+        "status": 0,
+    }
+    status = 0
+    try:
+        depth = tree_depths(parents)
+        if n and depth.max() + 1 > max_depth:
+            status |= STATUS_BAD_TREE
+    except ValueError:
+        status |= STATUS_BAD_TREE
+    for t in node_tokens:
+        if not (0 <= t < V):
+            status |= STATUS_BAD_TOKEN
+    if not greedy and not np.all((u >= 0.0) & (u < 1.0)):
+        status |= STATUS_BAD_UNIFORM
+    if status & STATUS_ERROR_MASK:
+        out["status"] = status
+        return out
+
+    node, d = -1, 0
+    while True:
+        row = logits[0 if node == -1 else 1 + node]
+        rs = _row_status(row)
+        if rs:
+            out = {**out, "tokens": np.full(max_depth + 1, -1, dtype=np.int64),
+                   "path": np.full(max_depth, -1, dtype=np.int64), "status": status | rs}
+            return out
+        if greedy:
+            y = lowest_argmax(row)
+        else:
+            y, _, _ = inverse_cdf(target_distribution(row, T), u[d])
+        out["tokens"][d] = y
+        child = next((j for j in range(n) if parents[j] == node and node_tokens[j] == y), None)
+        if child is None:
+            break
+        out["path"][d] = child
+        node, d = child, d + 1
+    out["n_accepted"] = d
+    out["status"] = status
+    return out
+
+
+def verify_tree(logits, node_tokens, parents, T, u, max_depth: int) -> dict:
+    """Batched tree verification: loop of verify_tree_sequence over the batch."""
+    B = np.asarray(logits).shape[0]
+    res = [verify_tree_sequence(logits[b], node_tokens[b], parents, float(T[b]), u[b], max_depth)
+           for b in range(B)]
+    return {
+        "tokens": np.stack([r["tokens"] for r in res]),
+        "path": np.stack([r["path"] for r in res]),
+        "n_accepted": np.array([r["n_accepted"] for r in res]),
+        "status": np.array([r["status"] for r in res]),
+    }
+
+
+def cartesian_tree_counts(tops) -> tuple[int, int]:
+    """(nodes, paths) of the full Cartesian candidate tree with s_i candidates at depth i.
+
+    Medusa notes, "Attention Tree": depth i holds prod_{j<=i} s_j nodes, so the tree has
+    sum_i prod_{j<=i} s_j tokens and prod_i s_i root-to-leaf paths.  Counted here by
+    enumerating the tree itself.
+    """
+    nodes = 0
+    level = [()]
+    for s in tops:
+        level = [path + (r,) for path in level for r in range(s)]
+        nodes += len(level)
+    return nodes, len(level)
+
+
+def medusa_sparse_tree(accuracy, n_nodes: int):
+    """Greedy sparse candidate tree from per-head top-k accuracies.
+
+    Medusa notes, section "OPTIMIZED TREE CONSTRUCTION": with a_k^(i) the accuracy of
+    head k's i-th candidate, a node reached by the path (i_1..i_m) is accepted with
+    probability prod_j a_j^(i_j) (accuracies assumed independent), and the expected
+    accepted length is the sum of these products over the tree's nodes; the tree is
+    grown by repeatedly adding the node of largest product.
+
+    accuracy[k][i] must be exact decimal strings or Fractions (READING: products are
+    compared exactly, so mathematically equal products tie exactly).  Because every
+    accuracy is <= 1, a child never outranks its parent, so the n_nodes largest
+    products form a tree; READING: ties resolve by (depth, lexicographic path).
+    Nodes are emitted ordered by (depth, lexicographic path), parents before children.
+
+    Returns (parents [n], paths list of tuples of 0-based ranks, values list of Fraction).
+    """
+    acc = [[Fraction(a) for a in head] for head in accuracy]
+    K = len(acc)
+    cand = []
+    for m in range(1, K + 1):
+        for path in itertools.product(*[range(len(acc[j])) for j in range(m)]):
+            v = Fraction(1)
+            for j, r in enumerate(path):
+                v *= acc[j][r]
+            cand.append((v, path))
+    cand.sort(key=lambda vp: (-vp[0], len(vp[1]), vp[1]))
+    chosen = cand[:n_nodes]
+    chosen.sort(key=lambda vp: (len(vp[1]), vp[1]))
+    index = {path: i for i, (_, path) in enumerate(chosen)}
+    parents = []
+    for _, path in chosen:
+        if len(path) == 1:
+            parents.append(-1)
+        else:
+            if path[:-1] not in index:
+                raise ValueError("selected nodes are not closed under parents")
+            parents.append(index[path[:-1]])
+    return parents, [p for _, p in chosen], [v for v, _ in chosen]
+
+
+def medusa_expected_length(values) -> Fraction:
+    """E[L] = sum over the tree's nodes of their path products (Medusa notes,
+    "OPTIMIZED TREE CONSTRUCTION"); the tree version of 1 + sum_i a_i counts the
+    extra token separately (Art of Guessing, "Token trees")."""
+    return sum(values, Fraction(0))
