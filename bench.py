@@ -1,0 +1,345 @@
+#!/usr/bin/env python3
+"""Benchmark of batched speculative-decoding verification on GB300.
+
+Default workload: chain verification at B=256, gamma=7, V=128256, bf16 logits, fp32
+draft probabilities (Zipf-biased synthetic logits), the configuration the throughput
+target is stated on.  One step = one specdec_verify_chain call over one batch (all rows:
+temperature softmax statistics, accept tests, first rejection, residual/bonus draw).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Metric: verified vocab rows per second, B*(gamma+1)
+rows per call, whole job over all ranks.  Several GPUs run independent replicas
+(sequences are independent; no collective is needed), scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "verified vocab rows/s (B*(gamma+1)) and achieved HBM GB/s vs GB300 peak"
+UNIT = "rows/s"
+DEFAULT_WORKLOAD = "chain_b256_v128256"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of chain_stats, from one ncu
+# capture of the benchmarked workload, keyed by the sha256 of the kernel source it was
+# taken on; reported as null once the source differs.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "speculative_decoding_token_temperature_gb300" / "csrc").glob("*")):
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text())
+        except Exception:
+            pass
+    return {}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.uuid = gpu_uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            for line in Path(self.path).read_text().splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def workload_shape(name):
+    import workloads
+    w = workloads.CHAIN_WORKLOADS[name]
+    return w["B"], w["gamma"], w["V"], w["dtype"]
+
+
+def cpu_oracle_rate(inputs_cpu: dict, target_seconds: float, max_seqs: int | None = None):
+    """Time the fp64 oracle (as it stands, one process) on the first sequences of one
+    batch until about target_seconds of work; returns (rows/s, sequences, seconds)."""
+    import numpy as np
+    from oracle import specdec_oracle as so
+
+    L = inputs_cpu["logits"]
+    L = L.float().numpy() if str(L.dtype) == "torch.bfloat16" else L.numpy()
+    q = inputs_cpu["draft_probs"].numpy()
+    d = inputs_cpu["draft_tokens"].numpy()
+    T = inputs_cpu["temperatures"].numpy()
+    u = inputs_cpu["uniforms"].numpy()
+    B, g1 = u.shape
+    n, t0 = 0, time.perf_counter()
+    while n < (max_seqs or B) and n < B:
+        so.verify_chain_sequence(L[n], q[n], d[n], float(T[n]), u[n])
+        n += 1
+        if time.perf_counter() - t0 >= target_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return n * g1 / dt, n, dt
+
+
+def run_reference(args, rank):
+    """The oracle as it stands, on the host cores, on the same workload and metric."""
+    if rank != 0:
+        return 0
+    import torch
+    import workloads
+    torch.set_num_threads(1)
+    B, g, V, dtype = workload_shape(args.workload)
+    per_step = args.ref_sequences
+    x = workloads.chain_workload(args.workload, 0, "cpu", B=per_step)
+    from oracle import specdec_oracle as so
+    import numpy as np
+    L = x["logits"].float().numpy() if dtype == "bf16" else x["logits"].numpy()
+    q, d, T, u = (x[k].numpy() for k in ("draft_probs", "draft_tokens", "temperatures", "uniforms"))
+
+    def step():
+        for b in range(per_step):
+            so.verify_chain_sequence(L[b], q[b], d[b], float(T[b]), u[b])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = per_step * (g + 1) / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "gamma": g, "V": V, "logits_dtype": dtype,
+                   "step_sample_sequences": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} sequences ({per_step * (g + 1)} rows) of {args.workload} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sets", type=int, default=3, help="input batches rotated between steps")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-sequences", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import workloads
+    import speculative_decoding_token_temperature_gb300 as sd
+    from speculative_decoding_token_temperature_gb300 import build as _build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.ensure_built()
+    sd.load_library()
+
+    B, g, V, dtype = workload_shape(args.workload)
+    esize = 2 if dtype == "bf16" else 4
+    rows = B * (g + 1)
+    sets = [workloads.chain_workload(args.workload, 100 * rank + s, dev) for s in range(args.sets)]
+    keys = ("logits", "draft_probs", "draft_tokens", "temperatures", "uniforms")
+    outs = [{"tokens": torch.empty(B, g + 1, dtype=torch.int32, device=dev),
+             "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+             "status": torch.empty(B, dtype=torch.int32, device=dev),
+             "p_draft": torch.empty(B, g, dtype=torch.float32, device=dev)} for _ in sets]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x = sets[i % len(sets)]
+        sd.verify_chain(*(x[k] for k in keys), out=outs[i % len(sets)], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    accepted = [float(o["num_accepted"].float().mean()) for o in outs]
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks, sd.KernelTimer(max_launches=4 * args.steps + 16) as kt:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        per_kernel = kt.read()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t)
+    ms_per_step = elapsed_ms / args.steps
+    value = rows * world / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel (the statistics pass over every logits row)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+    st_ms, st_n = per_kernel["chain_stats"]
+    dr_ms, dr_n = per_kernel["chain_sample"]
+    stats_bytes = rows * V * esize                       # every logits row read once
+    achieved = stats_bytes / (st_ms / st_n / 1e3) / 1e9 if st_n else None
+    sha = kernel_source_sha()
+    traffic = NCU_TRAFFIC.get("chain_stats", {})
+    traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
+    # bytes one whole call must move: all rows + the drawn row of logits and of q
+    n_rej = sum(float((o["num_accepted"] < g).float().sum()) for o in outs) / len(outs)
+    call_bytes = rows * V * esize + B * V * esize + n_rej * V * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "gamma": g, "V": V, "logits_dtype": dtype,
+                   "draft_probs_dtype": "fp32", "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2, {args.sets} seeded batches rotated"},
+        "hbm_gbs_call": call_bytes / (ms_per_step / 1e3) / 1e9,
+        "roofline": {"kernel": "chain_stats", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None,
+                     "algorithmic_bytes_per_launch": stats_bytes, "traffic": traffic_val},
+        "kernels_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items() if v[1]},
+        "gpu_launches": int(sum(v[1] for v in per_kernel.values())),
+        "mean_accepted": statistics.mean(accepted),
+        "clocks": clocks.summary(),
+        "kernel_src_sha": sha,
+    }
+
+    if not args.no_e2e:
+        host = {k: sets[0][k].cpu().pin_memory() for k in keys}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = B * (g + 1) * 4 + B * 4 + B * 4 + B * g * 4
+        for _ in range(2):
+            sd.verify_chain(*(host[k] for k in keys))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            res = sd.verify_chain(*(host[k] for k in keys))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        assert res["tokens"].device.type == "cpu"
+        line["e2e"] = {"value": rows * world / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x0 = {k: sets[0][k].cpu() for k in keys}
+        rate, nseq, secs = cpu_oracle_rate(x0, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"first {nseq} sequences ({nseq * (g + 1)} rows) of one batch, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

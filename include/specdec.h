@@ -1,0 +1,188 @@
+/*
+ * specdec.h -- C ABI of the GB300 (sm_103a) speculative-decoding verification library.
+ *
+ * The library implements the verification step of speculative decoding: it turns
+ * the target model's logits and the drafter's distributions into accepted tokens.
+ * Sources, cited by page title and section:
+ *   "Speculative decoding" (zerotofrontier.app, Chapter 20, Section 20.5)      -- SD 20.5
+ *   "Speculative-Decoding / Medusa" (s1mplewind.github.io)                    -- Medusa notes
+ *   "Speculative Decoding: The Art of Guessing Well" (astralord.github.io)    -- Art of Guessing
+ *
+ * Conventions shared by every entry point
+ *   - Array arguments are caller-owned DEVICE pointers to contiguous row-major arrays;
+ *     the library never allocates, frees or retains them.  Sizes are element counts.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Every call is asynchronous on `stream`; the caller synchronises before reading
+ *     outputs.  Work is launched only on `stream`.
+ *   - The return code covers host-side validation and launch errors only:
+ *       SPECDEC_OK, SPECDEC_ERR_INVALID_ARG (a null required pointer, a non-positive
+ *       size, an unknown dtype, misaligned workspace), SPECDEC_ERR_UNSUPPORTED (sizes the
+ *       kernels do not handle), SPECDEC_ERR_CUDA (a launch failed), SPECDEC_ERR_WORKSPACE
+ *       (workspace smaller than the matching *_workspace_bytes()).  On a non-OK return
+ *       nothing was launched, except for SPECDEC_ERR_CUDA.
+ *   - Problems in the DATA are reported per sequence in `out_status` (bit flags below).
+ *     A sequence with any error bit set gets num_accepted = -1 and all its tokens -1.
+ *     Warning bits leave the outputs valid.
+ *   - Temperatures below SPECDEC_GREEDY_TEMPERATURE (including 0 and negatives) select
+ *     greedy verification for that sequence (SD 20.5, "A round of greedy speculative
+ *     decoding"; the special case "A greedy target" of the sampling rule).
+ *   - Deterministic: the same inputs give bit-identical outputs on every call.
+ *   - Workspaces: a call's workspace must hold at least the size the matching
+ *     *_workspace_bytes() returns, be 256-byte aligned, and be ZERO-FILLED before its
+ *     first use (e.g. cudaMemsetAsync once).  Every call leaves the workspace zero-filled
+ *     again in the bytes later calls depend on, so one workspace can serve calls of any
+ *     shape that fits, one call at a time.  Calls that overlap on the GPU must not share
+ *     a workspace.
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
+
+/* return codes */
+#define SPECDEC_OK 0
+#define SPECDEC_ERR_INVALID_ARG 1
+#define SPECDEC_ERR_UNSUPPORTED 2
+#define SPECDEC_ERR_CUDA 3
+#define SPECDEC_ERR_WORKSPACE 4
+
+/* per-sequence status bits (errors: low byte; warnings: above) */
+#define SPECDEC_STATUS_BAD_LOGIT 1          /* NaN or +inf logit in a row the call reads      */
+#define SPECDEC_STATUS_EMPTY_ROW 2          /* a row whose logits are all -inf                */
+#define SPECDEC_STATUS_BAD_TOKEN 4          /* draft / node token outside [0, V)              */
+#define SPECDEC_STATUS_BAD_PROB 8           /* draft probability NaN, inf or negative         */
+#define SPECDEC_STATUS_BAD_UNIFORM 16       /* uniform outside [0, 1) on a sampled sequence   */
+#define SPECDEC_STATUS_BAD_TREE 32          /* parent not in [-1, i), or tree deeper than D   */
+#define SPECDEC_STATUS_BAD_TEMPERATURE 64   /* temperature NaN or infinite                    */
+#define SPECDEC_STATUS_ERROR_MASK 0xFF
+#define SPECDEC_STATUS_ZERO_Q 256           /* warning: q_i(x_i) == 0; accepted iff p_i(x_i) > 0 */
+#define SPECDEC_STATUS_ZERO_RESIDUAL 512    /* warning: residual mass 0 after rounding; drew from p */
+
+#define SPECDEC_GREEDY_TEMPERATURE 1e-3f
+
+/* ------------------------------------------------------------------------------------
+ * Chain verification: one round of speculative sampling per sequence.
+ *
+ * SD 20.5, "A round of speculative sampling" (Leviathan et al. Alg. 1) and the exercise
+ * "Verify one round of speculative sampling"; Art of Guessing, "Speculative sampling".
+ * For sequence b with temperature T = temperatures[b] >= SPECDEC_GREEDY_TEMPERATURE:
+ *   p_i = softmax(logits[b, i, :] / T), i = 0..g
+ *   draft i is accepted iff uniforms[b, i] * q_i(x_i) < p_i(x_i)   (u < p/q, min(1, .) implicit)
+ *   J = number of leading accepted drafts
+ *   the extra token y is the inverse-CDF draw with u = uniforms[b, g] from
+ *   (p_J - q_J)+ (normalised), where q_g == 0 so that J == g draws the bonus from p_g:
+ *   y = smallest k with C_k > u * S, C the running sum and S the total of the weights.
+ * Greedy sequences accept while x_i == argmax_k logits[b, i, k] (lowest index on ties)
+ * and emit the argmax of row J; draft_probs and uniforms are not read for them.
+ *
+ * logits          [B, g+1, V]  fp32 or bf16 (ldt)          row i: target after x_0..x_{i-1}
+ * draft_probs     [B, g, V]    fp32, the distribution each draft was sampled from, as given
+ * draft_tokens    [B, g]       int32
+ * temperatures    [B]          fp32
+ * uniforms        [B, g+1]     fp32 in [0, 1): slot i tests draft i, slot g drives y
+ * out_tokens      [B, g+1]     int32: x_0..x_{J-1}, y, then -1
+ * out_num_accepted[B]          int32: J (or -1 on a data error)
+ * out_p_draft     [B, g]       fp32, optional (NULL): p_i(x_i); NaN for greedy sequences
+ * out_status      [B]          int32, optional (NULL): status bits
+ * Every logits row is read once; row J and q row J are read again by the draw.
+ * Sizes: B >= 1, g >= 1, V >= 1, V < 2^31.
+ */
+size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
+
+int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                         const int32_t* draft_tokens, const float* temperatures,
+                         const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                         int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Greedy verification (SD 20.5, "A round of greedy speculative decoding"; Art of
+ * Guessing, "Draft and verify"): z_i = argmax logits[b, i, :] (lowest index on ties),
+ * J = longest prefix with x_i == z_i, emit x_0..x_{J-1}, z_J.  Shapes as for the chain
+ * call.  Every sequence is greedy whatever its temperature would be.
+ */
+size_t specdec_greedy_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
+
+int specdec_verify_greedy(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
+                          int B, int g, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                          int32_t* out_status, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Medusa tree verification: a walk of a candidate tree per sequence.
+ *
+ * Medusa notes, section "Attention Tree": at the current node the target draws a token
+ * (inverse CDF of softmax(logits / T) with uniforms[b, d] at depth d, or the argmax for a
+ * greedy sequence); if a child of the node carries that token the walk appends it and
+ * descends, otherwise it emits the token and stops.  SD 20.5 gives the greedy walk after
+ * the exercise "The tree attention mask".  Among children carrying the same token the
+ * lowest node index is taken.
+ *
+ * logits        [B, N+1, V]  row 0: after the committed prefix (the root); row 1+i: after node i
+ * node_tokens   [B, N]       int32
+ * parents       [N]          int32, shared by the batch, parents[i] in [-1, i)
+ * temperatures  [B]          fp32
+ * uniforms      [B, D+1]     fp32 in [0, 1), D = max_depth
+ * out_tokens    [B, D+1]     int32: the accepted node tokens then the final draw, -1 padded
+ * out_path      [B, D]       int32: node ids of the accepted path, -1 padded
+ * out_num_accepted [B]       int32: accepted nodes (or -1 on a data error)
+ * out_status    [B]          int32, optional
+ * max_depth D bounds the number of nodes on any root path (SPECDEC_STATUS_BAD_TREE if a
+ * path is longer).  Only the rows the walk visits are read.  N >= 0, 1 <= D <= 64.
+ */
+size_t specdec_tree_workspace_bytes(int B, int N, int V, int max_depth, specdec_dtype ldt);
+
+int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* node_tokens,
+                        const int32_t* parents, const float* temperatures, const float* uniforms,
+                        int B, int N, int V, int max_depth, int32_t* out_tokens,
+                        int32_t* out_path, int32_t* out_num_accepted, int32_t* out_status,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Tree-attention mask and position ids (SD 20.5, box "Token tree and tree attention").
+ *   out_mask          [N, P+N] uint8: row i is 1 on every prefix column j < P, on column
+ *                     P+i and on column P+a for every ancestor a of node i; 0 elsewhere
+ *   out_position_ids  [N] int64: P + depth(i), depth = number of ancestors
+ *   out_depth         [N] int32, optional
+ *   out_status        [1] int32: SPECDEC_STATUS_BAD_TREE if some parents[i] is not in
+ *                     [-1, i); the other outputs are then unspecified
+ * N >= 1, P >= 0, (P + N) * N < 2^31.
+ */
+int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* out_mask,
+                            int64_t* out_position_ids, int32_t* out_depth, int32_t* out_status,
+                            void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Kernel timing for benchmarks.  While enabled, every kernel the library launches is
+ * bracketed by a pair of CUDA events recorded on the launching stream.  The state is
+ * process-global and not thread-safe; enable it only around single-threaded timing.
+ *   specdec_profile_start(max_launches): creates the event pool; returns SPECDEC_OK.
+ *   specdec_profile_read(total_ms, launches, n): synchronises the recorded events and
+ *     writes per-kernel totals for kernel ids 0..n-1 (ids: SPECDEC_KERNEL_*); resets.
+ *   specdec_profile_stop(): disables timing and destroys the events.
+ */
+#define SPECDEC_KERNEL_CHAIN_STATS 0
+#define SPECDEC_KERNEL_CHAIN_SAMPLE 1
+#define SPECDEC_KERNEL_TREE_WALK 2
+#define SPECDEC_KERNEL_TREE_MASK 3
+#define SPECDEC_NUM_KERNELS 4
+
+int specdec_profile_start(int max_launches);
+int specdec_profile_read(double* total_ms, int* launches, int n);
+int specdec_profile_stop(void);
+
+/* Library version string, e.g. "0.1.0". */
+const char* specdec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H */

@@ -39,6 +39,7 @@ STATUS_BAD_TOKEN = 4        # a draft / node token outside [0, V) (error)
 STATUS_BAD_PROB = 8         # a draft probability that is NaN, inf or negative (error)
 STATUS_BAD_UNIFORM = 16     # a uniform outside [0, 1) on a sampled sequence (error)
 STATUS_BAD_TREE = 32        # parent not in [-1, i) or a tree deeper than max_depth (error)
+STATUS_BAD_TEMPERATURE = 64 # a NaN or infinite temperature (error)
 STATUS_ZERO_Q = 256         # q_i(x_i) == 0 for a drafted token (warning)
 STATUS_ZERO_RESIDUAL = 512  # residual mass was 0; the draw fell back to p (warning)
 STATUS_ERROR_MASK = 0xFF
@@ -169,7 +170,9 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
     drafts = [int(x) for x in np.asarray(drafts).reshape(-1)]
     assert len(drafts) == gamma
     u = widen(u).reshape(-1)
-    greedy = bool(T < GREEDY_T)
+    greedy = bool(T < GREEDY_T)   # READING: NaN is not >= the threshold; flagged below
+    if np.isnan(T):
+        greedy = True
     out = {
         "tokens": np.full(gamma + 1, -1, dtype=np.int64),
         "J": -1,
@@ -179,7 +182,7 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
         "margins": np.full(gamma, np.inf),
         "greedy": greedy,
     }
-    status = 0
+    status = 0 if np.isfinite(T) else STATUS_BAD_TEMPERATURE
     for i in range(g1):
         status |= _row_status(logits[i])
     for x in drafts:
@@ -188,8 +191,8 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
     if not greedy:
         if not np.all((u >= 0.0) & (u < 1.0)):
             status |= STATUS_BAD_UNIFORM
-        if not (status & STATUS_BAD_TOKEN):
-            for i, x in enumerate(drafts):
+        for i, x in enumerate(drafts):
+            if 0 <= x < V:
                 qx = float(widen(q[i][x]))
                 if not np.isfinite(qx) or qx < 0.0:
                     status |= STATUS_BAD_PROB
@@ -338,14 +341,14 @@ def verify_tree_sequence(logits, node_tokens, parents, T: float, u, max_depth: i
     parents = [int(x) for x in parents]
     node_tokens = [int(x) for x in node_tokens]
     u = widen(u).reshape(-1)
-    greedy = bool(T < GREEDY_T)
+    greedy = bool(T < GREEDY_T) or bool(np.isnan(T))
     out = {
         "tokens": np.full(max_depth + 1, -1, dtype=np.int64),
         "path": np.full(max_depth, -1, dtype=np.int64),
         "n_accepted": -1,
         "status": 0,
     }
-    status = 0
+    status = 0 if np.isfinite(T) else STATUS_BAD_TEMPERATURE
     try:
         depth = tree_depths(parents)
         if n and depth.max() + 1 > max_depth:

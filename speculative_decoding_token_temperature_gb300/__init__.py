@@ -1,0 +1,310 @@
+"""GB300 (sm_103a) speculative-decoding verification.
+
+A thin ctypes binding over the C ABI in ``include/specdec.h`` (``libspecdec.so``, built
+in-tree by ``build.py``).  The binding only marshals arguments: it checks shapes and
+dtypes, passes raw device pointers and the current CUDA stream to the library, and, for
+tensors that live on the host, copies inputs to the device and results back.  Every
+step of verification runs in the library's CUDA kernels; there is no CPU fallback, and
+calling without the compiled library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+__all__ = [
+    "SpecdecError", "verify_chain", "verify_greedy", "verify_tree", "build_tree_mask",
+    "chain_workspace_bytes", "library_path", "load_library", "KernelTimer",
+    "F32", "BF16", "GREEDY_TEMPERATURE",
+]
+
+F32, BF16 = 0, 1
+GREEDY_TEMPERATURE = 1e-3
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
+_ERR_NAMES = {1: "invalid argument", 2: "unsupported size", 3: "CUDA launch error",
+              4: "workspace too small"}
+
+STATUS_BAD_LOGIT = 1
+STATUS_EMPTY_ROW = 2
+STATUS_BAD_TOKEN = 4
+STATUS_BAD_PROB = 8
+STATUS_BAD_UNIFORM = 16
+STATUS_BAD_TREE = 32
+STATUS_BAD_TEMPERATURE = 64
+STATUS_ERROR_MASK = 0xFF
+STATUS_ZERO_Q = 256
+STATUS_ZERO_RESIDUAL = 512
+
+KERNEL_CHAIN_STATS, KERNEL_CHAIN_SAMPLE, KERNEL_TREE_WALK, KERNEL_TREE_MASK = 0, 1, 2, 3
+KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask")
+
+
+class SpecdecError(RuntimeError):
+    pass
+
+
+_LIB = None
+
+
+def library_path() -> Path:
+    return Path(__file__).resolve().with_name("libspecdec.so")
+
+
+def load_library():
+    """Load libspecdec.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not path.exists():
+        raise SpecdecError(f"{path.name} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(str(path))
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.specdec_chain_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.specdec_chain_workspace_bytes.restype = sz
+    lib.specdec_greedy_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.specdec_greedy_workspace_bytes.restype = sz
+    lib.specdec_tree_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.specdec_tree_workspace_bytes.restype = sz
+    lib.specdec_verify_chain.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.specdec_verify_chain.restype = i32
+    lib.specdec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.specdec_verify_greedy.restype = i32
+    lib.specdec_verify_tree.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.specdec_verify_tree.restype = i32
+    lib.specdec_build_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
+    lib.specdec_build_tree_mask.restype = i32
+    lib.specdec_profile_start.argtypes = [i32]
+    lib.specdec_profile_start.restype = i32
+    lib.specdec_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i32]
+    lib.specdec_profile_read.restype = i32
+    lib.specdec_profile_stop.argtypes = []
+    lib.specdec_profile_stop.restype = i32
+    lib.specdec_version.argtypes = []
+    lib.specdec_version.restype = ctypes.c_char_p
+    _LIB = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SpecdecError(f"{what}: {_ERR_NAMES.get(rc, rc)} (code {rc})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise ValueError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_WORKSPACES: dict = {}
+
+
+def _workspace(nbytes: int, device, stream_handle: int):
+    """A zero-filled device workspace per (device, stream); the library leaves it zeroed."""
+    if nbytes == 0:
+        return None, 0
+    key = (device, stream_handle)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws, ws.numel()
+
+
+def chain_workspace_bytes(B: int, gamma: int, V: int, dtype=torch.bfloat16) -> int:
+    code = BF16 if dtype == torch.bfloat16 else F32
+    return int(load_library().specdec_chain_workspace_bytes(B, gamma, V, code))
+
+
+class _HostRoundTrip:
+    """Copies host inputs to the device and device outputs back (argument marshalling)."""
+
+    def __init__(self, tensors):
+        self.on_host = tensors[0].device.type == "cpu"
+        self.device = torch.device("cuda", torch.cuda.current_device()) if self.on_host else tensors[0].device
+
+    def to_device(self, t):
+        if t is None or not self.on_host:
+            return t
+        return t.to(self.device, non_blocking=True)
+
+    def to_host(self, t):
+        if t is None or not self.on_host:
+            return t
+        return t.to("cpu", non_blocking=False)
+
+
+def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, out=None,
+                 with_p_draft: bool = True, stream=None) -> dict:
+    """One round of chain verification per sequence (specdec_verify_chain).
+
+    logits [B, g+1, V] bf16/fp32; draft_probs [B, g, V] fp32; draft_tokens [B, g] int32;
+    temperatures [B] fp32; uniforms [B, g+1] fp32.  Returns a dict with tokens
+    [B, g+1] int32 (-1 padded), num_accepted [B] int32, p_draft [B, g] fp32 (if
+    requested) and status [B] int32.  Host tensors are copied to the current device and
+    the results copied back.
+    """
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    logits, draft_probs, draft_tokens, temperatures, uniforms = (
+        rt.to_device(t) for t in (logits, draft_probs, draft_tokens, temperatures, uniforms))
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, g+1, V]")
+    B, g1, V = logits.shape
+    g = g1 - 1
+    dev = logits.device
+    code = _dtype_code(logits)
+    _need(draft_probs, "draft_probs", torch.float32, (B, g, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
+    _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, g1), dev)
+    _need(logits, "logits", None, (B, g1, V), dev)
+    if out is None:
+        out = {
+            "tokens": torch.empty(B, g1, dtype=torch.int32, device=dev),
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+        if with_p_draft:
+            out["p_draft"] = torch.empty(B, g, dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws, wsb = _workspace(int(lib.specdec_chain_workspace_bytes(B, g, V, code)), dev, s.cuda_stream)
+    rc = lib.specdec_verify_chain(
+        _ptr(logits), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperatures),
+        _ptr(uniforms), B, g, V, _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+        _ptr(out.get("p_draft")), _ptr(out.get("status")), _ptr(ws), wsb,
+        ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_chain")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def verify_greedy(logits, draft_tokens, *, out=None, stream=None) -> dict:
+    """Greedy verification (specdec_verify_greedy): tokens, num_accepted, status."""
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    logits, draft_tokens = rt.to_device(logits), rt.to_device(draft_tokens)
+    B, g1, V = logits.shape
+    g = g1 - 1
+    dev = logits.device
+    code = _dtype_code(logits)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
+    _need(logits, "logits", None, (B, g1, V), dev)
+    if out is None:
+        out = {
+            "tokens": torch.empty(B, g1, dtype=torch.int32, device=dev),
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws, wsb = _workspace(int(lib.specdec_greedy_workspace_bytes(B, g, V, code)), dev, s.cuda_stream)
+    rc = lib.specdec_verify_greedy(_ptr(logits), code, _ptr(draft_tokens), B, g, V,
+                                   _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                   _ptr(out.get("status")), _ptr(ws), wsb,
+                                   ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_greedy")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth: int, *,
+                out=None, stream=None) -> dict:
+    """Medusa tree walk (specdec_verify_tree): tokens [B, D+1], path [B, D],
+    num_accepted [B], status [B]."""
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    logits, node_tokens, parents, temperatures, uniforms = (
+        rt.to_device(t) for t in (logits, node_tokens, parents, temperatures, uniforms))
+    B, n1, V = logits.shape
+    N = n1 - 1
+    D = int(max_depth)
+    dev = logits.device
+    code = _dtype_code(logits)
+    _need(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    _need(parents, "parents", torch.int32, (N,), dev)
+    _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, D + 1), dev)
+    _need(logits, "logits", None, (B, n1, V), dev)
+    if out is None:
+        out = {
+            "tokens": torch.empty(B, D + 1, dtype=torch.int32, device=dev),
+            "path": torch.empty(B, D, dtype=torch.int32, device=dev),
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws, wsb = _workspace(int(lib.specdec_tree_workspace_bytes(B, N, V, D, code)), dev, s.cuda_stream)
+    rc = lib.specdec_verify_tree(_ptr(logits), code, _ptr(node_tokens), _ptr(parents),
+                                 _ptr(temperatures), _ptr(uniforms), B, N, V, D,
+                                 _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["num_accepted"]),
+                                 _ptr(out.get("status")), _ptr(ws), wsb,
+                                 ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_tree")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def build_tree_mask(parents, prefix_len: int, *, stream=None) -> dict:
+    """Tree-attention mask [N, P+N] uint8, position ids [N] int64, depth [N] int32 and a
+    one-element status (specdec_build_tree_mask)."""
+    lib = load_library()
+    rt = _HostRoundTrip([parents])
+    parents = rt.to_device(parents)
+    if parents.dim() != 1 or parents.dtype != torch.int32 or not parents.is_contiguous():
+        raise ValueError("parents must be a contiguous int32 vector")
+    N = parents.shape[0]
+    dev = parents.device
+    out = {
+        "mask": torch.empty(N, prefix_len + N, dtype=torch.uint8, device=dev),
+        "position_ids": torch.empty(N, dtype=torch.int64, device=dev),
+        "depth": torch.empty(N, dtype=torch.int32, device=dev),
+        "status": torch.empty(1, dtype=torch.int32, device=dev),
+    }
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.specdec_build_tree_mask(_ptr(parents), N, int(prefix_len), _ptr(out["mask"]),
+                                     _ptr(out["position_ids"]), _ptr(out["depth"]),
+                                     _ptr(out["status"]), ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_build_tree_mask")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+class KernelTimer:
+    """Per-kernel CUDA-event timing of every library launch while active."""
+
+    def __init__(self, max_launches: int = 4096):
+        self.max_launches = max_launches
+
+    def __enter__(self):
+        _check(load_library().specdec_profile_start(self.max_launches), "specdec_profile_start")
+        return self
+
+    def read(self) -> dict:
+        n = len(KERNEL_NAMES)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int * n)()
+        _check(load_library().specdec_profile_read(ms, cnt, n), "specdec_profile_read")
+        return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}
+
+    def __exit__(self, *exc):
+        load_library().specdec_profile_stop()
+        return False

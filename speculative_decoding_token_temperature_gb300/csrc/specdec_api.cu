@@ -1,0 +1,273 @@
+// C-ABI entry points: argument validation, workspace layout, launches, kernel timing.
+
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "specdec.h"
+#include "specdec_internal.h"
+
+namespace specdec {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(specdec_dtype t) { return t == SPECDEC_BF16 ? 2 : 4; }
+
+bool valid_dtype(int t) { return t == SPECDEC_F32 || t == SPECDEC_BF16; }
+
+// 16-byte vector loads need every row start 16-byte aligned.
+bool rows_vectorizable(const void* base, int64_t V, size_t esize) {
+  return aligned16(base) && ((V * static_cast<int64_t>(esize)) % 16 == 0);
+}
+
+// ---- kernel timing (process-global, single-threaded use) -----------------------------
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+bool g_prof_on = false;
+std::vector<cudaEvent_t> g_prof_pool;
+std::vector<ProfRecord> g_prof_records;
+size_t g_prof_next = 0;
+
+struct ProfScope {
+  cudaStream_t stream;
+  int kernel;
+  bool active = false;
+  ProfRecord rec{};
+  ProfScope(int k, cudaStream_t s) : stream(s), kernel(k) {
+    if (g_prof_on && g_prof_next + 2 <= g_prof_pool.size()) {
+      rec = {k, g_prof_pool[g_prof_next], g_prof_pool[g_prof_next + 1]};
+      g_prof_next += 2;
+      active = cudaEventRecord(rec.start, stream) == cudaSuccess;
+    }
+  }
+  ~ProfScope() {
+    if (active && cudaEventRecord(rec.stop, stream) == cudaSuccess) g_prof_records.push_back(rec);
+  }
+};
+
+}  // namespace
+
+size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, bool vector_path,
+                              void* base, ChainWorkspace* ws) {
+  const int seg = chain_segment_len(ldt, vector_path);
+  const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
+  const int64_t rows = static_cast<int64_t>(B) * (g + 1);
+  size_t off = 0;
+  const size_t o_counters = off; off += round_up(sizeof(unsigned) * 2 * static_cast<size_t>(B));
+  const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
+  const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(rows * nseg));
+  const size_t o_draw = off;     off += round_up(sizeof(double2) * static_cast<size_t>(B * nseg));
+  if (base != nullptr && ws != nullptr) {
+    char* p = static_cast<char*>(base);
+    ws->counters = reinterpret_cast<unsigned*>(p + o_counters);
+    ws->seq = reinterpret_cast<SeqState*>(p + o_seq);
+    ws->partials = reinterpret_cast<float4*>(p + o_part);
+    ws->draw = reinterpret_cast<double2*>(p + o_draw);
+  }
+  return off;
+}
+
+}  // namespace specdec
+
+using namespace specdec;
+
+namespace {
+
+// Workspace sizing must not depend on pointer alignment, so size for the shorter
+// (scalar-path) segment, which needs the most segments.
+size_t chain_ws_bytes(int B, int g, int V, specdec_dtype ldt) {
+  const size_t a = chain_workspace_layout(B, g, V, ldt, false, nullptr, nullptr);
+  const size_t b = chain_workspace_layout(B, g, V, ldt, true, nullptr, nullptr);
+  return a > b ? a : b;
+}
+
+bool chain_sizes_ok(int B, int g, int V) {
+  if (B <= 0 || g <= 0 || V <= 0) return false;
+  return true;
+}
+
+int chain_common(const void* logits, specdec_dtype ldt, const float* q, const int32_t* drafts,
+                 const float* temps, const float* u, int B, int g, int V, int32_t* out_tokens,
+                 int32_t* out_J, float* out_p, int32_t* out_status, void* workspace,
+                 size_t workspace_bytes, void* stream, bool greedy_only) {
+  if (!valid_dtype(ldt)) return SPECDEC_ERR_INVALID_ARG;
+  if (!chain_sizes_ok(B, g, V)) return SPECDEC_ERR_INVALID_ARG;
+  if (!logits || !drafts || !out_tokens || !out_J || !workspace) return SPECDEC_ERR_INVALID_ARG;
+  if (!greedy_only && (!q || !temps || !u)) return SPECDEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPECDEC_ERR_INVALID_ARG;
+  if (g > kMaxGamma) return SPECDEC_ERR_UNSUPPORTED;
+  const size_t es = elem_size(ldt);
+  bool vec = rows_vectorizable(logits, V, es);
+  if (!greedy_only) vec = vec && rows_vectorizable(q, V, 4);
+  const int seg = chain_segment_len(ldt, vec);
+  const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
+  const int64_t items = static_cast<int64_t>(B) * (g + 1) * nseg;
+  if (items > INT32_MAX || nseg > 65535 || B > 65535) return SPECDEC_ERR_UNSUPPORTED;
+  if (workspace_bytes < chain_ws_bytes(B, g, V, ldt)) return SPECDEC_ERR_WORKSPACE;
+
+  ChainParams P{};
+  P.logits = logits;
+  P.q = q;
+  P.drafts = drafts;
+  P.temps = greedy_only ? nullptr : temps;
+  P.u = greedy_only ? nullptr : u;
+  P.B = B;
+  P.gamma = g;
+  P.V = V;
+  P.nseg = static_cast<int>(nseg);
+  P.seg = seg;
+  P.greedy_only = greedy_only ? 1 : 0;
+  P.out_tokens = out_tokens;
+  P.out_J = out_J;
+  P.out_p_draft = greedy_only ? nullptr : out_p;
+  P.out_status = out_status;
+  chain_workspace_layout(B, g, V, ldt, vec, workspace, &P.ws);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    ProfScope prof(SPECDEC_KERNEL_CHAIN_STATS, s);
+    if (launch_chain_stats(P, ldt, vec, s) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  }
+  if (!greedy_only) {
+    ProfScope prof(SPECDEC_KERNEL_CHAIN_SAMPLE, s);
+    if (launch_chain_sample(P, ldt, vec, s) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  }
+  return SPECDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
+  if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return 0;
+  return chain_ws_bytes(B, g, V, ldt);
+}
+
+int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                         const int32_t* draft_tokens, const float* temperatures,
+                         const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                         int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return chain_common(logits, ldt, draft_probs, draft_tokens, temperatures, uniforms, B, g, V,
+                      out_tokens, out_num_accepted, out_p_draft, out_status, workspace,
+                      workspace_bytes, stream, false);
+}
+
+size_t specdec_greedy_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
+  return specdec_chain_workspace_bytes(B, g, V, ldt);
+}
+
+int specdec_verify_greedy(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
+                          int B, int g, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                          int32_t* out_status, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return chain_common(logits, ldt, nullptr, draft_tokens, nullptr, nullptr, B, g, V, out_tokens,
+                      out_num_accepted, nullptr, out_status, workspace, workspace_bytes, stream,
+                      true);
+}
+
+size_t specdec_tree_workspace_bytes(int B, int N, int V, int max_depth, specdec_dtype ldt) {
+  (void)B; (void)N; (void)V; (void)max_depth; (void)ldt;
+  return 0;  // the walk keeps all of its state on chip
+}
+
+int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* node_tokens,
+                        const int32_t* parents, const float* temperatures, const float* uniforms,
+                        int B, int N, int V, int max_depth, int32_t* out_tokens,
+                        int32_t* out_path, int32_t* out_num_accepted, int32_t* out_status,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (!valid_dtype(ldt)) return SPECDEC_ERR_INVALID_ARG;
+  if (B <= 0 || N < 0 || V <= 0 || max_depth < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (!logits || !temperatures || !uniforms || !out_tokens || !out_path || !out_num_accepted)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (N > 0 && (!node_tokens || !parents)) return SPECDEC_ERR_INVALID_ARG;
+  if (max_depth > kMaxTreeDepth || B > INT32_MAX) return SPECDEC_ERR_UNSUPPORTED;
+  TreeParams P{};
+  P.logits = logits;
+  P.node_tokens = node_tokens;
+  P.parents = parents;
+  P.temps = temperatures;
+  P.u = uniforms;
+  P.B = B;
+  P.N = N;
+  P.V = V;
+  P.D = max_depth;
+  P.out_tokens = out_tokens;
+  P.out_path = out_path;
+  P.out_J = out_num_accepted;
+  P.out_status = out_status;
+  const bool vec = rows_vectorizable(logits, V, elem_size(ldt));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_TREE_WALK, s);
+  return launch_tree_walk(P, ldt, vec, s) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
+int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* out_mask,
+                            int64_t* out_position_ids, int32_t* out_depth, int32_t* out_status,
+                            void* stream) {
+  if (!parents || !out_mask || !out_position_ids || !out_status) return SPECDEC_ERR_INVALID_ARG;
+  if (N <= 0 || prefix_len < 0) return SPECDEC_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(prefix_len) + N) * N >= INT32_MAX) return SPECDEC_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_TREE_MASK, s);
+  return launch_tree_mask(parents, N, prefix_len, out_mask, out_position_ids, out_depth,
+                          out_status, s) == cudaSuccess
+             ? SPECDEC_OK
+             : SPECDEC_ERR_CUDA;
+}
+
+int specdec_profile_start(int max_launches) {
+  if (max_launches <= 0) return SPECDEC_ERR_INVALID_ARG;
+  specdec_profile_stop();
+  g_prof_pool.resize(static_cast<size_t>(max_launches) * 2);
+  for (auto& e : g_prof_pool) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      specdec_profile_stop();
+      return SPECDEC_ERR_CUDA;
+    }
+  }
+  g_prof_records.clear();
+  g_prof_next = 0;
+  g_prof_on = true;
+  return SPECDEC_OK;
+}
+
+int specdec_profile_read(double* total_ms, int* launches, int n) {
+  if (!total_ms || !launches || n <= 0) return SPECDEC_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) { total_ms[i] = 0.0; launches[i] = 0; }
+  for (const auto& r : g_prof_records) {
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    if (r.kernel >= 0 && r.kernel < n) { total_ms[r.kernel] += ms; launches[r.kernel] += 1; }
+  }
+  g_prof_records.clear();
+  g_prof_next = 0;
+  return SPECDEC_OK;
+}
+
+int specdec_profile_stop(void) {
+  g_prof_on = false;
+  for (auto& e : g_prof_pool)
+    if (e) cudaEventDestroy(e);
+  g_prof_pool.clear();
+  g_prof_records.clear();
+  g_prof_next = 0;
+  return SPECDEC_OK;
+}
+
+const char* specdec_version(void) { return "0.1.0"; }
+
+}  // extern "C"

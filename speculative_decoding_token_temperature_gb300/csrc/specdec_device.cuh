@@ -1,0 +1,178 @@
+// Device-side building blocks shared by the verification kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specdec.h"
+
+namespace specdec {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kInf = __builtin_huge_valf();
+
+// ---------------------------------------------------------------------------------
+// Scalar helpers (inline PTX for the two instructions the hot loops are built on)
+// ---------------------------------------------------------------------------------
+
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32; results below the normal
+// range flush to +0, which only drops terms smaller than 2^-126 of the row maximum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max that propagates NaN (PTX max.NaN.f32), so one NaN logit poisons the row maximum.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float load(const float* p, int64_t k) { return __ldg(p + k); }
+};
+template <> struct Elem<uint16_t> {  // bf16 stored as raw 16-bit words
+  static __device__ __forceinline__ float load(const uint16_t* p, int64_t k) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(p + k)) << 16);
+  }
+};
+
+// A vector of VEC consecutive elements converted to fp32.  VEC == 16 / sizeof(T) uses one
+// 16-byte load (the caller guarantees 16-byte alignment); VEC == 1 is the scalar path for
+// rows that are not 16-byte aligned.
+template <typename T, int VEC> struct VecLoad;
+
+template <> struct VecLoad<uint16_t, 8> {
+  static __device__ __forceinline__ void load(const uint16_t* p, int64_t k, float (&v)[8]) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p + k));
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+  }
+};
+template <> struct VecLoad<float, 4> {
+  static __device__ __forceinline__ void load(const float* p, int64_t k, float (&v)[4]) {
+    const float4 w = __ldg(reinterpret_cast<const float4*>(p + k));
+    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+  }
+};
+template <typename T> struct VecLoad<T, 1> {
+  static __device__ __forceinline__ void load(const T* p, int64_t k, float (&v)[1]) {
+    v[0] = Elem<T>::load(p, k);
+  }
+};
+
+// fp32 draft probabilities in groups of VEC (VEC in {1, 4, 8}); 16-byte loads when VEC >= 4.
+template <int VEC> __device__ __forceinline__ void load_q(const float* p, int64_t k, float (&v)[VEC]) {
+  if constexpr (VEC == 1) {
+    v[0] = __ldg(p + k);
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC; j += 4) {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(p + k + j));
+      v[j] = w.x; v[j + 1] = w.y; v[j + 2] = w.z; v[j + 3] = w.w;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Block reductions and scans (NT threads, fixed order => deterministic)
+// ---------------------------------------------------------------------------------
+
+template <int NT> struct Block {
+  static constexpr int kWarps = NT / 32;
+  static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+
+  // Max with NaN propagation; result broadcast to all threads.
+  static __device__ __forceinline__ float max(float v, float* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    float r = sh[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = max_nan(r, sh[i]);
+    return r;
+  }
+
+  static __device__ __forceinline__ int min_int(int v, int* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = ::min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    int r = sh[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = ::min(r, sh[i]);
+    return r;
+  }
+
+  static __device__ __forceinline__ int or_int(int v, int* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r |= sh[i];
+    return r;
+  }
+
+  static __device__ __forceinline__ float sum(float v, float* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    float r = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r += sh[i];
+    return r;
+  }
+
+  static __device__ __forceinline__ double sum(double v, double* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    double r = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r += sh[i];
+    return r;
+  }
+
+  // Inclusive prefix sum in thread order; also returns the block total.
+  static __device__ __forceinline__ double inclusive_scan(double v, double* sh, double& total) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double n = __shfl_up_sync(0xffffffffu, v, o);
+      if (l >= o) v += n;
+    }
+    __syncthreads();
+    if (l == 31) sh[w] = v;
+    __syncthreads();
+    double off = 0.0;
+    for (int i = 0; i < w; ++i) off += sh[i];
+    double t = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) t += sh[i];
+    total = t;
+    return v + off;
+  }
+};
+
+}  // namespace specdec

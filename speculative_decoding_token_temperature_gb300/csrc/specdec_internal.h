@@ -1,0 +1,78 @@
+// Host/device interface between the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specdec.h"
+
+namespace specdec {
+
+constexpr int kChainThreads = 256;
+constexpr int kChainVectorsPerThread = 8;    // 16-byte vectors per thread per segment
+constexpr int kScalarElemsPerThread = 32;    // elements per thread per segment (scalar path)
+constexpr int kMaxGamma = 255;               // drafts per sequence handled by one decision CTA
+constexpr int kTreeThreads = 512;
+constexpr int kMaxTreeDepth = 64;
+
+// Per-sequence state handed from the decision step to the draw step.
+struct SeqState {
+  int4 meta;   // (J, mode, status, 0); mode 0: done, 1: draw from residual or bonus row
+  float4 row;  // (row max m, normaliser Z, c = log2(e)/T, uniform of the extra token)
+};
+
+struct ChainWorkspace {
+  float4* partials;   // [B*(g+1)*nseg]: per segment (max, sum of 2^((l-max)c), argmax bits, 0)
+  unsigned* counters; // [2B]: arrivals per sequence for the statistics and the draw kernels
+  SeqState* seq;      // [B]
+  double2* draw;      // [B*nseg]: per segment (residual mass, target mass) of the drawn row
+};
+
+struct ChainParams {
+  const void* logits;
+  const float* q;
+  const int32_t* drafts;
+  const float* temps;    // nullptr in greedy-only mode
+  const float* u;        // nullptr in greedy-only mode
+  int B, gamma, V;
+  int nseg;              // segments per row
+  int seg;               // elements per segment
+  int greedy_only;
+  int32_t* out_tokens;
+  int32_t* out_J;
+  float* out_p_draft;
+  int32_t* out_status;
+  ChainWorkspace ws;
+};
+
+// Segment length in elements for a logits dtype and load path.
+int chain_segment_len(specdec_dtype ldt, bool vector_path);
+// Workspace layout; returns the total bytes (and fills ws when base != nullptr).
+size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, bool vector_path,
+                              void* base, ChainWorkspace* ws);
+
+cudaError_t launch_chain_stats(const ChainParams& P, specdec_dtype ldt, bool vector_path,
+                               cudaStream_t stream);
+cudaError_t launch_chain_sample(const ChainParams& P, specdec_dtype ldt, bool vector_path,
+                                cudaStream_t stream);
+
+struct TreeParams {
+  const void* logits;
+  const int32_t* node_tokens;
+  const int32_t* parents;
+  const float* temps;
+  const float* u;
+  int B, N, V, D;
+  int32_t* out_tokens;
+  int32_t* out_path;
+  int32_t* out_J;
+  int32_t* out_status;
+};
+
+cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector_path,
+                             cudaStream_t stream);
+cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* mask,
+                             int64_t* pos, int32_t* depth, int32_t* status, cudaStream_t stream);
+
+}  // namespace specdec

@@ -1,0 +1,189 @@
+"""Element-by-element comparison of the CUDA path with the fp64 oracle.
+
+Rules (written here, used by every parity test):
+
+* Status bits, greedy tokens and greedy J: bit-exact.
+* p_i(x_i): within P_TOL absolute of the oracle's fp64 value.
+* Accept/reject decisions and drawn tokens: exact, except a FLAGGED disagreement:
+  - a decision may differ only at the first position where the two J differ, and only if
+    the oracle's uniform lies within FLAG_TOL of that test's boundary p/q;
+  - a drawn token may differ only if the GPU's token has positive weight and the
+    uniform lies within FLAG_TOL of that token's interval [C_{k-1}/S, C_k/S] of the
+    oracle's CDF.
+  Anything else is a hard failure.  Flagged counts are reported per workload, together
+  with the count the literal rule gives (every uniform within FLAG_TOL of any decision
+  boundary or of any boundary of the oracle's CDF).
+
+The oracle runs in a spawn-started process pool over memory-mapped inputs for the large
+workloads, so it never forks a process that holds a CUDA context.
+"""
+from __future__ import annotations
+
+import multiprocessing as mp
+import os
+import tempfile
+
+import numpy as np
+
+P_TOL = 1e-6
+FLAG_TOL = 1e-5
+
+_W = {}
+
+
+def _init_worker(folder):
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    for p in (root, here):
+        if p not in sys.path:
+            sys.path.insert(0, p)
+    for name in ("logits", "q", "drafts", "T", "u", "gpu_tokens", "gpu_J"):
+        _W[name] = np.load(os.path.join(folder, name + ".npy"), mmap_mode="r")
+
+
+def _oracle_one(b):
+    from oracle import specdec_oracle as so
+    logits = np.asarray(_W["logits"][b], dtype=np.float64)
+    q = np.asarray(_W["q"][b], dtype=np.float64) if _W["q"].size else None
+    drafts = np.asarray(_W["drafts"][b])
+    T = float(_W["T"][b])
+    u = np.asarray(_W["u"][b], dtype=np.float64)
+    r = so.verify_chain_sequence(logits, q, drafts, T, u, want_cdf=True)
+    gamma = len(drafts)
+    out = {
+        "tokens": r["tokens"], "J": r["J"], "status": r["status"], "p_draft": r["p_draft"],
+        "margins": r["margins"], "greedy": r["greedy"], "lit_draw": False,
+        "y_interval": None, "y_weight": None,
+    }
+    if "cdf" in r:
+        C, S = r["cdf"], r["S"]
+        uu = u[gamma]
+        t = uu * S
+        k = int(np.searchsorted(C, t, side="right"))
+        lo = C[k - 1] if k > 0 else 0.0
+        hi = C[k] if k < len(C) else S
+        out["lit_draw"] = bool(min(t - lo, hi - t) < FLAG_TOL * S)
+        gJ = int(_W["gpu_J"][b])
+        if gJ == r["J"]:
+            gy = int(_W["gpu_tokens"][b][gJ])
+            if 0 <= gy < len(C):
+                a = C[gy - 1] if gy > 0 else 0.0
+                out["y_interval"] = (a / S, C[gy] / S)
+                out["y_weight"] = C[gy] - a
+    return out
+
+
+def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None):
+    """Oracle summaries for every sequence (numpy inputs; logits already widened to
+    float32 for bf16 workloads, which is exact)."""
+    B = logits.shape[0]
+    with tempfile.TemporaryDirectory() as folder:
+        arrays = {"logits": logits, "q": q if q is not None else np.zeros(0, np.float32),
+                  "drafts": drafts, "T": T, "u": u, "gpu_tokens": gpu_tokens, "gpu_J": gpu_J}
+        for k, v in arrays.items():
+            np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(v))
+        nw = workers if workers is not None else min(os.cpu_count() or 1, 16)
+        if nw <= 1 or B <= 4:
+            _init_worker(folder)
+            res = [_oracle_one(b) for b in range(B)]
+            _W.clear()
+            return res
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(nw, initializer=_init_worker, initargs=(folder,)) as pool:
+            return pool.map(_oracle_one, range(B), chunksize=max(1, B // (4 * nw)))
+
+
+class ParityReport:
+    def __init__(self, name):
+        self.name = name
+        self.sequences = 0
+        self.rows = 0
+        self.draws = 0
+        self.flag_decision = 0
+        self.flag_draw = 0
+        self.literal = 0
+        self.accepted = 0
+        self.failures = []
+        self.max_p_err = 0.0
+
+    @property
+    def flagged(self):
+        return self.flag_decision + self.flag_draw
+
+    def summary(self) -> dict:
+        return {
+            "workload": self.name, "sequences": self.sequences, "rows": self.rows,
+            "draws": self.draws, "flagged_decisions": self.flag_decision,
+            "flagged_draws": self.flag_draw, "flagged_fraction_of_rows": self.flagged / max(self.rows, 1),
+            "literal_rule_flags": self.literal, "max_abs_p_error": self.max_p_err,
+            "mean_accepted": self.accepted / max(self.sequences, 1), "hard_failures": len(self.failures),
+        }
+
+    def fail(self, msg):
+        if len(self.failures) < 20:
+            self.failures.append(msg)
+        else:
+            self.failures.append("...")
+
+
+def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray):
+    """Compare one batch.  gpu: numpy tokens [B, g+1], num_accepted [B], status [B],
+    p_draft [B, g] (optional)."""
+    B, g1 = gpu["tokens"].shape
+    gamma = g1 - 1
+    for b in range(B):
+        o = orc[b]
+        report.sequences += 1
+        report.rows += g1
+        gt, gJ, gs = gpu["tokens"][b], int(gpu["num_accepted"][b]), int(gpu["status"][b])
+        os_ = int(o["status"])
+        if (gs & 0xFF) != (os_ & 0xFF) or (gs & 256) != (os_ & 256):
+            report.fail(f"seq {b}: status gpu {gs} oracle {os_}")
+            continue
+        if os_ & 0xFF:
+            if gJ != -1 or (gt != -1).any():
+                report.fail(f"seq {b}: error sequence has outputs J={gJ} {gt}")
+            continue
+        if "p_draft" in gpu and not o["greedy"]:
+            gp = gpu["p_draft"][b].astype(np.float64)
+            op = o["p_draft"]
+            ok = np.isfinite(op)
+            if ok.any():
+                err = float(np.max(np.abs(gp[ok] - op[ok])))
+                report.max_p_err = max(report.max_p_err, err)
+                if err > P_TOL:
+                    report.fail(f"seq {b}: |p_draft error| {err:.3g} > {P_TOL}")
+        if not o["greedy"]:
+            tested = min(o["J"] + 1, gamma)
+            report.literal += int(np.sum(o["margins"][:tested] < FLAG_TOL)) + int(o["lit_draw"])
+            report.draws += 1
+        if o["greedy"]:
+            if gJ != o["J"] or not np.array_equal(gt, o["tokens"]):
+                report.fail(f"seq {b}: greedy mismatch gpu J={gJ} {gt} oracle J={o['J']} {o['tokens']}")
+            report.accepted += o["J"]
+            continue
+        report.accepted += o["J"]
+        if gJ != o["J"]:
+            i = min(gJ, o["J"])
+            if 0 <= i < gamma and o["margins"][i] < FLAG_TOL:
+                report.flag_decision += 1
+            else:
+                report.fail(f"seq {b}: J gpu {gJ} oracle {o['J']} margin {o['margins'][i] if 0 <= i < gamma else None}")
+            continue
+        J = gJ
+        if not np.array_equal(gt[:J], o["tokens"][:J]) or (gt[J + 1:] != -1).any():
+            report.fail(f"seq {b}: accepted prefix or padding differs {gt} vs {o['tokens']}")
+            continue
+        if gt[J] != o["tokens"][J]:
+            if (gs & 512) != (os_ & 512):
+                report.flag_draw += 1  # zero-residual fallback decided by rounding
+                continue
+            iv, w = o["y_interval"], o["y_weight"]
+            uu = float(u[b, gamma])
+            if iv is not None and w is not None and w > 0 and iv[0] - FLAG_TOL <= uu <= iv[1] + FLAG_TOL:
+                report.flag_draw += 1
+            else:
+                report.fail(f"seq {b}: draw gpu {gt[J]} oracle {o['tokens'][J]} u {uu} gpu-interval {iv}")
+        elif (gs & 512) != (os_ & 512):
+            report.fail(f"seq {b}: zero-residual flag differs with equal tokens")

@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every declared
+symbol, and rejects invalid arguments on the host before touching the device."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "specdec.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(specdec_[A-Za-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_verification_calls():
+    names = declared_functions()
+    for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
+               "specdec_build_tree_mask"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(built_library):
+    lib = ctypes.CDLL(str(built_library))
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_loads_and_reports_version(built_library):
+    import speculative_decoding_token_temperature_gb300 as sd
+    lib = sd.load_library()
+    assert lib.specdec_version().decode().count(".") == 2
+
+
+def test_workspace_sizes(built_library):
+    import speculative_decoding_token_temperature_gb300 as sd
+    lib = sd.load_library()
+    a = lib.specdec_chain_workspace_bytes(256, 7, 128256, sd.BF16)
+    b = lib.specdec_chain_workspace_bytes(512, 8, 152064, sd.F32)
+    assert 0 < a < b
+    assert a % 256 == 0
+    assert lib.specdec_chain_workspace_bytes(0, 7, 10, sd.BF16) == 0
+    assert lib.specdec_chain_workspace_bytes(1, 7, 10, 9) == 0
+    assert lib.specdec_greedy_workspace_bytes(4, 3, 100, sd.F32) == lib.specdec_chain_workspace_bytes(4, 3, 100, sd.F32)
+
+
+def _fake(n=64):
+    """256-byte aligned host addresses that are never dereferenced: validation rejects
+    the call before any use."""
+    buf = (ctypes.c_byte * (n + 256))()
+    addr = ctypes.addressof(buf)
+    return ctypes.c_void_p((addr + 255) // 256 * 256), buf
+
+
+def test_host_validation_rejects_before_launch(built_library):
+    import speculative_decoding_token_temperature_gb300 as sd
+    lib = sd.load_library()
+    p, keep = _fake()
+    ws, keep2 = _fake(1 << 12)
+    # null logits
+    assert lib.specdec_verify_chain(None, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # bad dtype
+    assert lib.specdec_verify_chain(p, 7, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # non-positive sizes
+    for B, g, V in [(0, 1, 8), (1, 0, 8), (1, 1, 0), (-3, 1, 8)]:
+        assert lib.specdec_verify_chain(p, sd.BF16, p, p, p, p, B, g, V, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # missing q / temperatures / uniforms on the sampling call
+    assert lib.specdec_verify_chain(p, sd.BF16, None, p, p, p, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # workspace too small, null, or misaligned
+    assert lib.specdec_verify_chain(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 1, None) == sd.ERR_WORKSPACE
+    assert lib.specdec_verify_chain(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, None, 4096, None) == sd.ERR_INVALID_ARG
+    mis = ctypes.c_void_p(ws.value + 8)
+    assert lib.specdec_verify_chain(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, mis, 4000, None) == sd.ERR_INVALID_ARG
+    # too many drafts for one decision CTA
+    assert lib.specdec_verify_chain(p, sd.BF16, p, p, p, p, 1, 300, 8, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
+    # greedy: null drafts
+    assert lib.specdec_verify_greedy(p, sd.F32, None, 1, 1, 8, p, p, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # tree: bad depth, null outputs
+    assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None, 0, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 100, p, p, p, None, None, 0, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 2, None, p, p, None, None, 0, None) == sd.ERR_INVALID_ARG
+    # mask
+    assert lib.specdec_build_tree_mask(None, 4, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_build_tree_mask(p, 0, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_build_tree_mask(p, 4, -1, p, p, None, p, None) == sd.ERR_INVALID_ARG
+    del keep, keep2
+
+
+def test_binding_marshalling_errors_without_gpu(built_library):
+    import torch
+    import speculative_decoding_token_temperature_gb300 as sd
+    with pytest.raises(ValueError):
+        sd._dtype_code(torch.zeros(2, dtype=torch.float16))
+    t = torch.zeros(2, 3)
+    with pytest.raises(ValueError):
+        sd._need(t, "x", torch.float32, (3, 2), t.device)
+    with pytest.raises(ValueError):
+        sd._need(t.t(), "x", torch.float32, (3, 2), t.device)

@@ -1,0 +1,160 @@
+"""GPU parity of the Medusa tree walk and the tree-attention mask (via the C ABI)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from golden import read_fixture
+from oracle import specdec_oracle as so
+from parity import FLAG_TOL
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def sd(built_library):
+    import speculative_decoding_token_temperature_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.fixture(scope="module")
+def medusa64():
+    parents, paths, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
+    return parents, paths
+
+
+def _np(t):
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def _check_tree(gpu, x, D, stats):
+    L, toks, par = _np(x["logits"]), _np(x["node_tokens"]), _np(x["parents"])
+    T, u = _np(x["temperatures"]), _np(x["uniforms"])
+    B = L.shape[0]
+    for b in range(B):
+        o = so.verify_tree_sequence(L[b], toks[b], par, float(T[b]), u[b], D)
+        gt, gp, gJ, gs = (_np(gpu[k])[b] for k in ("tokens", "path", "num_accepted", "status"))
+        gJ, gs = int(gJ), int(gs)
+        stats["sequences"] += 1
+        assert gs == o["status"], (b, gs, o["status"])
+        if o["status"] & 0xFF:
+            assert gJ == -1 and (gt == -1).all() and (gp == -1).all()
+            continue
+        if np.array_equal(gt, o["tokens"]) and np.array_equal(gp, o["path"]) and gJ == o["n_accepted"]:
+            stats["accepted"] += gJ
+            continue
+        # the walks may differ only at a flagged draw: first differing depth
+        assert float(T[b]) >= so.GREEDY_T, f"greedy walk differs at seq {b}: {gt} vs {o['tokens']}"
+        d = int(np.flatnonzero(gt != o["tokens"])[0])
+        node = -1 if d == 0 else int(o["path"][d - 1])
+        row = L[b][0 if node < 0 else 1 + node]
+        p = so.target_distribution(row, float(T[b]))
+        _, C, S = so.inverse_cdf(p, u[b][d])
+        y = int(gt[d])
+        lo = (C[y - 1] if y > 0 else 0.0) / S
+        hi = C[y] / S
+        assert p[y] > 0 and lo - FLAG_TOL <= u[b][d] <= hi + FLAG_TOL, (b, d, y, lo, hi, u[b][d])
+        stats["flagged"] += 1
+
+
+def test_tree_b32_n64_v32000(sd, medusa64):
+    parents, paths = medusa64
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    for r in range(25):
+        x = workloads.tree_workload("tree_b32_n64_v32000", parents, paths, r, DEV)
+        out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+        torch.cuda.synchronize()
+        _check_tree(out, x, 4, stats)
+    path = os.environ.get("SPECDEC_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"workload": "tree_b32_n64_v32000 (25 rounds)", **stats}) + "\n")
+    assert stats["flagged"] <= max(1, 1e-4 * stats["sequences"] * 5)
+    assert stats["accepted"] > 0
+
+
+@pytest.mark.parametrize("V,dtype", [(32000, "bf16"), (1001, "fp32"), (4096, "fp32"), (37, "bf16")])
+def test_tree_shapes_and_edges(sd, medusa64, V, dtype):
+    parents, paths = medusa64
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    x = workloads.make_tree_inputs(8, V, parents, paths, depth=4, seed=V, device=DEV, dtype=dtype,
+                                   top=min(10, V))
+    out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+    _check_tree(out, x, 4, stats)
+
+
+def test_tree_degenerate(sd):
+    V, D = 50, 3
+    parents = torch.tensor([-1, -1, 0, 0, 2], dtype=torch.int32, device=DEV)
+    B = 6
+    g = torch.Generator(device=DEV).manual_seed(2)
+    logits = torch.randn(B, 6, V, generator=g, device=DEV)
+    toks = torch.randint(0, V, (B, 5), generator=g, device=DEV, dtype=torch.int32)
+    toks[0, 0] = toks[0, 1] = int(torch.argmax(logits[0, 0]))      # duplicate siblings
+    toks[1, 3] = V + 1                                               # bad token
+    logits[2, 0, 4] = float("nan")                                   # bad root row
+    T = torch.tensor([0.0, 0.5, 0.5, 0.5, 0.0, 0.9], device=DEV)
+    u = torch.rand(B, D + 1, generator=g, device=DEV)
+    u[3, 2] = 1.5                                                    # bad uniform
+    out = sd.verify_tree(logits, toks, parents, T, u, D)
+    x = {"logits": logits, "node_tokens": toks, "parents": parents, "temperatures": T, "uniforms": u}
+    _check_tree(out, x, D, {"sequences": 0, "flagged": 0, "accepted": 0})
+    # too deep for max_depth 2, and a bad parent
+    out = sd.verify_tree(logits, toks, parents, T, u[:, :3].contiguous(), 2)
+    assert (out["status"].cpu() & so.STATUS_BAD_TREE).all()
+    bad = torch.tensor([-1, 1, 0, 0, 2], dtype=torch.int32, device=DEV)
+    out = sd.verify_tree(logits, toks, bad, T, u, D)
+    assert (out["status"].cpu() & so.STATUS_BAD_TREE).all()
+    # a tree with no nodes: the root draw alone
+    out = sd.verify_tree(logits[:, :1].contiguous(), toks[:, :0].contiguous(),
+                         parents[:0].contiguous(), T, u, D)
+    assert (out["num_accepted"].cpu()[[0, 1, 4, 5]] == 0).all()
+
+
+def test_mask_worked_example(sd):
+    fx = read_fixture("tree_mask_6node.txt")
+    parents = torch.tensor([int(v) for v in fx["parents"]], dtype=torch.int32, device=DEV)
+    P = 3
+    r = sd.build_tree_mask(parents, P)
+    block = np.array([[int(v) for v in row] for row in fx["mask_row"]], dtype=np.uint8)
+    m = _np(r["mask"])
+    assert (m[:, :P] == 1).all()
+    assert np.array_equal(m[:, P:], block)
+    assert _np(r["depth"]).tolist() == [int(v) for v in fx["depth"]]
+    assert _np(r["position_ids"]).tolist() == [P + int(v) for v in fx["depth"]]
+    assert int(r["status"][0]) == 0
+
+
+@pytest.mark.parametrize("which", ["medusa64", "full4680", "chain", "random"])
+def test_mask_matches_oracle(sd, which):
+    if which == "medusa64":
+        parents, _, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
+    elif which == "full4680":
+        acc = [[1 / (2 + i + k) for i in range(8)] for k in range(4)]
+        from fractions import Fraction
+        acc = [[Fraction(a).limit_denominator(1000) for a in h] for h in acc]
+        parents, _, _ = so.medusa_sparse_tree(acc, 10 ** 6)
+        assert len(parents) == 4680
+    elif which == "chain":
+        parents = list(range(-1, 99))
+    else:
+        rng = np.random.default_rng(4)
+        parents = [-1] + [int(rng.integers(-1, i)) for i in range(1, 300)]
+    P = 17
+    r = sd.build_tree_mask(torch.tensor(parents, dtype=torch.int32, device=DEV), P)
+    mask, pos, depth = so.build_tree_mask(parents, P)
+    assert np.array_equal(_np(r["mask"]).astype(bool), mask)
+    assert np.array_equal(_np(r["position_ids"]), pos)
+    assert np.array_equal(_np(r["depth"]), depth)
+
+
+def test_mask_bad_parents(sd):
+    r = sd.build_tree_mask(torch.tensor([-1, 0, 5, 1], dtype=torch.int32, device=DEV), 2)
+    assert int(r["status"][0]) == so.STATUS_BAD_TREE
