@@ -19,9 +19,7 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 from pathlib import Path
 
@@ -36,7 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of chain_stats, from one ncu
 # capture of the benchmarked workload, keyed by the sha256 of the kernel source it was
 # taken on; reported as null once the source differs.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
+    "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
+}
 
 
 def kernel_source_sha() -> str:
@@ -57,72 +58,87 @@ def measured_peaks() -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """SM clock and clock-event reasons sampled every ~1 ms through NVML (ctypes, read
+    only) on a background thread while the timed region runs."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_uuid: str | None):
+    def __init__(self, device_index: int, gpu_uuid: str | None):
+        self.index = device_index
         self.uuid = gpu_uuid
-        self.proc = None
-        self.path = None
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self._nvml, self._handle = lib, h
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return True
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if get_reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(0.001)
 
     def __enter__(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
-        if self.uuid:
-            cmd += ["-i", self.uuid]
-        try:
-            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        import threading
+        if self._open_nvml():
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 1.0:
+                time.sleep(0.001)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
         return False
 
     def summary(self) -> dict:
-        rows = []
-        try:
-            for line in Path(self.path).read_text().splitlines():
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 8:
-                    rows.append(parts)
-        except Exception:
-            pass
-        finally:
-            try:
-                os.unlink(self.path)
-            except Exception:
-                pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-
-        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
-        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        sm = [c for c, _ in self.samples]
         reasons = set()
-        for r in rows:
-            for name, val in zip(names, r[4:8]):
-                if val.lower() == "active":
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
 def workload_shape(name):
@@ -197,14 +213,14 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--sets", type=int, default=3, help="input batches rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-sequences", type=int, default=4)
+    ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -256,8 +272,10 @@ def main():
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
+    # Timed region: K steps bracketed by a barrier and a synchronize on both sides, CUDA
+    # events on the launching stream, clocks sampled throughout.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(uuid) as clocks, sd.KernelTimer(max_launches=4 * args.steps + 16) as kt:
+    with ClockSampler(local_rank, uuid) as clocks:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
@@ -268,7 +286,6 @@ def main():
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        per_kernel = kt.read()
     elapsed_ms = ev0.elapsed_time(ev1)
     if dist is not None:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -277,13 +294,22 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = rows * world / (ms_per_step / 1e3)
 
+    # Per-kernel durations: the same K steps again with every library launch bracketed
+    # by CUDA events on the launching stream.
+    with sd.KernelTimer(max_launches=8 * args.steps + 16) as kt:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            step(i)
+        torch.cuda.synchronize()
+        per_kernel = kt.read()
+    launches_per_step = sum(v[1] for v in per_kernel.values()) / args.steps
+
     # roofline of the dominant kernel (the statistics pass over every logits row)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or FALLBACK_HBM_GBS
     st_ms, st_n = per_kernel["chain_stats"]
-    dr_ms, dr_n = per_kernel["chain_sample"]
     stats_bytes = rows * V * esize                       # every logits row read once
     achieved = stats_bytes / (st_ms / st_n / 1e3) / 1e9 if st_n else None
     sha = kernel_source_sha()
@@ -305,7 +331,7 @@ def main():
                      "frac": (achieved / peak) if achieved else None,
                      "algorithmic_bytes_per_launch": stats_bytes, "traffic": traffic_val},
         "kernels_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items() if v[1]},
-        "gpu_launches": int(sum(v[1] for v in per_kernel.values())),
+        "gpu_launches": int(round(launches_per_step * args.steps)),
         "mean_accepted": statistics.mean(accepted),
         "clocks": clocks.summary(),
         "kernel_src_sha": sha,

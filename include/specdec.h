@@ -28,11 +28,10 @@
  *     decoding"; the special case "A greedy target" of the sampling rule).
  *   - Deterministic: the same inputs give bit-identical outputs on every call.
  *   - Workspaces: a call's workspace must hold at least the size the matching
- *     *_workspace_bytes() returns, be 256-byte aligned, and be ZERO-FILLED before its
- *     first use (e.g. cudaMemsetAsync once).  Every call leaves the workspace zero-filled
- *     again in the bytes later calls depend on, so one workspace can serve calls of any
- *     shape that fits, one call at a time.  Calls that overlap on the GPU must not share
- *     a workspace.
+ *     *_workspace_bytes() returns and be 256-byte aligned.  Its contents need no
+ *     preparation: each call clears the counters it uses on its stream first.  One
+ *     workspace can serve calls of any shape that fits, one call at a time; calls that
+ *     overlap on the GPU must not share a workspace.
  */
 #ifndef SPECDEC_H
 #define SPECDEC_H
@@ -168,11 +167,13 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
  *     writes per-kernel totals for kernel ids 0..n-1 (ids: SPECDEC_KERNEL_*); resets.
  *   specdec_profile_stop(): disables timing and destroys the events.
  */
-#define SPECDEC_KERNEL_CHAIN_STATS 0
-#define SPECDEC_KERNEL_CHAIN_SAMPLE 1
+#define SPECDEC_KERNEL_CHAIN_STATS 0   /* row statistics over every logits row      */
+#define SPECDEC_KERNEL_CHAIN_SAMPLE 1  /* residual / bonus masses of the drawn rows */
 #define SPECDEC_KERNEL_TREE_WALK 2
 #define SPECDEC_KERNEL_TREE_MASK 3
-#define SPECDEC_NUM_KERNELS 4
+#define SPECDEC_KERNEL_CHAIN_DECIDE 4  /* accept tests and first rejection          */
+#define SPECDEC_KERNEL_CHAIN_FINISH 5  /* inverse-CDF search of the drawn rows      */
+#define SPECDEC_NUM_KERNELS 6
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);
@@ -180,6 +181,10 @@ int specdec_profile_stop(void);
 
 /* Library version string, e.g. "0.1.0". */
 const char* specdec_version(void);
+
+/* Description of the last SPECDEC_ERR_CUDA returned on the calling host thread: the step
+ * that failed and the CUDA error.  The string stays valid until the thread's next call. */
+const char* specdec_last_error(void);
 
 #ifdef __cplusplus
 }

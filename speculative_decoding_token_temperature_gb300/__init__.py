@@ -38,8 +38,7 @@ STATUS_ERROR_MASK = 0xFF
 STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
-KERNEL_CHAIN_STATS, KERNEL_CHAIN_SAMPLE, KERNEL_TREE_WALK, KERNEL_TREE_MASK = 0, 1, 2, 3
-KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask")
+KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish")
 
 
 class SpecdecError(RuntimeError):
@@ -85,13 +84,18 @@ def load_library():
     lib.specdec_profile_stop.restype = i32
     lib.specdec_version.argtypes = []
     lib.specdec_version.restype = ctypes.c_char_p
+    lib.specdec_last_error.argtypes = []
+    lib.specdec_last_error.restype = ctypes.c_char_p
     _LIB = lib
     return lib
 
 
 def _check(rc: int, what: str):
     if rc != OK:
-        raise SpecdecError(f"{what}: {_ERR_NAMES.get(rc, rc)} (code {rc})")
+        detail = ""
+        if rc == ERR_CUDA:
+            detail = ": " + load_library().specdec_last_error().decode(errors="replace")
+        raise SpecdecError(f"{what}: {_ERR_NAMES.get(rc, rc)} (code {rc}){detail}")
 
 
 def _ptr(t):
@@ -123,7 +127,7 @@ _WORKSPACES: dict = {}
 
 
 def _workspace(nbytes: int, device, stream_handle: int):
-    """A zero-filled device workspace per (device, stream); the library leaves it zeroed."""
+    """A device workspace per (device, stream); the library clears what it needs."""
     if nbytes == 0:
         return None, 0
     key = (device, stream_handle)

@@ -176,13 +176,12 @@ __global__ void __launch_bounds__(NT) chain_stats_kernel(const ChainParams P) {
   if (!greedy) {
     float zt = 0.f;
     if (mt > -kInf) {
-      const float mc = mt * c;
       float part[NV];
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         float a = 0.f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) a += ex2(fmaf(v[j][e], c, -mc));
+        for (int e = 0; e < VEC; ++e) a += ex2((v[j][e] - mt) * c);
         part[j] = a;
       }
 #pragma unroll
@@ -223,7 +222,7 @@ __global__ void __launch_bounds__(NT) chain_stats_kernel(const ChainParams P) {
 // two agree bit for bit on every vector.
 template <typename T, int VEC>
 __device__ __forceinline__ float draw_weights(const T* lrow, const float* qrow, int64_t k,
-                                              float c, float mc, float invZ, bool use_p,
+                                              float c, float m, float invZ, bool use_p,
                                               float (&w)[VEC], float& psum, bool& bad_q) {
   float l[VEC];
   VecLoad<T, VEC>::load(lrow, k, l);
@@ -238,7 +237,7 @@ __device__ __forceinline__ float draw_weights(const T* lrow, const float* qrow, 
 #pragma unroll
   for (int e = 0; e < VEC; ++e) {
     bad_q |= !(qv[e] >= 0.f && qv[e] < kInf);
-    const float p = ex2(fmaf(l[e], c, -mc)) * invZ;
+    const float p = ex2((l[e] - m) * c) * invZ;
     w[e] = fmaxf(p - qv[e], 0.f);
     acc += w[e];
     pacc += p;
@@ -303,7 +302,7 @@ __device__ void chain_draw_finish(const ChainParams& P, int b, const SeqState& s
 
   const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
   const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
-  const float c = st.row.z, mc = st.row.x * c, invZ = 1.f / st.row.y;
+  const float c = st.row.z, mrow = st.row.x, invZ = 1.f / st.row.y;
   const int k0 = seg * SEG;
   const int n = min(SEG, P.V - k0);
   int last_positive = -1;
@@ -314,7 +313,7 @@ __device__ void chain_draw_finish(const ChainParams& P, int b, const SeqState& s
     if (off < n) {
       // with use_p the weights are p itself (the zero-residual fallback)
       bool bad_q = false;
-      vs = draw_weights<T, VEC>(lrow, qrow, k0 + off, c, mc, invZ, use_p, w, ps, bad_q);
+      vs = draw_weights<T, VEC>(lrow, qrow, k0 + off, c, mrow, invZ, use_p, w, ps, bad_q);
 #pragma unroll
       for (int e = 0; e < VEC; ++e)
         if (w[e] > 0.f) last_positive = k0 + off + e;
@@ -374,7 +373,7 @@ __global__ void __launch_bounds__(NT) chain_sample_kernel(const ChainParams P) {
   const int J = st.meta.x;
   const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
   const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
-  const float c = st.row.z, mc = st.row.x * c, invZ = 1.f / st.row.y;
+  const float c = st.row.z, mrow = st.row.x, invZ = 1.f / st.row.y;
   const int k0 = s * SEG;
   const int n = min(SEG, P.V - k0);
 
@@ -385,7 +384,7 @@ __global__ void __launch_bounds__(NT) chain_sample_kernel(const ChainParams P) {
     const int off = (j * NT + threadIdx.x) * VEC;
     if (off < n) {
       float w[VEC], ps;
-      sr += static_cast<double>(draw_weights<T, VEC>(lrow, qrow, k0 + off, c, mc, invZ, false, w, ps, bad_q));
+      sr += static_cast<double>(draw_weights<T, VEC>(lrow, qrow, k0 + off, c, mrow, invZ, false, w, ps, bad_q));
       sp += static_cast<double>(ps);
     }
   }
@@ -408,16 +407,14 @@ __global__ void __launch_bounds__(NT) chain_sample_kernel(const ChainParams P) {
 template <typename T, int VEC, int NV>
 cudaError_t launch_stats_t(const ChainParams& P, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(P.B) * (P.gamma + 1) * P.nseg;
-  chain_stats_kernel<T, VEC, NV, kChainThreads>
-      <<<dim3(static_cast<unsigned>(items)), kChainThreads, 0, stream>>>(P);
-  return cudaGetLastError();
+  return launch_kernel(chain_stats_kernel<T, VEC, NV, kChainThreads>, dim3(static_cast<unsigned>(items)),
+                       dim3(kChainThreads), 0, stream, 0, P);
 }
 
 template <typename T, int VEC, int NV>
 cudaError_t launch_sample_t(const ChainParams& P, cudaStream_t stream) {
-  chain_sample_kernel<T, VEC, NV, kChainThreads>
-      <<<dim3(P.nseg, P.B), kChainThreads, 0, stream>>>(P);
-  return cudaGetLastError();
+  return launch_kernel(chain_sample_kernel<T, VEC, NV, kChainThreads>, dim3(P.nseg, P.B),
+                       dim3(kChainThreads), 0, stream, 0, P);
 }
 
 }  // namespace

@@ -1,6 +1,8 @@
 // C-ABI entry points: argument validation, workspace layout, launches, kernel timing.
 
 #include <cstdint>
+#include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <vector>
 
@@ -25,6 +27,19 @@ bool valid_dtype(int t) { return t == SPECDEC_F32 || t == SPECDEC_BF16; }
 // 16-byte vector loads need every row start 16-byte aligned.
 bool rows_vectorizable(const void* base, int64_t V, size_t esize) {
   return aligned16(base) && ((V * static_cast<int64_t>(esize)) % 16 == 0);
+}
+
+// ---- last error (per host thread) -----------------------------------------------------
+thread_local char g_last_error[256] = "no error";
+
+int fail_cuda(const char* step, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", step, cudaGetErrorString(e),
+                cudaGetErrorName(e));
+  return SPECDEC_ERR_CUDA;
+}
+int fail(int code, const char* what) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return code;
 }
 
 // ---- kernel timing (process-global, single-threaded use) -----------------------------
@@ -56,22 +71,43 @@ struct ProfScope {
 
 }  // namespace
 
-size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, bool vector_path,
-                              void* base, ChainWorkspace* ws) {
-  const int seg = chain_segment_len(ldt, vector_path);
-  const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
+// Layout: [error word, draw count | arrival counters] -- the counter block, cleared on
+// the stream at the start of every call -- then per-sequence state, the draw list, the
+// per-segment (or per-chunk) summaries and the draw masses.  Returns the total bytes and
+// the counter-block bytes (through counter_bytes when non-null).
+size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, void* base,
+                              ChainWorkspace* ws, size_t* counter_bytes) {
   const int64_t rows = static_cast<int64_t>(B) * (g + 1);
+  int64_t n_part, draw_bytes;
+  if (path == 2) {
+    const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(elem_size(ldt));
+    n_part = rows * ((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
+    draw_bytes = static_cast<int64_t>(B) * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float2));
+  } else {
+    const int seg = chain_segment_len(ldt, path == 1);
+    const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
+    n_part = rows * nseg;
+    draw_bytes = static_cast<int64_t>(B) * nseg * static_cast<int64_t>(sizeof(double2));
+  }
   size_t off = 0;
+  const size_t o_error = off;    off += kAlign;
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * 2 * static_cast<size_t>(B));
+  const size_t counters_end = off;
   const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
-  const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(rows * nseg));
-  const size_t o_draw = off;     off += round_up(sizeof(double2) * static_cast<size_t>(B * nseg));
+  const size_t o_list = off;     off += round_up(sizeof(int2) * static_cast<size_t>(B));
+  const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(n_part));
+  const size_t o_draw = off;     off += round_up(static_cast<size_t>(draw_bytes));
+  if (counter_bytes) *counter_bytes = counters_end;
   if (base != nullptr && ws != nullptr) {
     char* p = static_cast<char*>(base);
+    ws->error = reinterpret_cast<unsigned*>(p + o_error);
+    ws->draw_count = reinterpret_cast<unsigned*>(p + o_error) + 1;
     ws->counters = reinterpret_cast<unsigned*>(p + o_counters);
     ws->seq = reinterpret_cast<SeqState*>(p + o_seq);
+    ws->draw_list = reinterpret_cast<int2*>(p + o_list);
     ws->partials = reinterpret_cast<float4*>(p + o_part);
     ws->draw = reinterpret_cast<double2*>(p + o_draw);
+    ws->draw_mass = reinterpret_cast<float2*>(p + o_draw);
   }
   return off;
 }
@@ -85,9 +121,12 @@ namespace {
 // Workspace sizing must not depend on pointer alignment, so size for the shorter
 // (scalar-path) segment, which needs the most segments.
 size_t chain_ws_bytes(int B, int g, int V, specdec_dtype ldt) {
-  const size_t a = chain_workspace_layout(B, g, V, ldt, false, nullptr, nullptr);
-  const size_t b = chain_workspace_layout(B, g, V, ldt, true, nullptr, nullptr);
-  return a > b ? a : b;
+  size_t m = 0;
+  for (int path = 0; path < 3; ++path) {
+    const size_t b = chain_workspace_layout(B, g, V, ldt, path, nullptr, nullptr, nullptr);
+    m = b > m ? b : m;
+  }
+  return m;
 }
 
 bool chain_sizes_ok(int B, int g, int V) {
@@ -108,6 +147,8 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   const size_t es = elem_size(ldt);
   bool vec = rows_vectorizable(logits, V, es);
   if (!greedy_only) vec = vec && rows_vectorizable(q, V, 4);
+  // streaming path: aligned rows and a decision that fits one warp
+  const bool stream_path = vec && (g + 1) <= kStreamMaxRows;
   const int seg = chain_segment_len(ldt, vec);
   const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
   const int64_t items = static_cast<int64_t>(B) * (g + 1) * nseg;
@@ -130,16 +171,49 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   P.out_J = out_J;
   P.out_p_draft = greedy_only ? nullptr : out_p;
   P.out_status = out_status;
-  chain_workspace_layout(B, g, V, ldt, vec, workspace, &P.ws);
-
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int path = stream_path ? 2 : (vec ? 1 : 0);
+  size_t counter_bytes = 0;
+  chain_workspace_layout(B, g, V, ldt, path, workspace, &P.ws, &counter_bytes);
+  // Arrival counters and the draw list count must start at zero; other regions are
+  // always written before they are read.
+  if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
+    return fail_cuda("clearing the workspace counters", e);
+  if (stream_path) {
+    const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(es);
+    P.nch = static_cast<int>((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
+    P.nchd = (V + kDrawChunk - 1) / kDrawChunk;
+    const int sms = device_sm_count();
+    const int64_t stat_items = static_cast<int64_t>(B) * (g + 1) * P.nch;
+    const int64_t draw_items = static_cast<int64_t>(B) * P.nchd;
+    if (stat_items >= INT32_MAX || draw_items >= INT32_MAX) return SPECDEC_ERR_UNSUPPORTED;
+    P.grid_stats = static_cast<int>(std::min<int64_t>(sms, (stat_items + kStatsWarps - 1) / kStatsWarps));
+    P.grid_draw = static_cast<int>(std::min<int64_t>(sms, (draw_items + kDrawWarps - 1) / kDrawWarps));
+    {
+      ProfScope prof(SPECDEC_KERNEL_CHAIN_STATS, s);
+      if (cudaError_t e = launch_chain_stream_stats(P, ldt, s); e != cudaSuccess) return fail_cuda("statistics kernel (streaming)", e);
+    }
+    {
+      ProfScope prof(SPECDEC_KERNEL_CHAIN_DECIDE, s);
+      if (cudaError_t e = launch_chain_stream_decide(P, ldt, s); e != cudaSuccess) return fail_cuda("decision kernel", e);
+    }
+    if (!greedy_only) {
+      {
+        ProfScope prof(SPECDEC_KERNEL_CHAIN_SAMPLE, s);
+        if (cudaError_t e = launch_chain_stream_draw(P, ldt, s); e != cudaSuccess) return fail_cuda("draw kernel (streaming)", e);
+      }
+      ProfScope prof(SPECDEC_KERNEL_CHAIN_FINISH, s);
+      if (cudaError_t e = launch_chain_stream_finish(P, ldt, s); e != cudaSuccess) return fail_cuda("finish kernel", e);
+    }
+    return SPECDEC_OK;
+  }
   {
     ProfScope prof(SPECDEC_KERNEL_CHAIN_STATS, s);
-    if (launch_chain_stats(P, ldt, vec, s) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    if (cudaError_t e = launch_chain_stats(P, ldt, vec, s); e != cudaSuccess) return fail_cuda("statistics kernel", e);
   }
   if (!greedy_only) {
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SAMPLE, s);
-    if (launch_chain_sample(P, ldt, vec, s) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    if (cudaError_t e = launch_chain_sample(P, ldt, vec, s); e != cudaSuccess) return fail_cuda("draw kernel", e);
   }
   return SPECDEC_OK;
 }
@@ -210,7 +284,8 @@ int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* no
   const bool vec = rows_vectorizable(logits, V, elem_size(ldt));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope prof(SPECDEC_KERNEL_TREE_WALK, s);
-  return launch_tree_walk(P, ldt, vec, s) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+  if (cudaError_t e = launch_tree_walk(P, ldt, vec, s); e != cudaSuccess) return fail_cuda("tree walk kernel", e);
+  return SPECDEC_OK;
 }
 
 int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* out_mask,
@@ -221,10 +296,11 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
   if ((static_cast<int64_t>(prefix_len) + N) * N >= INT32_MAX) return SPECDEC_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope prof(SPECDEC_KERNEL_TREE_MASK, s);
-  return launch_tree_mask(parents, N, prefix_len, out_mask, out_position_ids, out_depth,
-                          out_status, s) == cudaSuccess
-             ? SPECDEC_OK
-             : SPECDEC_ERR_CUDA;
+  if (cudaError_t e = launch_tree_mask(parents, N, prefix_len, out_mask, out_position_ids, out_depth,
+                                       out_status, s);
+      e != cudaSuccess)
+    return fail_cuda("tree mask kernel", e);
+  return SPECDEC_OK;
 }
 
 int specdec_profile_start(int max_launches) {
@@ -269,5 +345,7 @@ int specdec_profile_stop(void) {
 }
 
 const char* specdec_version(void) { return "0.1.0"; }
+
+const char* specdec_last_error(void) { return g_last_error; }
 
 }  // extern "C"

@@ -27,7 +27,21 @@ struct ChainWorkspace {
   unsigned* counters; // [2B]: arrivals per sequence for the statistics and the draw kernels
   SeqState* seq;      // [B]
   double2* draw;      // [B*nseg]: per segment (residual mass, target mass) of the drawn row
+  // streaming path only
+  int2* draw_list;       // [B]: (sequence, J) of every sequence that draws, in any order
+  unsigned* draw_count;  // [1]: entries in draw_list
+  float2* draw_mass;     // [B*nchd]: per chunk (residual mass, target mass) of the drawn row
+  unsigned* error;       // [1]: set when a bounded wait gave up
 };
+
+// Streaming (bulk-copy) path geometry.
+constexpr int kStatsWarps = 16;       // warps per CTA, one CTA per SM
+constexpr int kStatsStages = 3;       // bulk-copy stages per warp
+constexpr int kStatsChunkBytes = 4096;
+constexpr int kDrawWarps = 8;
+constexpr int kDrawStages = 3;
+constexpr int kDrawChunk = 1024;      // elements of the drawn row per work item
+constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decision
 
 struct ChainParams {
   const void* logits;
@@ -39,6 +53,9 @@ struct ChainParams {
   int nseg;              // segments per row
   int seg;               // elements per segment
   int greedy_only;
+  int nch;               // streaming path: 4 KB chunks per logits row
+  int nchd;              // streaming path: draw chunks per row
+  int grid_stats, grid_draw;
   int32_t* out_tokens;
   int32_t* out_J;
   float* out_p_draft;
@@ -49,8 +66,17 @@ struct ChainParams {
 // Segment length in elements for a logits dtype and load path.
 int chain_segment_len(specdec_dtype ldt, bool vector_path);
 // Workspace layout; returns the total bytes (and fills ws when base != nullptr).
-size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, bool vector_path,
-                              void* base, ChainWorkspace* ws);
+// path: 0 scalar loads, 1 vector loads, 2 streaming (bulk copies).
+size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path,
+                              void* base, ChainWorkspace* ws, size_t* counter_bytes);
+
+// Streaming path: statistics, decision, draw, finish -- chained with programmatic
+// dependent launch; the first launch follows ordinary stream order.
+cudaError_t launch_chain_stream_stats(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+cudaError_t launch_chain_stream_decide(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+cudaError_t launch_chain_stream_draw(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+int device_sm_count();
 
 cudaError_t launch_chain_stats(const ChainParams& P, specdec_dtype ldt, bool vector_path,
                                cudaStream_t stream);

@@ -96,7 +96,6 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
 
       int y = z;
       if (!greedy) {
-        const float mc = m * c;
         // pass 2: total mass (per-vector fp32 running sums, fp64 across vectors)
         double tot = 0.0;
         for (int k = tid * VEC; k < V; k += NT * VEC) {
@@ -104,7 +103,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
           VecLoad<T, VEC>::load(lrow, k, v);
           float a = 0.f;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) a += ex2(fmaf(v[e], c, -mc));
+          for (int e = 0; e < VEC; ++e) a += ex2((v[e] - m) * c);
           tot += static_cast<double>(a);
         }
         const double S = Block<NT>::sum(tot, sh_d);
@@ -122,7 +121,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
             VecLoad<T, VEC>::load(lrow, k, v);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-              w[e] = ex2(fmaf(v[e], c, -mc));
+              w[e] = ex2((v[e] - m) * c);
               a += w[e];
               if (w[e] > 0.f) last_pos = k + e;
             }
@@ -182,8 +181,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
 
 template <typename T, int VEC>
 cudaError_t launch_walk_t(const TreeParams& P, cudaStream_t stream) {
-  tree_walk_kernel<T, VEC, kTreeThreads><<<P.B, kTreeThreads, 0, stream>>>(P);
-  return cudaGetLastError();
+  return launch_kernel(tree_walk_kernel<T, VEC, kTreeThreads>, dim3(P.B), dim3(kTreeThreads), 0, stream, 0, P);
 }
 
 __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restrict__ parents, int N,
@@ -250,9 +248,8 @@ cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  tree_mask_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(parents, N, prefix_len, mask,
-                                                                      pos, depth, status);
-  return cudaGetLastError();
+  return launch_kernel(tree_mask_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 0,
+                       parents, N, prefix_len, mask, pos, depth, status);
 }
 
 }  // namespace specdec
