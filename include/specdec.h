@@ -51,6 +51,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
 #define SPECDEC_ERR_UNSUPPORTED 2
 #define SPECDEC_ERR_CUDA 3
 #define SPECDEC_ERR_WORKSPACE 4
+#define SPECDEC_ERR_TOO_LARGE 5   /* the shape needs more scratch than the built-in array */
 
 /* per-sequence status bits (errors: low byte; warnings: above) */
 #define SPECDEC_STATUS_BAD_LOGIT 1          /* NaN or +inf logit in a row the call reads      */
@@ -178,6 +179,39 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);
 int specdec_profile_stop(void);
+
+/* ------------------------------------------------------------------------------------
+ * Chain verification without any allocation (no counterpart in the source pages; this is
+ * a deployment convenience).
+ *
+ * Some callers cannot allocate device memory, or must not: code running under an
+ * inference server's fixed memory plan that forbids allocations after start-up, plain C
+ * hosts that link only this library and receive their tensors from elsewhere, and
+ * latency-critical paths where cudaMalloc/cudaFree would synchronise the device.  This
+ * entry point takes the same arguments as specdec_verify_chain minus the workspace and
+ * uses scratch memory built into the library instead: one array of
+ * SPECDEC_NOALLOC_SCRATCH_BYTES in device memory, which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing and calls no allocating routine.
+ *
+ *   - Set-up: the first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture begins.
+ *   - Limit: a shape whose specdec_chain_workspace_bytes() exceeds
+ *     SPECDEC_NOALLOC_SCRATCH_BYTES is rejected with SPECDEC_ERR_TOO_LARGE (nothing is
+ *     launched; specdec_last_error() gives the sizes).  16 MiB covers, e.g., B=512, g=8,
+ *     V=152064 fp32.
+ *   - Sharing: every call on a device uses the same array and it keeps the last call's
+ *     contents; each call clears the counters it needs on its own stream first.  Calls
+ *     that overlap on the GPU (different streams, or host threads) race on the array and
+ *     must be serialised by the caller.
+ *   - Results are the same as specdec_verify_chain's for the same inputs.
+ */
+#define SPECDEC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+int specdec_verify_chain_noalloc(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                 const int32_t* draft_tokens, const float* temperatures,
+                                 const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                                 int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                                 void* stream);
 
 /* Library version string, e.g. "0.1.0". */
 const char* specdec_version(void);

@@ -2,6 +2,7 @@
 
 #include <cstdint>
 #include <algorithm>
+#include <mutex>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -218,6 +219,33 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   return SPECDEC_OK;
 }
 
+// ---- built-in scratch for specdec_verify_chain_noalloc ---------------------------------
+// One fixed array in device memory; every GPU that loads the library holds it until the
+// process exits.  Host code must not pass the symbol itself to a kernel: its address in
+// host code is a host-side stand-in.  The device address is looked up once per device.
+constexpr size_t kNoAllocScratchBytes = SPECDEC_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on first use).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return fail_cuda("querying the current device", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(SPECDEC_ERR_UNSUPPORTED, "device index beyond the scratch table");
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch); e != cudaSuccess)
+      return fail_cuda("looking up the built-in scratch array", e);
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return SPECDEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -347,5 +375,27 @@ int specdec_profile_stop(void) {
 const char* specdec_version(void) { return "0.1.0"; }
 
 const char* specdec_last_error(void) { return g_last_error; }
+
+int specdec_verify_chain_noalloc(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                 const int32_t* draft_tokens, const float* temperatures,
+                                 const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                                 int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                                 void* stream) {
+  if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return fail(SPECDEC_ERR_INVALID_ARG, "invalid dtype or size");
+  const size_t need = chain_ws_bytes(B, g, V, ldt);
+  if (need > kNoAllocScratchBytes) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "specdec_verify_chain_noalloc: this shape needs %zu bytes of scratch; the built-in "
+                  "scratch holds %zu bytes (use specdec_verify_chain with a caller workspace)",
+                  need, kNoAllocScratchBytes);
+    return SPECDEC_ERR_TOO_LARGE;
+  }
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(&scratch); rc != SPECDEC_OK) return rc;
+  // chain_common clears the counters it relies on, on this stream, before any kernel runs.
+  return chain_common(logits, ldt, draft_probs, draft_tokens, temperatures, uniforms, B, g, V,
+                      out_tokens, out_num_accepted, out_p_draft, out_status, scratch,
+                      kNoAllocScratchBytes, stream, false);
+}
 
 }  // extern "C"
