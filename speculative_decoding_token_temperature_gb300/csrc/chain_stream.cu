@@ -31,9 +31,12 @@ namespace specdec {
 namespace {
 
 constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
+#ifndef SPECDEC_DRAW_LIST_CACHE
+#define SPECDEC_DRAW_LIST_CACHE 256
+#endif
+constexpr int kDrawListCache = SPECDEC_DRAW_LIST_CACHE;  // draw-list entries kept in shared memory
 constexpr float kNaN = __builtin_nanf("");
 constexpr int kDecideThreads = 256;
-constexpr int kFinishWarps = 8;
 
 __device__ __forceinline__ bool is_greedy(float T) { return !(T >= SPECDEC_GREEDY_TEMPERATURE); }
 
@@ -43,11 +46,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 __device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
@@ -261,7 +259,6 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   __shared__ float s_m[kStreamMaxRows], s_Z[kStreamMaxRows];
   __shared__ int s_z[kStreamMaxRows];
   grid_launch_dependents();
-  grid_dependency_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = P.gamma + 1;
@@ -269,6 +266,27 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   const float Tb = P.greedy_only ? 0.f : __ldg(P.temps + b);
   const bool greedy = P.greedy_only || is_greedy(Tb);
   const float c = greedy ? 0.f : kLog2e / Tb;
+
+  // Inputs only (drafts, the logit and q at each draft, uniforms): fetched before waiting
+  // for the statistics kernel, so these loads overlap its tail.
+  int x = -1, st = 0;
+  float lx = 0.f, qx = 0.f, ux = 0.f;
+  if (warp == 0) {
+    if (lane < P.gamma) {
+      x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane);
+      if (x < 0 || x >= P.V) {
+        st |= SPECDEC_STATUS_BAD_TOKEN;
+      } else if (!greedy) {
+        lx = Elem<T>::load(static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + lane) * P.V, x);
+        qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + lane) * P.V + x);
+      }
+    }
+    if (!greedy && lane < R) {
+      ux = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
+      if (!(ux >= 0.f && ux < 1.f)) st |= SPECDEC_STATUS_BAD_UNIFORM;
+    }
+  }
+  grid_dependency_wait();
 
   // merge each row's chunk summaries (fixed order: deterministic); warps take rows
   for (int r = warp; r < R; r += kDecideThreads / 32) {
@@ -297,7 +315,7 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
 
   // accept tests, one lane per drafted position
   float m = -kInf, Z = 0.f;
-  int z = INT_MAX, st = 0;
+  int z = INT_MAX;
   if (lane < R) {
     m = s_m[lane];
     Z = s_Z[lane];
@@ -307,32 +325,22 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   }
   bool acc = false;
   float px = kNaN;
-  int x = -1;
-  if (lane < P.gamma) {
-    x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane);
-    if (x < 0 || x >= P.V) {
-      st |= SPECDEC_STATUS_BAD_TOKEN;
-    } else if (greedy) {
+  if (lane < P.gamma && !(st & SPECDEC_STATUS_BAD_TOKEN)) {
+    if (greedy) {
       acc = (x == z);
     } else {
-      const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + lane) * P.V;
-      px = ex2((Elem<T>::load(lrow, x) - m) * c) / Z;
-      const float qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + lane) * P.V + x);
+      px = ex2((lx - m) * c) / Z;
       if (!(qx >= 0.f && qx < kInf)) {
         st |= SPECDEC_STATUS_BAD_PROB;
       } else if (qx == 0.f) {
         st |= SPECDEC_STATUS_ZERO_Q;
         acc = px > 0.f;
       } else {
-        acc = __ldg(P.u + static_cast<int64_t>(b) * R + lane) * qx < px;
+        acc = ux * qx < px;
       }
     }
-    if (P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = px;
   }
-  if (!greedy && lane < R) {
-    const float uu = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
-    if (!(uu >= 0.f && uu < 1.f)) st |= SPECDEC_STATUS_BAD_UNIFORM;
-  }
+  if (lane < P.gamma && P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = px;
   if (lane == 0 && !P.greedy_only && !(Tb - Tb == 0.f)) st |= SPECDEC_STATUS_BAD_TEMPERATURE;
   st = __reduce_or_sync(0xffffffffu, st);
   const unsigned rej = __ballot_sync(0xffffffffu, !acc) | (0xffffffffu << P.gamma);  // gamma < 32
@@ -342,6 +350,7 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   const int zJ = __shfl_sync(0xffffffffu, z, src);
   const float mJ = __shfl_sync(0xffffffffu, m, src);
   const float ZJ = __shfl_sync(0xffffffffu, Z, src);
+  const float uG = __shfl_sync(0xffffffffu, ux, P.gamma);
   if (lane < R) {
     int tok = -1;
     if (J >= 0) {
@@ -356,10 +365,14 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
     const bool draw = (J >= 0) && !greedy;
     SeqState s;
     s.meta = make_int4(J, draw ? 1 : 0, st, 0);
-    s.row = make_float4(draw ? mJ : 0.f, draw ? ZJ : 0.f, c,
-                        draw ? __ldg(P.u + static_cast<int64_t>(b) * R + P.gamma) : 0.f);
+    s.row = make_float4(draw ? mJ : 0.f, draw ? ZJ : 0.f, c, draw ? uG : 0.f);
     P.ws.seq[b] = s;
-    if (draw) P.ws.draw_list[atomicAdd(P.ws.draw_count, 1u)] = make_int2(b, J);
+    if (draw) {
+      DrawEntry d;
+      d.loc = make_int4(b, J, 0, 0);
+      d.row = make_float4(mJ, c, 1.f / ZJ, 0.f);
+      P.ws.draw_list[atomicAdd(P.ws.draw_count, 1u)] = d;
+    }
   }
 }
 
@@ -367,51 +380,68 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
 // draw
 // ---------------------------------------------------------------------------------
 
-// Residual (or target) weights of one 16-byte vector of logits and the matching q values,
-// with their fp32 running sum in index order.  Shared by the chunk masses and the final
-// scan so both see identical per-vector values.
-template <typename T>
-__device__ __forceinline__ float vec_weights(const uint4& lw, const float* qv, float mJ, float c,
-                                             float invZ, bool no_q, float (&w)[Vec<T>::n],
-                                             float& psum, bool& bad_q) {
-  constexpr int VEC = Vec<T>::n;
-  float l[VEC];
-  if constexpr (sizeof(T) == 2) {
-    l[0] = bf16_lo(lw.x); l[1] = bf16_hi(lw.x); l[2] = bf16_lo(lw.y); l[3] = bf16_hi(lw.y);
-    l[4] = bf16_lo(lw.z); l[5] = bf16_hi(lw.z); l[6] = bf16_lo(lw.w); l[7] = bf16_hi(lw.w);
-  } else {
-    l[0] = __uint_as_float(lw.x); l[1] = __uint_as_float(lw.y);
-    l[2] = __uint_as_float(lw.z); l[3] = __uint_as_float(lw.w);
+// Logits of one group of 4 consecutive elements (8 bytes of bf16 or 16 bytes of fp32).
+template <typename T> struct Group;
+template <> struct Group<uint16_t> {
+  using L = uint2;
+  static __device__ __forceinline__ void unpack(const L& w, float (&l)[4]) {
+    l[0] = bf16_lo(w.x); l[1] = bf16_hi(w.x); l[2] = bf16_lo(w.y); l[3] = bf16_hi(w.y);
   }
+};
+template <> struct Group<float> {
+  using L = uint4;
+  static __device__ __forceinline__ void unpack(const L& w, float (&l)[4]) {
+    l[0] = __uint_as_float(w.x); l[1] = __uint_as_float(w.y);
+    l[2] = __uint_as_float(w.z); l[3] = __uint_as_float(w.w);
+  }
+};
+
+// Residual (or target) weights of one group of 4 elements and their fp32 running sum in
+// index order.  Shared by the chunk masses and the final scan, so both see identical
+// per-group values.
+// q values are checked by the caller (see q_check): a NaN, an infinity or a negative value
+// is reported as SPECDEC_STATUS_BAD_PROB.
+template <typename T>
+__device__ __forceinline__ float group_weights(const typename Group<T>::L& lw, const float4& q4, float mJ,
+                                               float c, float invZ, bool no_q, float (&w)[4]) {
+  float l[4];
+  Group<T>::unpack(lw, l);
+  const float qv[4] = {no_q ? 0.f : q4.x, no_q ? 0.f : q4.y, no_q ? 0.f : q4.z, no_q ? 0.f : q4.w};
   const unsigned long long m2 = f2pack(mJ, mJ), c2 = f2pack(c, c), z2 = f2pack(invZ, invZ);
-  float acc = 0.f, pacc = 0.f;
+  float acc = 0.f;
 #pragma unroll
-  for (int p = 0; p < VEC / 2; ++p) {
+  for (int p = 0; p < 2; ++p) {
     float y0, y1;
     f2unpack(f2mul(f2sub(f2pack(l[2 * p], l[2 * p + 1]), m2), c2), y0, y1);
     float p0, p1;
     f2unpack(f2mul(f2pack(ex2(y0), ex2(y1)), z2), p0, p1);
-    const float q0 = no_q ? 0.f : qv[2 * p], q1 = no_q ? 0.f : qv[2 * p + 1];
-    bad_q |= !(q0 >= 0.f && q0 < kInf) || !(q1 >= 0.f && q1 < kInf);
-    w[2 * p] = fmaxf(p0 - q0, 0.f);
-    w[2 * p + 1] = fmaxf(p1 - q1, 0.f);
+    w[2 * p] = fmaxf(p0 - qv[2 * p], 0.f);
+    w[2 * p + 1] = fmaxf(p1 - qv[2 * p + 1], 0.f);
     acc += w[2 * p];
     acc += w[2 * p + 1];
-    pacc += p0;
-    pacc += p1;
   }
-  psum = pacc;
   return acc;
 }
+
+// Running check of draft probabilities: the NaN-propagating maximum catches a NaN or an
+// infinity, the minimum a negative entry.
+struct QCheck {
+  float mx = 0.f, mn = 0.f;
+  __device__ __forceinline__ void add(const float4& q) {
+    mx = max_nan(mx, max_nan(max_nan(q.x, q.y), max_nan(q.z, q.w)));
+    mn = fminf(mn, fminf(fminf(q.x, q.y), fminf(q.z, q.w)));
+  }
+  __device__ __forceinline__ bool bad() const { return !(mx < kInf) || mn < 0.f; }
+};
 
 template <typename T>
 __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(const ChainParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kDrawWarps][kDrawStages];
-  constexpr int VEC = Vec<T>::n;
+  using GL = typename Group<T>::L;
   constexpr int LBYTES = kDrawChunk * static_cast<int>(sizeof(T));
   constexpr int STAGE = LBYTES + kDrawChunk * 4;
-  constexpr int VPL = (kDrawChunk / VEC) / 32;
+  constexpr int GPL = kDrawChunk / 4 / 32;  // 4-element groups per lane per chunk
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t NW = gridDim.x * kDrawWarps;
@@ -426,115 +456,151 @@ __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(c
     mbar_fence_init();
   }
   __syncwarp();
-  grid_dependency_wait();  // the decision kernel's list and states are visible from here
-  const uint32_t n_items = __ldcg(P.ws.draw_count) * nchd;
+  grid_dependency_wait();  // the decision kernel's list is visible from here
+  const uint32_t count = __ldcg(P.ws.draw_count);
+  const uint32_t n_items = count * nchd;
+  // The list, copied to shared memory when it fits: per-item metadata is then a shared
+  // load instead of an L2 round trip in every item's critical path.
+  DrawEntry* list_s = reinterpret_cast<DrawEntry*>(smem + static_cast<size_t>(kDrawWarps) * kDrawStages * STAGE);
+  const bool cached = count <= static_cast<uint32_t>(kDrawListCache);
+  if (cached) {
+    for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
+      list_s[i].loc = __ldcg(&P.ws.draw_list[i].loc);
+      list_s[i].row = __ldcg(&P.ws.draw_list[i].row);
+    }
+  }
+  __syncthreads();
+  const DrawEntry* list = cached ? list_s : P.ws.draw_list;
 
-  auto issue = [&](uint32_t it, int s) {
-    const int2 e = __ldcg(P.ws.draw_list + it / nchd);
+  auto issue = [&](uint32_t it, int s, int4 loc) {
     const uint32_t cd = it % nchd;
     const int n = min(kDrawChunk, P.V - static_cast<int>(cd) * kDrawChunk);
     const uint32_t lb = static_cast<uint32_t>(n) * sizeof(T);
-    const uint32_t qb = (e.y < P.gamma) ? static_cast<uint32_t>(n) * 4u : 0u;
+    const uint32_t qb = (loc.y < P.gamma) ? static_cast<uint32_t>(n) * 4u : 0u;
     mbar_expect_tx(&bar[s], lb + qb);
-    const T* src = static_cast<const T*>(P.logits) + (static_cast<int64_t>(e.x) * R + e.y) * P.V +
+    const T* src = static_cast<const T*>(P.logits) + (static_cast<int64_t>(loc.x) * R + loc.y) * P.V +
                    static_cast<int64_t>(cd) * kDrawChunk;
     bulk_copy_g2s(buf + s * STAGE, src, lb, &bar[s]);
     if (qb) {
-      const float* qs = P.q + (static_cast<int64_t>(e.x) * P.gamma + e.y) * P.V + static_cast<int64_t>(cd) * kDrawChunk;
+      const float* qs = P.q + (static_cast<int64_t>(loc.x) * P.gamma + loc.y) * P.V + static_cast<int64_t>(cd) * kDrawChunk;
       bulk_copy_g2s(buf + s * STAGE + LBYTES, qs, qb, &bar[s]);
     }
   };
   uint32_t issued = 0;
   for (uint32_t it = gw; issued < kDrawStages && it < n_items; it += NW, ++issued)
-    if (lane == 0) issue(it, issued);
+    if (lane == 0) issue(it, static_cast<int>(issued), list[it / nchd].loc);
 
   uint32_t k = 0;
   for (uint32_t it = gw; it < n_items; it += NW, ++k) {
     const int s = static_cast<int>(k % kDrawStages);
+    const uint32_t nx = it + kDrawStages * NW;  // the item this stage is refilled with
+    const bool refill = nx < n_items && nx > it;
+    int4 nloc = make_int4(0, 0, 0, 0);
+    if (lane == 0 && refill) nloc = list[nx / nchd].loc;
+    DrawEntry cur;
+    cur.loc = list[it / nchd].loc;
+    cur.row = list[it / nchd].row;
     if (!mbar_wait(&bar[s], (k / kDrawStages) & 1u)) {
       if (lane == 0) drain_after_timeout(bar, kDrawStages, k, issued, P.ws.error);
       break;
     }
-    const int2 e = __ldcg(P.ws.draw_list + it / nchd);
     const uint32_t cd = it % nchd;
-    const float4 row = __ldcg(&P.ws.seq[e.x].row);
-    const bool has_q = e.y < P.gamma;
-    const int n = min(kDrawChunk, P.V - static_cast<int>(cd) * kDrawChunk);
-    const int nv = n / VEC;
-    const float c = row.z, mJ = row.x, invZ = 1.f / row.y;
+    const bool has_q = cur.loc.y < P.gamma;
+    const int ng = min(kDrawChunk, P.V - static_cast<int>(cd) * kDrawChunk) / 4;
     const unsigned char* sb = buf + s * STAGE;
-    uint4 lw[VPL];
-    float qv[VPL][VEC];
+    GL lw[GPL];
+    float4 qv[GPL];
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int v = lane + 32 * j;
-      if (v < nv) {
-        lw[j] = reinterpret_cast<const uint4*>(sb)[v];
-        if (has_q) {
-#pragma unroll
-          for (int q4 = 0; q4 < VEC; q4 += 4) {
-            const float4 f = reinterpret_cast<const float4*>(sb + LBYTES)[(v * VEC + q4) / 4];
-            qv[j][q4] = f.x; qv[j][q4 + 1] = f.y; qv[j][q4 + 2] = f.z; qv[j][q4 + 3] = f.w;
-          }
-        }
+    for (int j = 0; j < GPL; ++j) {
+      const int g = lane + 32 * j;
+      if (g < ng) {
+        lw[j] = reinterpret_cast<const GL*>(sb)[g];
+        qv[j] = has_q ? reinterpret_cast<const float4*>(sb + LBYTES)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     __syncwarp();
-    const uint32_t nx = it + kDrawStages * NW;
-    const bool refill = nx < n_items && nx > it;
     if (lane == 0 && refill) {
       fence_proxy_async_smem();
-      issue(nx, s);
+      issue(nx, s, nloc);
     }
     issued += refill ? 1u : 0u;
-    float sr = 0.f, sp = 0.f;
-    bool bad = false;
+    float sr = 0.f;
+    QCheck qc;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int v = lane + 32 * j;
-      if (v < nv) {
-        float w[VEC], ps;
-        sr += vec_weights<T>(lw[j], qv[j], mJ, c, invZ, !has_q, w, ps, bad);
-        sp += ps;
+    for (int j = 0; j < GPL; ++j) {
+      if (lane + 32 * j < ng) {
+        float w[4];
+        sr += group_weights<T>(lw[j], qv[j], cur.row.x, cur.row.y, cur.row.z, !has_q, w);
+        qc.add(qv[j]);
       }
     }
-    if (__any_sync(0xffffffffu, bad)) sr = kNaN;
     sr = warp_sum(sr);
-    sp = warp_sum(sp);
-    if (lane == 0) P.ws.draw_mass[static_cast<int64_t>(e.x) * nchd + cd] = make_float2(sr, sp);
+    if (__any_sync(0xffffffffu, qc.bad())) sr = kNaN;
+    if (lane == 0) P.ws.draw_mass[static_cast<int64_t>(cur.loc.x) * nchd + cd] = sr;
   }
 }
 
 // ---------------------------------------------------------------------------------
 // finish: one warp per sequence
 // ---------------------------------------------------------------------------------
+
+// Mass of chunk q of the drawn row: the draw kernel's residual mass, or (zero-residual
+// fallback) the mass of p itself, recomputed here.
 template <typename T>
-__global__ void __launch_bounds__(kFinishWarps * 32) chain_finish_kernel(const ChainParams P) {
-  constexpr int VEC = Vec<T>::n;
-  constexpr int VPL = (kDrawChunk / VEC) / 32;  // contiguous vectors per lane in the scan
+__device__ __forceinline__ float chunk_mass(const ChainParams& P, const float* dm, bool use_p, const T* lrow,
+                                            int q, float mJ, float c, float invZ) {
+  if (!use_p) return __ldcg(dm + q);
+  using GL = typename Group<T>::L;
+  const int k0 = q * kDrawChunk;
+  const int ng = min(kDrawChunk, P.V - k0) / 4;
+  float acc = 0.f;
+  for (int g = 0; g < ng; ++g) {
+    float w[4];
+    acc += group_weights<T>(__ldg(reinterpret_cast<const GL*>(lrow + k0) + g), make_float4(0.f, 0.f, 0.f, 0.f),
+                            mJ, c, invZ, true, w);
+  }
+  return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
+  using GL = typename Group<T>::L;
+  constexpr int GPL = kDrawChunk / 4 / 32;  // contiguous groups per lane in the scan
+  constexpr int CPL = 16;                   // chunk masses per lane kept in registers
   grid_launch_dependents();
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kFinishWarps + (threadIdx.x >> 5);
-  if (b >= P.B) return;
+  const int b = blockIdx.x;
   SeqState st;
   st.meta = __ldcg(&P.ws.seq[b].meta);
-  if (st.meta.y == 0) return;
   st.row = __ldcg(&P.ws.seq[b].row);
+  if (st.meta.y == 0) return;
   const int R = P.gamma + 1;
   const int J = st.meta.x;
   const int nchd = P.nchd;
-  const float2* dm = P.ws.draw_mass + static_cast<int64_t>(b) * nchd;
+  const float* dm = P.ws.draw_mass + static_cast<int64_t>(b) * nchd;
   int32_t* tok_out = P.out_tokens + static_cast<int64_t>(b) * R;
+  const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
+  const float c = st.row.z, mJ = st.row.x, invZ = 1.f / st.row.y;
 
-  double S = 0.0, Sp = 0.0;
-  for (int q = lane; q < nchd; q += 32) {
-    const float2 d = __ldcg(dm + q);
-    S += static_cast<double>(d.x);
-    Sp += static_cast<double>(d.y);
+  // lane l owns the contiguous chunks [c0, c1); with at most CPL per lane their masses
+  // stay in registers
+  const int cpl = (nchd + 31) / 32;
+  const bool in_regs = cpl <= CPL;
+  const int c0 = min(lane * cpl, nchd), c1 = min(c0 + cpl, nchd);
+  float wq[CPL];
+  double mine = 0.0;
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) wq[j] = (c0 + j < c1) ? __ldcg(dm + c0 + j) : 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+      if (j < c1 - c0) mine += static_cast<double>(wq[j]);
+  } else {
+    for (int q = c0; q < c1; ++q) mine += static_cast<double>(__ldcg(dm + q));
   }
-  S = warp_sum(S);
-  Sp = warp_sum(Sp);
+  double incl = warp_incl_scan(mine, lane);
+  double S = __shfl_sync(0xffffffffu, incl, 31);
   if (S != S) {  // a NaN, infinite or negative draft probability in the drawn row
     if (lane < R) tok_out[lane] = -1;
     if (lane == 0) {
@@ -543,101 +609,125 @@ __global__ void __launch_bounds__(kFinishWarps * 32) chain_finish_kernel(const C
     }
     return;
   }
-  const bool use_p = !(S > 0.0);  // zero residual after rounding: draw from p
-  const double target = static_cast<double>(st.row.w) * (use_p ? Sp : S);
+  const bool use_p = !(S > 0.0);  // zero residual after rounding: draw from p instead
+  if (use_p) {  // rare: recompute every chunk's mass of p itself (and keep it from here on)
+    mine = 0.0;
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        wq[j] = (j < c1 - c0) ? chunk_mass<T>(P, dm, true, lrow, c0 + j, mJ, c, invZ) : 0.f;
+        mine += static_cast<double>(wq[j]);
+      }
+    } else {
+      for (int q = c0; q < c1; ++q) mine += static_cast<double>(chunk_mass<T>(P, dm, true, lrow, q, mJ, c, invZ));
+    }
+    incl = warp_incl_scan(mine, lane);
+    S = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const double target = static_cast<double>(st.row.w) * S;
+
+  // Walk this lane's chunks in order: the first whose running mass (from pre) exceeds
+  // target, else the last one with mass.  Also returns the running mass before it.
+  auto walk = [&](double pre, bool want_cross, int& found, double& before) {
+    found = -1;
+    before = 0.0;
+    int lastpos = -1;
+    double prelast = 0.0;
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        if (j < c1 - c0 && found < 0) {
+          const double w = static_cast<double>(wq[j]);
+          if (w > 0.0) { lastpos = c0 + j; prelast = pre; }
+          if (want_cross && pre + w > target) { found = c0 + j; before = pre; }
+          pre += w;
+        }
+      }
+    } else {
+      for (int q = c0; q < c1 && found < 0; ++q) {
+        const double w = static_cast<double>(chunk_mass<T>(P, dm, use_p, lrow, q, mJ, c, invZ));
+        if (w > 0.0) { lastpos = q; prelast = pre; }
+        if (want_cross && pre + w > target) { found = q; before = pre; }
+        pre += w;
+      }
+    }
+    if (found < 0) { found = lastpos; before = prelast; }
+  };
 
   // the chunk whose running mass first exceeds target (fp64 prefix in chunk order)
-  double base = 0.0, base_last = 0.0;
-  int cstar = -1, clast = -1;
-  for (int q0 = 0; q0 < nchd && cstar < 0; q0 += 32) {
-    const int q = q0 + lane;
-    double wq = 0.0;
-    if (q < nchd) {
-      const float2 d = __ldcg(dm + q);
-      wq = static_cast<double>(use_p ? d.y : d.x);
-    }
-    const double incl = warp_incl_scan(wq, lane);
-    const double tot = __shfl_sync(0xffffffffu, incl, 31);
-    const unsigned pos = __ballot_sync(0xffffffffu, wq > 0.0);
-    if (pos) {
-      const int hl = 31 - __clz(pos);
-      clast = q0 + hl;
-      base_last = base + __shfl_sync(0xffffffffu, incl - wq, hl);
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, base + incl > target);
-    if (hit) {
-      const int fl = __ffs(hit) - 1;
-      cstar = q0 + fl;
-      base = base + __shfl_sync(0xffffffffu, incl - wq, fl);
-    } else {
-      base += tot;
-    }
-  }
-  if (cstar < 0) {
-    cstar = clast < 0 ? 0 : clast;
-    base = base_last;
-  }
-
-  // scan that chunk in index order: lane l owns VPL contiguous vectors
-  const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
-  const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
-  const bool no_q = use_p || qrow == nullptr;
-  const float c = st.row.z, mJ = st.row.x, invZ = 1.f / st.row.y;
-  const int k0 = cstar * kDrawChunk;
-  const int nv = min(kDrawChunk, P.V - k0) / VEC;
-  float vsum[VPL];
-  double mine = 0.0;
-  int last_pos = -1;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int v = lane * VPL + j;
-    vsum[j] = 0.f;
-    if (v < nv) {
-      const uint4 lw = __ldg(reinterpret_cast<const uint4*>(lrow + k0 + v * VEC));
-      float qv[VEC];
-      if (!no_q) load_q<VEC>(qrow, k0 + v * VEC, qv);
-      float w[VEC], ps;
-      bool bad = false;
-      vsum[j] = vec_weights<T>(lw, qv, mJ, c, invZ, no_q, w, ps, bad);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e)
-        if (w[e] > 0.f) last_pos = k0 + v * VEC + e;
-      mine += static_cast<double>(vsum[j]);
-    }
-  }
-  const double incl = warp_incl_scan(mine, lane);
-  const unsigned hit = __ballot_sync(0xffffffffu, base + incl > target);
-  int y = -1;
+  const unsigned hit = __ballot_sync(0xffffffffu, incl > target);
+  int cstar = -1;
+  double base = 0.0;
   if (hit) {
     const int fl = __ffs(hit) - 1;
+    if (lane == fl) walk(incl - mine, true, cstar, base);
+    cstar = __shfl_sync(0xffffffffu, cstar, fl);
+    base = __shfl_sync(0xffffffffu, base, fl);
+  }
+  if (cstar < 0) {  // rounding put u * S at or past the end: last chunk with mass
+    int lastpos;
+    double before;
+    walk(incl - mine, false, lastpos, before);
+    const int best = warp_max_int(lastpos);
+    const unsigned owner = __ballot_sync(0xffffffffu, lastpos == best && best >= 0);
+    cstar = best < 0 ? 0 : best;
+    base = owner ? __shfl_sync(0xffffffffu, before, __ffs(owner) - 1) : 0.0;
+  }
+
+  // scan that chunk in index order: lane l owns GPL contiguous groups of 4 elements,
+  // whose weights stay in registers
+  const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
+  const bool no_q = use_p || qrow == nullptr;
+  const int k0 = cstar * kDrawChunk;
+  const int ng = min(kDrawChunk, P.V - k0) / 4;
+  float w[GPL][4];
+  float gsum[GPL];
+  double lane_tot = 0.0;
+#pragma unroll
+  for (int j = 0; j < GPL; ++j) {
+    const int g = lane * GPL + j;
+    gsum[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[j][e] = 0.f;
+    if (g < ng) {
+      const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
+      const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
+      gsum[j] = group_weights<T>(lw, q4, mJ, c, invZ, no_q, w[j]);
+      lane_tot += static_cast<double>(gsum[j]);
+    }
+  }
+  int last_pos = -1;
+#pragma unroll
+  for (int j = 0; j < GPL; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (w[j][e] > 0.f) last_pos = k0 + 4 * (lane * GPL + j) + e;
+  const double gincl = warp_incl_scan(lane_tot, lane);
+  const unsigned ghit = __ballot_sync(0xffffffffu, base + gincl > target);
+  int y = -1;
+  if (ghit) {
+    const int fl = __ffs(ghit) - 1;
     if (lane == fl) {
-      double pre = base + (incl - mine);
-      for (int j = 0; j < VPL && y < 0; ++j) {
-        const int v = lane * VPL + j;
-        if (v >= nv) break;
-        if (pre + static_cast<double>(vsum[j]) > target) {
-          const uint4 lw = __ldg(reinterpret_cast<const uint4*>(lrow + k0 + v * VEC));
-          float qv[VEC];
-          if (!no_q) load_q<VEC>(qrow, k0 + v * VEC, qv);
-          float w[VEC], ps;
-          bool bad = false;
-          vec_weights<T>(lw, qv, mJ, c, invZ, no_q, w, ps, bad);
+      double pre = base + (gincl - lane_tot);
+#pragma unroll
+      for (int j = 0; j < GPL; ++j) {
+        if (y < 0 && pre + static_cast<double>(gsum[j]) > target) {
           float run = 0.f;
           int lastp = -1;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            run += w[e];
-            if (w[e] > 0.f) lastp = k0 + v * VEC + e;
-            if (y < 0 && pre + static_cast<double>(run) > target) y = k0 + v * VEC + e;
+          for (int e = 0; e < 4; ++e) {
+            run += w[j][e];
+            if (w[j][e] > 0.f) lastp = k0 + 4 * (lane * GPL + j) + e;
+            if (y < 0 && pre + static_cast<double>(run) > target) y = k0 + 4 * (lane * GPL + j) + e;
           }
           if (y < 0) y = lastp;
         }
-        pre += static_cast<double>(vsum[j]);
+        pre += static_cast<double>(gsum[j]);
       }
     }
     y = __shfl_sync(0xffffffffu, y, fl);
   }
-  if (y < 0) y = warp_max_int(last_pos);  // rounding put u * S at or past the end
+  if (y < 0) y = warp_max_int(last_pos);  // rounding put u * S at or past the chunk's end
   if (lane == 0) {
     tok_out[J] = y;
     if (use_p && P.out_status) P.out_status[b] = st.meta.z | SPECDEC_STATUS_ZERO_RESIDUAL;
@@ -668,7 +758,8 @@ cudaError_t launch_stats_t(const ChainParams& P, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_draw_t(const ChainParams& P, cudaStream_t stream) {
-  constexpr int smem = kDrawWarps * kDrawStages * (kDrawChunk * static_cast<int>(sizeof(T)) + kDrawChunk * 4);
+  constexpr int smem = kDrawWarps * kDrawStages * (kDrawChunk * static_cast<int>(sizeof(T)) + kDrawChunk * 4) +
+                       kDrawListCache * static_cast<int>(sizeof(DrawEntry));
   static unsigned long long configured = 0;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(chain_draw_stream_kernel<T>), smem, configured);
   if (e != cudaSuccess) return e;
@@ -699,10 +790,9 @@ cudaError_t launch_chain_stream_draw(const ChainParams& P, specdec_dtype ldt, cu
 }
 
 cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
-  const dim3 grid((P.B + kFinishWarps - 1) / kFinishWarps);
   if (ldt == SPECDEC_BF16)
-    return launch_kernel(chain_finish_kernel<uint16_t>, grid, dim3(kFinishWarps * 32), 0, stream, 1, P);
-  return launch_kernel(chain_finish_kernel<float>, grid, dim3(kFinishWarps * 32), 0, stream, 1, P);
+    return launch_kernel(chain_finish_kernel<uint16_t>, dim3(P.B), dim3(32), 0, stream, 1, P);
+  return launch_kernel(chain_finish_kernel<float>, dim3(P.B), dim3(32), 0, stream, 1, P);
 }
 
 }  // namespace specdec

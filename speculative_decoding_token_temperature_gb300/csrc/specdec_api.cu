@@ -83,7 +83,7 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   if (path == 2) {
     const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(elem_size(ldt));
     n_part = rows * ((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
-    draw_bytes = static_cast<int64_t>(B) * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float2));
+    draw_bytes = static_cast<int64_t>(B) * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float));
   } else {
     const int seg = chain_segment_len(ldt, path == 1);
     const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
@@ -95,7 +95,7 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * 2 * static_cast<size_t>(B));
   const size_t counters_end = off;
   const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
-  const size_t o_list = off;     off += round_up(sizeof(int2) * static_cast<size_t>(B));
+  const size_t o_list = off;     off += round_up(sizeof(DrawEntry) * static_cast<size_t>(B));
   const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(n_part));
   const size_t o_draw = off;     off += round_up(static_cast<size_t>(draw_bytes));
   if (counter_bytes) *counter_bytes = counters_end;
@@ -105,10 +105,10 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->draw_count = reinterpret_cast<unsigned*>(p + o_error) + 1;
     ws->counters = reinterpret_cast<unsigned*>(p + o_counters);
     ws->seq = reinterpret_cast<SeqState*>(p + o_seq);
-    ws->draw_list = reinterpret_cast<int2*>(p + o_list);
+    ws->draw_list = reinterpret_cast<DrawEntry*>(p + o_list);
     ws->partials = reinterpret_cast<float4*>(p + o_part);
     ws->draw = reinterpret_cast<double2*>(p + o_draw);
-    ws->draw_mass = reinterpret_cast<float2*>(p + o_draw);
+    ws->draw_mass = reinterpret_cast<float*>(p + o_draw);
   }
   return off;
 }

@@ -22,25 +22,50 @@ struct SeqState {
   float4 row;  // (row max m, normaliser Z, c = log2(e)/T, uniform of the extra token)
 };
 
+// A sequence that draws an extra token: its drawn row and that row's softmax constants,
+// written by the decision kernel in one 32-byte record so a draw work item needs one load.
+struct DrawEntry {
+  int4 loc;    // (sequence b, drawn row J, 0, 0)
+  float4 row;  // (row max m, c = log2(e)/T, 1/Z, 0)
+};
+
 struct ChainWorkspace {
   float4* partials;   // [B*(g+1)*nseg]: per segment (max, sum of 2^((l-max)c), argmax bits, 0)
   unsigned* counters; // [2B]: arrivals per sequence for the statistics and the draw kernels
   SeqState* seq;      // [B]
   double2* draw;      // [B*nseg]: per segment (residual mass, target mass) of the drawn row
   // streaming path only
-  int2* draw_list;       // [B]: (sequence, J) of every sequence that draws, in any order
+  struct DrawEntry* draw_list;  // [B]: every sequence that draws an extra token, in any order
   unsigned* draw_count;  // [1]: entries in draw_list
-  float2* draw_mass;     // [B*nchd]: per chunk (residual mass, target mass) of the drawn row
+  float* draw_mass;      // [B*nchd]: residual (or bonus) mass per chunk of the drawn row
   unsigned* error;       // [1]: set when a bounded wait gave up
 };
 
 // Streaming (bulk-copy) path geometry.
-constexpr int kStatsWarps = 16;       // warps per CTA, one CTA per SM
-constexpr int kStatsStages = 3;       // bulk-copy stages per warp
-constexpr int kStatsChunkBytes = 4096;
-constexpr int kDrawWarps = 8;
-constexpr int kDrawStages = 3;
-constexpr int kDrawChunk = 1024;      // elements of the drawn row per work item
+#ifndef SPECDEC_STATS_WARPS
+#define SPECDEC_STATS_WARPS 16
+#endif
+#ifndef SPECDEC_STATS_STAGES
+#define SPECDEC_STATS_STAGES 3
+#endif
+#ifndef SPECDEC_STATS_CHUNK
+#define SPECDEC_STATS_CHUNK 4096
+#endif
+#ifndef SPECDEC_DRAW_WARPS
+#define SPECDEC_DRAW_WARPS 16
+#endif
+#ifndef SPECDEC_DRAW_STAGES
+#define SPECDEC_DRAW_STAGES 4
+#endif
+#ifndef SPECDEC_DRAW_CHUNK
+#define SPECDEC_DRAW_CHUNK 512
+#endif
+constexpr int kStatsWarps = SPECDEC_STATS_WARPS;     // warps per CTA, one CTA per SM
+constexpr int kStatsStages = SPECDEC_STATS_STAGES;   // bulk-copy stages per warp
+constexpr int kStatsChunkBytes = SPECDEC_STATS_CHUNK;
+constexpr int kDrawWarps = SPECDEC_DRAW_WARPS;
+constexpr int kDrawStages = SPECDEC_DRAW_STAGES;
+constexpr int kDrawChunk = SPECDEC_DRAW_CHUNK;       // elements of the drawn row per work item
 constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decision
 
 struct ChainParams {
