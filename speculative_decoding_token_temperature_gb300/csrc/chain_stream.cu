@@ -435,9 +435,22 @@ struct QCheck {
 };
 
 template <typename T>
+constexpr int draw_stages() { return sizeof(T) == 2 ? kDrawStages : kDrawStagesF32; }
+
+template <typename T>
+constexpr int draw_smem_bytes() {
+  return kDrawWarps * draw_stages<T>() * (kDrawChunk * static_cast<int>(sizeof(T)) + kDrawChunk * 4) +
+         kDrawListCache * static_cast<int>(sizeof(DrawEntry));
+}
+static_assert(draw_smem_bytes<uint16_t>() <= 227 * 1024, "bf16 draw stages exceed shared memory");
+static_assert(draw_smem_bytes<float>() <= 227 * 1024, "fp32 draw stages exceed shared memory");
+static_assert(kStatsWarps * kStatsStages * kStatsChunkBytes <= 227 * 1024, "statistics stages exceed shared memory");
+
+template <typename T>
 __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(const ChainParams P) {
+  constexpr int kStages = draw_stages<T>();
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t bars[kDrawWarps][kDrawStages];
+  __shared__ __align__(8) uint64_t bars[kDrawWarps][kStages];
   using GL = typename Group<T>::L;
   constexpr int LBYTES = kDrawChunk * static_cast<int>(sizeof(T));
   constexpr int STAGE = LBYTES + kDrawChunk * 4;
@@ -446,13 +459,13 @@ __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t NW = gridDim.x * kDrawWarps;
   const uint32_t gw = blockIdx.x * kDrawWarps + warp;
-  unsigned char* buf = smem + static_cast<size_t>(warp) * kDrawStages * STAGE;
+  unsigned char* buf = smem + static_cast<size_t>(warp) * kStages * STAGE;
   uint64_t* bar = bars[warp];
   const int R = P.gamma + 1;
   const uint32_t nchd = P.nchd;
 
   if (lane == 0) {
-    for (int s = 0; s < kDrawStages; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
     mbar_fence_init();
   }
   __syncwarp();
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(c
   const uint32_t n_items = count * nchd;
   // The list, copied to shared memory when it fits: per-item metadata is then a shared
   // load instead of an L2 round trip in every item's critical path.
-  DrawEntry* list_s = reinterpret_cast<DrawEntry*>(smem + static_cast<size_t>(kDrawWarps) * kDrawStages * STAGE);
+  DrawEntry* list_s = reinterpret_cast<DrawEntry*>(smem + static_cast<size_t>(kDrawWarps) * kStages * STAGE);
   const bool cached = count <= static_cast<uint32_t>(kDrawListCache);
   if (cached) {
     for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
@@ -487,21 +500,21 @@ __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(c
     }
   };
   uint32_t issued = 0;
-  for (uint32_t it = gw; issued < kDrawStages && it < n_items; it += NW, ++issued)
+  for (uint32_t it = gw; issued < kStages && it < n_items; it += NW, ++issued)
     if (lane == 0) issue(it, static_cast<int>(issued), list[it / nchd].loc);
 
   uint32_t k = 0;
   for (uint32_t it = gw; it < n_items; it += NW, ++k) {
-    const int s = static_cast<int>(k % kDrawStages);
-    const uint32_t nx = it + kDrawStages * NW;  // the item this stage is refilled with
+    const int s = static_cast<int>(k % kStages);
+    const uint32_t nx = it + kStages * NW;  // the item this stage is refilled with
     const bool refill = nx < n_items && nx > it;
     int4 nloc = make_int4(0, 0, 0, 0);
     if (lane == 0 && refill) nloc = list[nx / nchd].loc;
     DrawEntry cur;
     cur.loc = list[it / nchd].loc;
     cur.row = list[it / nchd].row;
-    if (!mbar_wait(&bar[s], (k / kDrawStages) & 1u)) {
-      if (lane == 0) drain_after_timeout(bar, kDrawStages, k, issued, P.ws.error);
+    if (!mbar_wait(&bar[s], (k / kStages) & 1u)) {
+      if (lane == 0) drain_after_timeout(bar, kStages, k, issued, P.ws.error);
       break;
     }
     const uint32_t cd = it % nchd;
@@ -758,8 +771,7 @@ cudaError_t launch_stats_t(const ChainParams& P, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_draw_t(const ChainParams& P, cudaStream_t stream) {
-  constexpr int smem = kDrawWarps * kDrawStages * (kDrawChunk * static_cast<int>(sizeof(T)) + kDrawChunk * 4) +
-                       kDrawListCache * static_cast<int>(sizeof(DrawEntry));
+  constexpr int smem = draw_smem_bytes<T>();
   static unsigned long long configured = 0;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(chain_draw_stream_kernel<T>), smem, configured);
   if (e != cudaSuccess) return e;

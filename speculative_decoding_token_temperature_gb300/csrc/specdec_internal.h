@@ -64,7 +64,8 @@ constexpr int kStatsWarps = SPECDEC_STATS_WARPS;     // warps per CTA, one CTA p
 constexpr int kStatsStages = SPECDEC_STATS_STAGES;   // bulk-copy stages per warp
 constexpr int kStatsChunkBytes = SPECDEC_STATS_CHUNK;
 constexpr int kDrawWarps = SPECDEC_DRAW_WARPS;
-constexpr int kDrawStages = SPECDEC_DRAW_STAGES;
+constexpr int kDrawStages = SPECDEC_DRAW_STAGES;       // for bf16 logits
+constexpr int kDrawStagesF32 = 3;                      // fp32 stages are larger
 constexpr int kDrawChunk = SPECDEC_DRAW_CHUNK;       // elements of the drawn row per work item
 constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decision
 
