@@ -304,20 +304,27 @@ def main():
         per_kernel = kt.read()
     launches_per_step = sum(v[1] for v in per_kernel.values()) / args.steps
 
-    # roofline of the dominant kernel (the statistics pass over every logits row)
+    # roofline of the dominant kernel
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or FALLBACK_HBM_GBS
-    st_ms, st_n = per_kernel["chain_stats"]
-    stats_bytes = rows * V * esize                       # every logits row read once
-    achieved = stats_bytes / (st_ms / st_n / 1e3) / 1e9 if st_n else None
-    sha = kernel_source_sha()
-    traffic = NCU_TRAFFIC.get("chain_stats", {})
-    traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
-    # bytes one whole call must move: all rows + the drawn row of logits and of q
+    # rows a left-to-right verifier must read: 0..J of every sequence (the bonus row too
+    # when all gamma drafts are accepted), and the draft row q_J of each rejection
     n_rej = sum(float((o["num_accepted"] < g).float().sum()) for o in outs) / len(outs)
-    call_bytes = rows * V * esize + B * V * esize + n_rej * V * 4
+    rows_read = sum(float((o["num_accepted"].clamp(max=g) + 1).float().sum()) for o in outs) / len(outs)
+    seq_bytes = rows_read * V * esize + n_rej * V * 4
+    if per_kernel.get("chain_seq", (0.0, 0))[1]:
+        kname, alg_bytes = "chain_seq", seq_bytes
+    else:
+        kname, alg_bytes = "chain_stats", rows * V * esize   # every logits row read once
+    k_ms, k_n = per_kernel[kname]
+    achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
+    sha = kernel_source_sha()
+    traffic = NCU_TRAFFIC.get(kname, {})
+    traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
+    # bytes one whole call must move (the same left-to-right count for either kernel set)
+    call_bytes = seq_bytes
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -326,10 +333,11 @@ def main():
                    "draft_probs_dtype": "fp32", "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2, {args.sets} seeded batches rotated"},
         "hbm_gbs_call": call_bytes / (ms_per_step / 1e3) / 1e9,
-        "roofline": {"kernel": "chain_stats", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None,
-                     "algorithmic_bytes_per_launch": stats_bytes, "traffic": traffic_val},
+                     "algorithmic_bytes_per_launch": alg_bytes, "traffic": traffic_val},
+        "rows_read_per_step": rows_read,
         "kernels_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items() if v[1]},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "mean_accepted": statistics.mean(accepted),

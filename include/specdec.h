@@ -89,9 +89,15 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
  * uniforms        [B, g+1]     fp32 in [0, 1): slot i tests draft i, slot g drives y
  * out_tokens      [B, g+1]     int32: x_0..x_{J-1}, y, then -1
  * out_num_accepted[B]          int32: J (or -1 on a data error)
- * out_p_draft     [B, g]       fp32, optional (NULL): p_i(x_i); NaN for greedy sequences
+ * out_p_draft     [B, g]       fp32, optional (NULL): p_i(x_i) for i <= J; NaN after J,
+ *                              for greedy sequences and on a data error
  * out_status      [B]          int32, optional (NULL): status bits
- * Every logits row is read once; row J and q row J are read again by the draw.
+ * Positions are evaluated left to right, as the round itself runs: row i (its logits,
+ * draft token, q_i(x_i) and uniform) counts only if drafts 0..i-1 were all accepted,
+ * and the first data error or rejection ends the scan.  Rows after J therefore neither
+ * change the outputs nor are validated (the default kernel does not read them at all),
+ * and status bits describe rows 0..J plus uniforms[b, g] and q row J where the draw
+ * uses them.  A non-finite temperature is an error whatever the rows hold.
  * Sizes: B >= 1, g >= 1, V >= 1, V < 2^31.
  */
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
@@ -174,7 +180,8 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_TREE_MASK 3
 #define SPECDEC_KERNEL_CHAIN_DECIDE 4  /* accept tests and first rejection          */
 #define SPECDEC_KERNEL_CHAIN_FINISH 5  /* inverse-CDF search of the drawn rows      */
-#define SPECDEC_NUM_KERNELS 6
+#define SPECDEC_KERNEL_CHAIN_SEQ 6     /* left-to-right chain verification          */
+#define SPECDEC_NUM_KERNELS 7
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

@@ -151,6 +151,13 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
       extra token y ~ (p_J - q_J)+ normalised, with q_gamma == 0 (bonus from p_gamma)
       emit x_0 .. x_{J-1}, y
 
+    The positions are evaluated left to right and evaluation stops at the first
+    rejection (SD 20.5, "A whole round of speculative sampling": the rule is applied to
+    the drafts from left to right and stops at the first rejection; the drafts after it
+    are discarded).  READING: only what is evaluated is validated -- row i, draft i,
+    q_i(x_i) and u_i for i <= J, u_gamma and the q row of the draw -- and p_draft is NaN
+    after J.
+
     A sequence with T < GREEDY_T is verified greedily (SD 20.5, "A round of greedy
     speculative decoding", and the special case "A greedy target" of the rule):
     accept while x_i == z_i = lowest argmax of row i, then emit z_J; q and u are unused.
@@ -182,61 +189,72 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
         "margins": np.full(gamma, np.inf),
         "greedy": greedy,
     }
-    status = 0 if np.isfinite(T) else STATUS_BAD_TEMPERATURE
-    for i in range(g1):
-        status |= _row_status(logits[i])
-    for x in drafts:
-        if not (0 <= x < V):
-            status |= STATUS_BAD_TOKEN
-    if not greedy:
-        if not np.all((u >= 0.0) & (u < 1.0)):
-            status |= STATUS_BAD_UNIFORM
-        for i, x in enumerate(drafts):
-            if 0 <= x < V:
-                qx = float(widen(q[i][x]))
-                if not np.isfinite(qx) or qx < 0.0:
-                    status |= STATUS_BAD_PROB
-    if status & STATUS_ERROR_MASK:
-        out["status"] = status
+
+    def error(bits):
+        out["status"] = bits
+        out["p_draft"][:] = np.nan
         return out
 
+    status = 0
+    if not np.isfinite(T):
+        return error(STATUS_BAD_TEMPERATURE)
+
+    # Checks of one position, in order: its logits row, then its draft token, then (when
+    # sampled) its draft probability and uniform together; the first failing check ends
+    # the round with that error.
+    p = {}
+    J = gamma
+    for i in range(g1):
+        rs = _row_status(logits[i])
+        if rs:
+            return error(status | rs)
+        if i == gamma:
+            break
+        x = drafts[i]
+        if not (0 <= x < V):
+            return error(status | STATUS_BAD_TOKEN)
+        if greedy:
+            ok = x == lowest_argmax(logits[i])
+        else:
+            qx = float(widen(q[i][x]))
+            bad = 0
+            if not np.isfinite(qx) or qx < 0.0:
+                bad |= STATUS_BAD_PROB
+            if not (0.0 <= u[i] < 1.0):
+                bad |= STATUS_BAD_UNIFORM
+            if bad:
+                return error(status | bad)
+            p[i] = target_distribution(logits[i], T)
+            px = p[i][x]
+            out["p_draft"][i] = px
+            out["q_draft"][i] = qx
+            if qx == 0.0:
+                # READING: a draft the drafter could not have produced; SD 20.5 notes the
+                # ratio is then never needed.  Accept iff p(x) > 0 and warn.
+                status |= STATUS_ZERO_Q
+                ok = px > 0.0
+            else:
+                ok = u[i] * qx < px
+                out["margins"][i] = abs(u[i] - px / qx)
+        if not ok:
+            J = i
+            break
+
     if greedy:
-        z = [lowest_argmax(logits[i]) for i in range(g1)]
-        J = 0
-        while J < gamma and drafts[J] == z[J]:
-            J += 1
         out["tokens"][:J] = drafts[:J]
-        out["tokens"][J] = z[J]
+        out["tokens"][J] = lowest_argmax(logits[J])
         out["J"] = J
         out["status"] = status
         return out
 
-    # Sampled: every row's probabilities are evaluated (the library reads every row).
-    p = [target_distribution(logits[i], T) for i in range(g1)]
-    accepted = []
-    for i, x in enumerate(drafts):
-        px = p[i][x]
-        qx = float(widen(q[i][x]))
-        out["p_draft"][i] = px
-        out["q_draft"][i] = qx
-        if qx == 0.0:
-            # READING: a draft the drafter could not have produced; SD 20.5 notes the
-            # ratio is then never needed.  Accept iff p(x) > 0 and warn.
-            status |= STATUS_ZERO_Q
-            ok = px > 0.0
-        else:
-            ok = u[i] * qx < px
-            out["margins"][i] = abs(u[i] - px / qx)
-        accepted.append(ok)
-    J = 0
-    while J < gamma and accepted[J]:
-        J += 1
-
+    if not (0.0 <= u[gamma] < 1.0):
+        return error(status | STATUS_BAD_UNIFORM)
+    if J not in p:
+        p[J] = target_distribution(logits[J], T)
     if J < gamma:
         qJ = widen(q[J])
         if np.isnan(qJ).any() or np.isinf(qJ).any() or (qJ < 0).any():
-            out["status"] = status | STATUS_BAD_PROB
-            return out
+            return error(status | STATUS_BAD_PROB)
         w = residual_distribution(p[J], qJ)
     else:
         # q_{gamma+1} == 0: the residual of the bonus row is p itself

@@ -38,7 +38,8 @@ STATUS_ERROR_MASK = 0xFF
 STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
-KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish")
+KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
+                "chain_seq")
 
 
 class SpecdecError(RuntimeError):

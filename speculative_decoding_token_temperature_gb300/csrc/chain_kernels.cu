@@ -33,15 +33,17 @@ __device__ void chain_decide(const ChainParams& P, int b) {
   __shared__ float s_m[kMaxGamma + 1];
   __shared__ float s_Z[kMaxGamma + 1];
   __shared__ int s_z[kMaxGamma + 1];
-  __shared__ int s_acc[kMaxGamma + 1];
+  __shared__ int s_err[kMaxGamma + 1];
+  __shared__ int s_warn[kMaxGamma + 1];
+  __shared__ unsigned char s_acc[kMaxGamma + 1];
+  __shared__ float s_px[kMaxGamma + 1];
   __shared__ int s_stat, s_J;
   const int tid = threadIdx.x;
   const int R = P.gamma + 1;
   const float Tb = P.greedy_only ? 0.f : __ldg(P.temps + b);
   const bool greedy = P.greedy_only || is_greedy(Tb);
   const float c = greedy ? 0.f : kLog2e / Tb;
-  if (tid == 0) s_stat = 0;
-  __syncthreads();
+  constexpr float kNaN = __builtin_nanf("");
 
   // Merge the segment statistics of every row (fixed segment order: deterministic).
   for (int r = tid; r < R; r += NT) {
@@ -56,58 +58,79 @@ __device__ void chain_decide(const ChainParams& P, int b) {
       if (!greedy && finite && f.x > -kInf) Z += f.y * ex2((f.x - m) * c);
       if (f.x == m && z == INT_MAX) z = __float_as_int(f.z);
     }
-    int st = 0;
-    if (!(m == m) || m == kInf) st |= SPECDEC_STATUS_BAD_LOGIT;
-    else if (m == -kInf) st |= SPECDEC_STATUS_EMPTY_ROW;
     s_m[r] = m;
     s_Z[r] = Z;
     s_z[r] = z;
-    if (st) atomicOr(&s_stat, st);
   }
   __syncthreads();
 
-  // Accept tests, one thread per drafted position.
-  for (int i = tid; i < P.gamma; i += NT) {
-    const int x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + i);
-    int st = 0, acc = 0;
-    float px = __int_as_float(0x7fc00000);  // NaN unless evaluated
-    if (x < 0 || x >= P.V) {
-      st |= SPECDEC_STATUS_BAD_TOKEN;
-    } else if (greedy) {
-      acc = (x == s_z[i]);
-    } else {
-      const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + i) * P.V;
-      const float lx = Elem<T>::load(lrow, x);
-      px = ex2((lx - s_m[i]) * c) / s_Z[i];
-      const float qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + i) * P.V + x);
-      if (!(qx >= 0.f && qx < kInf)) {
-        st |= SPECDEC_STATUS_BAD_PROB;
-      } else if (qx == 0.f) {
-        st |= SPECDEC_STATUS_ZERO_Q;
-        acc = px > 0.f;
+  // Every position's checks in parallel, in the order: logits row, draft token, then
+  // (when sampled) draft probability and uniform together.
+  for (int i = tid; i < R; i += NT) {
+    const float m = s_m[i];
+    int err = 0;
+    if (!(m == m) || m == kInf) err = SPECDEC_STATUS_BAD_LOGIT;
+    else if (m == -kInf) err = SPECDEC_STATUS_EMPTY_ROW;
+    int warn = 0, acc = 0;
+    float px = kNaN;
+    if (!err && i < P.gamma) {
+      const int x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + i);
+      if (x < 0 || x >= P.V) {
+        err = SPECDEC_STATUS_BAD_TOKEN;
+      } else if (greedy) {
+        acc = (x == s_z[i]);
       } else {
-        acc = __ldg(P.u + static_cast<int64_t>(b) * R + i) * qx < px;
+        const float qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + i) * P.V + x);
+        const float uu = __ldg(P.u + static_cast<int64_t>(b) * R + i);
+        if (!(qx >= 0.f && qx < kInf)) err |= SPECDEC_STATUS_BAD_PROB;
+        if (!(uu >= 0.f && uu < 1.f)) err |= SPECDEC_STATUS_BAD_UNIFORM;
+        if (!err) {
+          const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + i) * P.V;
+          px = ex2((Elem<T>::load(lrow, x) - m) * c) / s_Z[i];
+          if (qx == 0.f) {
+            warn = SPECDEC_STATUS_ZERO_Q;
+            acc = px > 0.f;
+          } else {
+            acc = uu * qx < px;
+          }
+        }
       }
     }
-    if (P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + i] = px;
-    s_acc[i] = acc;
-    if (st) atomicOr(&s_stat, st);
+    s_err[i] = err;
+    s_warn[i] = warn;
+    s_acc[i] = static_cast<unsigned char>(acc);
+    s_px[i] = px;
   }
-  if (!greedy) {
-    for (int i = tid; i < R; i += NT) {
-      const float uu = __ldg(P.u + static_cast<int64_t>(b) * R + i);
-      if (!(uu >= 0.f && uu < 1.f)) atomicOr(&s_stat, SPECDEC_STATUS_BAD_UNIFORM);
-    }
-  }
-  if (tid == 0 && !P.greedy_only && !(Tb - Tb == 0.f)) atomicOr(&s_stat, SPECDEC_STATUS_BAD_TEMPERATURE);
   __syncthreads();
 
+  // Left to right, stopping at the first error or rejection (SD 20.5, "A whole round of
+  // speculative sampling").
   if (tid == 0) {
-    int J = -1;
-    if (!(s_stat & SPECDEC_STATUS_ERROR_MASK)) {
-      J = 0;
-      while (J < P.gamma && s_acc[J]) ++J;
+    int st = 0, J = P.gamma;
+    for (int i = 0; i < R; ++i) {
+      if (s_err[i]) {
+        st |= s_err[i];
+        J = -1;
+        break;
+      }
+      st |= s_warn[i];
+      if (i == P.gamma || !s_acc[i]) {
+        J = i;
+        break;
+      }
     }
+    if (!P.greedy_only && !(Tb - Tb == 0.f)) {
+      st = SPECDEC_STATUS_BAD_TEMPERATURE;
+      J = -1;
+    }
+    if (J >= 0 && !greedy) {
+      const float uG = __ldg(P.u + static_cast<int64_t>(b) * R + P.gamma);
+      if (!(uG >= 0.f && uG < 1.f)) {
+        st |= SPECDEC_STATUS_BAD_UNIFORM;
+        J = -1;
+      }
+    }
+    s_stat = st;
     s_J = J;
   }
   __syncthreads();
@@ -121,6 +144,8 @@ __device__ void chain_decide(const ChainParams& P, int b) {
       else if (pos == J && greedy) tok = s_z[J];
     }
     tb[pos] = tok;
+    if (P.out_p_draft && pos < P.gamma)
+      P.out_p_draft[static_cast<int64_t>(b) * P.gamma + pos] = (J >= 0 && pos <= J) ? s_px[pos] : kNaN;
   }
   if (tid == 0) {
     P.out_J[b] = J;

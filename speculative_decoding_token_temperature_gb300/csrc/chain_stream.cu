@@ -268,23 +268,25 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   const float c = greedy ? 0.f : kLog2e / Tb;
 
   // Inputs only (drafts, the logit and q at each draft, uniforms): fetched before waiting
-  // for the statistics kernel, so these loads overlap its tail.
-  int x = -1, st = 0;
+  // for the statistics kernel, so these loads overlap its tail.  Lane i < gamma holds
+  // position i; lane gamma holds the bonus row and the draw's uniform.
+  // Checks of one position, in order: its logits row, then its draft token, then (when
+  // sampled) its draft probability and uniform together.
+  int x = -1, tok_err = 0, qu_err = 0;
   float lx = 0.f, qx = 0.f, ux = 0.f;
   if (warp == 0) {
     if (lane < P.gamma) {
       x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane);
       if (x < 0 || x >= P.V) {
-        st |= SPECDEC_STATUS_BAD_TOKEN;
+        tok_err = SPECDEC_STATUS_BAD_TOKEN;
       } else if (!greedy) {
         lx = Elem<T>::load(static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + lane) * P.V, x);
         qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + lane) * P.V + x);
+        if (!(qx >= 0.f && qx < kInf)) qu_err |= SPECDEC_STATUS_BAD_PROB;
       }
     }
-    if (!greedy && lane < R) {
-      ux = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
-      if (!(ux >= 0.f && ux < 1.f)) st |= SPECDEC_STATUS_BAD_UNIFORM;
-    }
+    if (!greedy && lane < R) ux = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
+    if (!greedy && lane < P.gamma && !(ux >= 0.f && ux < 1.f)) qu_err |= SPECDEC_STATUS_BAD_UNIFORM;
   }
   grid_dependency_wait();
 
@@ -313,44 +315,48 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
   __syncthreads();
   if (warp != 0) return;
 
-  // accept tests, one lane per drafted position
+  // Positions are evaluated left to right and evaluation stops at the first rejection
+  // (SD 20.5, "A whole round of speculative sampling"); lane i evaluates position i and
+  // the first lane that stops -- by an error or a rejection -- decides the round.
   float m = -kInf, Z = 0.f;
-  int z = INT_MAX;
+  int z = INT_MAX, warn = 0, row_err = 0;
   if (lane < R) {
     m = s_m[lane];
     Z = s_Z[lane];
     z = s_z[lane];
-    if (!(m == m) || m == kInf) st |= SPECDEC_STATUS_BAD_LOGIT;
-    else if (m == -kInf) st |= SPECDEC_STATUS_EMPTY_ROW;
+    if (!(m == m) || m == kInf) row_err = SPECDEC_STATUS_BAD_LOGIT;
+    else if (m == -kInf) row_err = SPECDEC_STATUS_EMPTY_ROW;
   }
+  const int err = row_err ? row_err : (tok_err ? tok_err : qu_err);
   bool acc = false;
   float px = kNaN;
-  if (lane < P.gamma && !(st & SPECDEC_STATUS_BAD_TOKEN)) {
+  if (lane < P.gamma && !err) {
     if (greedy) {
       acc = (x == z);
     } else {
       px = ex2((lx - m) * c) / Z;
-      if (!(qx >= 0.f && qx < kInf)) {
-        st |= SPECDEC_STATUS_BAD_PROB;
-      } else if (qx == 0.f) {
-        st |= SPECDEC_STATUS_ZERO_Q;
+      if (qx == 0.f) {
+        warn |= SPECDEC_STATUS_ZERO_Q;
         acc = px > 0.f;
       } else {
         acc = ux * qx < px;
       }
     }
   }
-  if (lane < P.gamma && P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = px;
-  if (lane == 0 && !P.greedy_only && !(Tb - Tb == 0.f)) st |= SPECDEC_STATUS_BAD_TEMPERATURE;
-  st = __reduce_or_sync(0xffffffffu, st);
-  const unsigned rej = __ballot_sync(0xffffffffu, !acc) | (0xffffffffu << P.gamma);  // gamma < 32
-  int J = __ffs(rej) - 1;
-  if (st & SPECDEC_STATUS_ERROR_MASK) J = -1;
-  const int src = J < 0 ? 0 : J;
-  const int zJ = __shfl_sync(0xffffffffu, z, src);
-  const float mJ = __shfl_sync(0xffffffffu, m, src);
-  const float ZJ = __shfl_sync(0xffffffffu, Z, src);
+  const bool stop = (lane < R) && (err != 0 || lane == P.gamma || !acc);
+  const int s_stop = __ffs(__ballot_sync(0xffffffffu, stop)) - 1;  // <= gamma
+  int st = __shfl_sync(0xffffffffu, err, s_stop);
+  st |= __reduce_or_sync(0xffffffffu, lane <= s_stop ? warn : 0);
+  if (!P.greedy_only && !(Tb - Tb == 0.f)) st = SPECDEC_STATUS_BAD_TEMPERATURE;
   const float uG = __shfl_sync(0xffffffffu, ux, P.gamma);
+  if (!(st & SPECDEC_STATUS_ERROR_MASK) && !greedy && !(uG >= 0.f && uG < 1.f)) st |= SPECDEC_STATUS_BAD_UNIFORM;
+  const bool failed = (st & SPECDEC_STATUS_ERROR_MASK) != 0;
+  const int J = failed ? -1 : s_stop;
+  if (lane < P.gamma && P.out_p_draft)
+    P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = (!failed && lane <= J) ? px : kNaN;
+  const int zJ = __shfl_sync(0xffffffffu, z, s_stop);
+  const float mJ = __shfl_sync(0xffffffffu, m, s_stop);
+  const float ZJ = __shfl_sync(0xffffffffu, Z, s_stop);
   if (lane < R) {
     int tok = -1;
     if (J >= 0) {
@@ -363,10 +369,10 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
     P.out_J[b] = J;
     if (P.out_status) P.out_status[b] = st;
     const bool draw = (J >= 0) && !greedy;
-    SeqState s;
-    s.meta = make_int4(J, draw ? 1 : 0, st, 0);
-    s.row = make_float4(draw ? mJ : 0.f, draw ? ZJ : 0.f, c, draw ? uG : 0.f);
-    P.ws.seq[b] = s;
+    SeqState sq;
+    sq.meta = make_int4(J, draw ? 1 : 0, st, 0);
+    sq.row = make_float4(draw ? mJ : 0.f, draw ? ZJ : 0.f, c, draw ? uG : 0.f);
+    P.ws.seq[b] = sq;
     if (draw) {
       DrawEntry d;
       d.loc = make_int4(b, J, 0, 0);

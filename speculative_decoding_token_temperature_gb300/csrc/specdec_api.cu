@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <mutex>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -28,6 +29,16 @@ bool valid_dtype(int t) { return t == SPECDEC_F32 || t == SPECDEC_BF16; }
 // 16-byte vector loads need every row start 16-byte aligned.
 bool rows_vectorizable(const void* base, int64_t V, size_t esize) {
   return aligned16(base) && ((V * static_cast<int64_t>(esize)) % 16 == 0);
+}
+
+// Aligned rows take the left-to-right kernel, which reads rows only up to the first
+// rejection, unless SPECDEC_CHAIN_SCAN=1 selects the kernels that scan every row first.
+bool use_left_to_right() {
+  static const bool v = [] {
+    const char* e = std::getenv("SPECDEC_CHAIN_SCAN");
+    return !(e && e[0] == '1');
+  }();
+  return v;
 }
 
 // ---- last error (per host thread) -----------------------------------------------------
@@ -180,6 +191,12 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   // always written before they are read.
   if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
     return fail_cuda("clearing the workspace counters", e);
+  if (stream_path && use_left_to_right() && V <= kSeqDrawChunk * kSeqMaxDrawChunks) {
+    P.grid_stats = device_sm_count();
+    ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
+    if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);
+    return SPECDEC_OK;
+  }
   if (stream_path) {
     const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(es);
     P.nch = static_cast<int>((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);

@@ -69,6 +69,14 @@ constexpr int kDrawStagesF32 = 3;                      // fp32 stages are larger
 constexpr int kDrawChunk = SPECDEC_DRAW_CHUNK;       // elements of the drawn row per work item
 constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decision
 
+// Left-to-right (early-exit) kernel geometry: one CTA per SM with kSeqGroups groups.
+constexpr int kSeqWarps = 16;
+constexpr int kSeqGroups = 2;
+constexpr int kSeqStages = 3;
+constexpr int kSeqChunkBytes = 4096;
+constexpr int kSeqDrawChunk = 512;        // drawn-row elements per copy (logits + q fit 4 KB)
+constexpr int kSeqMaxDrawChunks = 4096;   // chunk masses kept in shared memory: V <= 2^21
+
 struct ChainParams {
   const void* logits;
   const float* q;
@@ -103,6 +111,8 @@ cudaError_t launch_chain_stream_decide(const ChainParams& P, specdec_dtype ldt, 
 cudaError_t launch_chain_stream_draw(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 int device_sm_count();
+// Left-to-right chain verification reading rows only up to the first rejection.
+cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 
 cudaError_t launch_chain_stats(const ChainParams& P, specdec_dtype ldt, bool vector_path,
                                cudaStream_t stream);

@@ -149,6 +149,8 @@ def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray):
             gp = gpu["p_draft"][b].astype(np.float64)
             op = o["p_draft"]
             ok = np.isfinite(op)
+            if gJ == o["J"] and not np.array_equal(np.isnan(gp), np.isnan(op)):
+                report.fail(f"seq {b}: p_draft evaluated positions differ {gp} vs {op}")
             if ok.any():
                 err = float(np.max(np.abs(gp[ok] - op[ok])))
                 report.max_p_err = max(report.max_p_err, err)

@@ -310,6 +310,21 @@ def test_status_flags_and_degenerate_cases():
     assert r["J"] == 1 and r["status"] == 0
 
 
+def test_positions_after_the_first_rejection_are_not_evaluated():
+    """SD 20.5, "A whole round of speculative sampling": the rule runs left to right and
+    stops at the first rejection; what lies after it is never looked at."""
+    l = np.array([[0.0, 0.0], [np.nan, 0.0], [0.0, 0.0]])
+    q = np.array([[1.0, 0.0], [0.5, 0.5]])
+    r = so.verify_chain_sequence(l, q, [0, 99], 1.0, [0.9, 0.5, 0.25])
+    assert r["status"] == 0 and r["J"] == 0 and r["tokens"][0] == 1
+    assert r["p_draft"][0] == pytest.approx(0.5) and np.isnan(r["p_draft"][1])
+    r = so.verify_chain_sequence(l, q, [0, 99], 1.0, [0.1, 0.5, 0.25])
+    assert r["status"] == so.STATUS_BAD_LOGIT and r["J"] == -1 and np.isnan(r["p_draft"]).all()
+    # greedy: position 0 rejected (argmax is token 0 on ties), row 1 never read
+    r = so.verify_chain_sequence(l, None, [1, 99], 0.0, np.zeros(3))
+    assert r["status"] == 0 and r["J"] == 0 and list(r["tokens"]) == [0, -1, -1]
+
+
 def test_zero_residual_falls_back_to_p():
     # p slightly below q at the draft so it can be rejected, yet (p - q)+ == 0
     # everywhere is impossible in exact arithmetic; force it through q >= p elementwise.
