@@ -3,24 +3,30 @@
 // SD 20.5, "A whole round of speculative sampling": the one-token rule is applied to the
 // drafts left to right and the round stops at the first rejection; the drafts after it
 // are discarded, so their target rows are never needed.  This kernel follows that order
-// literally.  Each CTA (one per SM, persistent) holds kSeqGroups groups of warps; a group
-// takes whole sequences from a shared counter and, for each:
+// literally, as a dataflow over TASKS:
 //
-//   row i = 0, 1, ...  stream the row through the group's bulk-copy pipelines (every warp
-//                      keeps three cp.async.bulk copies in flight on mbarriers); each lane
-//                      keeps a running maximum and sum of 2^((l - m) * log2(e) / T) (or the
-//                      lowest index of the maximum for a greedy sequence); the group merges
-//                      them and tests draft i: accept iff u_i * q_i(x_i) < p_i(x_i)
-//                      (greedy: x_i == argmax).  A rejection, or row gamma, ends the loop.
-//   draw               for a sampled sequence, one more pass over the last row read (J)
-//                      and q row J: residual weights (p_J - q_J)+ (q == 0 for the bonus
-//                      row; SD 20.5, "The speculative sampling rule") summed per 512-element
-//                      chunk in shared memory, then an fp64 prefix over the chunks and an
-//                      index-order scan of the chosen chunk for the smallest k with
-//                      C_k > u * S.
+//   row task (b, i)   the softmax statistics of row i of sequence b and the test of draft
+//                     i: accept iff u_i * q_i(x_i) < p_i(x_i) (greedy: x_i == argmax).  An
+//                     acceptance publishes row task (b, i + 1); a rejection, or row gamma,
+//                     publishes the draw task (b, i) (a greedy sequence emits the argmax).
+//   draw task (b, J)  the residual weights (p_J - q_J)+ (q == 0 for the bonus row; SD 20.5,
+//                     "The speculative sampling rule") and the inverse-CDF draw: the
+//                     smallest k with C_k > u * S.
 //
-// Everything a sequence needs stays inside its group: no grid-wide synchronisation, no
-// fences.  The only shared datum is the sequence counter (cleared by the host per call).
+// Row tasks of all sequences are queued ahead of draw tasks, so every sequence's chain of
+// rows advances as early as possible while the draws fill the bandwidth behind them.
+//
+// A task is run by a TEAM: one group of warps in each of the kSeqCluster CTAs of a
+// thread-block cluster (one CTA per SM).  Member r owns the r-th contiguous part of the
+// row.  Each warp streams its chunks through a bulk-copy pipeline (cp.async.bulk copies
+// in flight on mbarriers); each lane keeps a running maximum and sum of
+// 2^((l - m) * log2(e) / T) (or the lowest index of the maximum), or, for a draw, sums
+// residual weights per 512-element chunk.  Members exchange their 16-byte summaries by
+// st.async into each other's shared memory (distributed shared memory); every member
+// merges them in member order, so all hold the same bits and take the same decision.
+// The member whose part holds u * S finds the drawn token.  The team's first member
+// claims the next task while the current one streams and sends it to the others, so
+// every warp has the next task's copies in flight before the current task ends.
 
 #include <climits>
 
@@ -35,12 +41,25 @@ constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
 constexpr float kNaN = __builtin_nanf("");
 constexpr int kWarpsPerGroup = kSeqWarps / kSeqGroups;
 constexpr int kGroupThreads = kWarpsPerGroup * 32;
+constexpr int kC = kSeqCluster;
+static_assert(kSeqWarps % kSeqGroups == 0, "groups must split the warps evenly");
+static_assert(kC >= 1 && kC <= 8, "portable cluster sizes only");
 
 __device__ __forceinline__ bool is_greedy(float T) { return !(T >= SPECDEC_GREEDY_TEMPERATURE); }
 
 // Barrier over the threads of one group (named barriers 1.., 0 stays __syncthreads).
 __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(kGroupThreads) : "memory");
+}
+// Barrier over the group that also returns whether any of its threads passed `v`.
+__device__ __forceinline__ bool group_any(int group, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(group + 1), "r"(kGroupThreads)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -131,16 +150,53 @@ __device__ __forceinline__ float group_weights(const typename Group<T>::L& lw, c
   return acc;
 }
 
-// Shared state of one group.
+// Shared state of one group (one team member).  Its layout is the same in every CTA, so
+// a member's slot in another CTA is this one's address mapped to that CTA.
 struct GroupShared {
+  float4 slot[2][kC];           // summary exchange slots by parity, one per member
+  uint64_t xbar[2];             // their mbarriers
+  float4 mbox[2][2];            // the next task's 32-byte entry, by task parity
+  uint64_t mbar_box[2];         // their mbarriers
   RowSum wsum[kWarpsPerGroup];  // per-warp row summaries
-  float mass[kSeqMaxDrawChunks];  // draw: residual mass per chunk
-  float4 row;                   // merged row (m, Z, argmax bits, 0)
-  int b;                        // current sequence (or >= B: done)
-  int stop;                     // decision broadcast
-  int qbad;                     // a bad draft probability in the drawn row
-  int y;                        // drawn token
+  // per task parity: draft token bits, its logit, its q, u_i, u_gamma, input error bits
+  float gq[2][8];
+  float mass[2][kSeqMaxDrawChunks];  // draw: mass per chunk of this member's part, by task parity
 };
+
+// This group's side of a team: its member index and the exchange sequence number.
+struct Team {
+  uint32_t rank = 0;
+  uint32_t xk = 0;
+  bool ok = true;  // false once a bounded wait gave up
+};
+
+// Every member contributes 16 bytes (`mine`, taken from the first thread of the group);
+// on return every thread of the group can read all contributions in gs.slot[par][*].
+// Two parities alternate and a group barrier closes each exchange; a member sends into a
+// parity only after every member finished the exchange before it, so a slot is never
+// rewritten while a thread may still read it.
+__device__ int exchange(GroupShared& gs, Team& tm, const float4& mine, int group, int gwarp, int lane,
+                        unsigned* error) {
+  const int par = static_cast<int>(tm.xk & 1u);
+  const uint32_t phase = (tm.xk >> 1) & 1u;
+  ++tm.xk;
+  bool waited = true;
+  if (tm.ok) {
+    if (gwarp == 0 && lane == 0) {
+      mbar_expect_tx(&gs.xbar[par], kC * 16);
+      const uint32_t sa = smem_addr(&gs.slot[par][tm.rank]);
+      const uint32_t ba = smem_addr(&gs.xbar[par]);
+#pragma unroll
+      for (int r = 0; r < kC; ++r) st_async_16(cluster_map(sa, r), mine, cluster_map(ba, r));
+    }
+    waited = mbar_wait_cluster(&gs.xbar[par], phase);
+  }
+  if (group_any(group, !waited)) {
+    if (gwarp == 0 && lane == 0) atomicOr(error, 2u);
+    tm.ok = false;
+  }
+  return par;
+}
 
 // One warp's bulk-copy pipeline: kSeqStages stages of kSeqChunkBytes in shared memory.
 // `k` counts completed stages and `issued` issued ones, over the kernel's lifetime.
@@ -152,10 +208,13 @@ struct Pipe {
 
   __device__ __forceinline__ unsigned char* stage(uint32_t i) { return buf + (i % kSeqStages) * kSeqChunkBytes; }
   __device__ __forceinline__ uint64_t* sbar(uint32_t i) { return bar + (i % kSeqStages); }
-  // Issue one copy group (one or two copies totalling `bytes`) into the next stage.
+  __device__ __forceinline__ uint32_t in_flight() const { return issued - k; }
+  // Issue one copy group (one or two copies) into the next stage.  The fence orders this
+  // warp's earlier reads of that stage (completed by a __syncwarp) before the copy.
   __device__ __forceinline__ void issue(const void* a, uint32_t na, const void* b, uint32_t nb, int off_b) {
     uint64_t* br = sbar(issued);
     unsigned char* dst = stage(issued);
+    fence_proxy_async_smem();
     mbar_expect_tx(br, na + nb);
     bulk_copy_g2s(dst, a, na, br);
     if (nb) bulk_copy_g2s(dst + off_b, b, nb, br);
@@ -163,333 +222,337 @@ struct Pipe {
   __device__ __forceinline__ bool wait() { return mbar_wait(sbar(k), (k / kSeqStages) & 1u); }
 };
 
-// ---------------------------------------------------------------------------------
-// One logits row: per-lane running summary across the warp's chunks, group merge.
-// ---------------------------------------------------------------------------------
+enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3 };
+
+// A task entry: 32 bytes, in the global rings and in a team's mailbox.
+//   e0 = (sequence b (-1: no more work), row | kind << 8 | warnings << 16, m, Z)
+//   e1 = (T, 0, 0, 0)
+// (m, Z) are the drawn row's maximum and normaliser for draw tasks; the warnings are
+// the sequence's status bits above the error byte, shifted down by 8.
+struct Entry {
+  int b, row, kind, warn;
+  float m, Z, T;
+};
+__device__ __forceinline__ void pack_entry(const Entry& e, float4& e0, float4& e1) {
+  e0 = make_float4(__int_as_float(e.b), __int_as_float(e.row | (e.kind << 8) | (e.warn << 16)), e.m, e.Z);
+  e1 = make_float4(e.T, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ Entry unpack_entry(const float4& e0, const float4& e1) {
+  Entry e;
+  e.b = __float_as_int(e0.x);
+  const int bits = __float_as_int(e0.y);
+  e.row = bits & 0xff;
+  e.kind = (bits >> 8) & 0xff;
+  e.warn = bits >> 16;
+  e.m = e0.z;
+  e.Z = e0.w;
+  e.T = e1.x;
+  return e;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Work that any team may take: the start of a sequence (its row 0; ticket s < B is
+// sequence s) and published draw tasks (draw ticket d is the d-th published draw).
+// Tickets are handed out by atomicAdd, so claiming never retries; a draw ticket taken
+// before its draw is published is waited for only after the claiming team finished the
+// task it was running, so no team ever waits on work that it must produce itself.
+struct Queue {
+  unsigned *start_ticket, *pub_draws, *draw_ticket, *finished;
+  int* ready_draws;
+  float4* ring_draws;
+  int B;
+};
+constexpr int kDrawTag = 1 << 30;
+
+__device__ __forceinline__ int take_ticket(const Queue& q) {
+  if (ld_relaxed(q.start_ticket) < static_cast<unsigned>(q.B)) {
+    const unsigned s = atomicAdd(q.start_ticket, 1u);
+    if (s < static_cast<unsigned>(q.B)) return static_cast<int>(s);
+  }
+  return kDrawTag | static_cast<int>(atomicAdd(q.draw_ticket, 1u));
+}
+
+// The entry behind a ticket: 1 = ready, 0 = not published yet (only if !blocking),
+// -1 = every sequence has finished (no more work), -2 = a bounded wait gave up.
+__device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, bool blocking, float4& e0, float4& e1) {
+  if (!(tk & kDrawTag)) {
+    Entry e;
+    e.b = tk;
+    e.row = 0;
+    e.kind = kTaskRow;
+    e.warn = 0;
+    e.m = 0.f;
+    e.Z = 1.f;
+    e.T = P.greedy_only ? 0.f : __ldg(P.temps + tk);
+    pack_entry(e, e0, e1);
+    return 1;
+  }
+  const int d = tk & ~kDrawTag;
+  uint64_t t0 = 0;
+  for (;;) {
+    if (d < 2 * q.B && ld_acquire(q.ready_draws + d) != 0) {
+      const float4* ent = q.ring_draws + 2 * static_cast<int64_t>(d);
+      e0 = __ldcg(ent);
+      e1 = __ldcg(ent + 1);
+      return 1;
+    }
+    if (ld_relaxed(q.finished) >= static_cast<unsigned>(q.B)) return -1;
+    if (!blocking) return 0;
+    if (t0 == 0) t0 = global_timer_ns();
+    else if (global_timer_ns() - t0 > kMaxWaitNs) return -2;
+    __nanosleep(128);
+  }
+}
+
+__device__ void publish_draw(const Queue& q, const Entry& e) {
+  float4 e0, e1;
+  pack_entry(e, e0, e1);
+  const unsigned k = atomicAdd(q.pub_draws, 1u);
+  float4* ent = q.ring_draws + 2 * static_cast<int64_t>(k);
+  __stcg(ent, e0);
+  __stcg(ent + 1, e1);
+  st_release(q.ready_draws + k, 1);
+}
+
+// The team leader hands a task entry to every member's mailbox of the given parity.
+__device__ __forceinline__ void send_entry(GroupShared& gs, int par, const float4& e0, const float4& e1) {
+  const uint32_t sa = smem_addr(&gs.mbox[par][0]);
+  const uint32_t ba = smem_addr(&gs.mbar_box[par]);
+#pragma unroll
+  for (int r = 0; r < kC; ++r) {
+    st_async_16(cluster_map(sa, r), e0, cluster_map(ba, r));
+    st_async_16(cluster_map(sa + 16, r), e1, cluster_map(ba, r));
+  }
+}
+
+// This member's copies of one task: the logits row (or drawn row) and, for a residual
+// draw, the q row; the member's chunk range [lo, hi) (4 KB chunks for a row, 512-element
+// chunks for a draw); this warp's jobs are the chunks lo + gwarp, lo + gwarp + W, ...
+struct Task {
+  int kind = 0;
+  const char* src = nullptr;
+  const float* q = nullptr;
+  int lo = 0, hi = 0, n = 0;
+};
+
 template <typename T>
-__device__ RowSum row_pass(const T* lrow, int V, bool greedy, float c, Pipe& pp, GroupShared& gs,
-                           int group, int gwarp, int lane, unsigned* error) {
+__device__ __forceinline__ void issue_job(Pipe& pp, const Task& t, int j, int gwarp, int lane, int V,
+                                          int64_t row_bytes) {
+  constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
+  if (lane == 0) {
+    const int ch = t.lo + gwarp + j * kWarpsPerGroup;
+    if (t.kind == kTaskRow) {
+      const uint32_t nb = static_cast<uint32_t>(
+          min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes));
+      pp.issue(t.src + static_cast<int64_t>(ch) * kSeqChunkBytes, nb, nullptr, 0, 0);
+    } else {
+      const int n = min(kSeqDrawChunk, V - ch * kSeqDrawChunk);
+      const int64_t off = static_cast<int64_t>(ch) * kSeqDrawChunk;
+      pp.issue(t.src + off * static_cast<int64_t>(sizeof(T)), static_cast<uint32_t>(n) * sizeof(T),
+               t.q ? t.q + off : nullptr, t.q ? static_cast<uint32_t>(n) * 4u : 0u, LB);
+    }
+  }
+  ++pp.issued;
+}
+
+// One 4 KB chunk of a row into this lane's running (max, sum, argmax).
+template <typename T>
+__device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512], int nv, int ch, bool greedy,
+                                          float c, int lane, float& ml, float& Zl, int& zl) {
   constexpr int VEC = Vec<T>::n;
   constexpr int VPL = kSeqChunkBytes / 16 / 32;
   constexpr int EPC = kSeqChunkBytes / static_cast<int>(sizeof(T));
-  const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(T);
-  const int nch = static_cast<int>((row_bytes + kSeqChunkBytes - 1) / kSeqChunkBytes);
-  const char* base = reinterpret_cast<const char*>(lrow);
-  auto chunk_bytes = [&](int ch) -> uint32_t {
-    return static_cast<uint32_t>(min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes));
-  };
-  // this warp's chunks: gwarp, gwarp + W, ...
-  int next = gwarp;
-  if (pp.ok) {
-    for (int s = 0; s < kSeqStages && next < nch; ++s, next += kWarpsPerGroup) {
-      if (lane == 0) pp.issue(base + static_cast<int64_t>(next) * kSeqChunkBytes, chunk_bytes(next), nullptr, 0, 0);
-      ++pp.issued;
-    }
+  // chunk maximum of this lane
+  float mt;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t mm = kNegInfBf16x2;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) mm = bf2max(bf2max(mm, w[j].x), bf2max(bf2max(w[j].y, w[j].z), w[j].w));
+    mt = max_nan(bf16_lo(mm), bf16_hi(mm));
+  } else {
+    mt = -kInf;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      mt = max_nan(mt, max_nan(max_nan(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
+                               max_nan(__uint_as_float(w[j].z), __uint_as_float(w[j].w))));
   }
-  float ml = -kInf, Zl = 0.f;
-  int zl = INT_MAX;
-  // After a bounded wait gives up (never expected) this warp stops copying but keeps
-  // taking part in its group's barriers; the kernel records the failure.
-  for (int ch = gwarp; ch < nch && pp.ok; ch += kWarpsPerGroup) {
-    if (!pp.wait()) {
-      if (lane == 0) atomicOr(error, 1u);
-      pp.ok = false;
-      break;
-    }
-    const int nv = static_cast<int>(chunk_bytes(ch) / 16);
-    const uint4* vb = reinterpret_cast<const uint4*>(pp.stage(pp.k));
-    uint4 w[VPL];
+  if (greedy) {
+    // strictly larger maximum: locate its first index in this chunk (earlier chunks keep ties)
+    if (mt > ml || (mt != mt && ml == ml)) {
+      int idx = INT_MAX;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int v = lane + 32 * j;
-      if (v < nv) {
-        w[j] = vb[v];
-      } else if constexpr (sizeof(T) == 2) {
-        w[j] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
-      } else {
-        const uint32_t ni = __float_as_uint(-kInf);
-        w[j] = make_uint4(ni, ni, ni, ni);
-      }
-    }
-    __syncwarp();
-    ++pp.k;
-    if (next < nch) {  // refill the stage just read with this warp's next chunk
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        pp.issue(base + static_cast<int64_t>(next) * kSeqChunkBytes, chunk_bytes(next), nullptr, 0, 0);
-      }
-      ++pp.issued;
-      next += kWarpsPerGroup;
-    }
-    // chunk maximum of this lane
-    float mt;
-    if constexpr (sizeof(T) == 2) {
-      uint32_t mm = kNegInfBf16x2;
+      for (int j = 0; j < VPL; ++j) {
+        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) mm = bf2max(bf2max(mm, w[j].x), bf2max(bf2max(w[j].y, w[j].z), w[j].w));
-      mt = max_nan(bf16_lo(mm), bf16_hi(mm));
-    } else {
-      mt = -kInf;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        mt = max_nan(mt, max_nan(max_nan(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
-                                 max_nan(__uint_as_float(w[j].z), __uint_as_float(w[j].w))));
-    }
-    if (greedy) {
-      // strictly larger maximum: locate its first index in this chunk (earlier chunks keep ties)
-      if (mt > ml || (mt != mt && ml == ml)) {
-        int idx = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            float v;
-            if constexpr (sizeof(T) == 2) v = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
-            else v = __uint_as_float(ww[e]);
-            if (idx == INT_MAX && v == mt && lane + 32 * j < nv) idx = ch * EPC + (lane + 32 * j) * VEC + e;
-          }
+        for (int e = 0; e < VEC; ++e) {
+          float v;
+          if constexpr (sizeof(T) == 2) v = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
+          else v = __uint_as_float(ww[e]);
+          if (idx == INT_MAX && v == mt && lane + 32 * j < nv) idx = ch * EPC + (lane + 32 * j) * VEC + e;
         }
-        ml = mt;
-        zl = idx;
       }
-    } else {
-      // online softmax: rescale the running sum when the maximum grows
-      const float mn = max_nan(ml, mt);
-      if (mn > -kInf) {
-        if (mn != ml) Zl = (ml > -kInf) ? Zl * ex2((ml - mn) * c) : 0.f;
-        ml = mn;
-        const unsigned long long m2 = f2pack(ml, ml), c2 = f2pack(c, c);
-        unsigned long long acc = f2pack(0.f, 0.f);
+      ml = mt;
+      zl = idx;
+    }
+  } else {
+    // online softmax: rescale the running sum when the maximum grows
+    const float mn = max_nan(ml, mt);
+    if (mn > -kInf) {
+      if (mn != ml) Zl = (ml > -kInf) ? Zl * ex2((ml - mn) * c) : 0.f;
+      ml = mn;
+      const unsigned long long m2 = f2pack(ml, ml), c2 = f2pack(c, c);
+      unsigned long long acc = f2pack(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-          unsigned long long e2[VEC / 2];
+      for (int j = 0; j < VPL; ++j) {
+        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+        unsigned long long e2[VEC / 2];
 #pragma unroll
-          for (int p = 0; p < VEC / 2; ++p) {
-            unsigned long long x2;
-            if constexpr (sizeof(T) == 2) x2 = f2pack(bf16_lo(ww[p]), bf16_hi(ww[p]));
-            else x2 = f2pack(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
-            float y0, y1;
-            f2unpack(f2mul(f2sub(x2, m2), c2), y0, y1);
-            e2[p] = f2pack(ex2(y0), ex2(y1));
-          }
-          unsigned long long vs;
-          if constexpr (VEC == 8) vs = f2add(f2add(e2[0], e2[1]), f2add(e2[2], e2[3]));
-          else vs = f2add(e2[0], e2[1]);
-          acc = f2add(acc, vs);
+        for (int p = 0; p < VEC / 2; ++p) {
+          unsigned long long x2;
+          if constexpr (sizeof(T) == 2) x2 = f2pack(bf16_lo(ww[p]), bf16_hi(ww[p]));
+          else x2 = f2pack(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
+          float y0, y1;
+          f2unpack(f2mul(f2sub(x2, m2), c2), y0, y1);
+          e2[p] = f2pack(ex2(y0), ex2(y1));
         }
-        float a0, a1;
-        f2unpack(acc, a0, a1);
-        Zl += a0 + a1;
-      } else {
-        ml = mn;  // NaN propagates; -inf stays
+        unsigned long long vs;
+        if constexpr (VEC == 8) vs = f2add(f2add(e2[0], e2[1]), f2add(e2[2], e2[3]));
+        else vs = f2add(e2[0], e2[1]);
+        acc = f2add(acc, vs);
       }
+      float a0, a1;
+      f2unpack(acc, a0, a1);
+      Zl += a0 + a1;
+    } else {
+      ml = mn;  // NaN propagates; -inf stays
     }
   }
-  RowSum r;
-  r.m = ml;
-  r.Z = Zl;
-  r.z = zl;
-  r = warp_merge(r, c);
-  if (lane == 0) gs.wsum[gwarp] = r;
-  group_sync(group);
-  if (gwarp == 0) {
-    RowSum t;
-    t.m = -kInf;
-    t.Z = 0.f;
-    t.z = INT_MAX;
-    if (lane < kWarpsPerGroup) t = gs.wsum[lane];
-    t = warp_merge(t, c);
-    if (lane == 0) gs.row = make_float4(t.m, t.Z, __int_as_float(t.z), 0.f);
-  }
-  group_sync(group);
-  const float4 f = gs.row;
-  RowSum out;
-  out.m = f.x;
-  out.Z = f.y;
-  out.z = __float_as_int(f.z);
-  return out;
 }
 
-// ---------------------------------------------------------------------------------
-// The draw over row J: chunk masses (group), then the inverse-CDF search (first warp).
-// ---------------------------------------------------------------------------------
+// fp64 scan of this member's chunk masses (first warp): each lane sums a contiguous run
+// of chunks.  The search repeats exactly this arithmetic, so the member's total and the
+// search's running prefixes agree to the bit.
+struct LocalScan {
+  int c0, c1;
+  double mine, incl, total;
+};
+__device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int lane) {
+  LocalScan s;
+  const int cpl = (n + 31) / 32;
+  s.c0 = min(lane * cpl, n);
+  s.c1 = min(s.c0 + cpl, n);
+  s.mine = 0.0;
+  for (int q = s.c0; q < s.c1; ++q) s.mine += static_cast<double>(mass[q]);
+  s.incl = warp_incl_scan(s.mine, lane);
+  s.total = __shfl_sync(0xffffffffu, s.incl, 31);
+  return s;
+}
+
+// Inverse-CDF search inside this member's part (first warp of the chosen member): the
+// chunk whose running mass (from `base`, the mass of all earlier members) first exceeds
+// `target`, then the element inside it.  If rounding leaves no such element, the last
+// positive-weight element of the part is taken.
 template <typename T>
-__device__ int draw_pass(const ChainParams& P, const T* lrow, const float* qrow, float mJ, float c,
-                         float invZ, float u, Pipe& pp, GroupShared& gs, int group, int gwarp, int lane,
-                         bool& zero_residual, bool& bad_q) {
+__device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, double base, double target,
+                            float mJ, float c, float invZ, bool no_q, const float* mass, int lane) {
   using GL = typename Group<T>::L;
-  constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
   constexpr int GPL = kSeqDrawChunk / 4 / 32;
-  const int V = P.V;
-  const int nchd = (V + kSeqDrawChunk - 1) / kSeqDrawChunk;
-  int next = gwarp;
-  auto issue = [&](int cd) {
-    const int n = min(kSeqDrawChunk, V - cd * kSeqDrawChunk);
-    const int64_t off = static_cast<int64_t>(cd) * kSeqDrawChunk;
-    if (lane == 0)
-      pp.issue(lrow + off, static_cast<uint32_t>(n) * sizeof(T), qrow ? qrow + off : nullptr,
-               qrow ? static_cast<uint32_t>(n) * 4u : 0u, LB);
-    ++pp.issued;
-  };
-  if (pp.ok)
-    for (int s = 0; s < kSeqStages && next < nchd; ++s, next += kWarpsPerGroup) issue(next);
-  float qmx = 0.f, qmn = 0.f;
-  for (int cd = gwarp; cd < nchd && pp.ok; cd += kWarpsPerGroup) {
-    if (!pp.wait()) {
-      if (lane == 0) atomicOr(P.ws.error, 1u);
-      pp.ok = false;
-      break;
-    }
-    const int ng = min(kSeqDrawChunk, V - cd * kSeqDrawChunk) / 4;
-    const unsigned char* sb = pp.stage(pp.k);
-    GL lw[GPL];
-    float4 qv[GPL];
-#pragma unroll
-    for (int j = 0; j < GPL; ++j) {
-      const int g = lane + 32 * j;
-      if (g < ng) {
-        lw[j] = reinterpret_cast<const GL*>(sb)[g];
-        qv[j] = qrow ? reinterpret_cast<const float4*>(sb + LB)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    __syncwarp();
-    ++pp.k;
-    if (next < nchd) {
-      if (lane == 0) fence_proxy_async_smem();
-      issue(next);
-      next += kWarpsPerGroup;
-    }
-    float sr = 0.f;
-#pragma unroll
-    for (int j = 0; j < GPL; ++j) {
-      if (lane + 32 * j < ng) {
-        float w[4];
-        sr += group_weights<T>(lw[j], qv[j], mJ, c, invZ, qrow == nullptr, w);
-        qmx = max_nan(qmx, max_nan(max_nan(qv[j].x, qv[j].y), max_nan(qv[j].z, qv[j].w)));
-        qmn = fminf(qmn, fminf(fminf(qv[j].x, qv[j].y), fminf(qv[j].z, qv[j].w)));
-      }
-    }
-    sr = warp_sum(sr);
-    if (lane == 0) gs.mass[cd] = sr;
+  const LocalScan s = local_scan(mass, n, lane);
+  int cstar = -1, lastpos = -1;
+  double cbase = 0.0, prelast = 0.0, pre = base + (s.incl - s.mine);
+  for (int q = s.c0; q < s.c1; ++q) {
+    const double w = static_cast<double>(mass[q]);
+    if (w > 0.0) { lastpos = q; prelast = pre; }
+    if (cstar < 0 && pre + w > target) { cstar = q; cbase = pre; }
+    pre += w;
   }
-  const bool mybad = !(qmx < kInf) || qmn < 0.f;
-  if (lane == 0 && gwarp == 0) gs.qbad = 0;
-  group_sync(group);
-  if (__any_sync(0xffffffffu, mybad) && lane == 0) atomicOr(&gs.qbad, 1);
-  group_sync(group);
-  bad_q = gs.qbad != 0;
-  zero_residual = false;
-  if (bad_q) return -1;
-
-  // total residual mass; zero (possible only through rounding) falls back to p itself
-  if (gwarp == 0) {
-    double tot = 0.0;
-    for (int q = lane; q < nchd; q += 32) tot += static_cast<double>(gs.mass[q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if (lane == 0) gs.stop = !(tot > 0.0);
+  const unsigned hit = __ballot_sync(0xffffffffu, cstar >= 0);
+  if (hit) {
+    const int fl = __ffs(hit) - 1;
+    cstar = __shfl_sync(0xffffffffu, cstar, fl);
+    cbase = __shfl_sync(0xffffffffu, cbase, fl);
+  } else {  // rounding put u * S at or past the end of the part: last chunk with mass
+    const int best = warp_max_int(lastpos);
+    const unsigned owner = __ballot_sync(0xffffffffu, lastpos == best && best >= 0);
+    cstar = best < 0 ? 0 : best;
+    cbase = owner ? __shfl_sync(0xffffffffu, prelast, __ffs(owner) - 1) : base;
   }
-  group_sync(group);
-  zero_residual = gs.stop != 0;
-  if (zero_residual) {
-    for (int cd = gwarp; cd < nchd; cd += kWarpsPerGroup) {  // rare: masses of p itself
-      const int ng = min(kSeqDrawChunk, V - cd * kSeqDrawChunk) / 4;
-      float sr = 0.f;
-      for (int g = lane; g < ng; g += 32) {
-        float w[4];
-        sr += group_weights<T>(__ldg(reinterpret_cast<const GL*>(lrow + static_cast<int64_t>(cd) * kSeqDrawChunk) + g),
-                               make_float4(0.f, 0.f, 0.f, 0.f), mJ, c, invZ, true, w);
-      }
-      sr = warp_sum(sr);
-      if (lane == 0) gs.mass[cd] = sr;
+  const int k0 = (d0 + cstar) * kSeqDrawChunk;
+  const int ng = min(kSeqDrawChunk, V - k0) / 4;
+  float w[GPL][4], gsum[GPL];
+  double lane_tot = 0.0;
+#pragma unroll
+  for (int j = 0; j < GPL; ++j) {
+    const int g = lane * GPL + j;
+    gsum[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[j][e] = 0.f;
+    if (g < ng) {
+      const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
+      const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
+      gsum[j] = group_weights<T>(lw, q4, mJ, c, invZ, no_q, w[j]);
+      lane_tot += static_cast<double>(gsum[j]);
     }
-    group_sync(group);
   }
-  const bool no_q = zero_residual || qrow == nullptr;
-
-  // inverse CDF: chunk by fp64 prefix, then an index-order scan inside the chunk
-  if (gwarp == 0) {
-    const int cpl = (nchd + 31) / 32;
-    const int c0 = min(lane * cpl, nchd), c1 = min(c0 + cpl, nchd);
-    double mine = 0.0;
-    for (int q = c0; q < c1; ++q) mine += static_cast<double>(gs.mass[q]);
-    const double incl = warp_incl_scan(mine, lane);
-    const double S = __shfl_sync(0xffffffffu, incl, 31);
-    const double target = static_cast<double>(u) * S;
-    int cstar = -1, lastpos = -1;
-    double base = 0.0, prelast = 0.0, pre = incl - mine;
-    for (int q = c0; q < c1; ++q) {
-      const double w = static_cast<double>(gs.mass[q]);
-      if (w > 0.0) { lastpos = q; prelast = pre; }
-      if (cstar < 0 && pre + w > target) { cstar = q; base = pre; }
-      pre += w;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, cstar >= 0);
-    if (hit) {
-      const int fl = __ffs(hit) - 1;
-      cstar = __shfl_sync(0xffffffffu, cstar, fl);
-      base = __shfl_sync(0xffffffffu, base, fl);
-    } else {  // rounding put u * S at or past the end: last chunk with mass
-      const int best = warp_max_int(lastpos);
-      const unsigned owner = __ballot_sync(0xffffffffu, lastpos == best && best >= 0);
-      cstar = best < 0 ? 0 : best;
-      base = owner ? __shfl_sync(0xffffffffu, prelast, __ffs(owner) - 1) : 0.0;
-    }
-    const int k0 = cstar * kSeqDrawChunk;
-    const int ng = min(kSeqDrawChunk, V - k0) / 4;
-    float w[GPL][4], gsum[GPL];
-    double lane_tot = 0.0;
+  int last_pos = -1;
 #pragma unroll
-    for (int j = 0; j < GPL; ++j) {
-      const int g = lane * GPL + j;
-      gsum[j] = 0.f;
+  for (int j = 0; j < GPL; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) w[j][e] = 0.f;
-      if (g < ng) {
-        const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
-        const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
-        gsum[j] = group_weights<T>(lw, q4, mJ, c, invZ, no_q, w[j]);
-        lane_tot += static_cast<double>(gsum[j]);
-      }
-    }
-    int last_pos = -1;
+    for (int e = 0; e < 4; ++e)
+      if (w[j][e] > 0.f) last_pos = k0 + 4 * (lane * GPL + j) + e;
+  const double gincl = warp_incl_scan(lane_tot, lane);
+  const unsigned ghit = __ballot_sync(0xffffffffu, cbase + gincl > target);
+  int y = -1;
+  if (ghit) {
+    const int fl = __ffs(ghit) - 1;
+    if (lane == fl) {
+      double p2 = cbase + (gincl - lane_tot);
 #pragma unroll
-    for (int j = 0; j < GPL; ++j)
+      for (int j = 0; j < GPL; ++j) {
+        if (y < 0 && p2 + static_cast<double>(gsum[j]) > target) {
+          float run = 0.f;
+          int lastp = -1;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (w[j][e] > 0.f) last_pos = k0 + 4 * (lane * GPL + j) + e;
-    const double gincl = warp_incl_scan(lane_tot, lane);
-    const unsigned ghit = __ballot_sync(0xffffffffu, base + gincl > target);
-    int y = -1;
-    if (ghit) {
-      const int fl = __ffs(ghit) - 1;
-      if (lane == fl) {
-        double p2 = base + (gincl - lane_tot);
-#pragma unroll
-        for (int j = 0; j < GPL; ++j) {
-          if (y < 0 && p2 + static_cast<double>(gsum[j]) > target) {
-            float run = 0.f;
-            int lastp = -1;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              run += w[j][e];
-              if (w[j][e] > 0.f) lastp = k0 + 4 * (lane * GPL + j) + e;
-              if (y < 0 && p2 + static_cast<double>(run) > target) y = k0 + 4 * (lane * GPL + j) + e;
-            }
-            if (y < 0) y = lastp;
+          for (int e = 0; e < 4; ++e) {
+            run += w[j][e];
+            if (w[j][e] > 0.f) lastp = k0 + 4 * (lane * GPL + j) + e;
+            if (y < 0 && p2 + static_cast<double>(run) > target) y = k0 + 4 * (lane * GPL + j) + e;
           }
-          p2 += static_cast<double>(gsum[j]);
+          if (y < 0) y = lastp;
         }
+        p2 += static_cast<double>(gsum[j]);
       }
-      y = __shfl_sync(0xffffffffu, y, fl);
     }
-    if (y < 0) y = warp_max_int(last_pos);
-    if (lane == 0) gs.y = y;
+    y = __shfl_sync(0xffffffffu, y, fl);
   }
-  group_sync(group);
-  return gs.y;
+  if (y < 0) y = warp_max_int(last_pos);
+  return y;
+}
+
+// A member's draw total (fp64), a flag and the leader's unclaimed sequence as one 16-byte
+// exchange payload.
+__device__ __forceinline__ float4 pack_total(double t, int flag, int bn) {
+  const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(t));
+  return make_float4(__uint_as_float(static_cast<uint32_t>(bits)), __uint_as_float(static_cast<uint32_t>(bits >> 32)),
+                     __int_as_float(flag), __int_as_float(bn));
+}
+__device__ __forceinline__ double unpack_total(const float4& v) {
+  const unsigned long long bits = static_cast<unsigned long long>(__float_as_uint(v.x)) |
+                                  (static_cast<unsigned long long>(__float_as_uint(v.y)) << 32);
+  return __longlong_as_double(static_cast<long long>(bits));
 }
 
 // ---------------------------------------------------------------------------------
@@ -497,6 +560,10 @@ __device__ int draw_pass(const ChainParams& P, const T* lrow, const float* qrow,
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const ChainParams P) {
+  using GL = typename Group<T>::L;
+  constexpr int VPL = kSeqChunkBytes / 16 / 32;
+  constexpr int GPL = kSeqDrawChunk / 4 / 32;
+  constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kSeqWarps][kSeqStages];
   __shared__ GroupShared gshared[kSeqGroups];
@@ -506,166 +573,516 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   Pipe pp;
   pp.buf = smem + static_cast<size_t>(warp) * kSeqStages * kSeqChunkBytes;
   pp.bar = bars[warp];
+  // Launched without the cluster shape this code maps addresses for: touch nothing.
+  if (cluster_size() != static_cast<uint32_t>(kC)) {
+    if (threadIdx.x == 0) atomicOr(P.ws.error, 4u);
+    return;
+  }
+  Team tm;
+  tm.rank = cluster_rank();
+  const bool first = gwarp == 0 && lane == 0;  // this member's first thread
+  const bool leader = tm.rank == 0 && first;   // the team's first thread
   if (lane == 0) {
     for (int s = 0; s < kSeqStages; ++s) mbar_init(&pp.bar[s], 1);
+    if (gwarp == 0) {
+      mbar_init(&gs.xbar[0], 1);
+      mbar_init(&gs.xbar[1], 1);
+      mbar_init(&gs.mbar_box[0], 1);
+      mbar_init(&gs.mbar_box[1], 1);
+    }
     mbar_fence_init();
   }
-  __syncwarp();
+  // Every member's barriers exist before any member writes into another's shared memory.
+  cluster_sync_all();
+
   const int R = P.gamma + 1;
+  const int V = P.V;
+  const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(T);
+  const int nch = static_cast<int>((row_bytes + kSeqChunkBytes - 1) / kSeqChunkBytes);
+  const int nchd = (V + kSeqDrawChunk - 1) / kSeqDrawChunk;
+  const int c0 = static_cast<int>(static_cast<int64_t>(nch) * tm.rank / kC);
+  const int c1 = static_cast<int>(static_cast<int64_t>(nch) * (tm.rank + 1) / kC);
+  const int d0 = static_cast<int>(static_cast<int64_t>(nchd) * tm.rank / kC);
+  const int d1 = static_cast<int>(static_cast<int64_t>(nchd) * (tm.rank + 1) / kC);
+  const char* logits = static_cast<const char*>(P.logits);
+  Queue qu;
+  qu.start_ticket = P.ws.queue;
+  qu.pub_draws = P.ws.queue + 1;
+  qu.draw_ticket = P.ws.queue + 2;
+  qu.finished = P.ws.queue + 3;
+  qu.ready_draws = P.ws.ready;
+  qu.ring_draws = P.ws.ring;
+  qu.B = P.B;
 
-  for (;;) {
-    if (threadIdx.x % kGroupThreads == 0) gs.b = static_cast<int>(atomicAdd(P.ws.draw_count, 1u));
-    group_sync(group);
-    const int b = gs.b;
-    if (b >= P.B) break;
-    const float Tb = P.greedy_only ? 0.f : __ldg(P.temps + b);
-    const bool greedy = P.greedy_only || is_greedy(Tb);
-    const float c = greedy ? 0.f : kLog2e / Tb;
-    const bool bad_T = !P.greedy_only && !(Tb - Tb == 0.f);
+  auto make_task = [&](const Entry& e) {
+    Task t;
+    t.kind = e.kind;
+    t.src = logits + (static_cast<int64_t>(e.b) * R + e.row) * row_bytes;
+    t.q = (e.kind == kTaskDraw && e.row < P.gamma) ? P.q + (static_cast<int64_t>(e.b) * P.gamma + e.row) * V : nullptr;
+    t.lo = (e.kind == kTaskRow) ? c0 : d0;
+    t.hi = (e.kind == kTaskRow) ? c1 : d1;
+    t.n = (t.hi > t.lo + gwarp) ? (t.hi - t.lo - gwarp + kWarpsPerGroup - 1) / kWarpsPerGroup : 0;
+    return t;
+  };
+  auto no_more = []() {
+    float4 e0, e1;
+    Entry e{};
+    e.b = -1;
+    pack_entry(e, e0, e1);
+    return e0;
+  };
 
-    // The group's first warp holds position i in lane i: its draft, the logit and q at
-    // the draft, and its uniform (lane gamma: the draw's uniform), fetched up front.
-    int x = -1, tok_err = 0, qu_err = 0;
-    float lx = 0.f, qx = 0.f, ux = 0.f, px = kNaN;
-    if (gwarp == 0) {
-      if (lane < P.gamma) {
-        x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane);
-        if (x < 0 || x >= P.V) {
-          tok_err = SPECDEC_STATUS_BAD_TOKEN;
-        } else if (!greedy) {
-          lx = Elem<T>::load(static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + lane) * P.V, x);
-          qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + lane) * P.V + x);
-          if (!(qx >= 0.f && qx < kInf)) qu_err |= SPECDEC_STATUS_BAD_PROB;
+  // Mailbox protocol: each use u is armed by every member (expect 32 bytes) and filled by
+  // exactly one send from the leader.  `box` marks a use armed but not yet read.
+  uint32_t mb = 0;
+  bool box = false;
+  int tk = -1;           // leader: the ticket behind the armed use
+  bool tk_sent = false;  // leader: its entry has been sent
+  auto arm_box = [&]() {
+    box = true;
+    if (first) mbar_expect_tx(&gs.mbar_box[mb & 1u], 32);
+    if (leader) {
+      tk = take_ticket(qu);
+      tk_sent = false;
+    }
+  };
+  auto try_send = [&](bool blocking) {
+    if (leader && box && !tk_sent) {
+      float4 e0, e1 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int r = resolve_ticket(P, qu, tk, blocking, e0, e1);
+      if (r != 0) {
+        if (r < 0) {
+          if (r == -2) atomicOr(P.ws.error, 8u);
+          e0 = no_more();
+        }
+        send_entry(gs, static_cast<int>(mb & 1u), e0, e1);
+        tk_sent = true;
+      }
+    }
+  };
+  // the team's next task through the mailbox (every thread)
+  auto take_box = [&]() {
+    if (!box) arm_box();
+    try_send(true);
+    __syncwarp();
+    if (group_any(group, !mbar_wait_cluster(&gs.mbar_box[mb & 1u], (mb >> 1) & 1u))) {
+      if (first) atomicOr(P.ws.error, 2u);
+      tm.ok = false;
+    }
+    const Entry e = unpack_entry(gs.mbox[mb & 1u][0], gs.mbox[mb & 1u][1]);
+    ++mb;
+    box = false;
+    return e;
+  };
+
+  Entry cur = take_box();
+  uint32_t t = 0;                // tasks done by this team
+  int pre = 0;                   // jobs of the next row this warp already issued
+  int pre_b = -1, pre_row = -1;  // and which row that is
+  // a drawn token still to be found by this member's first warp (at the next task's start)
+  bool srch = false;
+  int s_b = 0, s_J = 0, s_par = 0;
+  double s_base = 0.0, s_target = 0.0;
+  float s_m = 0.f, s_c = 0.f, s_invZ = 1.f;
+  bool s_noq = true;
+
+  while (cur.b >= 0 && tm.ok) {
+    const int par = static_cast<int>(t & 1u);
+    // the previous task's draw, if this member holds u * S (its masses stay put until the
+    // barrier at the end of this task's chunks)
+    if (srch && gwarp == 0) {
+      const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
+      const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
+      const int y = local_search<T>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
+                                    gs.mass[s_par], lane);
+      if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
+    }
+    srch = false;
+
+    const int b = cur.b, ri = cur.row, kind = cur.kind;
+    const float Tc = cur.T;
+    const bool greedy = P.greedy_only || is_greedy(Tc);
+    const float c = greedy ? 0.f : kLog2e / Tc;
+    const Task tc = make_task(cur);
+
+    // This task's inputs (first thread): the draft and the uniforms now, the logit and q at
+    // the draft once the draft has arrived.
+    const bool at_draft = kind == kTaskRow && ri < P.gamma;
+    int gx = -1;
+    float gu = 0.f, gug = 0.f, glx = 0.f, gqx = 0.f;
+    bool g2 = false;
+    if (first) {
+      if (at_draft) gx = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + ri);
+      if (!P.greedy_only) {
+        if (at_draft) gu = __ldg(P.u + static_cast<int64_t>(b) * R + ri);
+        gug = __ldg(P.u + static_cast<int64_t>(b) * R + P.gamma);
+      }
+    }
+    auto gather2 = [&]() {
+      if (first && !g2) {
+        g2 = true;
+        if (at_draft && !P.greedy_only && gx >= 0 && gx < V) {
+          glx = Elem<T>::load(reinterpret_cast<const T*>(tc.src), gx);
+          gqx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + ri) * V + gx);
         }
       }
-      if (!greedy && lane < R) ux = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
-      if (!greedy && lane < P.gamma && !(ux >= 0.f && ux < 1.f)) qu_err |= SPECDEC_STATUS_BAD_UNIFORM;
-    }
+    };
 
-    // rows in order until the first error or rejection
-    int J = -1, st = bad_T ? SPECDEC_STATUS_BAD_TEMPERATURE : 0, warn = 0;
-    RowSum rs;
-    rs.m = 0.f;
-    rs.Z = 1.f;
-    rs.z = 0;
-    if (!bad_T) {
-      for (int i = 0; i < R; ++i) {
-        rs = row_pass<T>(static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + i) * P.V, P.V, greedy, c,
-                         pp, gs, group, gwarp, lane, P.ws.error);
-        if (gwarp == 0) {
-          int err = 0;
-          if (!(rs.m == rs.m) || rs.m == kInf) err = SPECDEC_STATUS_BAD_LOGIT;
-          else if (rs.m == -kInf) err = SPECDEC_STATUS_EMPTY_ROW;
-          else if (i < P.gamma) err = __shfl_sync(0xffffffffu, tok_err ? tok_err : qu_err, i);
-          int stop = 0;
-          if (err) {
-            st |= err;
-            stop = 2;
-          } else if (i == P.gamma) {
-            stop = 1;
-          } else {
-            bool acc = false;
-            float pxi = kNaN;
-            if (lane == i) {
-              if (greedy) {
-                acc = (x == rs.z);
-              } else {
-                pxi = ex2((lx - rs.m) * c) / rs.Z;
-                if (qx == 0.f) {
-                  warn |= SPECDEC_STATUS_ZERO_Q;
-                  acc = pxi > 0.f;
-                } else {
-                  acc = ux * qx < pxi;
-                }
-                px = pxi;
-              }
-            }
-            stop = __shfl_sync(0xffffffffu, acc ? 0 : 1, i);
-          }
-          if (lane == 0) gs.stop = stop;
+    // This task's copies first, then, during a row of a chain, the next row's: the round
+    // goes on there whenever draft i is accepted.  Jobs copied ahead for a row that did
+    // not come are drained and dropped.
+    int ci = 0, ni = 0;
+    if (kind == kTaskRow && b == pre_b && ri == pre_row) {
+      ci = pre;
+    } else {
+      for (int j = 0; j < pre && pp.ok; ++j) {
+        if (!pp.wait()) {
+          if (lane == 0) atomicOr(P.ws.error, 1u);
+          pp.ok = false;
         }
-        group_sync(group);
-        const int stop = gs.stop;
-        if (stop) {
-          J = (stop == 2) ? -1 : i;  // -1: an error ended the round
+        ++pp.k;
+      }
+      __syncwarp();
+    }
+    Task tn;
+    if (kSpecRows && kind == kTaskRow && ri < P.gamma) {
+      Entry e = cur;
+      e.row = ri + 1;
+      tn = make_task(e);
+    }
+    auto refill = [&]() {
+      if (!pp.ok) return;
+      if (ci < tc.n) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+      else if (ni < tn.n) issue_job<T>(pp, tn, ni++, gwarp, lane, V, row_bytes);
+    };
+    auto top_up = [&]() {
+      while (pp.ok && pp.in_flight() < kSeqStages && ni < tn.n) issue_job<T>(pp, tn, ni++, gwarp, lane, V, row_bytes);
+    };
+    while (pp.ok && ci < tc.n && pp.in_flight() < kSeqStages) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+
+    float4 mine;
+    if (kind == kTaskRow) {
+      float ml = -kInf, Zl = 0.f;
+      int zl = INT_MAX;
+      for (int j = 0; j < tc.n && pp.ok; ++j) {
+        if (!pp.wait()) {
+          if (lane == 0) atomicOr(P.ws.error, 1u);
+          pp.ok = false;
           break;
         }
-        group_sync(group);  // gs.stop is rewritten by the next row's decision
+        const int ch = c0 + gwarp + j * kWarpsPerGroup;
+        const int nv = static_cast<int>(
+            min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes) / 16);
+        const uint4* vb = reinterpret_cast<const uint4*>(pp.stage(pp.k));
+        uint4 w[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          const int e = lane + 32 * v;
+          if (e < nv) {
+            w[v] = vb[e];
+          } else if constexpr (sizeof(T) == 2) {
+            w[v] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+          } else {
+            const uint32_t nf = __float_as_uint(-kInf);
+            w[v] = make_uint4(nf, nf, nf, nf);
+          }
+        }
+        __syncwarp();
+        ++pp.k;
+        refill();
+        row_chunk<T>(w, nv, ch, greedy, c, lane, ml, Zl, zl);
+        gather2();
       }
-    }
-    if (gwarp == 0) {
-      warn = __reduce_or_sync(0xffffffffu, warn);
-      st = __reduce_or_sync(0xffffffffu, st) | warn;
-    }
-    int y = -1;
-    bool failed = bad_T || J < 0;
-    if (!failed && !greedy) {
-      const float uG = __shfl_sync(0xffffffffu, ux, P.gamma);  // meaningful in the first warp
-      if (gwarp == 0 && lane == 0) gs.row.w = uG;
+      gather2();
+      top_up();
+      RowSum r;
+      r.m = ml;
+      r.Z = Zl;
+      r.z = zl;
+      r = warp_merge(r, c);
+      if (lane == 0) gs.wsum[gwarp] = r;
       group_sync(group);
-      const float ud = gs.row.w;
-      if (!(ud >= 0.f && ud < 1.f)) {
-        st |= SPECDEC_STATUS_BAD_UNIFORM;
-        failed = true;
-      } else {
-        const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
-        const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
-        bool zr = false, bq = false;
-        y = draw_pass<T>(P, lrow, qrow, rs.m, c, 1.f / rs.Z, ud, pp, gs, group, gwarp, lane, zr, bq);
-        if (bq) {
-          st |= SPECDEC_STATUS_BAD_PROB;
-          failed = true;
-        } else if (zr) {
-          st |= SPECDEC_STATUS_ZERO_RESIDUAL;
+      RowSum s;
+      s.m = -kInf;
+      s.Z = 0.f;
+      s.z = INT_MAX;
+      if (gwarp == 0) {
+        if (lane < kWarpsPerGroup) s = gs.wsum[lane];
+        s = warp_merge(s, c);
+      }
+      mine = make_float4(s.m, s.Z, __int_as_float(s.z), 0.f);
+    } else {
+      const float mJ = cur.m, invZ = 1.f / cur.Z;
+      const bool with_q = tc.q != nullptr;
+      float qmx = 0.f, qmn = 0.f;
+      for (int j = 0; j < tc.n && pp.ok; ++j) {
+        if (!pp.wait()) {
+          if (lane == 0) atomicOr(P.ws.error, 1u);
+          pp.ok = false;
+          break;
+        }
+        const int cd = d0 + gwarp + j * kWarpsPerGroup;
+        const int ng = min(kSeqDrawChunk, V - cd * kSeqDrawChunk) / 4;
+        const unsigned char* sbuf = pp.stage(pp.k);
+        GL lw[GPL];
+        float4 qv[GPL];
+#pragma unroll
+        for (int v = 0; v < GPL; ++v) {
+          const int g = lane + 32 * v;
+          if (g < ng) {
+            lw[v] = reinterpret_cast<const GL*>(sbuf)[g];
+            qv[v] = with_q ? reinterpret_cast<const float4*>(sbuf + LB)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        __syncwarp();
+        ++pp.k;
+        refill();
+        float sr = 0.f;
+#pragma unroll
+        for (int v = 0; v < GPL; ++v) {
+          if (lane + 32 * v < ng) {
+            float w4[4];
+            sr += group_weights<T>(lw[v], qv[v], mJ, c, invZ, !with_q, w4);
+            qmx = max_nan(qmx, max_nan(max_nan(qv[v].x, qv[v].y), max_nan(qv[v].z, qv[v].w)));
+            qmn = fminf(qmn, fminf(fminf(qv[v].x, qv[v].y), fminf(qv[v].z, qv[v].w)));
+          }
+        }
+        sr = warp_sum(sr);
+        if (lane == 0) gs.mass[par][cd - d0] = sr;
+      }
+      top_up();
+      const bool qbad = group_any(group, !(qmx < kInf) || qmn < 0.f);  // also: every chunk mass is in place
+      double tot = 0.0;
+      if (gwarp == 0) tot = local_scan(gs.mass[par], d1 - d0, lane).total;
+      mine = pack_total(tot, qbad ? 1 : 0, 0);
+    }
+    if (first) {  // this task's inputs for the decision
+      int err = 0;
+      if (at_draft) {
+        if (gx < 0 || gx >= V) {
+          err = SPECDEC_STATUS_BAD_TOKEN;
+        } else if (!greedy) {
+          if (!(gqx >= 0.f && gqx < kInf)) err |= SPECDEC_STATUS_BAD_PROB;
+          if (!(gu >= 0.f && gu < 1.f)) err |= SPECDEC_STATUS_BAD_UNIFORM;
         }
       }
-    } else if (!failed) {
-      y = rs.z;
+      float* g = gs.gq[par];
+      g[0] = __int_as_float(gx);
+      g[1] = glx;
+      g[2] = gqx;
+      g[3] = gu;
+      g[4] = gug;
+      g[5] = __int_as_float(err);
     }
+    __syncwarp();
+    pre = ni;
+    pre_b = b;
+    pre_row = ri + 1;
+    const int xp = exchange(gs, tm, mine, group, gwarp, lane, P.ws.error);
 
-    if (gwarp == 0) {
+    // The decision, taken by every thread on the same inputs.
+    const float* g = gs.gq[par];
+    int warn = cur.warn;  // status bits above the error byte, >> 8
+    bool done = false, failed = false, drawn = false;
+    int J = -1, y = -1, st = 0;
+    bool nxt_local = false;  // the next task stays with this team (next row, second draw pass)
+    Entry nxt = cur;
+    if (kind == kTaskRow) {
+      RowSum rs;
+      {
+        const float4 s0 = gs.slot[xp][0];
+        rs.m = s0.x;
+        rs.Z = s0.y;
+        rs.z = __float_as_int(s0.z);
+      }
+#pragma unroll
+      for (int r = 1; r < kC; ++r) {
+        const float4 sr = gs.slot[xp][r];
+        RowSum o;
+        o.m = sr.x;
+        o.Z = sr.y;
+        o.z = __float_as_int(sr.z);
+        rs = merge(rs, o, c);
+      }
+      int err = 0;
+      if (!P.greedy_only && !(Tc - Tc == 0.f)) err = SPECDEC_STATUS_BAD_TEMPERATURE;
+      else if (!(rs.m == rs.m) || rs.m == kInf) err = SPECDEC_STATUS_BAD_LOGIT;
+      else if (rs.m == -kInf) err = SPECDEC_STATUS_EMPTY_ROW;
+      else if (at_draft) err = __float_as_int(g[5]);
+      if (err) {
+        st = err;
+        done = failed = true;
+      } else {
+        bool acc = false;
+        float pxi = kNaN;
+        const int xi = __float_as_int(g[0]);
+        if (at_draft) {
+          if (greedy) {
+            acc = (xi == rs.z);
+          } else {
+            pxi = ex2((g[1] - rs.m) * c) / rs.Z;
+            if (g[2] == 0.f) {
+              warn |= SPECDEC_STATUS_ZERO_Q >> 8;
+              acc = pxi > 0.f;
+            } else {
+              acc = g[3] * g[2] < pxi;
+            }
+          }
+        }
+        if (at_draft && leader && P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + ri] = pxi;
+        if (acc) {
+          if (leader) P.out_tokens[static_cast<int64_t>(b) * R + ri] = xi;
+          nxt_local = true;
+          nxt.b = b;
+          nxt.row = ri + 1;
+          nxt.kind = kTaskRow;
+          nxt.warn = warn;
+          nxt.m = 0.f;
+          nxt.Z = 1.f;
+          nxt.T = Tc;
+        } else {  // rejection at ri, or row gamma: the extra token comes from row ri
+          J = ri;
+          if (greedy) {
+            y = rs.z;
+            done = true;
+          } else if (!(g[4] >= 0.f && g[4] < 1.f)) {
+            st = SPECDEC_STATUS_BAD_UNIFORM;
+            done = failed = true;
+          } else if (leader) {
+            Entry e;
+            e.b = b;
+            e.row = ri;
+            e.kind = kTaskDraw;
+            e.warn = warn;
+            e.m = rs.m;
+            e.Z = rs.Z;
+            e.T = Tc;
+            publish_draw(qu, e);
+          }
+        }
+      }
+    } else {  // the members' totals of the drawn row
+      J = ri;
+      double S = 0.0;
+      bool anybad = false;
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        S += unpack_total(gs.slot[xp][r]);
+        anybad |= __float_as_int(gs.slot[xp][r].z) != 0;
+      }
+      if (kind == kTaskDraw && anybad) {
+        st = SPECDEC_STATUS_BAD_PROB;
+        done = failed = true;
+      } else if (kind == kTaskDraw && !(S > 0.0)) {
+        // zero total residual (possible only through rounding): draw from p itself
+        nxt_local = true;
+        nxt = cur;
+        nxt.kind = kTaskDrawP;
+        nxt.warn = warn | (SPECDEC_STATUS_ZERO_RESIDUAL >> 8);
+      } else {
+        // the member whose part holds u * S (else the last member with mass) finds y
+        const double target = static_cast<double>(g[4]) * S;
+        int rstar = -1, rlast = 0;
+        double base = 0.0, run = 0.0, baselast = 0.0;
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+          const double tt = unpack_total(gs.slot[xp][r]);
+          if (tt > 0.0) { rlast = r; baselast = run; }
+          if (rstar < 0 && tt > 0.0 && run + tt > target) { rstar = r; base = run; }
+          run += tt;
+        }
+        if (rstar < 0) { rstar = rlast; base = baselast; }
+        if (static_cast<int>(tm.rank) == rstar) {
+          srch = true;
+          s_b = b;
+          s_J = J;
+          s_par = par;
+          s_base = base;
+          s_target = target;
+          s_m = cur.m;
+          s_c = c;
+          s_invZ = 1.f / cur.Z;
+          s_noq = kind == kTaskDrawP || tc.q == nullptr;
+        }
+        done = drawn = true;
+      }
+    }
+    if (done && tm.rank == 0 && gwarp == 0) {
+      // outputs of a finished sequence (the drawn token is written by the member that finds it)
       const int Jo = failed ? -1 : J;
       if (lane < R) {
-        int tok = -1;
-        if (Jo >= 0) {
-          if (lane < Jo) tok = x;
-          else if (lane == Jo) tok = y;
-        }
-        P.out_tokens[static_cast<int64_t>(b) * R + lane] = tok;
+        if (failed || lane > Jo) P.out_tokens[static_cast<int64_t>(b) * R + lane] = -1;
+        else if (lane == Jo && !drawn) P.out_tokens[static_cast<int64_t>(b) * R + lane] = y;
       }
-      if (lane < P.gamma && P.out_p_draft)
-        P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = (!failed && lane <= Jo) ? px : kNaN;
+      if (lane < P.gamma && P.out_p_draft && (failed || lane > Jo || (greedy && lane >= Jo)))
+        P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = kNaN;
       if (lane == 0) {
         P.out_J[b] = Jo;
-        if (P.out_status) P.out_status[b] = failed && bad_T ? SPECDEC_STATUS_BAD_TEMPERATURE : st;
+        if (P.out_status) P.out_status[b] = st | (warn << 8);
+        atomicAdd(qu.finished, 1u);
       }
     }
-    group_sync(group);
+    // the next task: this sequence's next step, or new work through the mailbox
+    cur = nxt_local ? nxt : take_box();
+    ++t;
   }
-  // Copies still in flight after a bounded wait gave up: wait (bounded) before exiting.
-  if (!pp.ok && lane == 0)
+  // a draw found in the last task
+  if (srch && gwarp == 0 && tm.ok) {
+    const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
+    const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
+    const int y = local_search<T>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
+                                  gs.mass[s_par], lane);
+    if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
+  }
+  // Copies still in flight (left by a bounded wait that gave up): wait for them, bounded,
+  // before the CTA exits.
+  if (lane == 0)
     for (; pp.k < pp.issued; ++pp.k) mbar_wait(pp.sbar(pp.k), (pp.k / kSeqStages) & 1u);
+  // No CTA leaves while another member may still write into its shared memory.
+  cluster_sync_all();
+}
+
+template <typename T>
+cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
+  constexpr int smem = kSeqWarps * kSeqStages * kSeqChunkBytes;
+  static unsigned long long configured = 0;
+  static int max_clusters[64] = {};
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kSeqWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!(configured & bit)) {
+    if (cudaError_t e = cudaFuncSetAttribute(chain_seq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e != cudaSuccess)
+      return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(kC * device_sm_count()));
+    int n = 0;
+    if (cudaError_t e = cudaOccupancyMaxActiveClusters(&n, chain_seq_kernel<T>, &cfg); e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev & 63] = n;
+    configured |= bit;
+  }
+  const int want = (P.B + kSeqGroups - 1) / kSeqGroups;
+  const int clusters = min(max_clusters[dev & 63], want);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kC));
+  return cudaLaunchKernelEx(&cfg, chain_seq_kernel<T>, P);
 }
 
 }  // namespace
 
 cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
-  constexpr int smem = kSeqWarps * kSeqStages * kSeqChunkBytes;
-  static unsigned long long configured_bf16 = 0, configured_f32 = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const unsigned long long bit = 1ull << (dev & 63);
-  const void* kern = (ldt == SPECDEC_BF16) ? reinterpret_cast<const void*>(chain_seq_kernel<uint16_t>)
-                                           : reinterpret_cast<const void*>(chain_seq_kernel<float>);
-  unsigned long long& configured = (ldt == SPECDEC_BF16) ? configured_bf16 : configured_f32;
-  if (!(configured & bit)) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
-  const dim3 grid(P.grid_stats), block(kSeqWarps * 32);
-  if (ldt == SPECDEC_BF16) return launch_kernel(chain_seq_kernel<uint16_t>, grid, block, smem, stream, 0, P);
-  return launch_kernel(chain_seq_kernel<float>, grid, block, smem, stream, 0, P);
+  if (ldt == SPECDEC_BF16) return launch_typed<uint16_t>(P, stream);
+  return launch_typed<float>(P, stream);
 }
 
 }  // namespace specdec

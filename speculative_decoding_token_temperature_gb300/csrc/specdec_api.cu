@@ -101,10 +101,14 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     n_part = rows * nseg;
     draw_bytes = static_cast<int64_t>(B) * nseg * static_cast<int64_t>(sizeof(double2));
   }
+  // queue entries of the left-to-right kernel (streaming layout only)
+  const int64_t n_entries = path == 2 ? static_cast<int64_t>(B) * g + 2 * static_cast<int64_t>(B) : 0;
+  const int64_t n_counters = std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries);
   size_t off = 0;
   const size_t o_error = off;    off += kAlign;
-  const size_t o_counters = off; off += round_up(sizeof(unsigned) * 2 * static_cast<size_t>(B));
+  const size_t o_counters = off; off += round_up(sizeof(unsigned) * static_cast<size_t>(n_counters));
   const size_t counters_end = off;
+  const size_t o_ring = off;     off += round_up(2 * sizeof(float4) * static_cast<size_t>(n_entries));
   const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
   const size_t o_list = off;     off += round_up(sizeof(DrawEntry) * static_cast<size_t>(B));
   const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(n_part));
@@ -120,6 +124,9 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->partials = reinterpret_cast<float4*>(p + o_part);
     ws->draw = reinterpret_cast<double2*>(p + o_draw);
     ws->draw_mass = reinterpret_cast<float*>(p + o_draw);
+    ws->queue = reinterpret_cast<unsigned*>(p + o_error) + 2;
+    ws->ready = reinterpret_cast<int*>(p + o_counters);
+    ws->ring = reinterpret_cast<float4*>(p + o_ring);
   }
   return off;
 }
@@ -191,7 +198,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   // always written before they are read.
   if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
     return fail_cuda("clearing the workspace counters", e);
-  if (stream_path && use_left_to_right() && V <= kSeqDrawChunk * kSeqMaxDrawChunks) {
+  if (stream_path && use_left_to_right() && V <= kSeqMaxV) {
     P.grid_stats = device_sm_count();
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
     if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);

@@ -39,6 +39,10 @@ struct ChainWorkspace {
   unsigned* draw_count;  // [1]: entries in draw_list
   float* draw_mass;      // [B*nchd]: residual (or bonus) mass per chunk of the drawn row
   unsigned* error;       // [1]: set when a bounded wait gave up
+  // left-to-right kernel: task queues (rows first, then draws)
+  unsigned* queue;       // [5]: rows published, rows claimed, draws published, draws claimed, sequences finished
+  int* ready;            // [B*g + 2B]: entry published (rows ring, then draws ring); cleared per call
+  float4* ring;          // [2 * (B*g + 2B)]: 32-byte task entries (rows ring, then draws ring)
 };
 
 // Streaming (bulk-copy) path geometry.
@@ -69,13 +73,18 @@ constexpr int kDrawStagesF32 = 3;                      // fp32 stages are larger
 constexpr int kDrawChunk = SPECDEC_DRAW_CHUNK;       // elements of the drawn row per work item
 constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decision
 
-// Left-to-right (early-exit) kernel geometry: one CTA per SM with kSeqGroups groups.
+// Left-to-right (early-exit) kernel geometry.  One CTA per SM holds kSeqGroups groups of
+// warps; a team is one group in each of the kSeqCluster CTAs of a thread-block cluster,
+// and verifies one sequence at a time with every row split across its members.
 constexpr int kSeqWarps = 16;
 constexpr int kSeqGroups = 2;
+constexpr int kSeqCluster = 2;
+constexpr bool kSpecRows = true;          // copy row i + 1 ahead while row i of a chain streams
 constexpr int kSeqStages = 3;
 constexpr int kSeqChunkBytes = 4096;
 constexpr int kSeqDrawChunk = 512;        // drawn-row elements per copy (logits + q fit 4 KB)
-constexpr int kSeqMaxDrawChunks = 4096;   // chunk masses kept in shared memory: V <= 2^21
+constexpr int kSeqMaxDrawChunks = 1024;   // chunk masses of one member's part of the drawn row
+constexpr int64_t kSeqMaxV = static_cast<int64_t>(kSeqDrawChunk) * kSeqMaxDrawChunks * kSeqCluster;
 
 struct ChainParams {
   const void* logits;
