@@ -3,8 +3,9 @@
 
 Default workload: chain verification at B=256, gamma=7, V=128256, bf16 logits, fp32
 draft probabilities (Zipf-biased synthetic logits), the configuration the throughput
-target is stated on.  One step = one specdec_verify_chain call over one batch (all rows:
-temperature softmax statistics, accept tests, first rejection, residual/bonus draw).
+target is stated on.  One step = one specdec_verify_chain call over one batch: each
+sequence evaluated left to right over rows 0..J (temperature softmax statistics, accept
+tests up to the first rejection, residual/bonus draw).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -31,12 +32,14 @@ UNIT = "rows/s"
 DEFAULT_WORKLOAD = "chain_b256_v128256"
 FALLBACK_HBM_GBS = 6800.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of chain_stats, from one ncu
-# capture of the benchmarked workload, keyed by the sha256 of the kernel source it was
-# taken on; reported as null once the source differs.
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from
+# one ncu capture of the benchmarked workload, keyed by the sha256 of the kernel source
+# it was taken on; reported as null once the source differs.
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
     "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
+    # profiles/chain_seq_b256_v128256.md: 320.67 MB read + 3.24 MB written (batch seed 0)
+    "chain_seq": {"bytes": 323_909_120, "src_sha": "392be0e2941a591a"},
 }
 
 

@@ -3,18 +3,15 @@
 // SD 20.5, "A whole round of speculative sampling": the one-token rule is applied to the
 // drafts left to right and the round stops at the first rejection; the drafts after it
 // are discarded, so their target rows are never needed.  This kernel follows that order
-// literally, as a dataflow over TASKS:
+// literally, as a dataflow of TASKS:
 //
 //   row task (b, i)   the softmax statistics of row i of sequence b and the test of draft
 //                     i: accept iff u_i * q_i(x_i) < p_i(x_i) (greedy: x_i == argmax).  An
-//                     acceptance publishes row task (b, i + 1); a rejection, or row gamma,
-//                     publishes the draw task (b, i) (a greedy sequence emits the argmax).
+//                     acceptance makes row i + 1 the next task; a rejection, or row gamma,
+//                     queues the draw task (b, i) (a greedy sequence emits the argmax).
 //   draw task (b, J)  the residual weights (p_J - q_J)+ (q == 0 for the bonus row; SD 20.5,
 //                     "The speculative sampling rule") and the inverse-CDF draw: the
 //                     smallest k with C_k > u * S.
-//
-// Row tasks of all sequences are queued ahead of draw tasks, so every sequence's chain of
-// rows advances as early as possible while the draws fill the bandwidth behind them.
 //
 // A task is run by a TEAM: one group of warps in each of the kSeqCluster CTAs of a
 // thread-block cluster (one CTA per SM).  Member r owns the r-th contiguous part of the
@@ -24,9 +21,11 @@
 // residual weights per 512-element chunk.  Members exchange their 16-byte summaries by
 // st.async into each other's shared memory (distributed shared memory); every member
 // merges them in member order, so all hold the same bits and take the same decision.
-// The member whose part holds u * S finds the drawn token.  The team's first member
-// claims the next task while the current one streams and sends it to the others, so
-// every warp has the next task's copies in flight before the current task ends.
+// The member whose part holds u * S finds the drawn token.
+//
+// A team follows its sequence's chain row after row.  When the chain ends, the team
+// takes new work from two ticket queues: sequence starts first, then queued draws.  So
+// every chain starts early, and the draws fill the machine behind the chains.
 
 #include <climits>
 
@@ -266,9 +265,10 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 
 // Work that any team may take: the start of a sequence (its row 0; ticket s < B is
 // sequence s) and published draw tasks (draw ticket d is the d-th published draw).
-// Tickets are handed out by atomicAdd, so claiming never retries; a draw ticket taken
-// before its draw is published is waited for only after the claiming team finished the
-// task it was running, so no team ever waits on work that it must produce itself.
+// Tickets are handed out by atomicAdd, so claiming never retries.  A team takes a ticket
+// only when it has no task; a draw ticket taken before its draw is published is waited
+// for then, and that draw comes from a team still following its chain, so no team ever
+// waits on work that it must produce itself.
 struct Queue {
   unsigned *start_ticket, *pub_draws, *draw_ticket, *finished;
   int* ready_draws;
@@ -285,9 +285,9 @@ __device__ __forceinline__ int take_ticket(const Queue& q) {
   return kDrawTag | static_cast<int>(atomicAdd(q.draw_ticket, 1u));
 }
 
-// The entry behind a ticket: 1 = ready, 0 = not published yet (only if !blocking),
-// -1 = every sequence has finished (no more work), -2 = a bounded wait gave up.
-__device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, bool blocking, float4& e0, float4& e1) {
+// The entry behind a ticket, waiting until it is published: 1 = ready, -1 = every
+// sequence has finished (no more work), -2 = the bounded wait gave up.
+__device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, float4& e0, float4& e1) {
   if (!(tk & kDrawTag)) {
     Entry e;
     e.b = tk;
@@ -310,7 +310,6 @@ __device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, bool
       return 1;
     }
     if (ld_relaxed(q.finished) >= static_cast<unsigned>(q.B)) return -1;
-    if (!blocking) return 0;
     if (t0 == 0) t0 = global_timer_ns();
     else if (global_timer_ns() - t0 > kMaxWaitNs) return -2;
     __nanosleep(128);
@@ -632,38 +631,21 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     return e0;
   };
 
-  // Mailbox protocol: each use u is armed by every member (expect 32 bytes) and filled by
-  // exactly one send from the leader.  `box` marks a use armed but not yet read.
+  // The team's next task through the mailbox (every thread).  Each use u is armed by
+  // every member (expect 32 bytes) and filled by one send from the team's leader, who
+  // takes a ticket and waits until its entry exists.
   uint32_t mb = 0;
-  bool box = false;
-  int tk = -1;           // leader: the ticket behind the armed use
-  bool tk_sent = false;  // leader: its entry has been sent
-  auto arm_box = [&]() {
-    box = true;
+  auto take_box = [&]() {
     if (first) mbar_expect_tx(&gs.mbar_box[mb & 1u], 32);
     if (leader) {
-      tk = take_ticket(qu);
-      tk_sent = false;
-    }
-  };
-  auto try_send = [&](bool blocking) {
-    if (leader && box && !tk_sent) {
       float4 e0, e1 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int r = resolve_ticket(P, qu, tk, blocking, e0, e1);
-      if (r != 0) {
-        if (r < 0) {
-          if (r == -2) atomicOr(P.ws.error, 8u);
-          e0 = no_more();
-        }
-        send_entry(gs, static_cast<int>(mb & 1u), e0, e1);
-        tk_sent = true;
+      const int r = resolve_ticket(P, qu, take_ticket(qu), e0, e1);
+      if (r < 0) {
+        if (r == -2) atomicOr(P.ws.error, 8u);
+        e0 = no_more();
       }
+      send_entry(gs, static_cast<int>(mb & 1u), e0, e1);
     }
-  };
-  // the team's next task through the mailbox (every thread)
-  auto take_box = [&]() {
-    if (!box) arm_box();
-    try_send(true);
     __syncwarp();
     if (group_any(group, !mbar_wait_cluster(&gs.mbar_box[mb & 1u], (mb >> 1) & 1u))) {
       if (first) atomicOr(P.ws.error, 2u);
@@ -671,14 +653,11 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     }
     const Entry e = unpack_entry(gs.mbox[mb & 1u][0], gs.mbox[mb & 1u][1]);
     ++mb;
-    box = false;
     return e;
   };
 
   Entry cur = take_box();
-  uint32_t t = 0;                // tasks done by this team
-  int pre = 0;                   // jobs of the next row this warp already issued
-  int pre_b = -1, pre_row = -1;  // and which row that is
+  uint32_t t = 0;  // tasks done by this team
   // a drawn token still to be found by this member's first warp (at the next task's start)
   bool srch = false;
   int s_b = 0, s_J = 0, s_par = 0;
@@ -728,35 +707,10 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       }
     };
 
-    // This task's copies first, then, during a row of a chain, the next row's: the round
-    // goes on there whenever draft i is accepted.  Jobs copied ahead for a row that did
-    // not come are drained and dropped.
-    int ci = 0, ni = 0;
-    if (kind == kTaskRow && b == pre_b && ri == pre_row) {
-      ci = pre;
-    } else {
-      for (int j = 0; j < pre && pp.ok; ++j) {
-        if (!pp.wait()) {
-          if (lane == 0) atomicOr(P.ws.error, 1u);
-          pp.ok = false;
-        }
-        ++pp.k;
-      }
-      __syncwarp();
-    }
-    Task tn;
-    if (kSpecRows && kind == kTaskRow && ri < P.gamma) {
-      Entry e = cur;
-      e.row = ri + 1;
-      tn = make_task(e);
-    }
+    // This task's copies: kSeqStages in flight, one more as each stage is read.
+    int ci = 0;
     auto refill = [&]() {
-      if (!pp.ok) return;
-      if (ci < tc.n) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
-      else if (ni < tn.n) issue_job<T>(pp, tn, ni++, gwarp, lane, V, row_bytes);
-    };
-    auto top_up = [&]() {
-      while (pp.ok && pp.in_flight() < kSeqStages && ni < tn.n) issue_job<T>(pp, tn, ni++, gwarp, lane, V, row_bytes);
+      if (pp.ok && ci < tc.n) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
     };
     while (pp.ok && ci < tc.n && pp.in_flight() < kSeqStages) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
@@ -794,7 +748,6 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         gather2();
       }
       gather2();
-      top_up();
       RowSum r;
       r.m = ml;
       r.Z = Zl;
@@ -850,7 +803,6 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         sr = warp_sum(sr);
         if (lane == 0) gs.mass[par][cd - d0] = sr;
       }
-      top_up();
       const bool qbad = group_any(group, !(qmx < kInf) || qmn < 0.f);  // also: every chunk mass is in place
       double tot = 0.0;
       if (gwarp == 0) tot = local_scan(gs.mass[par], d1 - d0, lane).total;
@@ -875,9 +827,6 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       g[5] = __int_as_float(err);
     }
     __syncwarp();
-    pre = ni;
-    pre_b = b;
-    pre_row = ri + 1;
     const int xp = exchange(gs, tm, mine, group, gwarp, lane, P.ws.error);
 
     // The decision, taken by every thread on the same inputs.
@@ -948,8 +897,8 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
           } else if (!(g[4] >= 0.f && g[4] < 1.f)) {
             st = SPECDEC_STATUS_BAD_UNIFORM;
             done = failed = true;
-          } else if (leader) {
-            Entry e;
+          } else {
+            Entry e;  // the draw goes to the queue; any team may take it
             e.b = b;
             e.row = ri;
             e.kind = kTaskDraw;
@@ -957,7 +906,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
             e.m = rs.m;
             e.Z = rs.Z;
             e.T = Tc;
-            publish_draw(qu, e);
+            if (leader) publish_draw(qu, e);
           }
         }
       }

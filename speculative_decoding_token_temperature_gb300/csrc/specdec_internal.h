@@ -79,7 +79,6 @@ constexpr int kStreamMaxRows = 32;    // gamma + 1 handled by one warp's decisio
 constexpr int kSeqWarps = 16;
 constexpr int kSeqGroups = 2;
 constexpr int kSeqCluster = 2;
-constexpr bool kSpecRows = true;          // copy row i + 1 ahead while row i of a chain streams
 constexpr int kSeqStages = 3;
 constexpr int kSeqChunkBytes = 4096;
 constexpr int kSeqDrawChunk = 512;        // drawn-row elements per copy (logits + q fit 4 KB)
