@@ -81,6 +81,10 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 }
 
 // (max, normaliser, lowest argmax) of a part of a row, and the merge of two parts.
+// Every exponent on this path is l * c - rnd(m * c), one fused multiply-add against the
+// rounded product of the maximum in force; a rescale between two maxima multiplies by
+// 2^(rnd(m_old * c) - rnd(m_new * c)).  The rounding of m * c then shifts every term of
+// a row alike, and cancels in p = 2^(l_x * c - rnd(m * c)) / Z.
 struct RowSum {
   float m, Z;
   int z;
@@ -88,8 +92,9 @@ struct RowSum {
 __device__ __forceinline__ RowSum merge(const RowSum& a, const RowSum& b, float c) {
   RowSum r;
   r.m = max_nan(a.m, b.m);
-  const float za = (a.m > -kInf) ? a.Z * ex2((a.m - r.m) * c) : 0.f;
-  const float zb = (b.m > -kInf) ? b.Z * ex2((b.m - r.m) * c) : 0.f;
+  const float mc = __fmul_rn(r.m, c);
+  const float za = (a.m > -kInf) ? a.Z * ex2(__fsub_rn(__fmul_rn(a.m, c), mc)) : 0.f;
+  const float zb = (b.m > -kInf) ? b.Z * ex2(__fsub_rn(__fmul_rn(b.m, c), mc)) : 0.f;
   r.Z = za + zb;
   r.z = min(a.m == r.m ? a.z : INT_MAX, b.m == r.m ? b.z : INT_MAX);
   return r;
@@ -126,23 +131,24 @@ template <> struct Group<float> {
 };
 
 // Residual (or target) weights of 4 consecutive elements and their fp32 running sum in
-// index order; the chunk masses and the final scan both use it.
+// index order; the chunk masses and the final scan both use it.  nmc = -rnd(m_J * c);
+// with q == 0 (the bonus row, or a zero residual) the weights are p itself.
 template <typename T>
-__device__ __forceinline__ float group_weights(const typename Group<T>::L& lw, const float4& q4, float mJ,
+__device__ __forceinline__ float group_weights(const typename Group<T>::L& lw, const float4& q4, float nmc,
                                                float c, float invZ, bool no_q, float (&w)[4]) {
   float l[4];
   Group<T>::unpack(lw, l);
-  const float qv[4] = {no_q ? 0.f : q4.x, no_q ? 0.f : q4.y, no_q ? 0.f : q4.z, no_q ? 0.f : q4.w};
-  const unsigned long long m2 = f2pack(mJ, mJ), c2 = f2pack(c, c), z2 = f2pack(invZ, invZ);
+  const unsigned long long c2 = f2pack(c, c), nmc2 = f2pack(nmc, nmc), niz2 = f2pack(-invZ, -invZ);
+  const unsigned long long q01 = no_q ? 0ull : f2pack(q4.x, q4.y), q23 = no_q ? 0ull : f2pack(q4.z, q4.w);
   float acc = 0.f;
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
     float y0, y1;
-    f2unpack(f2mul(f2sub(f2pack(l[2 * p], l[2 * p + 1]), m2), c2), y0, y1);
-    float p0, p1;
-    f2unpack(f2mul(f2pack(ex2(y0), ex2(y1)), z2), p0, p1);
-    w[2 * p] = fmaxf(p0 - qv[2 * p], 0.f);
-    w[2 * p + 1] = fmaxf(p1 - qv[2 * p + 1], 0.f);
+    f2unpack(f2fma(f2pack(l[2 * p], l[2 * p + 1]), c2, nmc2), y0, y1);
+    float r0, r1;  // q - p
+    f2unpack(f2fma(f2pack(ex2(y0), ex2(y1)), niz2, p == 0 ? q01 : q23), r0, r1);
+    w[2 * p] = fmaxf(-r0, 0.f);
+    w[2 * p + 1] = fmaxf(-r1, 0.f);
     acc += w[2 * p];
     acc += w[2 * p + 1];
   }
@@ -410,9 +416,10 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
     // online softmax: rescale the running sum when the maximum grows
     const float mn = max_nan(ml, mt);
     if (mn > -kInf) {
-      if (mn != ml) Zl = (ml > -kInf) ? Zl * ex2((ml - mn) * c) : 0.f;
+      const float mcn = __fmul_rn(mn, c);
+      if (mn != ml) Zl = (ml > -kInf) ? Zl * ex2(__fsub_rn(__fmul_rn(ml, c), mcn)) : 0.f;
       ml = mn;
-      const unsigned long long m2 = f2pack(ml, ml), c2 = f2pack(c, c);
+      const unsigned long long nmc2 = f2pack(-mcn, -mcn), c2 = f2pack(c, c);
       unsigned long long acc = f2pack(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
@@ -424,7 +431,7 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
           if constexpr (sizeof(T) == 2) x2 = f2pack(bf16_lo(ww[p]), bf16_hi(ww[p]));
           else x2 = f2pack(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
           float y0, y1;
-          f2unpack(f2mul(f2sub(x2, m2), c2), y0, y1);
+          f2unpack(f2fma(x2, c2, nmc2), y0, y1);
           e2[p] = f2pack(ex2(y0), ex2(y1));
         }
         unsigned long long vs;
@@ -502,7 +509,7 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
     if (g < ng) {
       const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
       const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
-      gsum[j] = group_weights<T>(lw, q4, mJ, c, invZ, no_q, w[j]);
+      gsum[j] = group_weights<T>(lw, q4, -__fmul_rn(mJ, c), c, invZ, no_q, w[j]);
       lane_tot += static_cast<double>(gsum[j]);
     }
   }
@@ -765,7 +772,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       }
       mine = make_float4(s.m, s.Z, __int_as_float(s.z), 0.f);
     } else {
-      const float mJ = cur.m, invZ = 1.f / cur.Z;
+      const float nmc = -__fmul_rn(cur.m, c), invZ = 1.f / cur.Z;
       const bool with_q = tc.q != nullptr;
       float qmx = 0.f, qmn = 0.f;
       for (int j = 0; j < tc.n && pp.ok; ++j) {
@@ -795,7 +802,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         for (int v = 0; v < GPL; ++v) {
           if (lane + 32 * v < ng) {
             float w4[4];
-            sr += group_weights<T>(lw[v], qv[v], mJ, c, invZ, !with_q, w4);
+            sr += group_weights<T>(lw[v], qv[v], nmc, c, invZ, !with_q, w4);
             qmx = max_nan(qmx, max_nan(max_nan(qv[v].x, qv[v].y), max_nan(qv[v].z, qv[v].w)));
             qmn = fminf(qmn, fminf(fminf(qv[v].x, qv[v].y), fminf(qv[v].z, qv[v].w)));
           }
@@ -869,7 +876,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
           if (greedy) {
             acc = (xi == rs.z);
           } else {
-            pxi = ex2((g[1] - rs.m) * c) / rs.Z;
+            pxi = ex2(fmaf(g[1], c, -__fmul_rn(rs.m, c))) / rs.Z;
             if (g[2] == 0.f) {
               warn |= SPECDEC_STATUS_ZERO_Q >> 8;
               acc = pxi > 0.f;

@@ -208,6 +208,12 @@ __device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsign
   return r;
 }
 // NaN-propagating maximum of two pairs of bf16 values.
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 __device__ __forceinline__ uint32_t bf2max(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
