@@ -294,6 +294,140 @@ def verify_chain(logits, q, drafts, T, u) -> dict:
     }
 
 
+# ---------------------------------------------------------------------------------------
+# Block verification (one round, one sequence)
+# ---------------------------------------------------------------------------------------
+
+def verify_block_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False) -> dict:
+    """One round of block verification for one sequence.
+
+    Art of Guessing, "Block verification" (Sun et al., 2024): the draft is judged jointly
+    rather than token by token.  With p_k = softmax(l_k / T) the target's and q_k the
+    drafter's distribution at draft position k (0-based here: row k predicts draft k):
+
+      w_0 = 1,  w_{k+1} = min(1, w_k * p_k(x_k) / q_k(x_k))           (running weight)
+      mass_k = sum_x (w_k p_k(x) - q_k(x))+  for k < gamma,   mass_gamma = w_gamma
+      survival_k = mass_k / (mass_k + 1 - w_k)  if w_k < 1, else 1
+      prefix length k (1..gamma) survives iff u[k-1] <= survival_k
+      n = the longest surviving prefix (0 if none survives)
+      extra token y ~ (w_n p_n - q_n)+ normalised, q_gamma == 0 (the bonus row)
+      emit x_0 .. x_{n-1}, y
+
+    READINGS: the survival test is `uniform <= survival`, as the page's block_verify
+    writes it; the extra token is the inverse-CDF draw of u[gamma], as for the chain rule;
+    a ratio with q_k(x_k) = 0 is +inf (p > 0) or 0 (p = 0) and 0 * inf = 0 in the weight
+    recursion, with the ZERO_Q warning; a residual that sums to 0 (rounding only) falls
+    back to p_n with the ZERO_RESIDUAL warning.  Every row, draft token, whole q row and
+    uniform is read by the rule, so all of them are validated and every error found is
+    reported (bits OR'd).  A sequence with T < GREEDY_T is verified greedily, exactly as
+    verify_chain_sequence does: with a one-hot target the block rule reduces to it (the
+    weights are 1 while x_k is the argmax and 0 after, and the residual is one-hot).
+
+    Returns tokens [gamma+1] (-1 padded), J (= n), status, p_draft [gamma] (p_k(x_k)),
+    w [gamma+1], survival [gamma+1], margins [gamma] (|u[k-1] - survival_k| for k =
+    1..gamma), and for a sampled draw 'y_u' plus, when want_cdf, 'cdf' and 'S'.
+    """
+    logits = np.asarray(logits)
+    g1, V = logits.shape
+    gamma = g1 - 1
+    drafts = [int(x) for x in np.asarray(drafts).reshape(-1)]
+    assert len(drafts) == gamma
+    u = widen(u).reshape(-1)
+    greedy = bool(T < GREEDY_T) or bool(np.isnan(T))
+    out = {
+        "tokens": np.full(gamma + 1, -1, dtype=np.int64),
+        "J": -1,
+        "status": 0,
+        "p_draft": np.full(gamma, np.nan),
+        "w": np.full(gamma + 1, np.nan),
+        "survival": np.full(gamma + 1, np.nan),
+        "margins": np.full(gamma, np.inf),
+        "greedy": greedy,
+    }
+    if not np.isfinite(T):
+        out["status"] = STATUS_BAD_TEMPERATURE
+        return out
+    err = 0
+    for i in range(g1):
+        err |= _row_status(logits[i])
+    for i in range(gamma):
+        if not (0 <= drafts[i] < V):
+            err |= STATUS_BAD_TOKEN
+    if not greedy:
+        qq = widen(q).reshape(gamma, V)
+        if np.isnan(qq).any() or np.isinf(qq).any() or (qq < 0).any():
+            err |= STATUS_BAD_PROB
+        if not ((0.0 <= u) & (u < 1.0)).all():
+            err |= STATUS_BAD_UNIFORM
+    if err:
+        out["status"] = err
+        return out
+
+    if greedy:
+        J = gamma
+        for i in range(gamma):
+            if drafts[i] != lowest_argmax(logits[i]):
+                J = i
+                break
+        out["tokens"][:J] = drafts[:J]
+        out["tokens"][J] = lowest_argmax(logits[J])
+        out["J"] = J
+        return out
+
+    status = 0
+    p = [target_distribution(logits[k], T) for k in range(g1)]
+    w = np.ones(g1)
+    for k in range(gamma):
+        px, qx = p[k][drafts[k]], qq[k][drafts[k]]
+        out["p_draft"][k] = px
+        if qx == 0.0:
+            status |= STATUS_ZERO_Q
+            ratio = np.inf if px > 0.0 else 0.0
+        else:
+            ratio = px / qx
+        w[k + 1] = 0.0 if w[k] == 0.0 else min(1.0, w[k] * ratio)
+    mass = np.empty(g1)
+    for k in range(gamma):
+        mass[k] = np.maximum(w[k] * p[k] - qq[k], 0.0).sum()
+    mass[gamma] = w[gamma]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        surv = np.where(w < 1.0, mass / (mass + 1.0 - w), 1.0)
+    out["w"], out["survival"] = w, surv
+    n = 0
+    for k in range(1, gamma + 1):
+        out["margins"][k - 1] = abs(u[k - 1] - surv[k])
+        if u[k - 1] <= surv[k]:
+            n = k
+    qn = qq[n] if n < gamma else np.zeros(V)
+    r = np.maximum(w[n] * p[n] - qn, 0.0)
+    if not (r.sum() > 0.0):
+        status |= STATUS_ZERO_RESIDUAL
+        r = p[n].copy()
+    y, C, S = inverse_cdf(r, u[gamma])
+    out["tokens"][:n] = drafts[:n]
+    out["tokens"][n] = y
+    out["J"] = n
+    out["status"] = status
+    out["y_u"] = u[gamma] * S
+    if want_cdf:
+        out["cdf"] = C
+        out["S"] = S
+    return out
+
+
+def verify_block(logits, q, drafts, T, u) -> dict:
+    """Batched block verification: a Python loop of verify_block_sequence over B."""
+    B = np.asarray(logits).shape[0]
+    res = [verify_block_sequence(logits[b], q[b], drafts[b], float(T[b]), u[b]) for b in range(B)]
+    return {
+        "tokens": np.stack([r["tokens"] for r in res]),
+        "J": np.array([r["J"] for r in res]),
+        "status": np.array([r["status"] for r in res]),
+        "p_draft": np.stack([r["p_draft"] for r in res]),
+        "per_seq": res,
+    }
+
+
 def verify_greedy_sequence(logits, drafts) -> dict:
     """Greedy verification only (SD 20.5, "A round of greedy speculative decoding";
     Art of Guessing, "Draft and verify"): J = longest prefix with x_i == z_i, emit z_J."""

@@ -98,7 +98,48 @@ def round_outcome_law(verify, drafts, gamma: int) -> dict:
     return dict(law)
 
 
-def bigram_round_law(verify_rows, P, Q, state: int, gamma: int) -> dict:
+def block_round_outcome_law(verify, drafts, gamma: int) -> dict:
+    """Law of the emitted tuple of one block-verification round with fixed drafts.
+
+    Structure assumed of the verifier (a wrong verifier then yields a wrong law, which
+    the pins catch): prefix length k survives iff its own uniform u[k-1] lies below a
+    threshold, the round keeps the longest surviving prefix, and the extra token is a
+    step function of u[gamma].  Each threshold is located by bisection on the verifier
+    with every other prefix's uniform near 1.
+    """
+    hi = np.nextafter(1.0, 0.0)
+
+    def n_of(u):
+        return len(verify(drafts, u)) - 1
+
+    t = {}
+    for k in range(1, gamma + 1):
+        def survives(x, k=k):
+            u = [hi] * gamma + [0.5]
+            u[k - 1] = x
+            return n_of(u) >= k
+        t[k] = _last_u_with(survives, 0.0, True) if survives(0.0) else 0.0
+    law = defaultdict(float)
+    for n in range(gamma + 1):
+        pn = t[n] if n >= 1 else 1.0
+        for j in range(n + 1, gamma + 1):
+            pn *= 1.0 - t[j]
+        if pn <= 0.0:
+            continue
+        base = [0.5] * gamma
+        if n >= 1:
+            base[n - 1] = 0.5 * t[n]
+        for j in range(n + 1, gamma + 1):
+            base[j - 1] = 0.5 * (1.0 + t[j])
+
+        def tok(x, base=base):
+            return verify(drafts, base + [x])
+        for out, m in step_function_masses(tok).items():
+            law[out] += pn * m
+    return dict(law)
+
+
+def bigram_round_law(verify_rows, P, Q, state: int, gamma: int, round_law=None) -> dict:
     """Exact law of the tokens one round emits from `state` under bigram models.
 
     P[s], Q[s] are the target's and draft's next-token distributions after token s.
@@ -121,16 +162,16 @@ def bigram_round_law(verify_rows, P, Q, state: int, gamma: int) -> dict:
         def verify(d, u, p_rows=p_rows, q_rows=q_rows):
             return verify_rows(p_rows, q_rows, d, u)
 
-        for out, m in round_outcome_law(verify, list(drafts), gamma).items():
+        for out, m in (round_law or round_outcome_law)(verify, list(drafts), gamma).items():
             law[out] += w * m
     return dict(law)
 
 
-def first_two_tokens_law(verify_rows, P, Q, start: int, gamma: int) -> np.ndarray:
+def first_two_tokens_law(verify_rows, P, Q, start: int, gamma: int, round_law=None) -> np.ndarray:
     """Exact joint law of the first two generated tokens (several rounds if needed)."""
     V = P.shape[0]
     joint = np.zeros((V, V))
-    first_round = bigram_round_law(verify_rows, P, Q, start, gamma)
+    first_round = bigram_round_law(verify_rows, P, Q, start, gamma, round_law)
     cache = {}
     for out, m in first_round.items():
         if len(out) >= 2:
@@ -138,7 +179,7 @@ def first_two_tokens_law(verify_rows, P, Q, start: int, gamma: int) -> np.ndarra
         else:
             y1 = out[0]
             if y1 not in cache:
-                cache[y1] = bigram_round_law(verify_rows, P, Q, y1, gamma)
+                cache[y1] = bigram_round_law(verify_rows, P, Q, y1, gamma, round_law)
             for out2, m2 in cache[y1].items():
                 joint[y1, out2[0]] += m * m2
     return joint
