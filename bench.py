@@ -8,6 +8,10 @@ sequence evaluated left to right over rows 0..J (temperature softmax statistics,
 tests up to the first rejection, residual/bonus draw).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--rule chain|block]
+
+--rule block times block verification (specdec_verify_block: the draft judged jointly,
+every row and q row read) on the same workload instead of the chain rule.
 
 Prints one JSON line (rank 0).  Metric: verified vocab rows per second, B*(gamma+1)
 rows per call, whole job over all ranks.  Several GPUs run independent replicas
@@ -150,12 +154,15 @@ def workload_shape(name):
     return w["B"], w["gamma"], w["V"], w["dtype"]
 
 
-def cpu_oracle_rate(inputs_cpu: dict, target_seconds: float, max_seqs: int | None = None):
+def oracle_rule(rule: str):
+    from oracle import specdec_oracle as so
+    return so.verify_block_sequence if rule == "block" else so.verify_chain_sequence
+
+
+def cpu_oracle_rate(inputs_cpu: dict, target_seconds: float, max_seqs: int | None = None, rule: str = "chain"):
     """Time the fp64 oracle (as it stands, one process) on the first sequences of one
     batch until about target_seconds of work; returns (rows/s, sequences, seconds)."""
-    import numpy as np
-    from oracle import specdec_oracle as so
-
+    verify = oracle_rule(rule)
     L = inputs_cpu["logits"]
     L = L.float().numpy() if str(L.dtype) == "torch.bfloat16" else L.numpy()
     q = inputs_cpu["draft_probs"].numpy()
@@ -165,7 +172,7 @@ def cpu_oracle_rate(inputs_cpu: dict, target_seconds: float, max_seqs: int | Non
     B, g1 = u.shape
     n, t0 = 0, time.perf_counter()
     while n < (max_seqs or B) and n < B:
-        so.verify_chain_sequence(L[n], q[n], d[n], float(T[n]), u[n])
+        verify(L[n], q[n], d[n], float(T[n]), u[n])
         n += 1
         if time.perf_counter() - t0 >= target_seconds:
             break
@@ -183,14 +190,13 @@ def run_reference(args, rank):
     B, g, V, dtype = workload_shape(args.workload)
     per_step = args.ref_sequences
     x = workloads.chain_workload(args.workload, 0, "cpu", B=per_step)
-    from oracle import specdec_oracle as so
-    import numpy as np
+    verify = oracle_rule(args.rule)
     L = x["logits"].float().numpy() if dtype == "bf16" else x["logits"].numpy()
     q, d, T, u = (x[k].numpy() for k in ("draft_probs", "draft_tokens", "temperatures", "uniforms"))
 
     def step():
         for b in range(per_step):
-            so.verify_chain_sequence(L[b], q[b], d[b], float(T[b]), u[b])
+            verify(L[b], q[b], d[b], float(T[b]), u[b])
 
     for _ in range(args.warmup):
         step()
@@ -203,8 +209,8 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "gamma": g, "V": V, "logits_dtype": dtype,
-                   "step_sample_sequences": per_step},
+        "config": {"workload": args.workload, "rule": args.rule, "B": B, "gamma": g, "V": V,
+                   "logits_dtype": dtype, "step_sample_sequences": per_step},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} sequences ({per_step * (g + 1)} rows) of {args.workload} per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -226,6 +232,7 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rule", choices=["chain", "block"], default="chain")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -261,9 +268,11 @@ def main():
              "p_draft": torch.empty(B, g, dtype=torch.float32, device=dev)} for _ in sets]
     stream = torch.cuda.current_stream(dev)
 
+    verify = sd.verify_block if args.rule == "block" else sd.verify_chain
+
     def step(i):
         x = sets[i % len(sets)]
-        sd.verify_chain(*(x[k] for k in keys), out=outs[i % len(sets)], stream=stream)
+        verify(*(x[k] for k in keys), out=outs[i % len(sets)], stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -317,7 +326,14 @@ def main():
     n_rej = sum(float((o["num_accepted"] < g).float().sum()) for o in outs) / len(outs)
     rows_read = sum(float((o["num_accepted"].clamp(max=g) + 1).float().sum()) for o in outs) / len(outs)
     seq_bytes = rows_read * V * esize + n_rej * V * 4
-    if per_kernel.get("chain_seq", (0.0, 0))[1]:
+    if args.rule == "block":
+        # block verification reads every logits row and every q row: the statistics pass
+        # reads the logits, the mass pass both
+        seq_bytes = rows * V * esize + B * g * V * 4
+        per_kernel_bytes = {"chain_stats": rows * V * esize, "chain_sample": seq_bytes}
+        kname = max(per_kernel_bytes, key=lambda k: per_kernel.get(k, (0.0, 0))[0])
+        alg_bytes = per_kernel_bytes[kname]
+    elif per_kernel.get("chain_seq", (0.0, 0))[1]:
         kname, alg_bytes = "chain_seq", seq_bytes
     else:
         kname, alg_bytes = "chain_stats", rows * V * esize   # every logits row read once
@@ -326,14 +342,15 @@ def main():
     sha = kernel_source_sha()
     traffic = NCU_TRAFFIC.get(kname, {})
     traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
-    # bytes one whole call must move (the same left-to-right count for either kernel set)
+    # bytes one whole call must move (the same left-to-right count for either chain
+    # kernel set; every row and q row for the block rule)
     call_bytes = seq_bytes
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "gamma": g, "V": V, "logits_dtype": dtype,
-                   "draft_probs_dtype": "fp32", "parallelism": f"replicas x{world}",
+        "config": {"workload": args.workload, "rule": args.rule, "B": B, "gamma": g, "V": V,
+                   "logits_dtype": dtype, "draft_probs_dtype": "fp32", "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2, {args.sets} seeded batches rotated"},
         "hbm_gbs_call": call_bytes / (ms_per_step / 1e3) / 1e9,
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -353,12 +370,12 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = B * (g + 1) * 4 + B * 4 + B * 4 + B * g * 4
         for _ in range(2):
-            sd.verify_chain(*(host[k] for k in keys))
+            verify(*(host[k] for k in keys))
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            res = sd.verify_chain(*(host[k] for k in keys))
+            res = verify(*(host[k] for k in keys))
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -368,7 +385,7 @@ def main():
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x0 = {k: sets[0][k].cpu() for k in keys}
-        rate, nseq, secs = cpu_oracle_rate(x0, args.cpu_seconds)
+        rate, nseq, secs = cpu_oracle_rate(x0, args.cpu_seconds, rule=args.rule)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {nseq} sequences ({nseq * (g + 1)} rows) of one batch, {secs:.1f} s"}
     if rank == 0:

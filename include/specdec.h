@@ -109,6 +109,39 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Block verification: one round per sequence, the draft judged jointly.
+ *
+ * Art of Guessing, "Block verification" (Sun et al.).  Same inputs, outputs and shapes as
+ * specdec_verify_chain.  For a sampled sequence (T >= SPECDEC_GREEDY_TEMPERATURE), with
+ * p_k = softmax(logits[b, k, :] / T) and q_k = draft_probs[b, k, :]:
+ *   w_0 = 1, w_{k+1} = min(1, w_k * p_k(x_k) / q_k(x_k))       (q(x) = 0: ratio +inf, or 0
+ *                                                              when p(x) = 0; 0 * inf = 0)
+ *   mass_k = sum_v (w_k p_k(v) - q_k(v))+ (k < g), mass_g = w_g
+ *   survival_k = mass_k / (mass_k + 1 - w_k) if w_k < 1, else 1
+ *   prefix length k (1..g) survives iff uniforms[b, k-1] <= survival_k
+ *   n = the longest surviving prefix (0 if none): out_num_accepted[b]
+ *   the extra token is the inverse-CDF draw with uniforms[b, g] from (w_n p_n - q_n)+
+ *   (q_g == 0): y = smallest v with C_v > u * S.  out_tokens = x_0..x_{n-1}, y, -1...
+ * Greedy sequences are verified exactly as by specdec_verify_greedy (a one-hot target
+ * reduces the rule to argmax matching).  The rule reads every row, every draft, every
+ * q row and every uniform, so all are validated and every error found is reported
+ * (status bits OR'd); an error gives J = -1, tokens -1 and p_draft NaN.  out_p_draft[b, k]
+ * = p_k(x_k) for every k of a clean sampled sequence.  Warnings: SPECDEC_STATUS_ZERO_Q
+ * (some q_k(x_k) == 0), SPECDEC_STATUS_ZERO_RESIDUAL (the residual of row n summed to 0
+ * after rounding; the token is drawn from p_n).
+ * Layout requirement: every logits row and q row starts on a 16-byte boundary (V * elem
+ * size and V * 4 multiples of 16, bases aligned) and g + 1 <= 32; other shapes return
+ * SPECDEC_ERR_UNSUPPORTED.  Sizes: B >= 1, g >= 1, V >= 1.
+ */
+size_t specdec_block_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
+
+int specdec_verify_block(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                         const int32_t* draft_tokens, const float* temperatures,
+                         const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                         int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Greedy verification (SD 20.5, "A round of greedy speculative decoding"; Art of
  * Guessing, "Draft and verify"): z_i = argmax logits[b, i, :] (lowest index on ties),
  * J = longest prefix with x_i == z_i, emit x_0..x_{J-1}, z_J.  Shapes as for the chain
@@ -181,7 +214,9 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_CHAIN_DECIDE 4  /* accept tests and first rejection          */
 #define SPECDEC_KERNEL_CHAIN_FINISH 5  /* inverse-CDF search of the drawn rows      */
 #define SPECDEC_KERNEL_CHAIN_SEQ 6     /* left-to-right chain verification          */
-#define SPECDEC_NUM_KERNELS 7
+#define SPECDEC_KERNEL_BLOCK_DECIDE 7  /* block verification: weights per prefix    */
+#define SPECDEC_KERNEL_BLOCK_FINISH 8  /* block verification: survival and the draw */
+#define SPECDEC_NUM_KERNELS 9
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

@@ -39,7 +39,7 @@ STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
 KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
-                "chain_seq")
+                "chain_seq", "block_decide", "block_finish")
 
 
 class SpecdecError(RuntimeError):
@@ -67,10 +67,14 @@ def load_library():
     lib.specdec_chain_workspace_bytes.restype = sz
     lib.specdec_greedy_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.specdec_greedy_workspace_bytes.restype = sz
+    lib.specdec_block_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.specdec_block_workspace_bytes.restype = sz
     lib.specdec_tree_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.specdec_tree_workspace_bytes.restype = sz
     lib.specdec_verify_chain.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_chain.restype = i32
+    lib.specdec_verify_block.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.specdec_verify_block.restype = i32
     lib.specdec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_greedy.restype = i32
     lib.specdec_verify_tree.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -172,6 +176,20 @@ def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
     requested) and status [B] int32.  Host tensors are copied to the current device and
     the results copied back.
     """
+    return _verify_round("specdec_verify_chain", "specdec_chain_workspace_bytes", logits, draft_probs,
+                         draft_tokens, temperatures, uniforms, out, with_p_draft, stream)
+
+
+def verify_block(logits, draft_probs, draft_tokens, temperatures, uniforms, *, out=None,
+                 with_p_draft: bool = True, stream=None) -> dict:
+    """One round of block verification per sequence (specdec_verify_block): the draft is
+    judged jointly.  Same arguments and results as verify_chain."""
+    return _verify_round("specdec_verify_block", "specdec_block_workspace_bytes", logits, draft_probs,
+                         draft_tokens, temperatures, uniforms, out, with_p_draft, stream)
+
+
+def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, temperatures, uniforms,
+                  out, with_p_draft, stream) -> dict:
     lib = load_library()
     rt = _HostRoundTrip([logits])
     logits, draft_probs, draft_tokens, temperatures, uniforms = (
@@ -196,13 +214,13 @@ def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
         if with_p_draft:
             out["p_draft"] = torch.empty(B, g, dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    ws, wsb = _workspace(int(lib.specdec_chain_workspace_bytes(B, g, V, code)), dev, s.cuda_stream)
-    rc = lib.specdec_verify_chain(
+    ws, wsb = _workspace(int(getattr(lib, ws_entry)(B, g, V, code)), dev, s.cuda_stream)
+    rc = getattr(lib, entry)(
         _ptr(logits), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperatures),
         _ptr(uniforms), B, g, V, _ptr(out["tokens"]), _ptr(out["num_accepted"]),
         _ptr(out.get("p_draft")), _ptr(out.get("status")), _ptr(ws), wsb,
         ctypes.c_void_p(s.cuda_stream))
-    _check(rc, "specdec_verify_chain")
+    _check(rc, entry)
     return {k: rt.to_host(v) for k, v in out.items()}
 
 

@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kDecideThreads) chain_decide_kernel(const Chai
     P.ws.seq[b] = sq;
     if (draw) {
       DrawEntry d;
-      d.loc = make_int4(b, J, 0, 0);
+      d.loc = make_int4(b, J, b, 0);  // (sequence, drawn row, mass slot, 0)
       d.row = make_float4(mJ, c, 1.f / ZJ, 0.f);
       P.ws.draw_list[atomicAdd(P.ws.draw_count, 1u)] = d;
     }
@@ -554,8 +554,11 @@ __global__ void __launch_bounds__(kDrawWarps * 32, 1) chain_draw_stream_kernel(c
       }
     }
     sr = warp_sum(sr);
-    if (__any_sync(0xffffffffu, qc.bad())) sr = kNaN;
-    if (lane == 0) P.ws.draw_mass[static_cast<int64_t>(cur.loc.x) * nchd + cd] = sr;
+    if (__any_sync(0xffffffffu, qc.bad())) {
+      sr = kNaN;
+      if (lane == 0) atomicOr(P.ws.qbad + cur.loc.x, 1);
+    }
+    if (lane == 0) P.ws.draw_mass[static_cast<int64_t>(cur.loc.z) * nchd + cd] = sr;
   }
 }
 
@@ -581,26 +584,20 @@ __device__ __forceinline__ float chunk_mass(const ChainParams& P, const float* d
   return acc;
 }
 
+// The inverse-CDF draw from one row's chunk masses (one warp): the chunk whose fp64
+// running mass first exceeds u * S, then an index-order scan of that chunk for the
+// smallest k with C_k > u * S.  invZ scales the weights the masses were made with
+// ((p - q)+ with p = 2^((l - m)c) * invZ, q == nullptr for none); a total of zero (possible
+// only through rounding) draws from p itself, whose chunk masses are recomputed with
+// invZp.  Returns the token, or -1 when a mass is NaN (a bad draft probability).
 template <typename T>
-__global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
+__device__ int draw_from_masses(const ChainParams& P, const float* dm, const T* lrow, const float* qrow, float mJ,
+                                float c, float invZ, float invZp, float u, int lane, bool& zero_residual) {
   using GL = typename Group<T>::L;
   constexpr int GPL = kDrawChunk / 4 / 32;  // contiguous groups per lane in the scan
   constexpr int CPL = 16;                   // chunk masses per lane kept in registers
-  grid_launch_dependents();
-  grid_dependency_wait();
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x;
-  SeqState st;
-  st.meta = __ldcg(&P.ws.seq[b].meta);
-  st.row = __ldcg(&P.ws.seq[b].row);
-  if (st.meta.y == 0) return;
-  const int R = P.gamma + 1;
-  const int J = st.meta.x;
   const int nchd = P.nchd;
-  const float* dm = P.ws.draw_mass + static_cast<int64_t>(b) * nchd;
-  int32_t* tok_out = P.out_tokens + static_cast<int64_t>(b) * R;
-  const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
-  const float c = st.row.z, mJ = st.row.x, invZ = 1.f / st.row.y;
+  zero_residual = false;
 
   // lane l owns the contiguous chunks [c0, c1); with at most CPL per lane their masses
   // stay in registers
@@ -620,30 +617,24 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
   }
   double incl = warp_incl_scan(mine, lane);
   double S = __shfl_sync(0xffffffffu, incl, 31);
-  if (S != S) {  // a NaN, infinite or negative draft probability in the drawn row
-    if (lane < R) tok_out[lane] = -1;
-    if (lane == 0) {
-      P.out_J[b] = -1;
-      if (P.out_status) P.out_status[b] = st.meta.z | SPECDEC_STATUS_BAD_PROB;
-    }
-    return;
-  }
+  if (S != S) return -1;  // a NaN, infinite or negative draft probability in the row
   const bool use_p = !(S > 0.0);  // zero residual after rounding: draw from p instead
   if (use_p) {  // rare: recompute every chunk's mass of p itself (and keep it from here on)
     mine = 0.0;
     if (in_regs) {
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
-        wq[j] = (j < c1 - c0) ? chunk_mass<T>(P, dm, true, lrow, c0 + j, mJ, c, invZ) : 0.f;
+        wq[j] = (j < c1 - c0) ? chunk_mass<T>(P, dm, true, lrow, c0 + j, mJ, c, invZp) : 0.f;
         mine += static_cast<double>(wq[j]);
       }
     } else {
-      for (int q = c0; q < c1; ++q) mine += static_cast<double>(chunk_mass<T>(P, dm, true, lrow, q, mJ, c, invZ));
+      for (int q = c0; q < c1; ++q) mine += static_cast<double>(chunk_mass<T>(P, dm, true, lrow, q, mJ, c, invZp));
     }
     incl = warp_incl_scan(mine, lane);
     S = __shfl_sync(0xffffffffu, incl, 31);
+    zero_residual = true;
   }
-  const double target = static_cast<double>(st.row.w) * S;
+  const double target = static_cast<double>(u) * S;
 
   // Walk this lane's chunks in order: the first whose running mass (from pre) exceeds
   // target, else the last one with mass.  Also returns the running mass before it.
@@ -664,7 +655,7 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
       }
     } else {
       for (int q = c0; q < c1 && found < 0; ++q) {
-        const double w = static_cast<double>(chunk_mass<T>(P, dm, use_p, lrow, q, mJ, c, invZ));
+        const double w = static_cast<double>(chunk_mass<T>(P, dm, use_p, lrow, q, mJ, c, invZp));
         if (w > 0.0) { lastpos = q; prelast = pre; }
         if (want_cross && pre + w > target) { found = q; before = pre; }
         pre += w;
@@ -695,8 +686,8 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
 
   // scan that chunk in index order: lane l owns GPL contiguous groups of 4 elements,
   // whose weights stay in registers
-  const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
   const bool no_q = use_p || qrow == nullptr;
+  const float iz = use_p ? invZp : invZ;
   const int k0 = cstar * kDrawChunk;
   const int ng = min(kDrawChunk, P.V - k0) / 4;
   float w[GPL][4];
@@ -711,7 +702,7 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
     if (g < ng) {
       const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
       const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
-      gsum[j] = group_weights<T>(lw, q4, mJ, c, invZ, no_q, w[j]);
+      gsum[j] = group_weights<T>(lw, q4, mJ, c, iz, no_q, w[j]);
       lane_tot += static_cast<double>(gsum[j]);
     }
   }
@@ -747,9 +738,256 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
     y = __shfl_sync(0xffffffffu, y, fl);
   }
   if (y < 0) y = warp_max_int(last_pos);  // rounding put u * S at or past the chunk's end
+  return y;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32) chain_finish_kernel(const ChainParams P) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  SeqState st;
+  st.meta = __ldcg(&P.ws.seq[b].meta);
+  st.row = __ldcg(&P.ws.seq[b].row);
+  if (st.meta.y != 1) return;
+  const int R = P.gamma + 1;
+  const int J = st.meta.x;
+  const float* dm = P.ws.draw_mass + static_cast<int64_t>(b) * P.nchd;
+  int32_t* tok_out = P.out_tokens + static_cast<int64_t>(b) * R;
+  const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + J) * P.V;
+  const float* qrow = (J < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + J) * P.V : nullptr;
+  const float invZ = 1.f / st.row.y;
+  bool zr = false;
+  const int y = draw_from_masses<T>(P, dm, lrow, qrow, st.row.x, st.row.z, invZ, invZ, st.row.w, lane, zr);
+  if (y < 0) {  // a bad draft probability in the drawn row
+    if (lane < R) tok_out[lane] = -1;
+    if (lane < P.gamma && P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = kNaN;
+    if (lane == 0) {
+      P.out_J[b] = -1;
+      if (P.out_status) P.out_status[b] = st.meta.z | SPECDEC_STATUS_BAD_PROB;
+    }
+    return;
+  }
   if (lane == 0) {
     tok_out[J] = y;
-    if (use_p && P.out_status) P.out_status[b] = st.meta.z | SPECDEC_STATUS_ZERO_RESIDUAL;
+    if (zr && P.out_status) P.out_status[b] = st.meta.z | SPECDEC_STATUS_ZERO_RESIDUAL;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Block verification (Art of Guessing, "Block verification", Sun et al.): the same
+// statistics pass, then
+//   block decide  one CTA per sequence: every row's (m, Z) and argmax, p_k(x_k), the
+//                 running weights w_{k+1} = min(1, w_k p_k(x_k) / q_k(x_k)) (w_0 = 1),
+//                 every input checked; lists all gamma + 1 rows for the mass pass with
+//                 their weights folded into the scale: (w_k p_k - q_k)+ (q_gamma = 0).
+//   mass pass     the draw kernel above, over every listed row.
+//   block finish  one CTA per sequence: mass_k per row (fp64), survival_k =
+//                 mass_k / (mass_k + 1 - w_k) (1 if w_k = 1), n = the longest prefix k
+//                 with u[k-1] <= survival_k, and the inverse-CDF draw from row n.
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kDecideThreads) block_decide_kernel(const ChainParams P) {
+  __shared__ float s_m[kStreamMaxRows], s_Z[kStreamMaxRows];
+  __shared__ int s_z[kStreamMaxRows];
+  grid_launch_dependents();
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = P.gamma + 1;
+  const int nch = P.nch;
+  const float Tb = P.greedy_only ? 0.f : __ldg(P.temps + b);
+  const bool greedy = P.greedy_only || is_greedy(Tb);
+  const float c = greedy ? 0.f : kLog2e / Tb;
+
+  // inputs (lane i: position i; lane gamma: the draw's uniform), before the wait
+  int x = -1, tok_err = 0, u_err = 0;
+  float lx = 0.f, qx = 0.f, ux = 0.f;
+  if (warp == 0) {
+    if (lane < P.gamma) {
+      x = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane);
+      if (x < 0 || x >= P.V) {
+        tok_err = SPECDEC_STATUS_BAD_TOKEN;
+      } else if (!greedy) {
+        lx = Elem<T>::load(static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + lane) * P.V, x);
+        qx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + lane) * P.V + x);
+      }
+    }
+    if (!greedy && lane < R) {
+      ux = __ldg(P.u + static_cast<int64_t>(b) * R + lane);
+      if (!(ux >= 0.f && ux < 1.f)) u_err = SPECDEC_STATUS_BAD_UNIFORM;
+    }
+  }
+  grid_dependency_wait();
+
+  for (int r = warp; r < R; r += kDecideThreads / 32) {
+    const float4* pp = P.ws.partials + (static_cast<int64_t>(b) * R + r) * nch;
+    RowSum acc;
+    acc.m = -kInf;
+    acc.Z = 0.f;
+    acc.z = INT_MAX;
+    for (int q = lane; q < nch; q += 32) {
+      const float4 f = __ldcg(pp + q);
+      RowSum t;
+      t.m = f.x;
+      t.Z = f.y;
+      t.z = __float_as_int(f.z);
+      acc = merge(acc, t, c);
+    }
+    acc = warp_merge(acc, c);
+    if (lane == 0) {
+      s_m[r] = acc.m;
+      s_Z[r] = acc.Z;
+      s_z[r] = acc.z;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  float m = -kInf, Z = 0.f;
+  int z = INT_MAX, row_err = 0;
+  if (lane < R) {
+    m = s_m[lane];
+    Z = s_Z[lane];
+    z = s_z[lane];
+    if (!(m == m) || m == kInf) row_err = SPECDEC_STATUS_BAD_LOGIT;
+    else if (m == -kInf) row_err = SPECDEC_STATUS_EMPTY_ROW;
+  }
+  // every row, draft and uniform is read by the rule: every error is reported
+  int err = __reduce_or_sync(0xffffffffu, row_err | tok_err | u_err);
+  const bool bad_T = !P.greedy_only && !(Tb - Tb == 0.f);
+  if (bad_T) err = SPECDEC_STATUS_BAD_TEMPERATURE;
+  int32_t* tok_out = P.out_tokens + static_cast<int64_t>(b) * R;
+  float* pd_out = P.out_p_draft ? P.out_p_draft + static_cast<int64_t>(b) * P.gamma : nullptr;
+
+  if (greedy || bad_T) {
+    // greedy matching (a one-hot target reduces the block rule to it)
+    const bool miss = lane < P.gamma && x != z;
+    const unsigned mm = __ballot_sync(0xffffffffu, miss);
+    const int J = err ? -1 : (mm ? __ffs(mm) - 1 : P.gamma);
+    const int zJ = __shfl_sync(0xffffffffu, z, J < 0 ? 0 : J);
+    if (lane < R) tok_out[lane] = (J < 0) ? -1 : (lane < J ? x : (lane == J ? zJ : -1));
+    if (lane < P.gamma && pd_out) pd_out[lane] = kNaN;
+    if (lane == 0) {
+      P.out_J[b] = J;
+      if (P.out_status) P.out_status[b] = err;
+      SeqState sq;
+      sq.meta = make_int4(J, 0, err, 0);
+      sq.row = make_float4(0.f, 0.f, 0.f, 0.f);
+      P.ws.seq[b] = sq;
+    }
+    return;
+  }
+
+  // p_k(x_k), the ratios and the running weights (one serial pass over the positions)
+  float px = kNaN;
+  int warn = 0;
+  float ratio = 0.f;
+  if (lane < P.gamma && !tok_err) {
+    px = ex2((lx - m) * c) / Z;
+    if (qx == 0.f) {
+      warn = SPECDEC_STATUS_ZERO_Q;
+      ratio = px > 0.f ? kInf : 0.f;
+    } else {
+      ratio = px / qx;
+    }
+  }
+  warn = __reduce_or_sync(0xffffffffu, warn);
+  float w = 1.f, wk = 1.f;  // wk: this lane's w_lane
+  for (int k = 0; k < P.gamma; ++k) {
+    const float rk = __shfl_sync(0xffffffffu, ratio, k);
+    w = (w == 0.f) ? 0.f : fminf(1.f, w * rk);
+    if (lane == k + 1) wk = w;
+  }
+  if (lane < P.gamma && pd_out) pd_out[lane] = err ? kNaN : px;
+  if (lane < R) P.ws.block_rows[static_cast<int64_t>(b) * R + lane] = make_float4(m, Z, wk, 0.f);
+  // Rows for the mass pass: the gamma rows with q always (their q rows are checked even
+  // when the sequence already failed), the bonus row only for a clean sequence.
+  const int nent = err ? P.gamma : R;
+  unsigned base = 0;
+  if (lane == 0) base = atomicAdd(P.ws.draw_count, static_cast<unsigned>(nent));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (lane < nent) {
+    DrawEntry d;
+    d.loc = make_int4(b, lane, b * R + lane, 0);
+    d.row = make_float4(m, c, wk / Z, 0.f);
+    P.ws.draw_list[base + lane] = d;
+  }
+  if (lane == 0) {
+    SeqState sq;
+    sq.meta = make_int4(-1, 2, err | warn, 0);
+    sq.row = make_float4(0.f, 0.f, c, 0.f);
+    P.ws.seq[b] = sq;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDecideThreads) block_finish_kernel(const ChainParams P) {
+  __shared__ double s_mass[kStreamMaxRows];
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  SeqState st;
+  st.meta = __ldcg(&P.ws.seq[b].meta);
+  st.row = __ldcg(&P.ws.seq[b].row);
+  if (st.meta.y != 2) return;
+  const int R = P.gamma + 1;
+  const int nchd = P.nchd;
+  int status = st.meta.z;
+  if (__ldcg(P.ws.qbad + b)) status |= SPECDEC_STATUS_BAD_PROB;
+  int32_t* tok_out = P.out_tokens + static_cast<int64_t>(b) * R;
+  if (status & SPECDEC_STATUS_ERROR_MASK) {  // errors only: warnings describe a clean round
+    status &= SPECDEC_STATUS_ERROR_MASK;
+    if (warp == 0) {
+      if (lane < R) tok_out[lane] = -1;
+      if (lane < P.gamma && P.out_p_draft) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = kNaN;
+      if (lane == 0) {
+        P.out_J[b] = -1;
+        if (P.out_status) P.out_status[b] = status;
+      }
+    }
+    return;
+  }
+  // mass_k of every row (fp64, fixed order: lane-contiguous runs, then the warp)
+  for (int k = warp; k < R; k += kDecideThreads / 32) {
+    const float* dm = P.ws.draw_mass + (static_cast<int64_t>(b) * R + k) * nchd;
+    const int cpl = (nchd + 31) / 32;
+    const int q0 = min(lane * cpl, nchd), q1 = min(q0 + cpl, nchd);
+    double mine = 0.0;
+    for (int q = q0; q < q1; ++q) mine += static_cast<double>(__ldcg(dm + q));
+    const double tot = warp_incl_scan(mine, lane);
+    if (lane == 31) s_mass[k] = tot;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // survival of every prefix and the longest surviving one
+  float4 br = make_float4(0.f, 1.f, 1.f, 0.f);
+  if (lane < R) br = __ldcg(P.ws.block_rows + static_cast<int64_t>(b) * R + lane);
+  const double wk = static_cast<double>(br.z);
+  bool survived = false;
+  if (lane >= 1 && lane < R) {
+    const double mass = s_mass[lane];
+    const double surv = (wk < 1.0) ? mass / (mass + 1.0 - wk) : 1.0;
+    const float uk = __ldg(P.u + static_cast<int64_t>(b) * R + lane - 1);
+    survived = static_cast<double>(uk) <= surv;
+  }
+  const unsigned sv = __ballot_sync(0xffffffffu, survived);
+  const int n = sv ? 31 - __clz(sv) : 0;
+  const float mN = __shfl_sync(0xffffffffu, br.x, n), zN = __shfl_sync(0xffffffffu, br.y, n);
+  const float wN = __shfl_sync(0xffffffffu, br.z, n);
+  const float c = st.row.z;
+  const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * R + n) * P.V;
+  const float* qrow = (n < P.gamma) ? P.q + (static_cast<int64_t>(b) * P.gamma + n) * P.V : nullptr;
+  const float uG = __ldg(P.u + static_cast<int64_t>(b) * R + P.gamma);
+  bool zr = false;
+  const int y = draw_from_masses<T>(P, P.ws.draw_mass + (static_cast<int64_t>(b) * R + n) * nchd, lrow, qrow, mN,
+                                    c, wN / zN, 1.f / zN, uG, lane, zr);
+  const int x = (lane < P.gamma) ? __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + lane) : -1;
+  if (lane < R) tok_out[lane] = lane < n ? x : (lane == n ? y : -1);
+  if (lane == 0) {
+    P.out_J[b] = n;
+    if (P.out_status) P.out_status[b] = status | (zr ? SPECDEC_STATUS_ZERO_RESIDUAL : 0);
   }
 }
 
@@ -805,6 +1043,18 @@ cudaError_t launch_chain_stream_decide(const ChainParams& P, specdec_dtype ldt, 
 
 cudaError_t launch_chain_stream_draw(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
   return ldt == SPECDEC_BF16 ? launch_draw_t<uint16_t>(P, stream) : launch_draw_t<float>(P, stream);
+}
+
+cudaError_t launch_block_decide(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
+  if (ldt == SPECDEC_BF16)
+    return launch_kernel(block_decide_kernel<uint16_t>, dim3(P.B), dim3(kDecideThreads), 0, stream, 1, P);
+  return launch_kernel(block_decide_kernel<float>, dim3(P.B), dim3(kDecideThreads), 0, stream, 1, P);
+}
+
+cudaError_t launch_block_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
+  if (ldt == SPECDEC_BF16)
+    return launch_kernel(block_finish_kernel<uint16_t>, dim3(P.B), dim3(kDecideThreads), 0, stream, 1, P);
+  return launch_kernel(block_finish_kernel<float>, dim3(P.B), dim3(kDecideThreads), 0, stream, 1, P);
 }
 
 cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {

@@ -88,13 +88,15 @@ struct ProfScope {
 // per-segment (or per-chunk) summaries and the draw masses.  Returns the total bytes and
 // the counter-block bytes (through counter_bytes when non-null).
 size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, void* base,
-                              ChainWorkspace* ws, size_t* counter_bytes) {
+                              ChainWorkspace* ws, size_t* counter_bytes, bool block) {
   const int64_t rows = static_cast<int64_t>(B) * (g + 1);
+  // drawn rows: one per sequence, or (block verification) every row's residual masses
+  const int64_t n_drawn = block ? rows : static_cast<int64_t>(B);
   int64_t n_part, draw_bytes;
   if (path == 2) {
     const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(elem_size(ldt));
     n_part = rows * ((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
-    draw_bytes = static_cast<int64_t>(B) * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float));
+    draw_bytes = n_drawn * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float));
   } else {
     const int seg = chain_segment_len(ldt, path == 1);
     const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
@@ -103,14 +105,16 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   }
   // queue entries of the left-to-right kernel (streaming layout only)
   const int64_t n_entries = path == 2 ? static_cast<int64_t>(B) * g + 2 * static_cast<int64_t>(B) : 0;
-  const int64_t n_counters = std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries);
+  // (the streaming layout also keeps a bad-draft-probability flag per sequence)
+  const int64_t n_counters = std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries + (path == 2 ? B : 0));
   size_t off = 0;
   const size_t o_error = off;    off += kAlign;
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * static_cast<size_t>(n_counters));
   const size_t counters_end = off;
   const size_t o_ring = off;     off += round_up(2 * sizeof(float4) * static_cast<size_t>(n_entries));
   const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
-  const size_t o_list = off;     off += round_up(sizeof(DrawEntry) * static_cast<size_t>(B));
+  const size_t o_list = off;     off += round_up(sizeof(DrawEntry) * static_cast<size_t>(n_drawn));
+  const size_t o_brows = off;    off += block ? round_up(sizeof(float4) * static_cast<size_t>(rows)) : 0;
   const size_t o_part = off;     off += round_up(sizeof(float4) * static_cast<size_t>(n_part));
   const size_t o_draw = off;     off += round_up(static_cast<size_t>(draw_bytes));
   if (counter_bytes) *counter_bytes = counters_end;
@@ -127,6 +131,8 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->queue = reinterpret_cast<unsigned*>(p + o_error) + 2;
     ws->ready = reinterpret_cast<int*>(p + o_counters);
     ws->ring = reinterpret_cast<float4*>(p + o_ring);
+    ws->qbad = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries : nullptr;
+    ws->block_rows = block ? reinterpret_cast<float4*>(p + o_brows) : nullptr;
   }
   return off;
 }
@@ -287,6 +293,73 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
   return chain_common(logits, ldt, draft_probs, draft_tokens, temperatures, uniforms, B, g, V,
                       out_tokens, out_num_accepted, out_p_draft, out_status, workspace,
                       workspace_bytes, stream, false);
+}
+
+size_t specdec_block_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
+  if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return 0;
+  return chain_workspace_layout(B, g, V, ldt, 2, nullptr, nullptr, nullptr, true);
+}
+
+int specdec_verify_block(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                         const int32_t* draft_tokens, const float* temperatures,
+                         const float* uniforms, int B, int g, int V, int32_t* out_tokens,
+                         int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(ldt)) return fail(SPECDEC_ERR_INVALID_ARG, "unknown logits dtype");
+  if (!chain_sizes_ok(B, g, V)) return fail(SPECDEC_ERR_INVALID_ARG, "B, g and V must be positive");
+  if (!logits || !draft_probs || !draft_tokens || !temperatures || !uniforms || !out_tokens ||
+      !out_num_accepted || !workspace)
+    return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(SPECDEC_ERR_INVALID_ARG, "the workspace must be 256-byte aligned");
+  const size_t es = elem_size(ldt);
+  if (!rows_vectorizable(logits, V, es) || !rows_vectorizable(draft_probs, V, 4) || g + 1 > kStreamMaxRows)
+    return fail(SPECDEC_ERR_UNSUPPORTED, "block verification needs 16-byte aligned rows and g + 1 <= 32");
+  if (workspace_bytes < specdec_block_workspace_bytes(B, g, V, ldt))
+    return fail(SPECDEC_ERR_WORKSPACE, "workspace smaller than specdec_block_workspace_bytes");
+  ChainParams P{};
+  P.logits = logits;
+  P.q = draft_probs;
+  P.drafts = draft_tokens;
+  P.temps = temperatures;
+  P.u = uniforms;
+  P.B = B;
+  P.gamma = g;
+  P.V = V;
+  P.out_tokens = out_tokens;
+  P.out_J = out_num_accepted;
+  P.out_p_draft = out_p_draft;
+  P.out_status = out_status;
+  const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(es);
+  P.nch = static_cast<int>((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
+  P.nchd = (V + kDrawChunk - 1) / kDrawChunk;
+  const int64_t stat_items = static_cast<int64_t>(B) * (g + 1) * P.nch;
+  const int64_t draw_items = static_cast<int64_t>(B) * (g + 1) * P.nchd;
+  if (stat_items >= INT32_MAX || draw_items >= INT32_MAX || B > 65535)
+    return fail(SPECDEC_ERR_UNSUPPORTED, "too many rows for one call");
+  const int sms = device_sm_count();
+  P.grid_stats = static_cast<int>(std::min<int64_t>(sms, (stat_items + kStatsWarps - 1) / kStatsWarps));
+  P.grid_draw = static_cast<int>(std::min<int64_t>(sms, (draw_items + kDrawWarps - 1) / kDrawWarps));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t counter_bytes = 0;
+  chain_workspace_layout(B, g, V, ldt, 2, workspace, &P.ws, &counter_bytes, true);
+  if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
+    return fail_cuda("clearing the workspace counters", e);
+  {
+    ProfScope prof(SPECDEC_KERNEL_CHAIN_STATS, s);
+    if (cudaError_t e = launch_chain_stream_stats(P, ldt, s); e != cudaSuccess) return fail_cuda("statistics kernel (block)", e);
+  }
+  {
+    ProfScope prof(SPECDEC_KERNEL_BLOCK_DECIDE, s);
+    if (cudaError_t e = launch_block_decide(P, ldt, s); e != cudaSuccess) return fail_cuda("block decision kernel", e);
+  }
+  {
+    ProfScope prof(SPECDEC_KERNEL_CHAIN_SAMPLE, s);
+    if (cudaError_t e = launch_chain_stream_draw(P, ldt, s); e != cudaSuccess) return fail_cuda("mass kernel (block)", e);
+  }
+  ProfScope prof(SPECDEC_KERNEL_BLOCK_FINISH, s);
+  if (cudaError_t e = launch_block_finish(P, ldt, s); e != cudaSuccess) return fail_cuda("block finish kernel", e);
+  return SPECDEC_OK;
 }
 
 size_t specdec_greedy_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {

@@ -39,6 +39,8 @@ struct ChainWorkspace {
   unsigned* draw_count;  // [1]: entries in draw_list
   float* draw_mass;      // [B*nchd]: residual (or bonus) mass per chunk of the drawn row
   unsigned* error;       // [1]: set when a bounded wait gave up
+  int* qbad;             // [B]: a bad draft probability met by the mass pass; cleared per call
+  float4* block_rows;    // [B*(g+1)]: block verification's (m, Z, w_k, 0) per row
   // left-to-right kernel: task queues (rows first, then draws)
   unsigned* queue;       // [5]: rows published, rows claimed, draws published, draws claimed, sequences finished
   int* ready;            // [B*g + 2B]: entry published (rows ring, then draws ring); cleared per call
@@ -110,7 +112,7 @@ int chain_segment_len(specdec_dtype ldt, bool vector_path);
 // Workspace layout; returns the total bytes (and fills ws when base != nullptr).
 // path: 0 scalar loads, 1 vector loads, 2 streaming (bulk copies).
 size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path,
-                              void* base, ChainWorkspace* ws, size_t* counter_bytes);
+                              void* base, ChainWorkspace* ws, size_t* counter_bytes, bool block = false);
 
 // Streaming path: statistics, decision, draw, finish -- chained with programmatic
 // dependent launch; the first launch follows ordinary stream order.
@@ -118,6 +120,9 @@ cudaError_t launch_chain_stream_stats(const ChainParams& P, specdec_dtype ldt, c
 cudaError_t launch_chain_stream_decide(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 cudaError_t launch_chain_stream_draw(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+// Block verification on the streaming statistics and mass kernels.
+cudaError_t launch_block_decide(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+cudaError_t launch_block_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 int device_sm_count();
 // Left-to-right chain verification reading rows only up to the first rejection.
 cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);

@@ -5,8 +5,11 @@ Rules (written here, used by every parity test):
 * Status bits, greedy tokens and greedy J: bit-exact.
 * p_i(x_i): within P_TOL absolute of the oracle's fp64 value.
 * Accept/reject decisions and drawn tokens: exact, except a FLAGGED disagreement:
-  - a decision may differ only at the first position where the two J differ, and only if
-    the oracle's uniform lies within FLAG_TOL of that test's boundary p/q;
+  - chain rule: a decision may differ only at the first position where the two J differ,
+    and only if the oracle's uniform lies within FLAG_TOL of that test's boundary p/q;
+  - block rule: the accepted lengths may differ only if the survival test of the longer
+    one lies within FLAG_TOL of its boundary (the test that one side passed and the
+    other did not);
   - a drawn token may differ only if the GPU's token has positive weight and the
     uniform lies within FLAG_TOL of that token's interval [C_{k-1}/S, C_k/S] of the
     oracle's CDF.
@@ -31,7 +34,7 @@ FLAG_TOL = 1e-5
 _W = {}
 
 
-def _init_worker(folder):
+def _init_worker(folder, mode="chain"):
     import sys
     here = os.path.dirname(os.path.abspath(__file__))
     root = os.path.dirname(here)
@@ -40,6 +43,7 @@ def _init_worker(folder):
             sys.path.insert(0, p)
     for name in ("logits", "q", "drafts", "T", "u", "gpu_tokens", "gpu_J"):
         _W[name] = np.load(os.path.join(folder, name + ".npy"), mmap_mode="r")
+    _W["mode"] = mode
 
 
 def _oracle_one(b):
@@ -49,7 +53,8 @@ def _oracle_one(b):
     drafts = np.asarray(_W["drafts"][b])
     T = float(_W["T"][b])
     u = np.asarray(_W["u"][b], dtype=np.float64)
-    r = so.verify_chain_sequence(logits, q, drafts, T, u, want_cdf=True)
+    verify = so.verify_block_sequence if _W["mode"] == "block" else so.verify_chain_sequence
+    r = verify(logits, q, drafts, T, u, want_cdf=True)
     gamma = len(drafts)
     out = {
         "tokens": r["tokens"], "J": r["J"], "status": r["status"], "p_draft": r["p_draft"],
@@ -74,9 +79,9 @@ def _oracle_one(b):
     return out
 
 
-def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None):
+def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None, mode="chain"):
     """Oracle summaries for every sequence (numpy inputs; logits already widened to
-    float32 for bf16 workloads, which is exact)."""
+    float32 for bf16 workloads, which is exact).  mode: "chain" or "block"."""
     B = logits.shape[0]
     with tempfile.TemporaryDirectory() as folder:
         arrays = {"logits": logits, "q": q if q is not None else np.zeros(0, np.float32),
@@ -85,12 +90,12 @@ def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None):
             np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(v))
         nw = workers if workers is not None else min(os.cpu_count() or 1, 16)
         if nw <= 1 or B <= 4:
-            _init_worker(folder)
+            _init_worker(folder, mode)
             res = [_oracle_one(b) for b in range(B)]
             _W.clear()
             return res
         ctx = mp.get_context("spawn")
-        with ctx.Pool(nw, initializer=_init_worker, initargs=(folder,)) as pool:
+        with ctx.Pool(nw, initializer=_init_worker, initargs=(folder, mode)) as pool:
             return pool.map(_oracle_one, range(B), chunksize=max(1, B // (4 * nw)))
 
 
@@ -127,9 +132,9 @@ class ParityReport:
             self.failures.append("...")
 
 
-def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray):
+def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray, rule: str = "chain"):
     """Compare one batch.  gpu: numpy tokens [B, g+1], num_accepted [B], status [B],
-    p_draft [B, g] (optional)."""
+    p_draft [B, g] (optional).  rule: "chain" or "block" (which test decides a length)."""
     B, g1 = gpu["tokens"].shape
     gamma = g1 - 1
     for b in range(B):
@@ -157,7 +162,7 @@ def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray):
                 if err > P_TOL:
                     report.fail(f"seq {b}: |p_draft error| {err:.3g} > {P_TOL}")
         if not o["greedy"]:
-            tested = min(o["J"] + 1, gamma)
+            tested = gamma if rule == "block" else min(o["J"] + 1, gamma)
             report.literal += int(np.sum(o["margins"][:tested] < FLAG_TOL)) + int(o["lit_draw"])
             report.draws += 1
         if o["greedy"]:
@@ -167,7 +172,7 @@ def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray):
             continue
         report.accepted += o["J"]
         if gJ != o["J"]:
-            i = min(gJ, o["J"])
+            i = (max(gJ, o["J"]) - 1) if rule == "block" else min(gJ, o["J"])
             if 0 <= i < gamma and o["margins"][i] < FLAG_TOL:
                 report.flag_decision += 1
             else:

@@ -21,7 +21,7 @@ def declared_functions():
 def test_header_declares_the_four_verification_calls():
     names = declared_functions()
     for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
-               "specdec_build_tree_mask"):
+               "specdec_build_tree_mask", "specdec_verify_block"):
         assert fn in names
 
 
@@ -47,6 +47,11 @@ def test_workspace_sizes(built_library):
     assert lib.specdec_chain_workspace_bytes(0, 7, 10, sd.BF16) == 0
     assert lib.specdec_chain_workspace_bytes(1, 7, 10, 9) == 0
     assert lib.specdec_greedy_workspace_bytes(4, 3, 100, sd.F32) == lib.specdec_chain_workspace_bytes(4, 3, 100, sd.F32)
+    # block verification keeps every row's residual masses: more than the chain's
+    blk = lib.specdec_block_workspace_bytes(256, 7, 128256, sd.BF16)
+    assert blk > a and blk % 256 == 0
+    assert lib.specdec_block_workspace_bytes(0, 7, 10, sd.BF16) == 0
+    assert lib.specdec_block_workspace_bytes(1, 7, 10, 9) == 0
 
 
 def _fake(n=64):
@@ -84,6 +89,13 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None, 0, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 100, p, p, p, None, None, 0, None) == sd.ERR_UNSUPPORTED
     assert lib.specdec_verify_tree(p, sd.BF16, p, p, p, p, 1, 2, 8, 2, None, p, p, None, None, 0, None) == sd.ERR_INVALID_ARG
+    # block: null q, unaligned rows (V = 4 bf16 is 8 bytes), too many drafts, small workspace
+    assert lib.specdec_verify_block(p, sd.BF16, None, p, p, p, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_block(p, sd.BF16, p, p, p, None, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 1, 4, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 32, 8, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 1, None) == sd.ERR_WORKSPACE
+    assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 0, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
     # mask
     assert lib.specdec_build_tree_mask(None, 4, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_build_tree_mask(p, 0, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
