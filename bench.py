@@ -330,7 +330,7 @@ def main():
         # block verification reads every logits row and every q row: the statistics pass
         # reads the logits, the mass pass both
         seq_bytes = rows * V * esize + B * g * V * 4
-        per_kernel_bytes = {"chain_stats": rows * V * esize, "chain_sample": seq_bytes}
+        per_kernel_bytes = {"chain_stats": rows * V * esize, "chain_sample": seq_bytes, "block_fused": seq_bytes}
         kname = max(per_kernel_bytes, key=lambda k: per_kernel.get(k, (0.0, 0))[0])
         alg_bytes = per_kernel_bytes[kname]
     elif per_kernel.get("chain_seq", (0.0, 0))[1]:

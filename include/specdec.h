@@ -216,7 +216,8 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_CHAIN_SEQ 6     /* left-to-right chain verification          */
 #define SPECDEC_KERNEL_BLOCK_DECIDE 7  /* block verification: weights per prefix    */
 #define SPECDEC_KERNEL_BLOCK_FINISH 8  /* block verification: survival and the draw */
-#define SPECDEC_NUM_KERNELS 9
+#define SPECDEC_KERNEL_BLOCK_FUSED 9   /* block verification in one launch           */
+#define SPECDEC_NUM_KERNELS 10
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

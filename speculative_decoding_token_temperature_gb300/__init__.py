@@ -39,7 +39,7 @@ STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
 KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
-                "chain_seq", "block_decide", "block_finish")
+                "chain_seq", "block_decide", "block_finish", "block_fused")
 
 
 class SpecdecError(RuntimeError):

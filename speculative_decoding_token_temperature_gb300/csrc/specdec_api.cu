@@ -41,6 +41,14 @@ bool use_left_to_right() {
   return v;
 }
 
+// Block verification runs as one launch that reads every row once, unless
+// SPECDEC_BLOCK_TWO_PASS=1 selects the statistics and mass kernels of the streaming path
+// (read at every call).
+bool block_two_pass() {
+  const char* e = std::getenv("SPECDEC_BLOCK_TWO_PASS");
+  return e && e[0] == '1';
+}
+
 // ---- last error (per host thread) -----------------------------------------------------
 thread_local char g_last_error[256] = "no error";
 
@@ -93,7 +101,10 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   // drawn rows: one per sequence, or (block verification) every row's residual masses
   const int64_t n_drawn = block ? rows : static_cast<int64_t>(B);
   int64_t n_part, draw_bytes;
-  if (path == 2) {
+  if (path == 3) {  // single-read block verification: only the error word
+    n_part = 0;
+    draw_bytes = 0;
+  } else if (path == 2) {
     const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(elem_size(ldt));
     n_part = rows * ((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
     draw_bytes = n_drawn * ((V + kDrawChunk - 1) / kDrawChunk) * static_cast<int64_t>(sizeof(float));
@@ -106,7 +117,8 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   // queue entries of the left-to-right kernel (streaming layout only)
   const int64_t n_entries = path == 2 ? static_cast<int64_t>(B) * g + 2 * static_cast<int64_t>(B) : 0;
   // (the streaming layout also keeps a bad-draft-probability flag per sequence)
-  const int64_t n_counters = std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries + (path == 2 ? B : 0));
+  const int64_t n_counters = path == 3 ? 0
+                                        : std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries + (path == 2 ? B : 0));
   size_t off = 0;
   const size_t o_error = off;    off += kAlign;
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * static_cast<size_t>(n_counters));
@@ -133,6 +145,7 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->ring = reinterpret_cast<float4*>(p + o_ring);
     ws->qbad = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries : nullptr;
     ws->block_rows = block ? reinterpret_cast<float4*>(p + o_brows) : nullptr;
+
   }
   return off;
 }
@@ -297,7 +310,8 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
 
 size_t specdec_block_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
   if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return 0;
-  return chain_workspace_layout(B, g, V, ldt, 2, nullptr, nullptr, nullptr, true);
+  return std::max(chain_workspace_layout(B, g, V, ldt, 2, nullptr, nullptr, nullptr, true),
+                  chain_workspace_layout(B, g, V, ldt, 3, nullptr, nullptr, nullptr, true));
 }
 
 int specdec_verify_block(const void* logits, specdec_dtype ldt, const float* draft_probs,
@@ -333,15 +347,25 @@ int specdec_verify_block(const void* logits, specdec_dtype ldt, const float* dra
   const int64_t row_bytes = static_cast<int64_t>(V) * static_cast<int64_t>(es);
   P.nch = static_cast<int>((row_bytes + kStatsChunkBytes - 1) / kStatsChunkBytes);
   P.nchd = (V + kDrawChunk - 1) / kDrawChunk;
+  const int sms = device_sm_count();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t counter_bytes = 0;
+  if (!block_two_pass() && block_fused_fits(g, V, ldt)) {  // one launch; every row read once
+    const int cm = block_mass_chunk(ldt);
+    P.nchm = (V + cm - 1) / cm;
+    chain_workspace_layout(B, g, V, ldt, 3, workspace, &P.ws, &counter_bytes, true);
+    if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
+      return fail_cuda("clearing the workspace counters", e);
+    ProfScope prof(SPECDEC_KERNEL_BLOCK_FUSED, s);
+    if (cudaError_t e = launch_block_fused(P, ldt, s); e != cudaSuccess) return fail_cuda("block verification kernel", e);
+    return SPECDEC_OK;
+  }
   const int64_t stat_items = static_cast<int64_t>(B) * (g + 1) * P.nch;
   const int64_t draw_items = static_cast<int64_t>(B) * (g + 1) * P.nchd;
   if (stat_items >= INT32_MAX || draw_items >= INT32_MAX || B > 65535)
     return fail(SPECDEC_ERR_UNSUPPORTED, "too many rows for one call");
-  const int sms = device_sm_count();
   P.grid_stats = static_cast<int>(std::min<int64_t>(sms, (stat_items + kStatsWarps - 1) / kStatsWarps));
   P.grid_draw = static_cast<int>(std::min<int64_t>(sms, (draw_items + kDrawWarps - 1) / kDrawWarps));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t counter_bytes = 0;
   chain_workspace_layout(B, g, V, ldt, 2, workspace, &P.ws, &counter_bytes, true);
   if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
     return fail_cuda("clearing the workspace counters", e);

@@ -40,7 +40,8 @@ struct ChainWorkspace {
   float* draw_mass;      // [B*nchd]: residual (or bonus) mass per chunk of the drawn row
   unsigned* error;       // [1]: set when a bounded wait gave up
   int* qbad;             // [B]: a bad draft probability met by the mass pass; cleared per call
-  float4* block_rows;    // [B*(g+1)]: block verification's (m, Z, w_k, 0) per row
+  float4* block_rows;    // [B*(g+1)]: block verification's (m, Z, w_k, w_k / Z) per row
+
   // left-to-right kernel: task queues (rows first, then draws)
   unsigned* queue;       // [5]: rows published, rows claimed, draws published, draws claimed, sequences finished
   int* ready;            // [B*g + 2B]: entry published (rows ring, then draws ring); cleared per call
@@ -100,6 +101,7 @@ struct ChainParams {
   int nch;               // streaming path: 4 KB chunks per logits row
   int nchd;              // streaming path: draw chunks per row
   int grid_stats, grid_draw;
+  int nchm;              // single-read block verification: mass chunks per row
   int32_t* out_tokens;
   int32_t* out_J;
   float* out_p_draft;
@@ -107,10 +109,22 @@ struct ChainParams {
   ChainWorkspace ws;
 };
 
+// Single-read block verification: elements of a row per mass item (logits + q fit 4 KB).
+constexpr int kBlockMassChunkBf16 = 640;
+constexpr int kBlockMassChunkF32 = 512;
+inline int block_mass_chunk(specdec_dtype ldt) {
+  return ldt == SPECDEC_BF16 ? kBlockMassChunkBf16 : kBlockMassChunkF32;
+}
+constexpr int kBlockWarps = 16;    // warps per CTA, one CTA per SM
+constexpr int kBlockStages = 3;    // 4 KB bulk-copy stages per warp
+constexpr int kBlockSlotsS = 512;  // 4 KB chunk summaries of one row (double-buffered)
+constexpr int kBlockSlotsM = 4096; // mass chunks of one sequence (all rows)
+
 // Segment length in elements for a logits dtype and load path.
 int chain_segment_len(specdec_dtype ldt, bool vector_path);
 // Workspace layout; returns the total bytes (and fills ws when base != nullptr).
-// path: 0 scalar loads, 1 vector loads, 2 streaming (bulk copies).
+// path: 0 scalar loads, 1 vector loads, 2 streaming (bulk copies), 3 single-read block
+// verification.
 size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path,
                               void* base, ChainWorkspace* ws, size_t* counter_bytes, bool block = false);
 
@@ -123,6 +137,11 @@ cudaError_t launch_chain_stream_finish(const ChainParams& P, specdec_dtype ldt, 
 // Block verification on the streaming statistics and mass kernels.
 cudaError_t launch_block_decide(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 cudaError_t launch_block_finish(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+// Block verification in one launch that reads every row once from HBM (each CTA walks
+// whole sequences row by row); block_fused_fits says whether a shape fits its
+// shared-memory tables.
+cudaError_t launch_block_fused(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+bool block_fused_fits(int g, int V, specdec_dtype ldt);
 int device_sm_count();
 // Left-to-right chain verification reading rows only up to the first rejection.
 cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);

@@ -25,6 +25,18 @@ def sd(built_library):
     return m
 
 
+@pytest.fixture(params=["one_launch", "two_pass"], autouse=True)
+def block_path(request, monkeypatch):
+    """Every test runs on both implementations: the single launch that reads each row
+    once (default) and the statistics + mass kernels (SPECDEC_BLOCK_TWO_PASS=1, read by
+    the library at every call)."""
+    if request.param == "two_pass":
+        monkeypatch.setenv("SPECDEC_BLOCK_TWO_PASS", "1")
+    else:
+        monkeypatch.delenv("SPECDEC_BLOCK_TWO_PASS", raising=False)
+    return request.param
+
+
 def _np(t):
     if t.dtype == torch.bfloat16:
         t = t.float()
@@ -32,6 +44,7 @@ def _np(t):
 
 
 def _run_and_check(sd, report, x, sample=None, workers=None):
+    report.name = report.name.split(" [")[0] + f" [{os.environ.get('SPECDEC_BLOCK_TWO_PASS') and 'two_pass' or 'one_launch'}]"
     out = sd.verify_block(*(x[k] for k in KEYS))
     torch.cuda.synchronize()
     idx = slice(None) if sample is None else sample
