@@ -539,6 +539,145 @@ def verify_tree_sequence(logits, node_tokens, parents, T: float, u, max_depth: i
     return out
 
 
+def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_depth: int,
+                            want_cdf: bool = False) -> dict:
+    """Sampled verification of a token tree by recursive rejection, for one sequence.
+
+    SD 20.5, box "Recursive rejection at a node with several children" (the multi-step
+    speculative sampling of Miao et al., SpecInfer): at the current node, whose children
+    s_1..s_k were drafted independently from q, start from R_1 = p (the target at the
+    node).  Try the children in turn: accept s_i when a uniform falls below
+    R_i(s_i) / q(s_i), and the walk moves to s_i's node; otherwise replace the target by
+    R_{i+1} = max(0, R_i - q) / sum max(0, R_i - q) and try the next child.  When every
+    child is rejected -- or the node has no children -- the extra token is drawn from the
+    last R and the walk ends.  The argument for a chain applies level by level.
+
+    logits [N+1, V]: row 0 is the target after the committed prefix (the root), row 1+i
+    after node i.  q [N+1, V]: row 0 is the distribution the root's children were drafted
+    from, row 1+i node i's children's.  u [N+1]: u[1+j] tests node j when it is tried,
+    u[0] drives the final draw.
+
+    READINGS: children are tried in node-index order; the test is `u * q(s) < R(s)` (the
+    chain rule's strict test, so q(s) = 0 accepts iff R(s) > 0, with the ZERO_Q warning);
+    the final draw is the inverse CDF of u[0] over R; a residual that sums to 0 after
+    rounding (R_i = q) keeps R_i, with the ZERO_RESIDUAL warning.  A greedy sequence
+    (T < GREEDY_T) descends into the lowest-index child carrying the argmax and emits the
+    argmax where none does (a one-hot target reduces the rule to it).  Validation: the
+    tree, every node token, T and (sampled) every uniform up front, as the Medusa walk
+    does; then, in walk order, the logits row of every visited node, q(s) of every tried
+    child, and the whole q row of a node at its first rejection (when the residual needs
+    it).  An error gives n_accepted -1 and -1 outputs.
+
+    Returns tokens [max_depth+1] (-1 padded), path [max_depth], n_accepted, status,
+    margins [N] (|u[1+j] - R(s_j)/q(s_j)| for every tried child j, inf otherwise) and,
+    for a sampled final draw, 'y_u' and (want_cdf) 'cdf', 'S'.
+    """
+    logits = np.asarray(logits)
+    n1, V = logits.shape
+    n = n1 - 1
+    parents = [int(x) for x in parents]
+    node_tokens = [int(x) for x in node_tokens]
+    u = widen(u).reshape(-1)
+    greedy = bool(T < GREEDY_T) or bool(np.isnan(T))
+    out = {
+        "tokens": np.full(max_depth + 1, -1, dtype=np.int64),
+        "path": np.full(max_depth, -1, dtype=np.int64),
+        "n_accepted": -1,
+        "status": 0,
+        "margins": np.full(n, np.inf),
+        "greedy": greedy,
+    }
+    status = 0 if np.isfinite(T) else STATUS_BAD_TEMPERATURE
+    try:
+        depth = tree_depths(parents)
+        if n and depth.max() + 1 > max_depth:
+            status |= STATUS_BAD_TREE
+    except ValueError:
+        status |= STATUS_BAD_TREE
+    for t in node_tokens:
+        if not (0 <= t < V):
+            status |= STATUS_BAD_TOKEN
+    if not greedy and not np.all((u >= 0.0) & (u < 1.0)):
+        status |= STATUS_BAD_UNIFORM
+    if status & STATUS_ERROR_MASK:
+        out["status"] = status
+        return out
+
+    def fail(bits):
+        out["tokens"][:] = -1
+        out["path"][:] = -1
+        out["n_accepted"] = -1
+        out["status"] = status | bits
+        return out
+
+    node, d = -1, 0
+    while True:
+        row = 0 if node == -1 else 1 + node
+        rs = _row_status(logits[row])
+        if rs:
+            return fail(rs)
+        children = [j for j in range(n) if parents[j] == node]
+        if greedy:
+            y = lowest_argmax(logits[row])
+            child = next((j for j in children if node_tokens[j] == y), None)
+        else:
+            R = target_distribution(logits[row], T)
+            qn = widen(q[row]) if children else None
+            q_checked = False
+            child = None
+            for j in children:
+                s = node_tokens[j]
+                qs = qn[s]
+                if not (np.isfinite(qs) and qs >= 0.0):
+                    return fail(STATUS_BAD_PROB)
+                if qs == 0.0:
+                    status |= STATUS_ZERO_Q
+                    out["margins"][j] = np.inf
+                    accept = R[s] > 0.0
+                else:
+                    out["margins"][j] = abs(u[1 + j] - R[s] / qs)
+                    accept = u[1 + j] * qs < R[s]
+                if accept:
+                    child = j
+                    break
+                if not q_checked:  # the residual reads the whole row
+                    if not np.all(np.isfinite(qn) & (qn >= 0.0)):
+                        return fail(STATUS_BAD_PROB)
+                    q_checked = True
+                r = np.maximum(R - qn, 0.0)
+                if r.sum() > 0.0:
+                    R = r / r.sum()
+                else:
+                    status |= STATUS_ZERO_RESIDUAL
+            if child is None:
+                y, C, S = inverse_cdf(R, u[0])
+                out["y_u"] = u[0] * S
+                if want_cdf:
+                    out["cdf"], out["S"] = C, S
+        if child is None:
+            out["tokens"][d] = y
+            break
+        out["tokens"][d] = node_tokens[child]
+        out["path"][d] = child
+        node, d = child, d + 1
+    out["n_accepted"] = d
+    out["status"] = status
+    return out
+
+
+def verify_tree_rr(logits, q, node_tokens, parents, T, u, max_depth: int) -> dict:
+    """Batched recursive-rejection tree verification: a loop of verify_tree_rr_sequence."""
+    B = np.asarray(logits).shape[0]
+    res = [verify_tree_rr_sequence(logits[b], q[b], node_tokens[b], parents, float(T[b]), u[b], max_depth)
+           for b in range(B)]
+    return {
+        "tokens": np.stack([r["tokens"] for r in res]),
+        "path": np.stack([r["path"] for r in res]),
+        "n_accepted": np.array([r["n_accepted"] for r in res]),
+        "status": np.array([r["status"] for r in res]),
+    }
+
+
 def verify_tree(logits, node_tokens, parents, T, u, max_depth: int) -> dict:
     """Batched tree verification: loop of verify_tree_sequence over the batch."""
     B = np.asarray(logits).shape[0]

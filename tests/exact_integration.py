@@ -183,3 +183,47 @@ def first_two_tokens_law(verify_rows, P, Q, start: int, gamma: int, round_law=No
             for out2, m2 in cache[y1].items():
                 joint[y1, out2[0]] += m * m2
     return joint
+
+
+def tree_rr_outcome_law(verify, parents) -> dict:
+    """Law of the emitted token tuple of one tree round with fixed node tokens.
+
+    verify(u) -> (emitted tokens, accepted path), both tuples; u has N + 1 entries: u[1+j]
+    tests node j when the walk tries it, u[0] drives the final draw.  Structure assumed
+    of the verifier (a wrong verifier then yields a wrong law, which the pins catch): at
+    a node the children are tried in index order; child j is accepted on [0, t_j) of
+    u[1+j] given the decisions before it, and the walk then continues below j; when every
+    child is rejected the emitted token is a step function of u[0].  Each t_j is located
+    by bisection on the verifier, with the decided uniforms held inside their intervals.
+    """
+    N = len(parents)
+    law = defaultdict(float)
+
+    def uniforms(fixed, slot=None, x=None):
+        uu = [0.5] * (N + 1)
+        for k, v in fixed.items():
+            uu[k] = v
+        if slot is not None:
+            uu[slot] = x
+        return uu
+
+    def recurse(fixed, node, weight):
+        fixed = dict(fixed)
+        for j in [j for j in range(N) if parents[j] == node]:
+            def accepted(x, j=j, fixed=dict(fixed)):
+                return j in verify(uniforms(fixed, 1 + j, x))[1]
+            t = _last_u_with(accepted, 0.0, True) if accepted(0.0) else 0.0
+            if t > 0.0:
+                recurse({**fixed, 1 + j: 0.5 * t}, j, weight * t)
+            if t >= 1.0:
+                return
+            fixed[1 + j] = 0.5 * (1.0 + t)
+            weight *= 1.0 - t
+
+        def tok(x, fixed=fixed):
+            return verify(uniforms(fixed, 0, x))[0]
+        for out, m in step_function_masses(tok).items():
+            law[out] += weight * m
+
+    recurse({}, -1, 1.0)
+    return dict(law)
