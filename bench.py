@@ -12,6 +12,9 @@ tests up to the first rejection, residual/bonus draw).
 
 --rule block times block verification (specdec_verify_block: the draft judged jointly,
 every row and q row read) on the same workload instead of the chain rule.
+--rule tree_recursive times sampled tree verification by recursive rejection
+(specdec_verify_tree_recursive) on tree_rr_b32_n64_v32000 (the Medusa sparse tree's
+topology, tokens drafted i.i.d. per node); rows are B*(N+1) candidate rows per call.
 
 Prints one JSON line (rank 0).  Metric: verified vocab rows per second, B*(gamma+1)
 rows per call, whole job over all ranks.  Several GPUs run independent replicas
@@ -219,6 +222,159 @@ def run_reference(args, rank):
     return 0
 
 
+TREE_RR_WORKLOAD = "tree_rr_b32_n64_v32000"
+
+
+def run_tree_rr(args, rank, world, local_rank):
+    """Sampled tree verification by recursive rejection: the same timing contract."""
+    import numpy as np
+    import torch
+    import workloads
+    from oracle import specdec_oracle as so  # the tree topology and the CPU baseline only
+
+    w = workloads.TREE_RR_WORKLOADS[TREE_RR_WORKLOAD]
+    B, V, D = w["B"], w["V"], w["depth"]
+    parents, _, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
+    N = len(parents)
+    rows = B * (N + 1)
+    keys = ("logits", "draft_probs", "node_tokens", "parents", "temperatures", "uniforms")
+    base = {"metric": METRIC, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+    cfg = {"workload": TREE_RR_WORKLOAD, "rule": "tree_recursive", "B": B, "N": N, "V": V, "max_depth": D,
+           "logits_dtype": w["dtype"], "draft_probs_dtype": "fp32"}
+
+    def oracle_rate(x, seconds, max_seqs):
+        L = x["logits"].float().numpy() if w["dtype"] == "bf16" else x["logits"].numpy()
+        q, t, T, u = (x[k].numpy() for k in ("draft_probs", "node_tokens", "temperatures", "uniforms"))
+        n, t0 = 0, time.perf_counter()
+        while n < max_seqs:
+            so.verify_tree_rr_sequence(L[n % B], q[n % B], t[n % B], parents, float(T[n % B]), u[n % B], D)
+            n += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        return n * (N + 1) / dt, n, dt
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        torch.set_num_threads(1)
+        x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 0, "cpu")
+        per_step = args.ref_sequences
+        for _ in range(args.warmup):
+            oracle_rate(x, 1e9, per_step)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_rate(x, 1e9, per_step)
+        dt = (time.perf_counter() - t0) / args.steps
+        value = per_step * (N + 1) / dt
+        line = dict(base, impl="reference", value=value, ms_per_step=dt * 1e3, dtype="f64",
+                    config=dict(cfg, step_sample_sequences=per_step),
+                    cpu_baseline={"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": f"{per_step} sequences of {TREE_RR_WORKLOAD} per step"},
+                    e2e={"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import speculative_decoding_token_temperature_gb300 as sd
+    from speculative_decoding_token_temperature_gb300 import build as _build
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.ensure_built()
+    sd.load_library()
+    sets = [workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 100 * rank + s, dev) for s in range(args.sets)]
+    outs = [{"tokens": torch.empty(B, D + 1, dtype=torch.int32, device=dev),
+             "path": torch.empty(B, D, dtype=torch.int32, device=dev),
+             "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+             "status": torch.empty(B, dtype=torch.int32, device=dev)} for _ in sets]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x = sets[i % len(sets)]
+        sd.verify_tree_recursive(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank, uuid) as clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t)
+    ms_per_step = elapsed_ms / args.steps
+    with sd.KernelTimer(max_launches=2 * args.steps + 16) as kt:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            step(i)
+        torch.cuda.synchronize()
+        per_kernel = kt.read()
+    k_ms, k_n = per_kernel["tree_rr"]
+    # a lower bound on the bytes the walk must read: every visited node's logits row once,
+    # and the q row of every node where the walk ended with children (all rejected)
+    es = 2 if w["dtype"] == "bf16" else 4
+    has_kids = np.zeros(N + 1, dtype=bool)
+    for j, a in enumerate(parents):
+        has_kids[0 if a < 0 else 1 + a] = True
+    alg = []
+    for o in outs:
+        J = o["num_accepted"].cpu().numpy()
+        path = o["path"].cpu().numpy()
+        tot = 0
+        for b in range(B):
+            if J[b] < 0:
+                continue
+            tot += (J[b] + 1) * V * es
+            last = 0 if J[b] == 0 else 1 + int(path[b][J[b] - 1])
+            if has_kids[last]:
+                tot += V * 4
+        alg.append(tot)
+    alg_bytes = float(np.mean(alg))
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
+    achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
+    line = dict(base, value=rows * world / (ms_per_step / 1e3), ms_per_step=ms_per_step, dtype="f32", config=dict(
+        cfg, parallelism=f"replicas x{world}", l2=f"{args.sets} seeded batches rotated (inputs smaller than L2)"),
+        roofline={"kernel": "tree_rr", "bound": "latency", "achieved": achieved,
+                  "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
+                  "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,
+                  "traffic": None},
+        kernels_ms_per_launch={k: v[0] / v[1] for k, v in per_kernel.items() if v[1]},
+        gpu_launches=int(round(sum(v[1] for v in per_kernel.values()))),
+        mean_accepted=float(np.mean([o["num_accepted"].float().mean().item() for o in outs])),
+        clocks=clocks.summary(), kernel_src_sha=kernel_source_sha())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x0 = {k: v.cpu() for k, v in sets[0].items()}
+        rate, nseq, secs = oracle_rate(x0, args.cpu_seconds, 10 ** 9)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{nseq} sequences of one batch, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -232,7 +388,7 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--rule", choices=["chain", "block"], default="chain")
+    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive"], default="chain")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -240,6 +396,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.rule == "tree_recursive":
+        return run_tree_rr(args, rank, world, local_rank)
     if args.impl == "reference":
         return run_reference(args, rank)
 

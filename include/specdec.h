@@ -185,6 +185,46 @@ int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* no
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Sampled tree verification by recursive rejection (SD 20.5, box "Recursive rejection at
+ * a node with several children"; the multi-step speculative sampling of SpecInfer).
+ *
+ * At the current node, whose children s_1..s_k were drafted independently from q, start
+ * from R_1 = p = softmax(logits / T) at the node; try the children in node-index order:
+ * accept s_i when uniforms[b, 1 + s_i's node id] * q(s_i) < R_i(s_i) and move to it;
+ * otherwise R_{i+1} = (R_i - q)+ normalised and try the next child.  When every child is
+ * rejected (or the node is a leaf) the extra token is the inverse-CDF draw of
+ * uniforms[b, 0] from the last R (smallest v with C_v > u * S) and the walk ends.  The
+ * emitted tokens follow the target exactly when every node's children are independent
+ * draws from that node's q.  A greedy sequence descends into the lowest-index child
+ * carrying the argmax and emits the argmax where none does.
+ *
+ * logits        [B, N+1, V]  row 0: after the committed prefix (the root); row 1+i: after node i
+ * draft_probs   [B, N+1, V]  fp32: row 0: the distribution the root's children were drafted
+ *                            from; row 1+i: node i's children's (leaf rows are not read)
+ * node_tokens   [B, N]       int32
+ * parents       [N]          int32, shared by the batch, parents[i] in [-1, i)
+ * temperatures  [B]          fp32
+ * uniforms      [B, N+1]     fp32 in [0, 1): slot 1+j tests node j, slot 0 the final draw
+ * out_tokens    [B, D+1]     int32: the accepted node tokens then the final draw, -1 padded
+ * out_path      [B, D]       int32: node ids of the accepted path, -1 padded
+ * out_num_accepted [B]       int32: accepted nodes (or -1 on a data error)
+ * out_status    [B]          int32, optional: the tree, every token, T and (sampled) every
+ *                            uniform are checked first; then, along the walk, each visited
+ *                            row (BAD_LOGIT, EMPTY_ROW), q(s) of each tried child and a q
+ *                            row read whole at its node's first rejection (BAD_PROB).  An
+ *                            error reports error bits only.  Warnings: ZERO_Q (a tried
+ *                            child with q(s) = 0: accepted iff R(s) > 0), ZERO_RESIDUAL
+ *                            (a residual summed to 0 after rounding; R_i is kept).
+ * max_depth D bounds the number of nodes on any root path.  N >= 0, 1 <= D <= 64.  No
+ * workspace is needed (specdec_tree_workspace_bytes applies and returns 0).
+ */
+int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                  const int32_t* node_tokens, const int32_t* parents,
+                                  const float* temperatures, const float* uniforms, int B, int N, int V,
+                                  int max_depth, int32_t* out_tokens, int32_t* out_path,
+                                  int32_t* out_num_accepted, int32_t* out_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Tree-attention mask and position ids (SD 20.5, box "Token tree and tree attention").
  *   out_mask          [N, P+N] uint8: row i is 1 on every prefix column j < P, on column
  *                     P+i and on column P+a for every ancestor a of node i; 0 elsewhere
@@ -217,7 +257,8 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_BLOCK_DECIDE 7  /* block verification: weights per prefix    */
 #define SPECDEC_KERNEL_BLOCK_FINISH 8  /* block verification: survival and the draw */
 #define SPECDEC_KERNEL_BLOCK_FUSED 9   /* block verification in one launch           */
-#define SPECDEC_NUM_KERNELS 10
+#define SPECDEC_KERNEL_TREE_RR 10      /* tree verification by recursive rejection   */
+#define SPECDEC_NUM_KERNELS 11
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

@@ -603,11 +603,11 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
         out["status"] = status
         return out
 
-    def fail(bits):
+    def fail(bits):  # an error reports error bits only (warnings describe a clean round)
         out["tokens"][:] = -1
         out["path"][:] = -1
         out["n_accepted"] = -1
-        out["status"] = status | bits
+        out["status"] = (status | bits) & STATUS_ERROR_MASK
         return out
 
     node, d = -1, 0

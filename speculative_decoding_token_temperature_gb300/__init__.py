@@ -39,7 +39,7 @@ STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
 KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
-                "chain_seq", "block_decide", "block_finish", "block_fused")
+                "chain_seq", "block_decide", "block_finish", "block_fused", "tree_rr")
 
 
 class SpecdecError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library():
     lib.specdec_verify_greedy.restype = i32
     lib.specdec_verify_tree.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_tree.restype = i32
+    lib.specdec_verify_tree_recursive.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.specdec_verify_tree_recursive.restype = i32
     lib.specdec_build_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_build_tree_mask.restype = i32
     lib.specdec_profile_start.argtypes = [i32]
@@ -284,6 +286,45 @@ def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth:
                                  _ptr(out.get("status")), _ptr(ws), wsb,
                                  ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_tree")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperatures, uniforms, max_depth: int, *,
+                          out=None, stream=None) -> dict:
+    """Sampled tree verification by recursive rejection (specdec_verify_tree_recursive).
+
+    logits [B, N+1, V] bf16/fp32; draft_probs [B, N+1, V] fp32 (row 0: the root's children
+    were drafted from it, row 1+i: node i's children); node_tokens [B, N] int32; parents
+    [N] int32; temperatures [B]; uniforms [B, N+1] (slot 1+j tests node j, slot 0 the final
+    draw).  Returns tokens [B, D+1], path [B, D], num_accepted [B], status [B]."""
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    logits, draft_probs, node_tokens, parents, temperatures, uniforms = (
+        rt.to_device(t) for t in (logits, draft_probs, node_tokens, parents, temperatures, uniforms))
+    B, n1, V = logits.shape
+    N = n1 - 1
+    D = int(max_depth)
+    dev = logits.device
+    code = _dtype_code(logits)
+    _need(draft_probs, "draft_probs", torch.float32, (B, n1, V), dev)
+    _need(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    _need(parents, "parents", torch.int32, (N,), dev)
+    _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, n1), dev)
+    _need(logits, "logits", None, (B, n1, V), dev)
+    if out is None:
+        out = {
+            "tokens": torch.empty(B, D + 1, dtype=torch.int32, device=dev),
+            "path": torch.empty(B, D, dtype=torch.int32, device=dev),
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.specdec_verify_tree_recursive(_ptr(logits), code, _ptr(draft_probs), _ptr(node_tokens), _ptr(parents),
+                                           _ptr(temperatures), _ptr(uniforms), B, N, V, D,
+                                           _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["num_accepted"]),
+                                           _ptr(out.get("status")), ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_tree_recursive")
     return {k: rt.to_host(v) for k, v in out.items()}
 
 

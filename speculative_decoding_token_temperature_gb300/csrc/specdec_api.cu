@@ -437,6 +437,39 @@ int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* no
   return SPECDEC_OK;
 }
 
+int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                  const int32_t* node_tokens, const int32_t* parents,
+                                  const float* temperatures, const float* uniforms, int B, int N, int V,
+                                  int max_depth, int32_t* out_tokens, int32_t* out_path,
+                                  int32_t* out_num_accepted, int32_t* out_status, void* stream) {
+  if (!valid_dtype(ldt)) return fail(SPECDEC_ERR_INVALID_ARG, "unknown logits dtype");
+  if (B <= 0 || N < 0 || V <= 0 || max_depth < 1) return fail(SPECDEC_ERR_INVALID_ARG, "bad sizes");
+  if (!logits || !draft_probs || !temperatures || !uniforms || !out_tokens || !out_path || !out_num_accepted)
+    return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  if (N > 0 && (!node_tokens || !parents)) return fail(SPECDEC_ERR_INVALID_ARG, "node tokens and parents needed");
+  if (max_depth > kMaxTreeDepth) return fail(SPECDEC_ERR_UNSUPPORTED, "max_depth above 64");
+  TreeParams P{};
+  P.logits = logits;
+  P.q = draft_probs;
+  P.node_tokens = node_tokens;
+  P.parents = parents;
+  P.temps = temperatures;
+  P.u = uniforms;
+  P.B = B;
+  P.N = N;
+  P.V = V;
+  P.D = max_depth;
+  P.out_tokens = out_tokens;
+  P.out_path = out_path;
+  P.out_J = out_num_accepted;
+  P.out_status = out_status;
+  const bool vec = rows_vectorizable(logits, V, elem_size(ldt)) && rows_vectorizable(draft_probs, V, 4);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_TREE_RR, s);
+  if (cudaError_t e = launch_tree_rr(P, ldt, vec, s); e != cudaSuccess) return fail_cuda("tree recursive-rejection kernel", e);
+  return SPECDEC_OK;
+}
+
 int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* out_mask,
                             int64_t* out_position_ids, int32_t* out_depth, int32_t* out_status,
                             void* stream) {

@@ -153,6 +153,7 @@ cudaError_t launch_chain_sample(const ChainParams& P, specdec_dtype ldt, bool ve
 
 struct TreeParams {
   const void* logits;
+  const float* q;        // recursive rejection: [B, N+1, V] drafting distributions per node
   const int32_t* node_tokens;
   const int32_t* parents;
   const float* temps;
@@ -166,6 +167,8 @@ struct TreeParams {
 
 cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector_path,
                              cudaStream_t stream);
+// Sampled tree verification by recursive rejection at every node.
+cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream);
 cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* mask,
                              int64_t* pos, int32_t* depth, int32_t* status, cudaStream_t stream);
 

@@ -21,7 +21,7 @@ def declared_functions():
 def test_header_declares_the_four_verification_calls():
     names = declared_functions()
     for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
-               "specdec_build_tree_mask", "specdec_verify_block"):
+               "specdec_build_tree_mask", "specdec_verify_block", "specdec_verify_tree_recursive"):
         assert fn in names
 
 
@@ -96,6 +96,11 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 32, 8, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
     assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 1, None) == sd.ERR_WORKSPACE
     assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 0, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    # recursive-rejection tree walk: null q, bad depth
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, None, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 65, p, p, p, None, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_tree_recursive(p, 5, p, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
     # mask
     assert lib.specdec_build_tree_mask(None, 4, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_build_tree_mask(p, 0, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG

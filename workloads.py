@@ -47,6 +47,12 @@ CHAIN_WORKLOADS = {
                                scale=3.0, zipf_s=1.0, noise="uniform:0.5:2.5", temps="uniform:0.0:1.2"),
 }
 
+TREE_RR_WORKLOADS = {
+    # the Medusa sparse tree's topology (64 nodes, depth 4), tokens drafted i.i.d. per node
+    "tree_rr_b32_n64_v32000": dict(number=7, B=32, V=32000, dtype="bf16", depth=4, recipe="spikes",
+                                   scale=4.0, n_spikes=8, spike=8.0, noise=1.0, temps="uniform:0.0:1.2"),
+}
+
 TREE_WORKLOADS = {
     "tree_b32_n64_v32000": dict(number=4, B=32, V=32000, dtype="bf16", depth=4, top=10,
                                 scale=4.0, spike=8.0, spike_prob=0.5, temps="half_greedy:0.7"),
@@ -185,6 +191,62 @@ def make_tree_inputs(B: int, V: int, parents, paths, *, depth: int, seed: int = 
         "temperatures": T.contiguous(),
         "uniforms": u.contiguous(),
     }
+
+
+def make_tree_rr_inputs(B: int, V: int, parents, *, depth: int, seed: int = 0, device="cpu",
+                        dtype: str = "bf16", recipe: str = "spikes", scale: float = 4.0, n_spikes: int = 8,
+                        spike: float = 8.0, noise=1.0, temps: str = "const:1.0") -> dict:
+    """Seeded inputs for sampled tree verification with per-node drafting distributions.
+
+    Target logits per node (row 0: the root), a drafter that sees the target logits plus
+    Gaussian noise (q = softmax((l + noise) / T), one-hot at its argmax for a greedy
+    sequence), and every node's token drawn from its parent's q row, independently for
+    siblings.  Returns logits [B, N+1, V], draft_probs [B, N+1, V] fp32, node_tokens
+    [B, N] int32, parents [N] int32, temperatures [B], uniforms [B, N+1].
+    """
+    g = _gen(device, seed)
+    N = len(parents)
+    rows = B * (N + 1)
+    t = scale * torch.randn(B, N + 1, V, generator=g, device=device)
+    if recipe == "spikes":
+        ids = _spike_ids(rows, V, min(n_spikes, V), g, device)
+        t.view(rows, V).scatter_add_(1, ids, torch.full(ids.shape, spike, device=device))
+    else:
+        raise ValueError(recipe)
+    sigma = _noise_scale(noise, B, g, device)
+    d = t + sigma * torch.randn(B, N + 1, V, generator=g, device=device)
+    T = _temperatures(temps, B, g, device)
+    greedy = T < GREEDY_BELOW
+    Tq = torch.where(greedy, torch.ones_like(T), T).view(B, 1, 1)
+    q = torch.softmax(d / Tq, dim=-1)
+    if greedy.any():
+        hot = torch.zeros_like(q[greedy])
+        hot.scatter_(2, d[greedy].argmax(dim=-1, keepdim=True), 1.0)
+        q[greedy] = hot
+    del d
+    parent_row = torch.tensor([0 if a < 0 else 1 + a for a in parents], dtype=torch.long, device=device)
+    if N:
+        qp = q[:, parent_row, :].reshape(B * N, V)
+        node_tokens = torch.multinomial(qp, 1, generator=g).view(B, N)
+    else:
+        node_tokens = torch.zeros(B, 0, dtype=torch.long, device=device)
+    u = torch.rand(B, N + 1, generator=g, device=device)
+    logits = t.to(torch.bfloat16) if dtype == "bf16" else t
+    return {
+        "logits": logits.contiguous(),
+        "draft_probs": q.contiguous(),
+        "node_tokens": node_tokens.to(torch.int32).contiguous(),
+        "parents": torch.tensor(list(parents), dtype=torch.int32, device=device),
+        "temperatures": T.contiguous(),
+        "uniforms": u.contiguous(),
+    }
+
+
+def tree_rr_workload(name: str, parents, round_idx: int = 0, device="cpu") -> dict:
+    w = dict(TREE_RR_WORKLOADS[name])
+    number = w.pop("number")
+    return make_tree_rr_inputs(w.pop("B"), w.pop("V"), parents, depth=w.pop("depth"),
+                               seed=seed_for(number, round_idx), device=device, **w)
 
 
 def tree_workload(name: str, parents, paths, round_idx: int = 0, device="cpu") -> dict:
