@@ -61,6 +61,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
 #define SPECDEC_STATUS_BAD_UNIFORM 16       /* uniform outside [0, 1) on a sampled sequence   */
 #define SPECDEC_STATUS_BAD_TREE 32          /* parent not in [-1, i), or tree deeper than D   */
 #define SPECDEC_STATUS_BAD_TEMPERATURE 64   /* temperature NaN or infinite                    */
+#define SPECDEC_STATUS_TIMEOUT 128          /* a bounded wait inside a kernel gave up (internal) */
 #define SPECDEC_STATUS_ERROR_MASK 0xFF
 #define SPECDEC_STATUS_ZERO_Q 256           /* warning: q_i(x_i) == 0; accepted iff p_i(x_i) > 0 */
 #define SPECDEC_STATUS_ZERO_RESIDUAL 512    /* warning: residual mass 0 after rounding; drew from p */

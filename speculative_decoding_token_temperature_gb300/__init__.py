@@ -34,6 +34,7 @@ STATUS_BAD_PROB = 8
 STATUS_BAD_UNIFORM = 16
 STATUS_BAD_TREE = 32
 STATUS_BAD_TEMPERATURE = 64
+STATUS_TIMEOUT = 128
 STATUS_ERROR_MASK = 0xFF
 STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512

@@ -142,37 +142,77 @@ template <int NT> struct Block {
     return r;
   }
 
+  // fp64 sum; the cross-warp step runs in warp 0 only (fp64 is slow on this part), and
+  // the result is broadcast through sh[kWarps].  sh holds 2 * kWarps doubles.
   static __device__ __forceinline__ double sum(double v, double* sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) sh[w] = v;
-    __syncthreads();
-    double r = 0.0;
+    return cross_warp_sum(v, sh);
+  }
+  // Sum of fp32 values: fp32 within each warp, fp64 across warps.
+  static __device__ __forceinline__ double sum_f(float v, double* sh) {
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) r += sh[i];
-    return r;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return cross_warp_sum(static_cast<double>(v), sh);
   }
 
-  // Inclusive prefix sum in thread order; also returns the block total.
+  // Inclusive prefix sum in thread order (fp64); also returns the block total.
   static __device__ __forceinline__ double inclusive_scan(double v, double* sh, double& total) {
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int l = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double n = __shfl_up_sync(0xffffffffu, v, o);
       if (l >= o) v += n;
     }
-    __syncthreads();
-    if (l == 31) sh[w] = v;
-    __syncthreads();
-    double off = 0.0;
-    for (int i = 0; i < w; ++i) off += sh[i];
-    double t = 0.0;
+    return cross_warp_scan(v, sh, total);
+  }
+  // The same for fp32 values: fp32 within each warp, fp64 across warps.
+  static __device__ __forceinline__ double inclusive_scan_f(float v, double* sh, double& total) {
+    const int l = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) t += sh[i];
-    total = t;
-    return v + off;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, v, o);
+      if (l >= o) v += n;
+    }
+    return cross_warp_scan(static_cast<double>(v), sh, total);
+  }
+
+ private:
+  // v: this warp's total (every lane).  Warp 0 adds the kWarps totals in a fixed order.
+  static __device__ __forceinline__ double cross_warp_sum(double v, double* sh) {
+    static_assert(kWarps <= 16, "sh holds 2 * kWarps doubles in 32-entry arrays");
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    if (w == 0) {
+      double x = (l < kWarps) ? sh[l] : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (l == 0) sh[kWarps] = x;
+    }
+    __syncthreads();
+    return sh[kWarps];
+  }
+  // incl: this thread's inclusive prefix within its warp; the warp total is lane 31's.
+  static __device__ __forceinline__ double cross_warp_scan(double incl, double* sh, double& total) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 31) sh[w] = incl;
+    __syncthreads();
+    if (w == 0) {  // inclusive scan of the warp totals
+      double x = (l < kWarps) ? sh[l] : 0.0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, x, o);
+        if (l >= o) x += n;
+      }
+      __syncwarp();
+      if (l < kWarps) sh[kWarps + l] = x;
+    }
+    __syncthreads();
+    total = sh[2 * kWarps - 1];
+    return (w ? sh[kWarps + w - 1] : 0.0) + incl;
   }
 };
 

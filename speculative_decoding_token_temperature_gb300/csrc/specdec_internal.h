@@ -15,6 +15,7 @@ constexpr int kScalarElemsPerThread = 32;    // elements per thread per segment 
 constexpr int kMaxGamma = 255;               // drafts per sequence handled by one decision CTA
 constexpr int kTreeThreads = 512;
 constexpr int kMaxTreeDepth = 64;
+constexpr int kTreeStageBytes = 200 * 1024;  // a node's logits + q rows staged in shared memory
 
 // Per-sequence state handed from the decision step to the draw step.
 struct SeqState {

@@ -96,17 +96,17 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
 
       int y = z;
       if (!greedy) {
-        // pass 2: total mass (per-vector fp32 running sums, fp64 across vectors)
-        double tot = 0.0;
+        // pass 2: total mass (fp32 within a thread and a warp, fp64 across warps)
+        float tot = 0.f;
         for (int k = tid * VEC; k < V; k += NT * VEC) {
           float v[VEC];
           VecLoad<T, VEC>::load(lrow, k, v);
           float a = 0.f;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) a += ex2((v[e] - m) * c);
-          tot += static_cast<double>(a);
+          tot += a;
         }
-        const double S = Block<NT>::sum(tot, sh_d);
+        const double S = Block<NT>::sum_f(tot, sh_d);
         const double target = static_cast<double>(__ldg(P.u + static_cast<int64_t>(b) * (D + 1) + d)) * S;
         // pass 3: tiles of NT vectors in index order until the running mass passes target
         double base = 0.0;
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
             for (int e = 0; e < VEC; ++e) w[e] = 0.f;
           }
           double total;
-          const double incl = Block<NT>::inclusive_scan(static_cast<double>(a), sh_d, total);
+          const double incl = Block<NT>::inclusive_scan_f(a, sh_d, total);
           if (base + total > target) {
             const int first = Block<NT>::min_int((base + incl > target) ? tid : INT_MAX, sh_i);
             if (tid == first) {

@@ -16,7 +16,10 @@
 //   tests    in child order; each rejection: one residual pass (also checks the q row
 //            the first time it is read whole)
 //   draw     tiles in index order until the running weight passes u[0] * S
-// Only the rows the walk visits are read.
+// Only the rows the walk visits are read.  When a node's logits and q rows fit in shared
+// memory (V = 32000 bf16: 64 KB + 128 KB), they are staged there by bulk copies as the walk
+// reaches the node, and every pass reads shared memory instead of making a round trip to
+// L2 or HBM.
 
 #include <climits>
 
@@ -27,12 +30,54 @@ namespace specdec {
 
 namespace {
 
-template <typename T, int VEC, int NT>
+// Row reads from global memory (read-only path) or from the rows staged in shared memory.
+template <typename T, int VEC, bool SMEM> struct RowAccess {
+  static __device__ __forceinline__ void vec(const T* p, int64_t k, float (&v)[VEC]) {
+    if constexpr (!SMEM || VEC == 1) {
+      VecLoad<T, VEC>::load(p, k, v);
+    } else if constexpr (sizeof(T) == 2) {
+      const uint4 w = *reinterpret_cast<const uint4*>(p + k);
+      v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+      v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    } else {
+      const float4 w = *reinterpret_cast<const float4*>(p + k);
+      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    }
+  }
+  static __device__ __forceinline__ float one(const T* p, int64_t k) {
+    if constexpr (!SMEM) return Elem<T>::load(p, k);
+    else if constexpr (sizeof(T) == 2) return __uint_as_float(static_cast<uint32_t>(p[k]) << 16);
+    else return p[k];
+  }
+  static __device__ __forceinline__ void qvec(const float* p, int64_t k, float (&v)[VEC]) {
+    if constexpr (!SMEM) {
+      load_q<VEC>(p, k, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VEC; j += 4) {
+        const float4 w = *reinterpret_cast<const float4*>(p + k + j);
+        v[j] = w.x; v[j + 1] = w.y; v[j + 2] = w.z; v[j + 3] = w.w;
+      }
+    }
+  }
+  static __device__ __forceinline__ float qone(const float* p, int64_t k) {
+    if constexpr (!SMEM) return __ldg(p + k);
+    else return p[k];
+  }
+};
+
+constexpr int kStageCopy = 32768;  // bytes per bulk copy when staging a row
+
+template <typename T, int VEC, int NT, bool STAGED>
 __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
+  extern __shared__ __align__(128) unsigned char stage[];
   __shared__ float sh_f[32];
   __shared__ int sh_i[32];
   __shared__ double sh_d[32];
   __shared__ int s_y;
+  __shared__ __align__(8) uint64_t sbar;
+  using A = RowAccess<T, VEC, STAGED>;
+  const int64_t lbytes = (static_cast<int64_t>(P.V) * static_cast<int64_t>(sizeof(T)) + 15) / 16 * 16;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int N = P.N, V = P.V, D = P.D;
@@ -73,6 +118,14 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
   }
   st = Block<NT>::or_int(st, sh_i);
 
+  if constexpr (STAGED) {
+    if (tid == 0) {
+      mbar_init(&sbar, 1);
+      mbar_fence_init();
+    }
+    __syncthreads();
+  }
+  uint32_t sphase = 0;
   int node = -1, d = 0;
   if (!(st & SPECDEC_STATUS_ERROR_MASK)) {
     for (;;) {
@@ -80,13 +133,38 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
       const int64_t roff = (static_cast<int64_t>(b) * (N + 1) + row) * V;
       const T* lrow = static_cast<const T*>(P.logits) + roff;
       const float* qrow = P.q + roff;
+      if constexpr (STAGED) {  // bring the node's rows into shared memory (q only if it has children)
+        int kids = 0;
+        for (int j = tid; j < N; j += NT) kids |= (__ldg(P.parents + j) == node) ? 1 : 0;
+        kids = Block<NT>::or_int(kids, sh_i);  // also orders every earlier read of the stage
+        if (tid == 0) {
+          fence_proxy_async_smem();
+          const uint32_t lb = static_cast<uint32_t>(static_cast<int64_t>(V) * sizeof(T));
+          const uint32_t qb = (kids && !greedy) ? static_cast<uint32_t>(V) * 4u : 0u;
+          mbar_expect_tx(&sbar, lb + qb);
+          for (uint32_t o = 0; o < lb; o += kStageCopy)
+            bulk_copy_g2s(stage + o, reinterpret_cast<const char*>(lrow) + o, min(static_cast<uint32_t>(kStageCopy), lb - o),
+                          &sbar);
+          for (uint32_t o = 0; o < qb; o += kStageCopy)
+            bulk_copy_g2s(stage + lbytes + o, reinterpret_cast<const char*>(qrow) + o,
+                          min(static_cast<uint32_t>(kStageCopy), qb - o), &sbar);
+        }
+        const int gave_up = Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i);  // uniform decision
+        if (gave_up) {
+          st |= SPECDEC_STATUS_TIMEOUT;
+          break;
+        }
+        sphase ^= 1u;
+        lrow = reinterpret_cast<const T*>(stage);
+        qrow = reinterpret_cast<const float*>(stage + lbytes);
+      }
       // pass 1: maximum and its lowest index (each thread walks its vectors in index order)
       float best = -kInf;
       int bidx = INT_MAX;
       bool nan = false;
       for (int k = tid * VEC; k < V; k += NT * VEC) {
         float v[VEC];
-        VecLoad<T, VEC>::load(lrow, k, v);
+        A::vec(lrow, k, v);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           nan |= (v[e] != v[e]);
@@ -107,17 +185,17 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
           if (__ldg(P.parents + j) == node && __ldg(toks + j) == z) child = min(child, j);
         child = Block<NT>::min_int(child, sh_i);
       } else {
-        // pass 2: Z (per-vector fp32 sums, fp64 across vectors)
-        double zt = 0.0;
+        // pass 2: Z (fp32 within a thread and a warp, fp64 across warps)
+        float zt = 0.f;
         for (int k = tid * VEC; k < V; k += NT * VEC) {
           float v[VEC];
-          VecLoad<T, VEC>::load(lrow, k, v);
+          A::vec(lrow, k, v);
           float a = 0.f;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) a += ex2((v[e] - m) * c);
-          zt += static_cast<double>(a);
+          zt += a;
         }
-        const double Zd = Block<NT>::sum(zt, sh_d);
+        const double Zd = Block<NT>::sum_f(zt, sh_d);
         const float invZ = static_cast<float>(1.0 / Zd);
         // the current residual is (p - a q)+ / S
         double a = 0.0, S = 1.0;
@@ -131,9 +209,9 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
           if (j == INT_MAX) break;
           prev = j;
           const int s = __ldg(toks + j);
-          const float qs = __ldg(qrow + s);
+          const float qs = A::qone(qrow, s);
           if (!(qs >= 0.f && qs < kInf)) { st |= SPECDEC_STATUS_BAD_PROB; break; }
-          const float ps = ex2((Elem<T>::load(lrow, s) - m) * c) * invZ;
+          const float ps = ex2((A::one(lrow, s) - m) * c) * invZ;
           const double Rs = fmax(static_cast<double>(ps) - a * static_cast<double>(qs), 0.0) / S;
           bool accept;
           if (qs == 0.f) {
@@ -146,26 +224,26 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
           // rejected: S' = sum (p - (a + S) q)+, and the q row is read whole
           const double an = a + S;
           const float anf = static_cast<float>(an);
-          double rt = 0.0;
+          float rt = 0.f;
           int qbad = 0;
           for (int k = tid * VEC; k < V; k += NT * VEC) {
             float v[VEC], qv[VEC];
-            VecLoad<T, VEC>::load(lrow, k, v);
-            load_q<VEC>(qrow, k, qv);
+            A::vec(lrow, k, v);
+            A::qvec(qrow, k, qv);
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               if (!(qv[e] >= 0.f && qv[e] < kInf)) qbad = 1;
               acc += fmaxf(ex2((v[e] - m) * c) * invZ - anf * qv[e], 0.f);
             }
-            rt += static_cast<double>(acc);
+            rt += acc;
           }
           if (!q_checked) {
             qbad = Block<NT>::or_int(qbad, sh_i);
             if (qbad) { st |= SPECDEC_STATUS_BAD_PROB; break; }
             q_checked = true;
           }
-          const double Sn = Block<NT>::sum(rt, sh_d);
+          const double Sn = Block<NT>::sum_f(rt, sh_d);
           if (Sn > 0.0) {
             a = an;
             S = Sn;
@@ -190,8 +268,8 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
             float acc = 0.f;
             if (k < V) {
               float v[VEC], qv[VEC];
-              VecLoad<T, VEC>::load(lrow, k, v);
-              if (resid) load_q<VEC>(qrow, k, qv);
+              A::vec(lrow, k, v);
+              if (resid) A::qvec(qrow, k, qv);
 #pragma unroll
               for (int e = 0; e < VEC; ++e) {
                 const float ex = ex2((v[e] - m) * c);
@@ -204,7 +282,7 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
               for (int e = 0; e < VEC; ++e) w[e] = 0.f;
             }
             double tile;
-            const double incl = Block<NT>::inclusive_scan(static_cast<double>(acc), sh_d, tile);
+            const double incl = Block<NT>::inclusive_scan_f(acc, sh_d, tile);
             if (base + tile > target) {
               const int first = Block<NT>::min_int((base + incl > target) ? tid : INT_MAX, sh_i);
               if (tid == first) {
@@ -253,20 +331,43 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
   }
 }
 
-template <typename T, int VEC>
+template <typename T, int VEC, bool STAGED>
 cudaError_t launch_rr_t(const TreeParams& P, cudaStream_t stream) {
-  return launch_kernel(tree_rr_kernel<T, VEC, kTreeThreads>, dim3(P.B), dim3(kTreeThreads), 0, stream, 0, P);
+  int smem = 0;
+  if constexpr (STAGED) {
+    smem = static_cast<int>((static_cast<int64_t>(P.V) * static_cast<int64_t>(sizeof(T)) + 15) / 16 * 16 +
+                            static_cast<int64_t>(P.V) * 4);
+    static unsigned long long configured = 0;
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured & bit)) {
+      if (cudaError_t e = cudaFuncSetAttribute(tree_rr_kernel<T, VEC, kTreeThreads, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTreeStageBytes);
+          e != cudaSuccess)
+        return e;
+      configured |= bit;
+    }
+  }
+  return launch_kernel(tree_rr_kernel<T, VEC, kTreeThreads, STAGED>, dim3(P.B), dim3(kTreeThreads),
+                       static_cast<size_t>(smem), stream, 0, P);
 }
 
 }  // namespace
 
 cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream) {
   if (vector_path) {
-    if (ldt == SPECDEC_BF16) return launch_rr_t<uint16_t, 8>(P, stream);
-    return launch_rr_t<float, 4>(P, stream);
+    const int64_t need = (static_cast<int64_t>(P.V) * (ldt == SPECDEC_BF16 ? 2 : 4) + 15) / 16 * 16 +
+                         static_cast<int64_t>(P.V) * 4;
+    if (need <= kTreeStageBytes) {
+      if (ldt == SPECDEC_BF16) return launch_rr_t<uint16_t, 8, true>(P, stream);
+      return launch_rr_t<float, 4, true>(P, stream);
+    }
+    if (ldt == SPECDEC_BF16) return launch_rr_t<uint16_t, 8, false>(P, stream);
+    return launch_rr_t<float, 4, false>(P, stream);
   }
-  if (ldt == SPECDEC_BF16) return launch_rr_t<uint16_t, 1>(P, stream);
-  return launch_rr_t<float, 1>(P, stream);
+  if (ldt == SPECDEC_BF16) return launch_rr_t<uint16_t, 1, false>(P, stream);
+  return launch_rr_t<float, 1, false>(P, stream);
 }
 
 }  // namespace specdec
