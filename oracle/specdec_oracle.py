@@ -428,6 +428,150 @@ def verify_block(logits, q, drafts, T, u) -> dict:
     }
 
 
+# ---------------------------------------------------------------------------------
+# Gumbel coupling (Art of Guessing, "Speculative sampling" -> the Gumbel-max trick and
+# "Gumbel coupling", Daliri et al.): the drafter and the target share the noise g_k at
+# position k; the drafter proposes argmax(log q_k + g_k), the target samples
+# argmax(log p_k + g_k), and the round keeps the longest agreeing prefix plus the target's
+# token at the first disagreement.
+#
+# The noise is not an input: both sides generate it with Philox4x32-10 (Salmon, Moraes,
+# Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), written here from
+# that definition.  READINGS (the page leaves the generator open): the uniforms of
+# vocabulary entries 4j..4j+3 at row k of sequence b are the four outputs of counter
+# (j, k, b, 0) under key (seed mod 2^32, seed div 2^32); a 32-bit output x gives
+# u = ((x >> 9) + 0.5) / 2^23, exactly representable in float32 and inside (0, 1); the
+# race is run in log2 units, score_i = a_i - log2(xi_i) with xi_i = -ln(u_i) = -log1p(u_i - 1)
+# (argmax(a_i / ln 2 + g_i) with g = -ln(xi) is the same argmax), a_i = l_i * log2(e) / T
+# for the target and log2(q_i) for the drafter; ties go to the lowest index.  The scores
+# are formed in float32, the precision the pages' code computes in.
+# ---------------------------------------------------------------------------------
+LOG2E = 1.0 / np.log(2.0)
+PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
+PHILOX_W = (0x9E3779B9, 0xBB67AE85)   # key increments (golden ratio, sqrt(3) - 1)
+_MASK32 = 0xFFFFFFFF
+
+
+def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):
+    """Ten Philox4x32 rounds on counters (arrays of values < 2^32) under key (k0, k1).
+    A round: (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+    lo(M0 c0)); the key grows by (W0, W1) between rounds.  Returns four uint32 arrays."""
+    c = [np.asarray(x, dtype=np.uint64) & _MASK32 for x in (c0, c1, c2, c3)]
+    c = np.broadcast_arrays(*c)
+    c = [x.copy() for x in c]
+    k0, k1 = int(k0) & _MASK32, int(k1) & _MASK32
+    for r in range(10):
+        if r:
+            k0 = (k0 + PHILOX_W[0]) & _MASK32
+            k1 = (k1 + PHILOX_W[1]) & _MASK32
+        p0 = np.uint64(PHILOX_M[0]) * c[0]
+        p1 = np.uint64(PHILOX_M[1]) * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(_MASK32)
+        hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(_MASK32)
+        c = [hi1 ^ c[1] ^ np.uint64(k0), lo1, hi0 ^ c[3] ^ np.uint64(k1), lo0]
+    return [x.astype(np.uint32) for x in c]
+
+
+def gumbel_uniforms(seed: int, b, k, V: int) -> np.ndarray:
+    """float32 uniforms of row k of sequence b (b, k scalars or broadcastable arrays):
+    shape broadcast(b, k) + (V,)."""
+    seed = int(seed)
+    b = np.asarray(b, dtype=np.uint64)[..., None]
+    k = np.asarray(k, dtype=np.uint64)[..., None]
+    j = np.arange((V + 3) // 4, dtype=np.uint64)
+    outs = philox4x32_10(j, k, b, np.uint64(0), seed & _MASK32, (seed >> 32) & _MASK32)
+    x = np.stack(outs, axis=-1).reshape(np.broadcast_shapes(b.shape, k.shape)[:-1] + (-1,))[..., :V]
+    return ((x >> np.uint32(9)).astype(np.float32) + np.float32(0.5)) * np.float32(2.0 ** -23)
+
+
+def gumbel_scores(a32, u32) -> np.ndarray:
+    """The race in log2 units, float32: a - log2(xi), xi = -log1p(u - 1)."""
+    a32 = np.asarray(a32, dtype=np.float32)
+    u32 = np.asarray(u32, dtype=np.float32)
+    with np.errstate(divide="ignore"):
+        xi = -np.log1p(u32 - np.float32(1.0))
+        return a32 - np.log2(xi)
+
+
+def _lowest_argmax32(s) -> int:
+    s = np.asarray(s)
+    return int(np.flatnonzero(s == s.max())[0])
+
+
+def _top2_gap(s) -> float:
+    s = np.sort(np.asarray(s, dtype=np.float64)[np.isfinite(s)])
+    return float(s[-1] - s[-2]) if len(s) >= 2 else np.inf
+
+
+def gumbel_draft_sequence(q, seed: int, b: int) -> dict:
+    """The drafter's side: x_k = argmax_i (log2 q_k(i) - log2 xi_{k,i}) for k < gamma.
+    Returns drafts and each row's top-two score gap (for the parity flag rule)."""
+    q = widen(q)
+    gamma, V = q.shape
+    u = gumbel_uniforms(seed, b, np.arange(gamma), V)
+    with np.errstate(divide="ignore"):
+        a = np.log2(q.astype(np.float32))
+    drafts, gaps = [], []
+    for kk in range(gamma):
+        s = gumbel_scores(a[kk], u[kk])
+        drafts.append(_lowest_argmax32(s))
+        gaps.append(_top2_gap(s))
+    return {"drafts": np.array(drafts, dtype=np.int64), "gaps": np.array(gaps)}
+
+
+def gumbel_target_token(logits_row, T: float, seed: int, b: int, k: int) -> tuple[int, float]:
+    """The target's Gumbel-max sample at row k: argmax_i (l_i * c - log2 xi_i), c =
+    log2(e) / T in float32; returns (token, top-two score gap)."""
+    c = np.float32(np.float32(LOG2E) / np.float32(T))
+    a = np.asarray(logits_row, dtype=np.float32) * c
+    s = gumbel_scores(a, gumbel_uniforms(seed, b, k, len(a)))
+    return _lowest_argmax32(s), _top2_gap(s)
+
+
+def verify_gumbel_sequence(logits, drafts, T: float, seed: int, b: int) -> dict:
+    """One round of Gumbel-coupled verification for sequence b.
+
+    Art of Guessing, "Gumbel coupling": t_k = the target's Gumbel-max sample at row k with
+    the shared noise; n = the first k < gamma with x_k != t_k (gamma if none); emit
+    x_0..x_{n-1}, t_n.  The output is what the target alone samples with that noise,
+    whatever the drafter.  Rows are evaluated left to right and the round stops at n, so
+    rows after n are neither read nor validated (the chain rule's reading).  A greedy
+    sequence (T < GREEDY_T) uses the plain argmax (T -> 0 of the race).  Returns tokens,
+    J, status, targets (t_k of the rows evaluated, -1 after) and gaps (each evaluated
+    row's top-two score gap)."""
+    logits = np.asarray(logits)
+    g1, V = logits.shape
+    gamma = g1 - 1
+    drafts = [int(x) for x in np.asarray(drafts).reshape(-1)]
+    greedy = bool(T < GREEDY_T) or bool(np.isnan(T))
+    out = {"tokens": np.full(g1, -1, dtype=np.int64), "J": -1, "status": 0,
+           "targets": np.full(g1, -1, dtype=np.int64), "gaps": np.full(g1, np.inf), "greedy": greedy}
+    if not np.isfinite(T):
+        out["status"] = STATUS_BAD_TEMPERATURE
+        return out
+    for k in range(g1):
+        rs = _row_status(logits[k])
+        if rs:
+            out["status"] = rs
+            out["targets"][:] = -1
+            return out
+        if k < gamma and not (0 <= drafts[k] < V):
+            out["status"] = STATUS_BAD_TOKEN
+            out["targets"][:] = -1
+            return out
+        if greedy:
+            t, gap = lowest_argmax(logits[k]), np.inf
+        else:
+            t, gap = gumbel_target_token(logits[k], T, seed, b, k)
+        out["targets"][k], out["gaps"][k] = t, gap
+        if k == gamma or drafts[k] != t:
+            out["tokens"][:k] = drafts[:k]
+            out["tokens"][k] = t
+            out["J"] = k
+            return out
+    raise AssertionError("unreachable")
+
+
 def verify_greedy_sequence(logits, drafts) -> dict:
     """Greedy verification only (SD 20.5, "A round of greedy speculative decoding";
     Art of Guessing, "Draft and verify"): J = longest prefix with x_i == z_i, emit z_J."""
