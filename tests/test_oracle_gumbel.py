@@ -135,3 +135,13 @@ def test_status_follows_the_rows_read():
     assert r["status"] == so.STATUS_BAD_LOGIT and r["J"] == -1
     assert so.verify_gumbel_sequence(logits, [7, 99, 3], 1.0, 0, 0)["status"] == so.STATUS_BAD_TOKEN
     assert so.verify_gumbel_sequence(logits, d, np.inf, 0, 0)["status"] == so.STATUS_BAD_TEMPERATURE
+
+
+def test_target_sample_follows_softmax_at_temperature():
+    """The oracle's own target sampler (the one verification uses) draws softmax(l / T)."""
+    logits = np.array([0.7, -0.2, 1.5, 0.1])
+    T = 0.6
+    n = 40000
+    toks = np.array([so.gumbel_target_token(logits, T, 21, b, 2)[0] for b in range(n)])
+    counts = np.bincount(toks, minlength=len(logits))
+    assert stats.chisquare(counts, so.target_distribution(logits, T) * n).pvalue > 1e-4
