@@ -15,6 +15,9 @@ every row and q row read) on the same workload instead of the chain rule.
 --rule tree_recursive times sampled tree verification by recursive rejection
 (specdec_verify_tree_recursive) on tree_rr_b32_n64_v32000 (the Medusa sparse tree's
 topology, tokens drafted i.i.d. per node); rows are B*(N+1) candidate rows per call.
+--rule gumbel times Gumbel-coupled verification (specdec_verify_gumbel) on the same
+workload as the chain rule, with drafts from the drafter's shared-noise sampler (made
+before the timed region).
 
 Prints one JSON line (rank 0).  Metric: verified vocab rows per second, B*(gamma+1)
 rows per call, whole job over all ranks.  Several GPUs run independent replicas
@@ -388,7 +391,7 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive"], default="chain")
+    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive", "gumbel"], default="chain")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -427,6 +430,15 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     verify = sd.verify_block if args.rule == "block" else sd.verify_chain
+    if args.rule == "gumbel":
+        gseed = 20241202
+        for x in sets:  # the drafter's proposals under the shared noise
+            x["draft_tokens"] = sd.gumbel_draft(x["draft_probs"], gseed)
+        for o in outs:
+            o.pop("p_draft")
+
+        def verify(logits, draft_probs, draft_tokens, temperatures, uniforms, out=None, stream=None):
+            return sd.verify_gumbel(logits, draft_tokens, temperatures, gseed, out=out, stream=stream)
 
     def step(i):
         x = sets[i % len(sets)]
@@ -484,7 +496,11 @@ def main():
     n_rej = sum(float((o["num_accepted"] < g).float().sum()) for o in outs) / len(outs)
     rows_read = sum(float((o["num_accepted"].clamp(max=g) + 1).float().sum()) for o in outs) / len(outs)
     seq_bytes = rows_read * V * esize + n_rej * V * 4
-    if args.rule == "block":
+    if args.rule == "gumbel":
+        # rows 0..J of every sequence (no q row: the race needs only the target's logits)
+        seq_bytes = rows_read * V * esize
+        kname, alg_bytes = "gumbel", seq_bytes
+    elif args.rule == "block":
         # block verification reads every logits row and every q row: the statistics pass
         # reads the logits, the mass pass both
         seq_bytes = rows * V * esize + B * g * V * 4
@@ -526,7 +542,7 @@ def main():
     if not args.no_e2e:
         host = {k: sets[0][k].cpu().pin_memory() for k in keys}
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = B * (g + 1) * 4 + B * 4 + B * 4 + B * g * 4
+        d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
         for _ in range(2):
             verify(*(host[k] for k in keys))
         torch.cuda.synchronize()

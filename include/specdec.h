@@ -226,6 +226,48 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
                                   int32_t* out_num_accepted, int32_t* out_status, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Gumbel-coupled verification (Art of Guessing, "Gumbel coupling", Daliri et al.).
+ *
+ * The drafter and the target share the noise g_k at position k: the drafter proposed
+ * x_k = argmax_i (log q_k(i) + g_k,i) (specdec_gumbel_draft below), the target samples
+ * t_k = argmax_i (log p_k(i) + g_k,i) with p_k = softmax(logits[b, k, :] / T); the round keeps
+ * x_0..x_{n-1} for the first n with x_n != t_n (n = g if none) and appends t_n.  The emitted
+ * tokens are what the target alone samples with that noise, whatever the drafter.
+ *
+ * Noise: Philox4x32-10 (Salmon et al., SC 2011).  Entries 4j..4j+3 of row k of sequence b
+ * use the outputs of counter (j, k, b, 0) under key (seed & 0xffffffff, seed >> 32); an
+ * output x gives u = ((x >> 9) + 0.5) / 2^23.  Race in log2 units, float32:
+ * score_i = a_i - log2(xi_i), xi_i = -log1p(u_i - 1), a_i = logit_i * log2(e) / T (target) or
+ * log2(q_i) (drafter); ties go to the lowest index.  A greedy sequence (T < 1e-3) uses the
+ * plain argmax of the logits.
+ *
+ * logits [B, g+1, V] (bf16/fp32), draft_tokens [B, g] int32, temperatures [B] fp32.
+ * out_tokens [B, g+1] int32 (-1 padded), out_num_accepted [B] int32 (n, or -1 on an error),
+ * out_status [B] int32 (optional).  Rows are evaluated left to right and the round stops at
+ * n: rows after n are neither read nor validated.  Errors: BAD_TEMPERATURE (non-finite T),
+ * then in row order BAD_LOGIT / EMPTY_ROW (row k) and BAD_TOKEN (draft k).
+ * Sizes: B >= 1, g >= 1, V >= 1; 16-byte aligned rows (V * element size a multiple of 16,
+ * aligned base) take 16-byte loads, others scalar loads.
+ */
+int specdec_verify_gumbel(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
+                          const float* temperatures, uint64_t seed, int B, int g, int V,
+                          int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_status,
+                          void* stream);
+
+/* The drafter's side of Gumbel coupling: out_draft_tokens[b, k] = argmax_i (log q[b, k, i]
+ * + g_{k,i}) with the noise above (same seed, counter (j, k, b, 0)).  draft_probs [B, g, V]
+ * fp32; entries that are 0 are never chosen, nor are NaN or negative ones (-1 if no entry
+ * qualifies). */
+int specdec_gumbel_draft(const float* draft_probs, uint64_t seed, int B, int g, int V,
+                         int32_t* out_draft_tokens, void* stream);
+
+/* The shared noise itself, for a drafter that runs its race elsewhere:
+ * out_noise[(b * rows + k) * V + i] = G = -log2(xi), xi = -ln(u), of entry i at row k of
+ * sequence b (the race adds it to a_i).  out_noise [B, rows, V] fp32.  The library evaluates
+ * G with its own approximation (absolute error below 4e-6 against the float64 definition). */
+int specdec_gumbel_noise(uint64_t seed, int B, int rows, int V, float* out_noise, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Tree-attention mask and position ids (SD 20.5, box "Token tree and tree attention").
  *   out_mask          [N, P+N] uint8: row i is 1 on every prefix column j < P, on column
  *                     P+i and on column P+a for every ancestor a of node i; 0 elsewhere
@@ -259,7 +301,9 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_BLOCK_FINISH 8  /* block verification: survival and the draw */
 #define SPECDEC_KERNEL_BLOCK_FUSED 9   /* block verification in one launch           */
 #define SPECDEC_KERNEL_TREE_RR 10      /* tree verification by recursive rejection   */
-#define SPECDEC_NUM_KERNELS 11
+#define SPECDEC_KERNEL_GUMBEL 11       /* Gumbel-coupled verification                */
+#define SPECDEC_KERNEL_GUMBEL_DRAFT 12 /* the drafter's shared-noise sampler          */
+#define SPECDEC_NUM_KERNELS 13
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

@@ -494,8 +494,13 @@ def gumbel_scores(a32, u32) -> np.ndarray:
 
 
 def _lowest_argmax32(s) -> int:
+    """Lowest index of the largest score; a NaN score (a NaN or negative q) never wins;
+    -1 when no score is a number."""
     s = np.asarray(s)
-    return int(np.flatnonzero(s == s.max())[0])
+    ok = ~np.isnan(s)
+    if not ok.any():
+        return -1
+    return int(np.flatnonzero(ok & (s == s[ok].max()))[0])
 
 
 def _top2_gap(s) -> float:

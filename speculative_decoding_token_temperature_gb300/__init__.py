@@ -40,7 +40,8 @@ STATUS_ZERO_Q = 256
 STATUS_ZERO_RESIDUAL = 512
 
 KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
-                "chain_seq", "block_decide", "block_finish", "block_fused", "tree_rr")
+                "chain_seq", "block_decide", "block_finish", "block_fused", "tree_rr", "gumbel",
+                "gumbel_draft")
 
 
 class SpecdecError(RuntimeError):
@@ -82,6 +83,13 @@ def load_library():
     lib.specdec_verify_tree.restype = i32
     lib.specdec_verify_tree_recursive.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_verify_tree_recursive.restype = i32
+    u64 = ctypes.c_uint64
+    lib.specdec_verify_gumbel.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp]
+    lib.specdec_verify_gumbel.restype = i32
+    lib.specdec_gumbel_draft.argtypes = [vp, u64, i32, i32, i32, vp, vp]
+    lib.specdec_gumbel_draft.restype = i32
+    lib.specdec_gumbel_noise.argtypes = [u64, i32, i32, i32, vp, vp]
+    lib.specdec_gumbel_noise.restype = i32
     lib.specdec_build_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_build_tree_mask.restype = i32
     lib.specdec_profile_start.argtypes = [i32]
@@ -327,6 +335,58 @@ def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperature
                                            _ptr(out.get("status")), ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_tree_recursive")
     return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def verify_gumbel(logits, draft_tokens, temperatures, seed: int, *, out=None, stream=None) -> dict:
+    """Gumbel-coupled verification (specdec_verify_gumbel): tokens [B, g+1], num_accepted
+    [B], status [B].  The noise is Philox4x32-10 keyed by `seed` (0 <= seed < 2^64)."""
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    logits, draft_tokens, temperatures = (rt.to_device(t) for t in (logits, draft_tokens, temperatures))
+    B, g1, V = logits.shape
+    g = g1 - 1
+    dev = logits.device
+    code = _dtype_code(logits)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
+    _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    _need(logits, "logits", None, (B, g1, V), dev)
+    if out is None:
+        out = {"tokens": torch.empty(B, g1, dtype=torch.int32, device=dev),
+               "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+               "status": torch.empty(B, dtype=torch.int32, device=dev)}
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.specdec_verify_gumbel(_ptr(logits), code, _ptr(draft_tokens), _ptr(temperatures), int(seed), B, g, V,
+                                   _ptr(out["tokens"]), _ptr(out["num_accepted"]), _ptr(out.get("status")),
+                                   ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_gumbel")
+    return {k: rt.to_host(v) for k, v in out.items()}
+
+
+def gumbel_draft(draft_probs, seed: int, *, out=None, stream=None):
+    """The drafter's shared-noise sampler (specdec_gumbel_draft): draft tokens [B, g]."""
+    lib = load_library()
+    rt = _HostRoundTrip([draft_probs])
+    draft_probs = rt.to_device(draft_probs)
+    B, g, V = draft_probs.shape
+    dev = draft_probs.device
+    _need(draft_probs, "draft_probs", torch.float32, (B, g, V), dev)
+    if out is None:
+        out = torch.empty(B, g, dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.specdec_gumbel_draft(_ptr(draft_probs), int(seed), B, g, V, _ptr(out), ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_gumbel_draft")
+    return rt.to_host(out)
+
+
+def gumbel_noise(seed: int, B: int, rows: int, V: int, device=None, stream=None):
+    """The shared Gumbel noise G [B, rows, V] fp32 (specdec_gumbel_noise)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = torch.empty(B, rows, V, dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    _check(lib.specdec_gumbel_noise(int(seed), B, rows, V, _ptr(out), ctypes.c_void_p(s.cuda_stream)),
+           "specdec_gumbel_noise")
+    return out
 
 
 def build_tree_mask(parents, prefix_len: int, *, stream=None) -> dict:

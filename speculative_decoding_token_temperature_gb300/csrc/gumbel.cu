@@ -1,0 +1,384 @@
+// Gumbel-coupled verification and the drafter's shared-noise sampler.
+//
+// Art of Guessing, "Gumbel coupling" (Daliri et al.): the drafter and the target share the
+// noise g_k at draft position k.  The drafter proposes x_k = argmax_i (log q_k(i) + g_k,i);
+// the target samples t_k = argmax_i (log p_k(i) + g_k,i); the round keeps the longest
+// prefix with x_k == t_k and appends the target's token at the first disagreement.
+// Verification is exact matching, and the emitted text is what the target alone samples
+// with that noise, whatever the drafter.
+//
+// The noise never touches memory: every thread regenerates it with Philox4x32-10 (Salmon,
+// Moraes, Dror, Shaw, SC 2011), written from that definition.  Entries 4j..4j+3 of row k
+// of sequence b take the four outputs of counter (j, k, b, 0) under key (seed low, seed
+// high); an output x gives u = ((x >> 9) + 0.5) / 2^23 (exact in float32, inside (0, 1)).
+// The race runs in log2 units: score_i = a_i - log2(xi_i), xi_i = -ln(u_i) computed as
+// -log1p(u_i - 1) (u - 1 is exact, so xi keeps its relative accuracy where u is near 1,
+// which is where the winners are), a_i = l_i * log2(e) / T for the target, log2(q_i) for
+// the drafter.  Ties go to the lowest index.
+//
+// The noise value G = -log2(xi) is evaluated with the hardware base-2 logarithm where its
+// absolute error is small against the result: t = -log2(u) directly for u <= 0.75, and for
+// u > 0.75 xi = -ln(1 + x), x = u - 1, from the series ln(1 + x) = 2 atanh(y) =
+// 2 (y + y^3/3 + y^5/5 + y^7/7 + y^9/9), y = x / (2 + x), |y| <= 1/7 (truncation below
+// 1e-9 relative); then G = -log2(t) + log2(log2(e)) or -log2(xi).  Against the float64
+// definition the error stays within two float32 ulps of G (below 4e-6, tested), far inside
+// the parity rule's tie band.
+//
+// Entries that cannot win are skipped: u <= 1 - 2^-24 bounds G <= 24, so once some entry
+// has score L, any entry with a_i + 24.25 < L is out of the race.  Each row first finds the
+// largest a and scores that entry (L), then races only the entries within 24.25 of L.
+//
+// verify: one CTA per sequence walks rows 0..n left to right (the rows after the first
+//         disagreement are not read), each thread racing its groups of 4 entries.
+// draft:  one CTA per (sequence, position) races the q row.
+
+#include <algorithm>
+#include <climits>
+
+#include "specdec_device.cuh"
+#include "specdec_internal.h"
+
+namespace specdec {
+
+namespace {
+
+constexpr int kGumbelThreads = 512;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ float uniform_of(uint32_t x) {
+  return (static_cast<float>(x >> 9) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
+}
+
+constexpr float kLog2Log2e = 0.52876637294489777f;  // log2(log2(e))
+constexpr float kNoiseMax = 24.25f;                  // above every G (u <= 1 - 2^-24)
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// G = -log2(xi), xi = -ln(u)
+__device__ __forceinline__ float neg_log2_xi(float u) {
+  if (u <= 0.75f) return kLog2Log2e - lg2_approx(-lg2_approx(u));  // -log2(-log2(u) ln 2)
+  const float x = u - 1.f;                                         // exact
+  const float y = __fdividef(x, 2.f + x);
+  const float y2 = y * y;
+  const float s = fmaf(y2, fmaf(y2, fmaf(y2, fmaf(y2, 1.f / 9.f, 1.f / 7.f), 1.f / 5.f), 1.f / 3.f), 1.f);
+  return -lg2_approx(-2.f * y * s);                                // xi = -ln(1 + x) = -2 atanh(y)
+}
+
+struct Best {
+  float s;
+  int i;
+};
+__device__ __forceinline__ void take(Best& b, float s, int i) {  // entries arrive in index order
+  if (s > b.s) {
+    b.s = s;
+    b.i = i;
+  }
+}
+__device__ __forceinline__ Best better(const Best& a, const Best& b) {
+  if (a.s > b.s) return a;
+  if (b.s > a.s) return b;
+  return a.i <= b.i ? a : b;
+}
+
+// Block-wide (best score, lowest index) and the NaN-propagating maximum logit.
+template <int NT>
+__device__ __forceinline__ void block_best(Best& b, float& mx, Best* sh_b, float* sh_m) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Best t;
+    t.s = __shfl_xor_sync(0xffffffffu, b.s, o);
+    t.i = __shfl_xor_sync(0xffffffffu, b.i, o);
+    b = better(b, t);
+    mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if (l == 0) {
+    sh_b[w] = b;
+    sh_m[w] = mx;
+  }
+  __syncthreads();
+  b = sh_b[0];
+  mx = sh_m[0];
+#pragma unroll
+  for (int i = 1; i < NT / 32; ++i) {
+    b = better(b, sh_b[i]);
+    mx = max_nan(mx, sh_m[i]);
+  }
+}
+
+// Every group of 4 entries of a row, in index order per thread: thread t takes 16-byte
+// vectors t, t + NT, ... (2 groups per bf16 vector, 1 per fp32 vector), kUnroll vectors
+// loaded before any is used, so that many loads are in flight; f(j, v) gets group j's four
+// values (-inf past V).  VEC needs rows of whole, 16-byte aligned vectors; other rows are
+// read entry by entry.
+constexpr int kUnroll = 4;
+template <typename T, bool VEC, int NT, typename F>
+__device__ __forceinline__ void for_groups(const T* row, int V, F&& f) {
+  const int ng = (V + 3) / 4;
+  if constexpr (VEC) {
+    constexpr int GPV = 16 / (4 * static_cast<int>(sizeof(T)));  // groups per 16-byte vector
+    const int nv = (ng + GPV - 1) / GPV;
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * NT) {
+      uint4 w[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int vi = v0 + u * NT;
+        if (vi < nv) w[u] = __ldg(reinterpret_cast<const uint4*>(row) + vi);  // rows hold whole vectors
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int vi = v0 + u * NT;
+        if (vi >= nv) break;
+#pragma unroll
+        for (int g = 0; g < GPV; ++g) {
+          const int j = vi * GPV + g;
+          if (j >= ng) break;
+          float v[4];
+          if constexpr (sizeof(T) == 2) {
+            const uint32_t a = g ? w[u].z : w[u].x, c = g ? w[u].w : w[u].y;
+            v[0] = bf16_lo(a); v[1] = bf16_hi(a); v[2] = bf16_lo(c); v[3] = bf16_hi(c);
+          } else {
+            v[0] = __uint_as_float(w[u].x); v[1] = __uint_as_float(w[u].y);
+            v[2] = __uint_as_float(w[u].z); v[3] = __uint_as_float(w[u].w);
+          }
+          f(j, v);
+        }
+      }
+    }
+  } else {
+    for (int j0 = threadIdx.x; j0 < ng; j0 += kUnroll * NT) {
+      float v[kUnroll][4];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + u * NT;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[u][e] = (j < ng && 4 * j + e < V) ? Elem<T>::load(row, 4 * j + e) : -kInf;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (j0 + u * NT < ng) f(j0 + u * NT, v[u]);
+    }
+  }
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_verify_kernel(const void* __restrict__ logits,
+                                                                       const int32_t* __restrict__ drafts,
+                                                                       const float* __restrict__ temps,
+                                                                       uint32_t key0, uint32_t key1, int B, int G,
+                                                                       int V, int32_t* __restrict__ out_tokens,
+                                                                       int32_t* __restrict__ out_J,
+                                                                       int32_t* __restrict__ out_status) {
+  __shared__ Best sh_b[kGumbelThreads / 32];
+  __shared__ float sh_m[kGumbelThreads / 32];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int R = G + 1;
+  const float Tb = __ldg(temps + b);
+  const bool greedy = !(Tb >= SPECDEC_GREEDY_TEMPERATURE);
+  const float c = greedy ? 1.f : kLog2e / Tb;
+  int32_t* tok = out_tokens + static_cast<int64_t>(b) * R;
+  int st = (Tb - Tb == 0.f) ? 0 : SPECDEC_STATUS_BAD_TEMPERATURE;
+  int J = -1, last = -1;
+  for (int k = 0; k < R && !st; ++k) {
+    const T* row = static_cast<const T*>(logits) + (static_cast<int64_t>(b) * R + k) * V;
+    // the largest logit and its lowest index (the greedy token; the row checks)
+    Best top;
+    top.s = -kInf;
+    top.i = INT_MAX;
+    float mx = -kInf;
+    for_groups<T, VEC, kGumbelThreads>(row, V, [&](int j, const float (&v)[4]) {
+      mx = max_nan(mx, max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])));
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * j + e < V) take(top, v[e], 4 * j + e);
+    });
+    block_best<kGumbelThreads>(top, mx, sh_b, sh_m);
+    if (!(mx == mx) || mx == kInf) {
+      st = SPECDEC_STATUS_BAD_LOGIT;
+      break;
+    }
+    if (mx == -kInf) {
+      st = SPECDEC_STATUS_EMPTY_ROW;
+      break;
+    }
+    int t = top.i;
+    if (!greedy) {
+      // the race, skipping the entries that cannot reach the top logit's own score L
+      const int jt = t >> 2;
+      const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), static_cast<uint32_t>(k),
+                                                static_cast<uint32_t>(b), 0u),
+                                     key0, key1);
+      const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
+      const float L = __fsub_rn(__fmul_rn(mx, c), -neg_log2_xi(uniform_of(xts[t & 3])));
+      const float cut = L - kNoiseMax;  // a_i below cut cannot win
+      Best best;
+      best.s = -kInf;
+      best.i = INT_MAX;
+      float unused = -kInf;
+      for_groups<T, VEC, kGumbelThreads>(row, V, [&](int j, const float (&v)[4]) {
+        float a[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V) ? __fmul_rn(v[e], c) : -kInf;
+        if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
+        const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
+                                                 static_cast<uint32_t>(b), 0u),
+                                      key0, key1);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (a[e] >= cut) take(best, __fsub_rn(a[e], -neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
+      });
+      block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
+      t = best.i;
+    }
+    int x = -1;
+    if (k < G) {
+      x = __ldg(drafts + static_cast<int64_t>(b) * G + k);
+      if (x < 0 || x >= V) {
+        st = SPECDEC_STATUS_BAD_TOKEN;
+        break;
+      }
+    }
+    if (k == G || x != t) {
+      J = k;
+      last = t;
+      break;
+    }
+  }
+  if (tid < R) {
+    int v = -1;
+    if (!st) v = tid < J ? __ldg(drafts + static_cast<int64_t>(b) * G + tid) : (tid == J ? last : -1);
+    tok[tid] = v;
+  }
+  if (tid == 0) {
+    out_J[b] = st ? -1 : J;
+    if (out_status) out_status[b] = st;
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const float* __restrict__ q, uint32_t key0,
+                                                                      uint32_t key1, int G, int V,
+                                                                      int32_t* __restrict__ out) {
+  __shared__ Best sh_b[kGumbelThreads / 32];
+  __shared__ float sh_m[kGumbelThreads / 32];
+  const int row = blockIdx.x;  // b * G + k
+  const int b = row / G, k = row - b * G;
+  const float* qr = q + static_cast<int64_t>(row) * V;
+  // the largest q (NaN and negative entries never count) and its lowest index
+  Best top;
+  top.s = -kInf;
+  top.i = INT_MAX;
+  float unused = -kInf;
+  for_groups<float, VEC, kGumbelThreads>(qr, V, [&](int j, const float (&v)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * j + e < V && v[e] > 0.f) take(top, v[e], 4 * j + e);
+  });
+  block_best<kGumbelThreads>(top, unused, sh_b, sh_m);
+  if (top.i == INT_MAX) {  // no positive entry
+    if (threadIdx.x == 0) out[row] = -1;
+    return;
+  }
+  const int jt = top.i >> 2;
+  const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), static_cast<uint32_t>(k),
+                                            static_cast<uint32_t>(b), 0u),
+                                 key0, key1);
+  const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
+  const float cut = __fadd_rn(log2f(top.s), neg_log2_xi(uniform_of(xts[top.i & 3]))) - kNoiseMax;
+  Best best;
+  best.s = -kInf;
+  best.i = INT_MAX;
+  for_groups<float, VEC, kGumbelThreads>(qr, V, [&](int j, const float (&v)[4]) {
+    float a[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V && v[e] > 0.f) ? log2f(v[e]) : -kInf;
+    if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
+    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
+                                             static_cast<uint32_t>(b), 0u),
+                                  key0, key1);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (a[e] >= cut) take(best, __fadd_rn(a[e], neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
+  });
+  block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
+  if (threadIdx.x == 0) out[row] = best.i;
+}
+
+// The shared noise itself: out[(b * R + k) * V + i] = G of entry i, row k, sequence b.
+__global__ void __launch_bounds__(256) gumbel_noise_kernel(uint32_t key0, uint32_t key1, int B, int R, int V,
+                                                           float* __restrict__ out) {
+  const int ng = (V + 3) / 4;
+  const int64_t total = static_cast<int64_t>(B) * R * ng;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t rowi = t / ng;
+    const int j = static_cast<int>(t - rowi * ng);
+    const int k = static_cast<int>(rowi % R), b = static_cast<int>(rowi / R);
+    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
+                                             static_cast<uint32_t>(b), 0u),
+                                  key0, key1);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * j + e < V) out[rowi * V + 4 * j + e] = neg_log2_xi(uniform_of(xs[e]));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gumbel_noise(uint64_t seed, int B, int R, int V, float* out, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(B) * R * ((V + 3) / 4);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 8);
+  return launch_kernel(gumbel_noise_kernel, dim3(static_cast<unsigned>(std::max<int64_t>(blocks, 1))), dim3(256), 0,
+                       stream, 0, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), B, R, V, out);
+}
+
+cudaError_t launch_gumbel_verify(const void* logits, specdec_dtype ldt, const int32_t* drafts, const float* temps,
+                                 uint64_t seed, int B, int G, int V, bool vec, int32_t* out_tokens, int32_t* out_J,
+                                 int32_t* out_status, cudaStream_t stream) {
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  const dim3 grid(B), block(kGumbelThreads);
+  if (ldt == SPECDEC_BF16) {
+    if (vec)
+      return launch_kernel(gumbel_verify_kernel<uint16_t, true>, grid, block, 0, stream, 0, logits, drafts, temps,
+                           k0, k1, B, G, V, out_tokens, out_J, out_status);
+    return launch_kernel(gumbel_verify_kernel<uint16_t, false>, grid, block, 0, stream, 0, logits, drafts, temps,
+                         k0, k1, B, G, V, out_tokens, out_J, out_status);
+  }
+  if (vec)
+    return launch_kernel(gumbel_verify_kernel<float, true>, grid, block, 0, stream, 0, logits, drafts, temps, k0, k1,
+                         B, G, V, out_tokens, out_J, out_status);
+  return launch_kernel(gumbel_verify_kernel<float, false>, grid, block, 0, stream, 0, logits, drafts, temps, k0, k1,
+                       B, G, V, out_tokens, out_J, out_status);
+}
+
+cudaError_t launch_gumbel_draft(const float* q, uint64_t seed, int B, int G, int V, bool vec, int32_t* out,
+                                cudaStream_t stream) {
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(G)), block(kGumbelThreads);
+  if (vec) return launch_kernel(gumbel_draft_kernel<true>, grid, block, 0, stream, 0, q, k0, k1, G, V, out);
+  return launch_kernel(gumbel_draft_kernel<false>, grid, block, 0, stream, 0, q, k0, k1, G, V, out);
+}
+
+}  // namespace specdec

@@ -470,6 +470,52 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
   return SPECDEC_OK;
 }
 
+namespace {
+bool gumbel_vec(const void* p, int V, size_t es) { return rows_vectorizable(p, V, es); }
+}  // namespace
+
+int specdec_verify_gumbel(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
+                          const float* temperatures, uint64_t seed, int B, int g, int V,
+                          int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_status,
+                          void* stream) {
+  if (!valid_dtype(ldt)) return fail(SPECDEC_ERR_INVALID_ARG, "unknown logits dtype");
+  if (!chain_sizes_ok(B, g, V)) return fail(SPECDEC_ERR_INVALID_ARG, "B, g and V must be positive");
+  if (!logits || !draft_tokens || !temperatures || !out_tokens || !out_num_accepted)
+    return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  if (g + 1 > 512 || B > INT32_MAX / 2) return fail(SPECDEC_ERR_UNSUPPORTED, "g + 1 above 512");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_GUMBEL, s);
+  if (cudaError_t e = launch_gumbel_verify(logits, ldt, draft_tokens, temperatures, seed, B, g, V,
+                                           gumbel_vec(logits, V, elem_size(ldt)), out_tokens, out_num_accepted,
+                                           out_status, s);
+      e != cudaSuccess)
+    return fail_cuda("Gumbel verification kernel", e);
+  return SPECDEC_OK;
+}
+
+int specdec_gumbel_draft(const float* draft_probs, uint64_t seed, int B, int g, int V,
+                         int32_t* out_draft_tokens, void* stream) {
+  if (!chain_sizes_ok(B, g, V)) return fail(SPECDEC_ERR_INVALID_ARG, "B, g and V must be positive");
+  if (!draft_probs || !out_draft_tokens) return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  if (static_cast<int64_t>(B) * g > INT32_MAX) return fail(SPECDEC_ERR_UNSUPPORTED, "too many rows");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_GUMBEL_DRAFT, s);
+  if (cudaError_t e = launch_gumbel_draft(draft_probs, seed, B, g, V, gumbel_vec(draft_probs, V, 4),
+                                          out_draft_tokens, s);
+      e != cudaSuccess)
+    return fail_cuda("Gumbel draft kernel", e);
+  return SPECDEC_OK;
+}
+
+int specdec_gumbel_noise(uint64_t seed, int B, int rows, int V, float* out_noise, void* stream) {
+  if (B <= 0 || rows <= 0 || V <= 0) return fail(SPECDEC_ERR_INVALID_ARG, "B, rows and V must be positive");
+  if (!out_noise) return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaError_t e = launch_gumbel_noise(seed, B, rows, V, out_noise, s); e != cudaSuccess)
+    return fail_cuda("Gumbel noise kernel", e);
+  return SPECDEC_OK;
+}
+
 int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* out_mask,
                             int64_t* out_position_ids, int32_t* out_depth, int32_t* out_status,
                             void* stream) {

@@ -170,6 +170,13 @@ cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector
                              cudaStream_t stream);
 // Sampled tree verification by recursive rejection at every node.
 cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream);
+// Gumbel-coupled verification and the drafter's shared-noise sampler (Philox noise).
+cudaError_t launch_gumbel_verify(const void* logits, specdec_dtype ldt, const int32_t* drafts, const float* temps,
+                                 uint64_t seed, int B, int G, int V, bool vec, int32_t* out_tokens, int32_t* out_J,
+                                 int32_t* out_status, cudaStream_t stream);
+cudaError_t launch_gumbel_noise(uint64_t seed, int B, int R, int V, float* out, cudaStream_t stream);
+cudaError_t launch_gumbel_draft(const float* q, uint64_t seed, int B, int G, int V, bool vec, int32_t* out,
+                                cudaStream_t stream);
 cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* mask,
                              int64_t* pos, int32_t* depth, int32_t* status, cudaStream_t stream);
 

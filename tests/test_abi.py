@@ -21,7 +21,8 @@ def declared_functions():
 def test_header_declares_the_four_verification_calls():
     names = declared_functions()
     for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
-               "specdec_build_tree_mask", "specdec_verify_block", "specdec_verify_tree_recursive"):
+               "specdec_build_tree_mask", "specdec_verify_block", "specdec_verify_tree_recursive",
+               "specdec_verify_gumbel", "specdec_gumbel_draft", "specdec_gumbel_noise"):
         assert fn in names
 
 
@@ -101,6 +102,14 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 65, p, p, p, None, None) == sd.ERR_UNSUPPORTED
     assert lib.specdec_verify_tree_recursive(p, 5, p, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    # Gumbel coupling: null drafts, bad sizes, too many rows per sequence
+    assert lib.specdec_verify_gumbel(p, sd.BF16, None, p, 1, 1, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 0, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 1, 600, 8, p, p, None, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_gumbel_draft(None, 1, 1, 1, 8, p, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_gumbel_draft(p, 1, 1, 1, 0, p, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_gumbel_noise(1, 1, 1, 8, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_gumbel_noise(1, 0, 1, 8, p, None) == sd.ERR_INVALID_ARG
     # mask
     assert lib.specdec_build_tree_mask(None, 4, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_build_tree_mask(p, 0, 2, p, p, None, p, None) == sd.ERR_INVALID_ARG
