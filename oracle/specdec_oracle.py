@@ -298,6 +298,39 @@ def verify_chain(logits, q, drafts, T, u) -> dict:
 # Block verification (one round, one sequence)
 # ---------------------------------------------------------------------------------------
 
+def verify_chain_varlen_sequence(logits, q, drafts, T: float, u, gamma_b: int, want_cdf: bool = False) -> dict:
+    """One chain round that verifies only the first gamma_b drafts of a padded draft.
+
+    SD 20.5, "Choosing how much to verify at every step" (adaptive verification): a step
+    verifies l_r drafts of request r and the rest of its draft is dropped.  The round is the
+    chain rule on the first gamma_b + 1 rows: drafts 0..gamma_b-1 are tested with
+    u[0..gamma_b-1], and the extra token comes from row gamma_b (a rejection's residual, or
+    the bonus row p_{gamma_b} with q = 0) with uniform u[gamma_b].  READINGS: the extra
+    token's uniform sits at slot gamma_b of the padded [gamma+1] uniforms; gamma_b = 0
+    samples row 0 directly; gamma_b outside [0, gamma] is an input error reported as
+    STATUS_BAD_TOKEN (the count of drafts to verify is out of range).  Exactness needs
+    gamma_b chosen without looking at the drafts it decides on (the page's
+    non-anticipating requirement); the verifier cannot check that.
+    Returns the chain result padded to gamma + 1 tokens and gamma p_draft entries."""
+    logits = np.asarray(logits)
+    g1, V = logits.shape
+    gamma = g1 - 1
+    gb = int(gamma_b)
+    if not (0 <= gb <= gamma):
+        return {"tokens": np.full(g1, -1, dtype=np.int64), "J": -1, "status": STATUS_BAD_TOKEN,
+                "p_draft": np.full(gamma, np.nan), "margins": np.full(gamma, np.inf), "greedy": False}
+    qq = None if q is None else np.asarray(q)[:gb]
+    r = verify_chain_sequence(logits[:gb + 1], qq, list(np.asarray(drafts).reshape(-1)[:gb]), T,
+                              widen(u).reshape(-1)[:gb + 1], want_cdf=want_cdf)
+    tokens = np.full(g1, -1, dtype=np.int64)
+    tokens[:gb + 1] = r["tokens"]
+    p_draft = np.full(gamma, np.nan)
+    p_draft[:gb] = r["p_draft"]
+    margins = np.full(gamma, np.inf)
+    margins[:gb] = r["margins"]
+    return {**r, "tokens": tokens, "p_draft": p_draft, "margins": margins}
+
+
 def verify_block_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False) -> dict:
     """One round of block verification for one sequence.
 
