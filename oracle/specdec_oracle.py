@@ -873,6 +873,47 @@ def verify_tree(logits, node_tokens, parents, T, u, max_depth: int) -> dict:
     }
 
 
+def compact_kv(cache, prefix_len, path, num_accepted, block_table=None, block_size: int = 0):
+    """Accepted-branch compaction of a KV cache after a tree round (SD 20.5, "Keeping the
+    caches consistent after a rejection": the accepted branch's entries, scattered among
+    discarded siblings, are gathered into consecutive slots; a chain only moves a length).
+
+    cache [B, S, W] (contiguous) or [num_blocks, block_size, W] with block_table [B, max
+    blocks] (paged: logical slot s of sequence b lives in block block_table[b, s //
+    block_size], row s % block_size).  Node i of sequence b's tree sits at logical slot
+    prefix_len[b] + i; after the round the entry of path[b, d] moves to slot prefix_len[b] + d
+    for d < num_accepted[b].  Returns (new cache, new lengths prefix_len + num_accepted, status
+    per sequence).  The definition gathers from the cache as it was before the round.
+    READINGS: a path must climb the tree (path[d] >= d and strictly increasing, as node ids
+    along a root path do), else the sequence is left alone with STATUS_BAD_TREE; a sequence
+    with num_accepted < 0 (a failed round) is left alone and keeps its length."""
+    src = np.asarray(cache)
+    out = src.copy()
+    B = len(prefix_len)
+    new_len = np.array([int(prefix_len[b]) + max(int(num_accepted[b]), 0) for b in range(B)])
+    status = np.zeros(B, dtype=np.int64)
+
+    def at(b, s):
+        if block_table is None:
+            return (b, s)
+        return (int(block_table[b][s // block_size]), s % block_size)
+
+    for b in range(B):
+        J = int(num_accepted[b])
+        if J < 0:
+            new_len[b] = int(prefix_len[b])
+            continue
+        pth = [int(x) for x in np.asarray(path[b])[:J]]
+        if any(pth[d] < d for d in range(J)) or any(pth[d + 1] <= pth[d] for d in range(J - 1)):
+            status[b] = STATUS_BAD_TREE
+            new_len[b] = int(prefix_len[b])
+            continue
+        P0 = int(prefix_len[b])
+        for d in range(J):
+            out[at(b, P0 + d)] = src[at(b, P0 + pth[d])]
+    return out, new_len, status
+
+
 def cartesian_tree_counts(tops) -> tuple[int, int]:
     """(nodes, paths) of the full Cartesian candidate tree with s_i candidates at depth i.
 
