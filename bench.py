@@ -15,6 +15,12 @@ every row and q row read) on the same workload instead of the chain rule.
 --rule tree_recursive times sampled tree verification by recursive rejection
 (specdec_verify_tree_recursive) on tree_rr_b32_n64_v32000 (the Medusa sparse tree's
 topology, tokens drafted i.i.d. per node); rows are B*(N+1) candidate rows per call.
+--rule chain_varlen times chain verification with a per-request number of verified
+drafts (specdec_verify_chain_varlen), gamma_b ~ U{0..gamma} seeded per batch; rows are the
+candidate rows sum(gamma_b + 1).
+--rule kv_compact times accepted-branch KV compaction (specdec_compact_kv) of 128 KB cache
+slots along the recursive-rejection walks of tree_rr_b32_n64_v32000; the metric is bytes
+moved per second.
 --rule gumbel times Gumbel-coupled verification (specdec_verify_gumbel) on the same
 workload as the chain rule, with drafts from the drafter's shared-noise sampler (made
 before the timed region).
@@ -226,6 +232,76 @@ def run_reference(args, rank):
 
 
 TREE_RR_WORKLOAD = "tree_rr_b32_n64_v32000"
+KV_SLOT_BYTES = 128 * 1024  # one cache slot: 32 layers x 8 KV heads x 128 x (K, V) x bf16
+KV_PREFIX = 64
+
+
+def run_kv_compact(args, rank, world, local_rank):
+    """Accepted-branch KV compaction along the recursive-rejection walks of the tree
+    workload: the timing contract, metric = cache bytes moved (read + written) per second."""
+    import numpy as np
+    import torch
+    import workloads
+    from oracle import specdec_oracle as so  # the tree topology only
+    import speculative_decoding_token_temperature_gb300 as sd
+    from speculative_decoding_token_temperature_gb300 import build as _build
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the KV compaction rule has no CPU arm"}))
+        return 0
+    w = workloads.TREE_RR_WORKLOADS[TREE_RR_WORKLOAD]
+    B, D = w["B"], w["depth"]
+    parents, _, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
+    N = len(parents)
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.ensure_built()
+    sd.load_library()
+    x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 100 * rank, dev)
+    walk = sd.verify_tree_recursive(*(x[k] for k in ("logits", "draft_probs", "node_tokens", "parents",
+                                                     "temperatures", "uniforms")), D)
+    cache = torch.zeros(B, KV_PREFIX + N, KV_SLOT_BYTES // 2, dtype=torch.bfloat16, device=dev)
+    prefix = torch.full((B,), KV_PREFIX, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        sd.compact_kv(cache, prefix, walk["path"], walk["num_accepted"], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    J = walk["num_accepted"].cpu().numpy()
+    moves = int(sum(sum(1 for d in range(max(j, 0)) if int(walk["path"][b, d]) != d) for b, j in enumerate(J)))
+    moved = 2 * moves * KV_SLOT_BYTES
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank, uuid) as clocks:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
+    gbs = moved / (ms / 1e3) / 1e9
+    line = {"metric": "KV cache bytes moved/s", "value": gbs * 1e9 * world, "unit": "B/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": TREE_RR_WORKLOAD, "rule": "kv_compact", "B": B, "N": N,
+                       "slot_bytes": KV_SLOT_BYTES, "prefix": KV_PREFIX, "moves_per_step": moves},
+            "roofline": {"kernel": "kv_compact", "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "algorithmic_bytes_per_launch": moved, "traffic": None},
+            "gpu_launches": args.steps, "clocks": clocks.summary(), "kernel_src_sha": kernel_source_sha()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_tree_rr(args, rank, world, local_rank):
@@ -391,7 +467,8 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive", "gumbel"], default="chain")
+    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive", "gumbel", "chain_varlen", "kv_compact"],
+                    default="chain")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -401,9 +478,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.rule == "tree_recursive":
         return run_tree_rr(args, rank, world, local_rank)
+    if args.rule == "kv_compact":
+        return run_kv_compact(args, rank, world, local_rank)
     if args.impl == "reference":
         return run_reference(args, rank)
 
+    import numpy as np
     import torch
     import workloads
     import speculative_decoding_token_temperature_gb300 as sd
@@ -430,6 +510,16 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     verify = sd.verify_block if args.rule == "block" else sd.verify_chain
+    if args.rule == "chain_varlen":
+        for si, x in enumerate(sets):  # counts chosen without looking at the drafts
+            gen = torch.Generator(device="cpu").manual_seed(7000 + si)
+            x["gammas"] = torch.randint(0, g + 1, (B,), generator=gen, dtype=torch.int32).to(dev)
+
+        def verify(logits, draft_probs, draft_tokens, temperatures, uniforms, out=None, stream=None, _sets=sets):
+            gm = next(x["gammas"] for x in _sets if x["logits"] is logits)
+            return sd.verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniforms, gm, out=out,
+                                          stream=stream)
+        rows = float(np.mean([float((x["gammas"] + 1).sum()) for x in sets]))
     if args.rule == "gumbel":
         gseed = 20241202
         for x in sets:  # the drafter's proposals under the shared noise
@@ -493,8 +583,10 @@ def main():
     peak = peak or FALLBACK_HBM_GBS
     # rows a left-to-right verifier must read: 0..J of every sequence (the bonus row too
     # when all gamma drafts are accepted), and the draft row q_J of each rejection
-    n_rej = sum(float((o["num_accepted"] < g).float().sum()) for o in outs) / len(outs)
-    rows_read = sum(float((o["num_accepted"].clamp(max=g) + 1).float().sum()) for o in outs) / len(outs)
+    gcap = [x["gammas"] if "gammas" in x else torch.full((B,), g, dtype=torch.int32, device=dev) for x in sets]
+    n_rej = sum(float((o["num_accepted"] < gc).float().sum()) for o, gc in zip(outs, gcap)) / len(outs)
+    rows_read = sum(float((torch.minimum(o["num_accepted"], gc) + 1).float().sum())
+                    for o, gc in zip(outs, gcap)) / len(outs)
     seq_bytes = rows_read * V * esize + n_rej * V * 4
     if args.rule == "gumbel":
         # rows 0..J of every sequence (no q row: the race needs only the target's logits)

@@ -110,6 +110,29 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Chain verification with a per-request number of verified drafts (SD 20.5, "Choosing how
+ * much to verify at every step": adaptive verification verifies l_r drafts of request r).
+ *
+ * The arguments of specdec_verify_chain, padded to g drafts, plus gammas [B] int32 with
+ * 0 <= gammas[b] <= g: sequence b's round is the chain round on its first gammas[b] + 1
+ * rows -- drafts 0..gammas[b]-1 tested with uniforms[b, 0..gammas[b]-1], the extra token
+ * from row J (a rejection's residual, or the bonus row gammas[b]) with uniforms[b,
+ * gammas[b]].  Rows, q rows and uniforms past gammas[b] are not read; out_tokens are -1
+ * past J, out_p_draft NaN past J.  A count outside [0, g] gives SPECDEC_STATUS_BAD_TOKEN.
+ * Exactness needs each count chosen without looking at the drafts it decides on (the
+ * page's non-anticipating requirement, box "Trimming a draft can break exactness"); the
+ * verifier cannot check it.  Needs 16-byte aligned rows, g + 1 <= 32 and V <= 2,097,152
+ * (the left-to-right kernel), else SPECDEC_ERR_UNSUPPORTED.  Workspace:
+ * specdec_chain_workspace_bytes.
+ */
+int specdec_verify_chain_varlen(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                const int32_t* draft_tokens, const float* temperatures,
+                                const float* uniforms, const int32_t* gammas, int B, int g, int V,
+                                int32_t* out_tokens, int32_t* out_num_accepted, float* out_p_draft,
+                                int32_t* out_status, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Block verification: one round per sequence, the draft judged jointly.
  *
  * Art of Guessing, "Block verification" (Sun et al.).  Same inputs, outputs and shapes as
@@ -268,6 +291,34 @@ int specdec_gumbel_draft(const float* draft_probs, uint64_t seed, int B, int g, 
 int specdec_gumbel_noise(uint64_t seed, int B, int rows, int V, float* out_noise, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Accepted-branch KV compaction (SD 20.5, "Keeping the caches consistent after a
+ * rejection": after a tree round the accepted branch's cache entries, scattered among
+ * discarded siblings, are gathered into consecutive slots; a chain only moves a length).
+ *
+ * Node i of sequence b's candidates sits at logical slot prefix_len[b] + i; for
+ * d < num_accepted[b] the entry of node path[b, d] moves to slot prefix_len[b] + d, in place.
+ * A slot is row_bytes bytes:
+ *   contiguous (block_table == NULL): slot s of sequence b at cache + b * seq_stride +
+ *     s * slot_stride, num_slots slots per sequence;
+ *   paged: at cache + block_table[b * max_blocks + s / block_size] * block_stride +
+ *     (s % block_size) * slot_stride (num_slots = max_blocks * block_size).
+ * Call it once per cache tensor (per layer, keys and values, or one call for a fused
+ * layout).  path [B, max_depth] int32 (the tree verifier's out_path), num_accepted [B]
+ * (its out_num_accepted; a negative count leaves the sequence alone).
+ * out_new_len [B] int32 (optional): prefix_len + num_accepted, the entries to keep (the
+ * extra token has no entry yet).  out_status [B] (optional): SPECDEC_STATUS_BAD_TREE when
+ * a path does not climb the tree (path[d] >= d, strictly increasing) or leaves the cache;
+ * that sequence is left alone.  Freeing emptied pages is the allocator's business.
+ * 16-byte aligned layouts move 16-byte words, others bytes.  All pointers are device
+ * pointers; strides and sizes in bytes.
+ */
+int specdec_compact_kv(void* cache, int64_t row_bytes, int64_t slot_stride, int64_t seq_stride,
+                       int64_t num_slots, const int32_t* block_table, int block_size, int max_blocks,
+                       int64_t block_stride, int B, const int32_t* prefix_len, const int32_t* path,
+                       int max_depth, const int32_t* num_accepted, int32_t* out_new_len,
+                       int32_t* out_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Tree-attention mask and position ids (SD 20.5, box "Token tree and tree attention").
  *   out_mask          [N, P+N] uint8: row i is 1 on every prefix column j < P, on column
  *                     P+i and on column P+a for every ancestor a of node i; 0 elsewhere
@@ -303,7 +354,8 @@ int specdec_build_tree_mask(const int32_t* parents, int N, int prefix_len, uint8
 #define SPECDEC_KERNEL_TREE_RR 10      /* tree verification by recursive rejection   */
 #define SPECDEC_KERNEL_GUMBEL 11       /* Gumbel-coupled verification                */
 #define SPECDEC_KERNEL_GUMBEL_DRAFT 12 /* the drafter's shared-noise sampler          */
-#define SPECDEC_NUM_KERNELS 13
+#define SPECDEC_KERNEL_KV_COMPACT 13   /* accepted-branch KV compaction              */
+#define SPECDEC_NUM_KERNELS 14
 
 int specdec_profile_start(int max_launches);
 int specdec_profile_read(double* total_ms, int* launches, int n);

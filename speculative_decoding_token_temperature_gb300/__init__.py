@@ -41,7 +41,7 @@ STATUS_ZERO_RESIDUAL = 512
 
 KERNEL_NAMES = ("chain_stats", "chain_sample", "tree_walk", "tree_mask", "chain_decide", "chain_finish",
                 "chain_seq", "block_decide", "block_finish", "block_fused", "tree_rr", "gumbel",
-                "gumbel_draft")
+                "gumbel_draft", "kv_compact")
 
 
 class SpecdecError(RuntimeError):
@@ -75,6 +75,9 @@ def load_library():
     lib.specdec_tree_workspace_bytes.restype = sz
     lib.specdec_verify_chain.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_chain.restype = i32
+    lib.specdec_verify_chain_varlen.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz,
+                                                vp]
+    lib.specdec_verify_chain_varlen.restype = i32
     lib.specdec_verify_block.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_block.restype = i32
     lib.specdec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -90,6 +93,9 @@ def load_library():
     lib.specdec_gumbel_draft.restype = i32
     lib.specdec_gumbel_noise.argtypes = [u64, i32, i32, i32, vp, vp]
     lib.specdec_gumbel_noise.restype = i32
+    i64 = ctypes.c_int64
+    lib.specdec_compact_kv.argtypes = [vp, i64, i64, i64, i64, vp, i32, i32, i64, i32, vp, vp, i32, vp, vp, vp, vp]
+    lib.specdec_compact_kv.restype = i32
     lib.specdec_build_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_build_tree_mask.restype = i32
     lib.specdec_profile_start.argtypes = [i32]
@@ -191,6 +197,25 @@ def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
                          draft_tokens, temperatures, uniforms, out, with_p_draft, stream)
 
 
+def verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniforms, gammas, *, out=None,
+                        with_p_draft: bool = True, stream=None) -> dict:
+    """Chain verification of the first gammas[b] drafts of each sequence
+    (specdec_verify_chain_varlen); gammas [B] int32 in [0, g].  Results as verify_chain."""
+    lib = load_library()
+    rt = _HostRoundTrip([logits])
+    gammas = rt.to_device(gammas)
+    B = logits.shape[0]
+    _need(gammas, "gammas", torch.int32, (B,), gammas.device)
+
+    class _Entry:  # the varlen call with the chain call's argument order
+        def __call__(self, lg, code, q, d, T, u, B_, g, V, t, J, pd, st, ws, wsb, s_):
+            return lib.specdec_verify_chain_varlen(lg, code, q, d, T, u, _ptr(gammas), B_, g, V, t, J, pd, st, ws,
+                                                   wsb, s_)
+
+    return _verify_round(_Entry(), "specdec_chain_workspace_bytes", logits, draft_probs, draft_tokens,
+                         temperatures, uniforms, out, with_p_draft, stream)
+
+
 def verify_block(logits, draft_probs, draft_tokens, temperatures, uniforms, *, out=None,
                  with_p_draft: bool = True, stream=None) -> dict:
     """One round of block verification per sequence (specdec_verify_block): the draft is
@@ -226,12 +251,13 @@ def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, 
             out["p_draft"] = torch.empty(B, g, dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     ws, wsb = _workspace(int(getattr(lib, ws_entry)(B, g, V, code)), dev, s.cuda_stream)
-    rc = getattr(lib, entry)(
+    fn = getattr(lib, entry) if isinstance(entry, str) else entry
+    rc = fn(
         _ptr(logits), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperatures),
         _ptr(uniforms), B, g, V, _ptr(out["tokens"]), _ptr(out["num_accepted"]),
         _ptr(out.get("p_draft")), _ptr(out.get("status")), _ptr(ws), wsb,
         ctypes.c_void_p(s.cuda_stream))
-    _check(rc, entry)
+    _check(rc, entry if isinstance(entry, str) else "specdec_verify_chain_varlen")
     return {k: rt.to_host(v) for k, v in out.items()}
 
 
@@ -387,6 +413,40 @@ def gumbel_noise(seed: int, B: int, rows: int, V: int, device=None, stream=None)
     _check(lib.specdec_gumbel_noise(int(seed), B, rows, V, _ptr(out), ctypes.c_void_p(s.cuda_stream)),
            "specdec_gumbel_noise")
     return out
+
+
+def compact_kv(cache, prefix_len, path, num_accepted, *, block_table=None, stream=None) -> dict:
+    """Accepted-branch KV compaction in place (specdec_compact_kv).
+
+    cache: a device tensor [B, S, ...] (contiguous per sequence) or, with block_table
+    [B, max_blocks] int32, a page pool [num_blocks, block_size, ...]; the trailing
+    dimensions are one slot.  prefix_len [B], path [B, D], num_accepted [B] int32 (the tree
+    verifier's outputs).  Returns new_len [B] and status [B]."""
+    lib = load_library()
+    if not cache.is_contiguous():
+        raise ValueError("cache must be contiguous")
+    dev = cache.device
+    B = prefix_len.shape[0]
+    D = path.shape[1]
+    _need(prefix_len, "prefix_len", torch.int32, (B,), dev)
+    _need(path, "path", torch.int32, (B, D), dev)
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    row = cache[0, 0].numel() * cache.element_size()
+    slots = cache.shape[1]
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, (B, block_table.shape[1]), dev)
+        bs, mb, bstride, sstride, nslots = slots, block_table.shape[1], slots * row, 0, 0
+    else:
+        if cache.shape[0] != B:
+            raise ValueError("cache must be [B, S, ...] without a block table")
+        bs, mb, bstride, sstride, nslots = 0, 0, 0, slots * row, slots
+    new_len = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    _check(lib.specdec_compact_kv(_ptr(cache), row, row, sstride, nslots, _ptr(block_table), bs, mb, bstride, B,
+                                  _ptr(prefix_len), _ptr(path), D, _ptr(num_accepted), _ptr(new_len), _ptr(status),
+                                  ctypes.c_void_p(s.cuda_stream)), "specdec_compact_kv")
+    return {"new_len": new_len, "status": status}
 
 
 def build_tree_mask(parents, prefix_len: int, *, stream=None) -> dict:

@@ -620,11 +620,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   qu.ring_draws = P.ws.ring;
   qu.B = P.B;
 
+  // drafts to verify for sequence b: gamma, or its own count (the bonus row is row gb)
+  auto gamma_of = [&](int b) { return P.gammas ? __ldg(P.gammas + b) : P.gamma; };
   auto make_task = [&](const Entry& e) {
     Task t;
     t.kind = e.kind;
     t.src = logits + (static_cast<int64_t>(e.b) * R + e.row) * row_bytes;
-    t.q = (e.kind == kTaskDraw && e.row < P.gamma) ? P.q + (static_cast<int64_t>(e.b) * P.gamma + e.row) * V : nullptr;
+    t.q = (e.kind == kTaskDraw && e.row < gamma_of(e.b)) ? P.q + (static_cast<int64_t>(e.b) * P.gamma + e.row) * V
+                                                          : nullptr;
     t.lo = (e.kind == kTaskRow) ? c0 : d0;
     t.hi = (e.kind == kTaskRow) ? c1 : d1;
     t.n = (t.hi > t.lo + gwarp) ? (t.hi - t.lo - gwarp + kWarpsPerGroup - 1) / kWarpsPerGroup : 0;
@@ -690,10 +693,12 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     const bool greedy = P.greedy_only || is_greedy(Tc);
     const float c = greedy ? 0.f : kLog2e / Tc;
     const Task tc = make_task(cur);
+    const int gb = gamma_of(b);
+    const bool gbad = gb < 0 || gb > P.gamma;  // a count of drafts out of range
 
     // This task's inputs (first thread): the draft and the uniforms now, the logit and q at
     // the draft once the draft has arrived.
-    const bool at_draft = kind == kTaskRow && ri < P.gamma;
+    const bool at_draft = kind == kTaskRow && !gbad && ri < gb;
     int gx = -1;
     float gu = 0.f, gug = 0.f, glx = 0.f, gqx = 0.f;
     bool g2 = false;
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       if (at_draft) gx = __ldg(P.drafts + static_cast<int64_t>(b) * P.gamma + ri);
       if (!P.greedy_only) {
         if (at_draft) gu = __ldg(P.u + static_cast<int64_t>(b) * R + ri);
-        gug = __ldg(P.u + static_cast<int64_t>(b) * R + P.gamma);
+        if (!gbad) gug = __ldg(P.u + static_cast<int64_t>(b) * R + gb);
       }
     }
     auto gather2 = [&]() {
@@ -861,7 +866,8 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         rs = merge(rs, o, c);
       }
       int err = 0;
-      if (!P.greedy_only && !(Tc - Tc == 0.f)) err = SPECDEC_STATUS_BAD_TEMPERATURE;
+      if (gbad) err = SPECDEC_STATUS_BAD_TOKEN;
+      else if (!P.greedy_only && !(Tc - Tc == 0.f)) err = SPECDEC_STATUS_BAD_TEMPERATURE;
       else if (!(rs.m == rs.m) || rs.m == kInf) err = SPECDEC_STATUS_BAD_LOGIT;
       else if (rs.m == -kInf) err = SPECDEC_STATUS_EMPTY_ROW;
       else if (at_draft) err = __float_as_int(g[5]);
@@ -970,7 +976,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         if (failed || lane > Jo) P.out_tokens[static_cast<int64_t>(b) * R + lane] = -1;
         else if (lane == Jo && !drawn) P.out_tokens[static_cast<int64_t>(b) * R + lane] = y;
       }
-      if (lane < P.gamma && P.out_p_draft && (failed || lane > Jo || (greedy && lane >= Jo)))
+      if (lane < P.gamma && P.out_p_draft && (failed || lane > Jo || lane >= gb || (greedy && lane >= Jo)))
         P.out_p_draft[static_cast<int64_t>(b) * P.gamma + lane] = kNaN;
       if (lane == 0) {
         P.out_J[b] = Jo;

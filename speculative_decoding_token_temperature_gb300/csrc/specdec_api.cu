@@ -175,7 +175,8 @@ bool chain_sizes_ok(int B, int g, int V) {
 int chain_common(const void* logits, specdec_dtype ldt, const float* q, const int32_t* drafts,
                  const float* temps, const float* u, int B, int g, int V, int32_t* out_tokens,
                  int32_t* out_J, float* out_p, int32_t* out_status, void* workspace,
-                 size_t workspace_bytes, void* stream, bool greedy_only) {
+                 size_t workspace_bytes, void* stream, bool greedy_only,
+                 const int32_t* gammas = nullptr) {
   if (!valid_dtype(ldt)) return SPECDEC_ERR_INVALID_ARG;
   if (!chain_sizes_ok(B, g, V)) return SPECDEC_ERR_INVALID_ARG;
   if (!logits || !drafts || !out_tokens || !out_J || !workspace) return SPECDEC_ERR_INVALID_ARG;
@@ -191,6 +192,8 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
   const int64_t items = static_cast<int64_t>(B) * (g + 1) * nseg;
   if (items > INT32_MAX || nseg > 65535 || B > 65535) return SPECDEC_ERR_UNSUPPORTED;
+  if (gammas && !(stream_path && V <= kSeqMaxV))  // per-sequence counts: left-to-right kernel only
+    return fail(SPECDEC_ERR_UNSUPPORTED, "per-sequence draft counts need 16-byte rows, g + 1 <= 32");
   if (workspace_bytes < chain_ws_bytes(B, g, V, ldt)) return SPECDEC_ERR_WORKSPACE;
 
   ChainParams P{};
@@ -205,6 +208,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   P.nseg = static_cast<int>(nseg);
   P.seg = seg;
   P.greedy_only = greedy_only ? 1 : 0;
+  P.gammas = gammas;
   P.out_tokens = out_tokens;
   P.out_J = out_J;
   P.out_p_draft = greedy_only ? nullptr : out_p;
@@ -217,7 +221,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   // always written before they are read.
   if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
     return fail_cuda("clearing the workspace counters", e);
-  if (stream_path && use_left_to_right() && V <= kSeqMaxV) {
+  if (stream_path && (gammas || use_left_to_right()) && V <= kSeqMaxV) {
     P.grid_stats = device_sm_count();
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
     if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);
@@ -306,6 +310,18 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
   return chain_common(logits, ldt, draft_probs, draft_tokens, temperatures, uniforms, B, g, V,
                       out_tokens, out_num_accepted, out_p_draft, out_status, workspace,
                       workspace_bytes, stream, false);
+}
+
+int specdec_verify_chain_varlen(const void* logits, specdec_dtype ldt, const float* draft_probs,
+                                const int32_t* draft_tokens, const float* temperatures,
+                                const float* uniforms, const int32_t* gammas, int B, int g, int V,
+                                int32_t* out_tokens, int32_t* out_num_accepted, float* out_p_draft,
+                                int32_t* out_status, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!gammas) return fail(SPECDEC_ERR_INVALID_ARG, "gammas is null");
+  return chain_common(logits, ldt, draft_probs, draft_tokens, temperatures, uniforms, B, g, V, out_tokens,
+                      out_num_accepted, out_p_draft, out_status, workspace, workspace_bytes, stream, false,
+                      gammas);
 }
 
 size_t specdec_block_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
@@ -513,6 +529,41 @@ int specdec_gumbel_noise(uint64_t seed, int B, int rows, int V, float* out_noise
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaError_t e = launch_gumbel_noise(seed, B, rows, V, out_noise, s); e != cudaSuccess)
     return fail_cuda("Gumbel noise kernel", e);
+  return SPECDEC_OK;
+}
+
+int specdec_compact_kv(void* cache, int64_t row_bytes, int64_t slot_stride, int64_t seq_stride,
+                       int64_t num_slots, const int32_t* block_table, int block_size, int max_blocks,
+                       int64_t block_stride, int B, const int32_t* prefix_len, const int32_t* path,
+                       int max_depth, const int32_t* num_accepted, int32_t* out_new_len,
+                       int32_t* out_status, void* stream) {
+  if (!cache || !prefix_len || !path || !num_accepted) return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
+  if (B <= 0 || B > 65535 || max_depth < 1 || row_bytes <= 0 || slot_stride < row_bytes)
+    return fail(SPECDEC_ERR_INVALID_ARG, "bad sizes");
+  if (block_table && (block_size <= 0 || max_blocks <= 0 || block_stride < static_cast<int64_t>(block_size) * slot_stride))
+    return fail(SPECDEC_ERR_INVALID_ARG, "bad paged layout");
+  if (!block_table && (num_slots <= 0 || (B > 1 && seq_stride < num_slots * slot_stride)))
+    return fail(SPECDEC_ERR_INVALID_ARG, "bad contiguous layout");
+  KvCompactParams P{};
+  P.base = static_cast<char*>(cache);
+  P.row_bytes = row_bytes;
+  P.slot_stride = slot_stride;
+  P.seq_stride = seq_stride;
+  P.block_stride = block_stride;
+  P.num_slots = block_table ? static_cast<int64_t>(max_blocks) * block_size : num_slots;
+  P.block_table = block_table;
+  P.block_size = block_size;
+  P.max_blocks = max_blocks;
+  P.B = B;
+  P.max_depth = max_depth;
+  P.prefix_len = prefix_len;
+  P.path = path;
+  P.num_accepted = num_accepted;
+  P.out_new_len = out_new_len;
+  P.out_status = out_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof(SPECDEC_KERNEL_KV_COMPACT, s);
+  if (cudaError_t e = launch_kv_compact(P, s); e != cudaSuccess) return fail_cuda("KV compaction kernel", e);
   return SPECDEC_OK;
 }
 

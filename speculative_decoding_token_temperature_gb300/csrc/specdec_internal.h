@@ -95,6 +95,7 @@ struct ChainParams {
   const int32_t* drafts;
   const float* temps;    // nullptr in greedy-only mode
   const float* u;        // nullptr in greedy-only mode
+  const int32_t* gammas; // per-sequence count of drafts to verify, or nullptr (all gamma)
   int B, gamma, V;
   int nseg;              // segments per row
   int seg;               // elements per segment
@@ -168,6 +169,21 @@ struct TreeParams {
 
 cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector_path,
                              cudaStream_t stream);
+// Accepted-branch KV compaction (contiguous or paged caches).
+struct KvCompactParams {
+  char* base;
+  int64_t row_bytes, slot_stride, seq_stride, block_stride, num_slots;
+  const int32_t* block_table;  // nullptr: contiguous
+  int block_size, max_blocks;
+  int B, max_depth;
+  const int32_t* prefix_len;
+  const int32_t* path;
+  const int32_t* num_accepted;
+  int32_t* out_new_len;
+  int32_t* out_status;
+};
+cudaError_t launch_kv_compact(const KvCompactParams& P, cudaStream_t stream);
+
 // Sampled tree verification by recursive rejection at every node.
 cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream);
 // Gumbel-coupled verification and the drafter's shared-noise sampler (Philox noise).

@@ -41,7 +41,7 @@ def _init_worker(folder, mode="chain"):
     for p in (root, here):
         if p not in sys.path:
             sys.path.insert(0, p)
-    for name in ("logits", "q", "drafts", "T", "u", "gpu_tokens", "gpu_J"):
+    for name in ("logits", "q", "drafts", "T", "u", "gpu_tokens", "gpu_J", "gammas"):
         _W[name] = np.load(os.path.join(folder, name + ".npy"), mmap_mode="r")
     _W["mode"] = mode
 
@@ -53,9 +53,14 @@ def _oracle_one(b):
     drafts = np.asarray(_W["drafts"][b])
     T = float(_W["T"][b])
     u = np.asarray(_W["u"][b], dtype=np.float64)
-    verify = so.verify_block_sequence if _W["mode"] == "block" else so.verify_chain_sequence
-    r = verify(logits, q, drafts, T, u, want_cdf=True)
     gamma = len(drafts)
+    if _W["mode"] == "varlen":  # the extra token's uniform sits at slot gamma_b
+        gb = int(_W["gammas"][b])
+        r = so.verify_chain_varlen_sequence(logits, q, drafts, T, u, gb, want_cdf=True)
+        gamma = gb
+    else:
+        verify = so.verify_block_sequence if _W["mode"] == "block" else so.verify_chain_sequence
+        r = verify(logits, q, drafts, T, u, want_cdf=True)
     out = {
         "tokens": r["tokens"], "J": r["J"], "status": r["status"], "p_draft": r["p_draft"],
         "margins": r["margins"], "greedy": r["greedy"], "lit_draw": False,
@@ -79,13 +84,15 @@ def _oracle_one(b):
     return out
 
 
-def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None, mode="chain"):
+def run_oracle_chain(logits, q, drafts, T, u, gpu_tokens, gpu_J, workers=None, mode="chain", gammas=None):
     """Oracle summaries for every sequence (numpy inputs; logits already widened to
-    float32 for bf16 workloads, which is exact).  mode: "chain" or "block"."""
+    float32 for bf16 workloads, which is exact).  mode: "chain", "block" or "varlen"
+    (gammas [B]: the drafts each sequence verifies)."""
     B = logits.shape[0]
     with tempfile.TemporaryDirectory() as folder:
         arrays = {"logits": logits, "q": q if q is not None else np.zeros(0, np.float32),
-                  "drafts": drafts, "T": T, "u": u, "gpu_tokens": gpu_tokens, "gpu_J": gpu_J}
+                  "drafts": drafts, "T": T, "u": u, "gpu_tokens": gpu_tokens, "gpu_J": gpu_J,
+                  "gammas": gammas if gammas is not None else np.zeros(0, np.int32)}
         for k, v in arrays.items():
             np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(v))
         nw = workers if workers is not None else min(os.cpu_count() or 1, 16)
@@ -132,9 +139,11 @@ class ParityReport:
             self.failures.append("...")
 
 
-def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray, rule: str = "chain"):
+def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray, rule: str = "chain",
+                extra_slot=None):
     """Compare one batch.  gpu: numpy tokens [B, g+1], num_accepted [B], status [B],
-    p_draft [B, g] (optional).  rule: "chain" or "block" (which test decides a length)."""
+    p_draft [B, g] (optional).  rule: "chain" or "block" (which test decides a length);
+    extra_slot [B]: the uniform slot of each sequence's extra token (default gamma)."""
     B, g1 = gpu["tokens"].shape
     gamma = g1 - 1
     for b in range(B):
@@ -187,7 +196,7 @@ def check_chain(report: ParityReport, gpu: dict, orc: list, u: np.ndarray, rule:
                 report.flag_draw += 1  # zero-residual fallback decided by rounding
                 continue
             iv, w = o["y_interval"], o["y_weight"]
-            uu = float(u[b, gamma])
+            uu = float(u[b, gamma if extra_slot is None else int(extra_slot[b])])
             if iv is not None and w is not None and w > 0 and iv[0] - FLAG_TOL <= uu <= iv[1] + FLAG_TOL:
                 report.flag_draw += 1
             else:

@@ -22,7 +22,8 @@ def test_header_declares_the_four_verification_calls():
     names = declared_functions()
     for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
                "specdec_build_tree_mask", "specdec_verify_block", "specdec_verify_tree_recursive",
-               "specdec_verify_gumbel", "specdec_gumbel_draft", "specdec_gumbel_noise"):
+               "specdec_verify_gumbel", "specdec_gumbel_draft", "specdec_gumbel_noise",
+               "specdec_verify_chain_varlen", "specdec_compact_kv"):
         assert fn in names
 
 
@@ -102,6 +103,13 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 65, p, p, p, None, None) == sd.ERR_UNSUPPORTED
     assert lib.specdec_verify_tree_recursive(p, 5, p, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    # per-sequence draft counts: null counts; unaligned rows (V = 4 bf16) are refused
+    assert lib.specdec_verify_chain_varlen(p, sd.BF16, p, p, p, p, None, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_chain_varlen(p, sd.BF16, p, p, p, p, p, 1, 1, 4, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
+    # KV compaction: null cache, bad sizes, a paged layout without a block size
+    assert lib.specdec_compact_kv(None, 16, 16, 160, 10, None, 0, 0, 0, 1, p, p, 2, p, None, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_compact_kv(p, 0, 16, 160, 10, None, 0, 0, 0, 1, p, p, 2, p, None, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_compact_kv(p, 16, 16, 0, 10, p, 0, 4, 64, 1, p, p, 2, p, None, None, None) == sd.ERR_INVALID_ARG
     # Gumbel coupling: null drafts, bad sizes, too many rows per sequence
     assert lib.specdec_verify_gumbel(p, sd.BF16, None, p, 1, 1, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 0, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG

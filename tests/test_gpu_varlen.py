@@ -1,0 +1,112 @@
+"""GPU parity of chain verification with a per-request number of verified drafts
+(SD 20.5, "Choosing how much to verify at every step") against the oracle, through the C
+ABI.  Rules: tests/parity.py's chain rule, the extra token's uniform at slot gamma_b."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import ParityReport, check_chain, run_oracle_chain
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+KEYS = ("logits", "draft_probs", "draft_tokens", "temperatures", "uniforms")
+
+
+@pytest.fixture(scope="module")
+def sd(built_library):
+    import speculative_decoding_token_temperature_gb300 as m
+    m.load_library()
+    return m
+
+
+def _np(t):
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def _gammas(B, g, seed, device=DEV):
+    return torch.from_numpy(np.random.default_rng(seed).integers(0, g + 1, B).astype(np.int32)).to(device)
+
+
+def _run_and_check(sd, rep, x, gammas, sample=None, workers=None):
+    out = sd.verify_chain_varlen(*(x[k] for k in KEYS), gammas)
+    torch.cuda.synchronize()
+    idx = slice(None) if sample is None else sample
+    gpu = {k: _np(v)[idx] for k, v in out.items()}
+    gm = gammas.cpu().numpy()[idx]
+    orc = run_oracle_chain(*(_np(x[k])[idx] for k in KEYS), gpu["tokens"], gpu["num_accepted"], workers=workers,
+                           mode="varlen", gammas=gm)
+    check_chain(rep, gpu, orc, _np(x["uniforms"])[idx], extra_slot=gm)
+    J = gpu["num_accepted"]
+    assert (J <= np.maximum(gm, -1)).all()
+    return out
+
+
+def _finish(rep, max_flag_fraction=None):
+    path = os.environ.get("SPECDEC_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(rep.summary(), rule="varlen")) + "\n")
+    assert not rep.failures, rep.failures[:10]
+    if max_flag_fraction is not None:
+        assert rep.flagged <= max(1, max_flag_fraction * rep.rows), rep.summary()
+
+
+def test_varlen_b64_v32000_rounds(sd):
+    rep = ParityReport("varlen chain_b64_v32000 (30 rounds)")
+    for r in range(30):
+        x = workloads.chain_workload("chain_b64_v32000", r, DEV)
+        _run_and_check(sd, rep, x, _gammas(64, 4, r))
+    _finish(rep, 1e-4)
+
+
+def test_varlen_b256_v128256_full_size_sampled(sd):
+    rep = ParityReport("varlen chain_b256_v128256 (1 round, 64 sequences)")
+    x = workloads.chain_workload("chain_b256_v128256", 1, DEV)
+    _run_and_check(sd, rep, x, _gammas(256, 7, 9), sample=np.sort(np.random.default_rng(4).choice(256, 64, False)))
+    _finish(rep)
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", [(5, 3, 1000, "fp32"), (4, 5, 4096, "bf16"), (3, 31, 64, "fp32")])
+def test_varlen_shapes(sd, B, gamma, V, dtype):
+    rep = ParityReport(f"varlen B={B} g={gamma} V={V} {dtype}")
+    for seed in range(3):
+        x = workloads.make_chain_inputs(B, gamma, V, dtype, seed=seed, device=DEV, recipe="spikes", scale=2.0,
+                                        n_spikes=3, spike=4.0, noise=0.7, temps="uniform:0.0:1.5")
+        _run_and_check(sd, rep, x, _gammas(B, gamma, 100 + seed), workers=1)
+    _finish(rep)
+
+
+def test_full_counts_equal_the_chain_call(sd):
+    x = workloads.chain_workload("chain_b64_v32000", 5, DEV)
+    full = torch.full((64,), 4, dtype=torch.int32, device=DEV)
+    a = sd.verify_chain_varlen(*(x[k] for k in KEYS), full)
+    b = sd.verify_chain(*(x[k] for k in KEYS))
+    torch.cuda.synchronize()
+    for k in ("tokens", "num_accepted", "status"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_counts_out_of_range_and_rows_past_the_count(sd):
+    from oracle import specdec_oracle as so
+    B, g, V = 6, 3, 256
+    x = workloads.make_chain_inputs(B, g, V, "fp32", seed=2, device=DEV, temps="const:1.0")
+    L = x["logits"].clone()
+    gm = torch.tensor([3, 0, 1, -1, 4, 2], dtype=torch.int32, device=DEV)
+    L[1, 1:, 0] = float("nan")   # past the count: never read
+    L[2, 2:, :] = float("nan")
+    L[5, 2, 7] = float("nan")    # the bonus row of a count of 2: read when both drafts pass
+    out = sd.verify_chain_varlen(L, x["draft_probs"], x["draft_tokens"], x["temperatures"], x["uniforms"], gm)
+    torch.cuda.synchronize()
+    Ln, q, d, T, u = (_np(v) for v in (L, x["draft_probs"], x["draft_tokens"], x["temperatures"], x["uniforms"]))
+    for b in range(B):
+        o = so.verify_chain_varlen_sequence(Ln[b], q[b], d[b], float(T[b]), u[b], int(gm[b]))
+        assert int(out["status"][b]) & 0xFF == o["status"] & 0xFF, (b, int(out["status"][b]), o["status"])
+        if o["status"] & 0xFF:
+            assert int(out["num_accepted"][b]) == -1
