@@ -625,7 +625,8 @@ def main():
                      "algorithmic_bytes_per_launch": alg_bytes, "traffic": traffic_val},
         "rows_read_per_step": rows_read,
         "kernels_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items() if v[1]},
-        "gpu_launches": int(round(launches_per_step * args.steps)),
+        # the Gumbel call is one timed scope of 2 launches per wave of two rows
+        "gpu_launches": int(round(launches_per_step * args.steps)) * (2 * ((g + 2) // 2) if args.rule == "gumbel" else 1),
         "mean_accepted": statistics.mean(accepted),
         "clocks": clocks.summary(),
         "kernel_src_sha": sha,

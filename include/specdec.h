@@ -269,13 +269,18 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
  * out_status [B] int32 (optional).  Rows are evaluated left to right and the round stops at
  * n: rows after n are neither read nor validated.  Errors: BAD_TEMPERATURE (non-finite T),
  * then in row order BAD_LOGIT / EMPTY_ROW (row k) and BAD_TOKEN (draft k).
- * Sizes: B >= 1, g >= 1, V >= 1; 16-byte aligned rows (V * element size a multiple of 16,
- * aligned base) take 16-byte loads, others scalar loads.
+ * Sizes: B >= 1, g >= 1, V >= 1, B <= 65535; 16-byte aligned rows (V * element size a
+ * multiple of 16, aligned base) take 16-byte loads, others scalar loads.  Workspace:
+ * specdec_gumbel_workspace_bytes(B, g) bytes, 256-byte aligned, device memory (rows are
+ * evaluated in waves of two across the GPU; the workspace holds each wave's partial races
+ * and which rounds are still open).
  */
+size_t specdec_gumbel_workspace_bytes(int B, int g);
+
 int specdec_verify_gumbel(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
                           const float* temperatures, uint64_t seed, int B, int g, int V,
                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_status,
-                          void* stream);
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* The drafter's side of Gumbel coupling: out_draft_tokens[b, k] = argmax_i (log q[b, k, i]
  * + g_{k,i}) with the noise above (same seed, counter (j, k, b, 0)).  draft_probs [B, g, V]

@@ -87,7 +87,9 @@ def load_library():
     lib.specdec_verify_tree_recursive.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_verify_tree_recursive.restype = i32
     u64 = ctypes.c_uint64
-    lib.specdec_verify_gumbel.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp]
+    lib.specdec_gumbel_workspace_bytes.argtypes = [i32, i32]
+    lib.specdec_gumbel_workspace_bytes.restype = sz
+    lib.specdec_verify_gumbel.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_gumbel.restype = i32
     lib.specdec_gumbel_draft.argtypes = [vp, u64, i32, i32, i32, vp, vp]
     lib.specdec_gumbel_draft.restype = i32
@@ -381,9 +383,10 @@ def verify_gumbel(logits, draft_tokens, temperatures, seed: int, *, out=None, st
                "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
                "status": torch.empty(B, dtype=torch.int32, device=dev)}
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws, wsb = _workspace(int(lib.specdec_gumbel_workspace_bytes(B, g)), dev, s.cuda_stream)
     rc = lib.specdec_verify_gumbel(_ptr(logits), code, _ptr(draft_tokens), _ptr(temperatures), int(seed), B, g, V,
                                    _ptr(out["tokens"]), _ptr(out["num_accepted"]), _ptr(out.get("status")),
-                                   ctypes.c_void_p(s.cuda_stream))
+                                   _ptr(ws), wsb, ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_gumbel")
     return {k: rt.to_host(v) for k, v in out.items()}
 

@@ -25,11 +25,15 @@
 // the parity rule's tie band.
 //
 // Entries that cannot win are skipped: u <= 1 - 2^-24 bounds G <= 24, so once some entry
-// has score L, any entry with a_i + 24.25 < L is out of the race.  Each row first finds the
-// largest a and scores that entry (L), then races only the entries within 24.25 of L.
+// has score L, any entry with a_i + 24.25 < L is out of the race.  Each part of a row first
+// finds its largest a and scores that entry (L), then races only its entries within 24.25
+// of L.
 //
-// verify: one CTA per sequence walks rows 0..n left to right (the rows after the first
-//         disagreement are not read), each thread racing its groups of 4 entries.
+// verify: rows are evaluated left to right in waves of two rows of every sequence still
+//         open, each row split across CTAs (parts); a decision kernel merges the parts,
+//         compares with the drafts and closes the sequences whose round is decided, so
+//         the rows after the first disagreement's wave are not read.  The whole GPU works
+//         on every wave instead of one CTA walking each sequence.
 // draft:  one CTA per (sequence, position) races the q row.
 
 #include <algorithm>
@@ -43,6 +47,7 @@ namespace specdec {
 namespace {
 
 constexpr int kGumbelThreads = 512;
+constexpr int kGumbelMaxParts = 16;  // CTAs per row at most
 
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
@@ -131,22 +136,24 @@ __device__ __forceinline__ void block_best(Best& b, float& mx, Best* sh_b, float
 // read entry by entry.
 constexpr int kUnroll = 4;
 template <typename T, bool VEC, int NT, typename F>
-__device__ __forceinline__ void for_groups(const T* row, int V, F&& f) {
+__device__ __forceinline__ void for_groups(const T* row, int V, int part, int parts, F&& f) {
   const int ng = (V + 3) / 4;
   if constexpr (VEC) {
     constexpr int GPV = 16 / (4 * static_cast<int>(sizeof(T)));  // groups per 16-byte vector
     const int nv = (ng + GPV - 1) / GPV;
-    for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * NT) {
+    const int va = static_cast<int>(static_cast<int64_t>(nv) * part / parts);
+    const int vb = static_cast<int>(static_cast<int64_t>(nv) * (part + 1) / parts);
+    for (int v0 = va + threadIdx.x; v0 < vb; v0 += kUnroll * NT) {
       uint4 w[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int vi = v0 + u * NT;
-        if (vi < nv) w[u] = __ldg(reinterpret_cast<const uint4*>(row) + vi);  // rows hold whole vectors
+        if (vi < vb) w[u] = __ldg(reinterpret_cast<const uint4*>(row) + vi);  // rows hold whole vectors
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int vi = v0 + u * NT;
-        if (vi >= nv) break;
+        if (vi >= vb) break;
 #pragma unroll
         for (int g = 0; g < GPV; ++g) {
           const int j = vi * GPV + g;
@@ -164,54 +171,131 @@ __device__ __forceinline__ void for_groups(const T* row, int V, F&& f) {
       }
     }
   } else {
-    for (int j0 = threadIdx.x; j0 < ng; j0 += kUnroll * NT) {
+    const int ga = static_cast<int>(static_cast<int64_t>(ng) * part / parts);
+    const int gb = static_cast<int>(static_cast<int64_t>(ng) * (part + 1) / parts);
+    for (int j0 = ga + threadIdx.x; j0 < gb; j0 += kUnroll * NT) {
       float v[kUnroll][4];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int j = j0 + u * NT;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[u][e] = (j < ng && 4 * j + e < V) ? Elem<T>::load(row, 4 * j + e) : -kInf;
+        for (int e = 0; e < 4; ++e) v[u][e] = (j < gb && 4 * j + e < V) ? Elem<T>::load(row, 4 * j + e) : -kInf;
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
-        if (j0 + u * NT < ng) f(j0 + u * NT, v[u]);
+        if (j0 + u * NT < gb) f(j0 + u * NT, v[u]);
     }
   }
 }
 
+// One part of one row's race (a CTA): the part's largest logit and its lowest index, then
+// the race over the part's entries within kNoiseMax of the part's own top score (an entry
+// below that cannot win the part, so it cannot win the row).  Greedy: the top entry only.
+struct Partial {
+  float best;  // best score (greedy: the largest logit)
+  int idx;     // its lowest index
+  float mx;    // the largest logit (NaN if any logit is NaN)
+  int pad;
+};
+
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_verify_kernel(const void* __restrict__ logits,
-                                                                       const int32_t* __restrict__ drafts,
-                                                                       const float* __restrict__ temps,
-                                                                       uint32_t key0, uint32_t key1, int B, int G,
-                                                                       int V, int32_t* __restrict__ out_tokens,
-                                                                       int32_t* __restrict__ out_J,
-                                                                       int32_t* __restrict__ out_status) {
+__device__ Partial race_part(const T* row, int V, int part, int parts, bool greedy, float c, uint32_t k, uint32_t b,
+                             uint32_t key0, uint32_t key1, Best* sh_b, float* sh_m) {
+  Best top;
+  top.s = -kInf;
+  top.i = INT_MAX;
+  float mx = -kInf;
+  for_groups<T, VEC, kGumbelThreads>(row, V, part, parts, [&](int j, const float (&v)[4]) {
+    mx = max_nan(mx, max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])));
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * j + e < V) take(top, v[e], 4 * j + e);
+  });
+  block_best<kGumbelThreads>(top, mx, sh_b, sh_m);
+  Partial out;
+  out.mx = mx;
+  out.pad = 0;
+  if (greedy || top.i == INT_MAX || !(mx == mx) || mx == kInf) {
+    out.best = top.s;
+    out.idx = top.i;
+    return out;
+  }
+  const int jt = top.i >> 2;
+  const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), k, b, 0u), key0, key1);
+  const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
+  const float cut = __fsub_rn(__fmul_rn(top.s, c), -neg_log2_xi(uniform_of(xts[top.i & 3]))) - kNoiseMax;
+  Best best;
+  best.s = -kInf;
+  best.i = INT_MAX;
+  float unused = -kInf;
+  for_groups<T, VEC, kGumbelThreads>(row, V, part, parts, [&](int j, const float (&v)[4]) {
+    float a[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V) ? __fmul_rn(v[e], c) : -kInf;
+    if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
+    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), k, b, 0u), key0, key1);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (a[e] >= cut) take(best, __fsub_rn(a[e], -neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
+  });
+  block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
+  out.best = best.s;
+  out.idx = best.i;
+  return out;
+}
+
+// Rows are evaluated in waves of kWaveRows rows of every sequence still open: one CTA per
+// (sequence, row of the wave, part of the row), then one decision per sequence.
+constexpr int kWaveRows = 2;
+
+__device__ __forceinline__ const Partial* partials_of(const GumbelParams& P, int b, int r) {
+  return reinterpret_cast<const Partial*>(P.partials) + (static_cast<int64_t>(b) * kWaveRows + r) * P.parts;
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_wave_kernel(const GumbelParams P, int wave) {
   __shared__ Best sh_b[kGumbelThreads / 32];
   __shared__ float sh_m[kGumbelThreads / 32];
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int R = G + 1;
-  const float Tb = __ldg(temps + b);
+  const int part = blockIdx.x % P.parts;
+  const int r = (blockIdx.x / P.parts) % kWaveRows;
+  const int b = blockIdx.x / (P.parts * kWaveRows);
+  const int k = wave * kWaveRows + r;
+  if (k > P.G || __ldcg(P.state + b) != 0) return;  // past the last row, or the round is decided
+  const float Tb = __ldg(P.temps + b);
   const bool greedy = !(Tb >= SPECDEC_GREEDY_TEMPERATURE);
   const float c = greedy ? 1.f : kLog2e / Tb;
-  int32_t* tok = out_tokens + static_cast<int64_t>(b) * R;
+  const T* row = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * (P.G + 1) + k) * P.V;
+  const Partial out = race_part<T, VEC>(row, P.V, part, P.parts, greedy, c, static_cast<uint32_t>(k),
+                                        static_cast<uint32_t>(b), P.key0, P.key1, sh_b, sh_m);
+  if (threadIdx.x == 0)
+    reinterpret_cast<Partial*>(P.partials)[(static_cast<int64_t>(b) * kWaveRows + r) * P.parts + part] = out;
+}
+
+// One thread per sequence: merge the parts of the wave's rows in order and decide.
+__global__ void __launch_bounds__(128) gumbel_decide_kernel(const GumbelParams P, int wave) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= P.B || P.state[b] != 0) return;
+  const int R = P.G + 1;
+  const float Tb = __ldg(P.temps + b);
   int st = (Tb - Tb == 0.f) ? 0 : SPECDEC_STATUS_BAD_TEMPERATURE;
   int J = -1, last = -1;
-  for (int k = 0; k < R && !st; ++k) {
-    const T* row = static_cast<const T*>(logits) + (static_cast<int64_t>(b) * R + k) * V;
-    // the largest logit and its lowest index (the greedy token; the row checks)
-    Best top;
-    top.s = -kInf;
-    top.i = INT_MAX;
+  for (int r = 0; r < kWaveRows && !st && J < 0; ++r) {
+    const int k = wave * kWaveRows + r;
+    if (k > P.G) break;
+    const Partial* pp = partials_of(P, b, r);
+    Best best;
+    best.s = -kInf;
+    best.i = INT_MAX;
     float mx = -kInf;
-    for_groups<T, VEC, kGumbelThreads>(row, V, [&](int j, const float (&v)[4]) {
-      mx = max_nan(mx, max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])));
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (4 * j + e < V) take(top, v[e], 4 * j + e);
-    });
-    block_best<kGumbelThreads>(top, mx, sh_b, sh_m);
+    for (int q = 0; q < P.parts; ++q) {
+      const Partial x = pp[q];
+      mx = max_nan(mx, x.mx);
+      Best t;
+      t.s = x.best;
+      t.i = x.idx;
+      best = better(best, t);
+    }
     if (!(mx == mx) || mx == kInf) {
       st = SPECDEC_STATUS_BAD_LOGIT;
       break;
@@ -220,59 +304,26 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_verify_kernel(const 
       st = SPECDEC_STATUS_EMPTY_ROW;
       break;
     }
-    int t = top.i;
-    if (!greedy) {
-      // the race, skipping the entries that cannot reach the top logit's own score L
-      const int jt = t >> 2;
-      const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), static_cast<uint32_t>(k),
-                                                static_cast<uint32_t>(b), 0u),
-                                     key0, key1);
-      const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
-      const float L = __fsub_rn(__fmul_rn(mx, c), -neg_log2_xi(uniform_of(xts[t & 3])));
-      const float cut = L - kNoiseMax;  // a_i below cut cannot win
-      Best best;
-      best.s = -kInf;
-      best.i = INT_MAX;
-      float unused = -kInf;
-      for_groups<T, VEC, kGumbelThreads>(row, V, [&](int j, const float (&v)[4]) {
-        float a[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V) ? __fmul_rn(v[e], c) : -kInf;
-        if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
-        const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
-                                                 static_cast<uint32_t>(b), 0u),
-                                      key0, key1);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (a[e] >= cut) take(best, __fsub_rn(a[e], -neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
-      });
-      block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
-      t = best.i;
-    }
     int x = -1;
-    if (k < G) {
-      x = __ldg(drafts + static_cast<int64_t>(b) * G + k);
-      if (x < 0 || x >= V) {
+    if (k < P.G) {
+      x = __ldg(P.drafts + static_cast<int64_t>(b) * P.G + k);
+      if (x < 0 || x >= P.V) {
         st = SPECDEC_STATUS_BAD_TOKEN;
         break;
       }
     }
-    if (k == G || x != t) {
+    if (k == P.G || x != best.i) {
       J = k;
-      last = t;
-      break;
+      last = best.i;
     }
   }
-  if (tid < R) {
-    int v = -1;
-    if (!st) v = tid < J ? __ldg(drafts + static_cast<int64_t>(b) * G + tid) : (tid == J ? last : -1);
-    tok[tid] = v;
-  }
-  if (tid == 0) {
-    out_J[b] = st ? -1 : J;
-    if (out_status) out_status[b] = st;
-  }
+  if (!st && J < 0) return;  // every row of this wave agreed: the next wave continues
+  int32_t* tok = P.out_tokens + static_cast<int64_t>(b) * R;
+  for (int i = 0; i < R; ++i)
+    tok[i] = st ? -1 : (i < J ? __ldg(P.drafts + static_cast<int64_t>(b) * P.G + i) : (i == J ? last : -1));
+  P.out_J[b] = st ? -1 : J;
+  if (P.out_status) P.out_status[b] = st;
+  P.state[b] = 1;
 }
 
 template <bool VEC>
@@ -289,7 +340,7 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
   top.s = -kInf;
   top.i = INT_MAX;
   float unused = -kInf;
-  for_groups<float, VEC, kGumbelThreads>(qr, V, [&](int j, const float (&v)[4]) {
+  for_groups<float, VEC, kGumbelThreads>(qr, V, 0, 1, [&](int j, const float (&v)[4]) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (4 * j + e < V && v[e] > 0.f) take(top, v[e], 4 * j + e);
@@ -308,7 +359,7 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
   Best best;
   best.s = -kInf;
   best.i = INT_MAX;
-  for_groups<float, VEC, kGumbelThreads>(qr, V, [&](int j, const float (&v)[4]) {
+  for_groups<float, VEC, kGumbelThreads>(qr, V, 0, 1, [&](int j, const float (&v)[4]) {
     float a[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V && v[e] > 0.f) ? log2f(v[e]) : -kInf;
@@ -354,23 +405,34 @@ cudaError_t launch_gumbel_noise(uint64_t seed, int B, int R, int V, float* out, 
                        stream, 0, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), B, R, V, out);
 }
 
-cudaError_t launch_gumbel_verify(const void* logits, specdec_dtype ldt, const int32_t* drafts, const float* temps,
-                                 uint64_t seed, int B, int G, int V, bool vec, int32_t* out_tokens, int32_t* out_J,
-                                 int32_t* out_status, cudaStream_t stream) {
-  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-  const dim3 grid(B), block(kGumbelThreads);
-  if (ldt == SPECDEC_BF16) {
-    if (vec)
-      return launch_kernel(gumbel_verify_kernel<uint16_t, true>, grid, block, 0, stream, 0, logits, drafts, temps,
-                           k0, k1, B, G, V, out_tokens, out_J, out_status);
-    return launch_kernel(gumbel_verify_kernel<uint16_t, false>, grid, block, 0, stream, 0, logits, drafts, temps,
-                         k0, k1, B, G, V, out_tokens, out_J, out_status);
+cudaError_t launch_gumbel_verify(const GumbelParams& P, specdec_dtype ldt, bool vec, cudaStream_t stream) {
+  const int waves = (P.G + 1 + kWaveRows - 1) / kWaveRows;
+  const dim3 grid(static_cast<unsigned>(P.B) * kWaveRows * static_cast<unsigned>(P.parts)), block(kGumbelThreads);
+  const dim3 dgrid((P.B + 127) / 128), dblock(128);
+  for (int w = 0; w < waves; ++w) {
+    cudaError_t e;
+    if (ldt == SPECDEC_BF16)
+      e = vec ? launch_kernel(gumbel_wave_kernel<uint16_t, true>, grid, block, 0, stream, 0, P, w)
+              : launch_kernel(gumbel_wave_kernel<uint16_t, false>, grid, block, 0, stream, 0, P, w);
+    else
+      e = vec ? launch_kernel(gumbel_wave_kernel<float, true>, grid, block, 0, stream, 0, P, w)
+              : launch_kernel(gumbel_wave_kernel<float, false>, grid, block, 0, stream, 0, P, w);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_kernel(gumbel_decide_kernel, dgrid, dblock, 0, stream, 0, P, w)) != cudaSuccess) return e;
   }
-  if (vec)
-    return launch_kernel(gumbel_verify_kernel<float, true>, grid, block, 0, stream, 0, logits, drafts, temps, k0, k1,
-                         B, G, V, out_tokens, out_J, out_status);
-  return launch_kernel(gumbel_verify_kernel<float, false>, grid, block, 0, stream, 0, logits, drafts, temps, k0, k1,
-                       B, G, V, out_tokens, out_J, out_status);
+  return cudaSuccess;
+}
+
+int gumbel_parts(int B) {
+  // about four CTAs per SM in the first wave (two resident at a time)
+  const int want = 4 * device_sm_count();
+  const int parts = (want + B * kWaveRows - 1) / (B * kWaveRows);
+  return parts < 1 ? 1 : (parts > kGumbelMaxParts ? kGumbelMaxParts : parts);
+}
+
+size_t gumbel_workspace_bytes(int B) {
+  const size_t state = (static_cast<size_t>(B) * sizeof(int) + 255) / 256 * 256;
+  return state + static_cast<size_t>(B) * kWaveRows * kGumbelMaxParts * sizeof(Partial);
 }
 
 cudaError_t launch_gumbel_draft(const float* q, uint64_t seed, int B, int G, int V, bool vec, int32_t* out,

@@ -490,22 +490,46 @@ namespace {
 bool gumbel_vec(const void* p, int V, size_t es) { return rows_vectorizable(p, V, es); }
 }  // namespace
 
+size_t specdec_gumbel_workspace_bytes(int B, int g) {
+  if (B <= 0 || g <= 0) return 0;
+  return gumbel_workspace_bytes(B);
+}
+
 int specdec_verify_gumbel(const void* logits, specdec_dtype ldt, const int32_t* draft_tokens,
                           const float* temperatures, uint64_t seed, int B, int g, int V,
                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_status,
-                          void* stream) {
+                          void* workspace, size_t workspace_bytes, void* stream) {
   if (!valid_dtype(ldt)) return fail(SPECDEC_ERR_INVALID_ARG, "unknown logits dtype");
   if (!chain_sizes_ok(B, g, V)) return fail(SPECDEC_ERR_INVALID_ARG, "B, g and V must be positive");
-  if (!logits || !draft_tokens || !temperatures || !out_tokens || !out_num_accepted)
+  if (!logits || !draft_tokens || !temperatures || !out_tokens || !out_num_accepted || !workspace)
     return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
-  if (g + 1 > 512 || B > INT32_MAX / 2) return fail(SPECDEC_ERR_UNSUPPORTED, "g + 1 above 512");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(SPECDEC_ERR_INVALID_ARG, "the workspace must be 256-byte aligned");
+  if (g + 1 > 512 || B > 65535) return fail(SPECDEC_ERR_UNSUPPORTED, "g + 1 above 512 or B above 65535");
+  if (workspace_bytes < gumbel_workspace_bytes(B))
+    return fail(SPECDEC_ERR_WORKSPACE, "workspace smaller than specdec_gumbel_workspace_bytes");
+  GumbelParams P{};
+  P.logits = logits;
+  P.drafts = draft_tokens;
+  P.temps = temperatures;
+  P.key0 = static_cast<uint32_t>(seed);
+  P.key1 = static_cast<uint32_t>(seed >> 32);
+  P.B = B;
+  P.G = g;
+  P.V = V;
+  P.parts = gumbel_parts(B);
+  P.out_tokens = out_tokens;
+  P.out_J = out_num_accepted;
+  P.out_status = out_status;
+  const size_t state_bytes = (static_cast<size_t>(B) * sizeof(int) + 255) / 256 * 256;
+  P.state = static_cast<int*>(workspace);
+  P.partials = static_cast<char*>(workspace) + state_bytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaError_t e = cudaMemsetAsync(workspace, 0, state_bytes, s); e != cudaSuccess)
+    return fail_cuda("clearing the workspace", e);
   ProfScope prof(SPECDEC_KERNEL_GUMBEL, s);
-  if (cudaError_t e = launch_gumbel_verify(logits, ldt, draft_tokens, temperatures, seed, B, g, V,
-                                           gumbel_vec(logits, V, elem_size(ldt)), out_tokens, out_num_accepted,
-                                           out_status, s);
-      e != cudaSuccess)
-    return fail_cuda("Gumbel verification kernel", e);
+  if (cudaError_t e = launch_gumbel_verify(P, ldt, gumbel_vec(logits, V, elem_size(ldt)), s); e != cudaSuccess)
+    return fail_cuda("Gumbel verification kernels", e);
   return SPECDEC_OK;
 }
 

@@ -187,9 +187,21 @@ cudaError_t launch_kv_compact(const KvCompactParams& P, cudaStream_t stream);
 // Sampled tree verification by recursive rejection at every node.
 cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream);
 // Gumbel-coupled verification and the drafter's shared-noise sampler (Philox noise).
-cudaError_t launch_gumbel_verify(const void* logits, specdec_dtype ldt, const int32_t* drafts, const float* temps,
-                                 uint64_t seed, int B, int G, int V, bool vec, int32_t* out_tokens, int32_t* out_J,
-                                 int32_t* out_status, cudaStream_t stream);
+struct GumbelParams {
+  const void* logits;
+  const int32_t* drafts;
+  const float* temps;
+  uint32_t key0, key1;
+  int B, G, V, parts;
+  int32_t* out_tokens;
+  int32_t* out_J;
+  int32_t* out_status;
+  void* partials;  // workspace: [B, 2, parts] parts of the current wave's rows
+  int* state;      // workspace: [B] 0 while the round is open (cleared per call)
+};
+cudaError_t launch_gumbel_verify(const GumbelParams& P, specdec_dtype ldt, bool vec, cudaStream_t stream);
+int gumbel_parts(int B);
+size_t gumbel_workspace_bytes(int B);  // [B] state (cleared per call), then the wave's parts
 cudaError_t launch_gumbel_noise(uint64_t seed, int B, int R, int V, float* out, cudaStream_t stream);
 cudaError_t launch_gumbel_draft(const float* q, uint64_t seed, int B, int G, int V, bool vec, int32_t* out,
                                 cudaStream_t stream);

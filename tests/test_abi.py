@@ -23,7 +23,7 @@ def test_header_declares_the_four_verification_calls():
     for fn in ("specdec_verify_chain", "specdec_verify_greedy", "specdec_verify_tree",
                "specdec_build_tree_mask", "specdec_verify_block", "specdec_verify_tree_recursive",
                "specdec_verify_gumbel", "specdec_gumbel_draft", "specdec_gumbel_noise",
-               "specdec_verify_chain_varlen", "specdec_compact_kv"):
+               "specdec_verify_chain_varlen", "specdec_compact_kv", "specdec_gumbel_workspace_bytes"):
         assert fn in names
 
 
@@ -111,9 +111,11 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_compact_kv(p, 0, 16, 160, 10, None, 0, 0, 0, 1, p, p, 2, p, None, None, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_compact_kv(p, 16, 16, 0, 10, p, 0, 4, 64, 1, p, p, 2, p, None, None, None) == sd.ERR_INVALID_ARG
     # Gumbel coupling: null drafts, bad sizes, too many rows per sequence
-    assert lib.specdec_verify_gumbel(p, sd.BF16, None, p, 1, 1, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG
-    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 0, 1, 8, p, p, None, None) == sd.ERR_INVALID_ARG
-    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 1, 600, 8, p, p, None, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_gumbel(p, sd.BF16, None, p, 1, 1, 1, 8, p, p, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 0, 1, 8, p, p, None, ws, 4096, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 1, 600, 8, p, p, None, ws, 4096, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_gumbel(p, sd.BF16, p, p, 1, 64, 1, 8, p, p, None, ws, 16, None) == sd.ERR_WORKSPACE
+    assert lib.specdec_gumbel_workspace_bytes(256, 7) > 0 and lib.specdec_gumbel_workspace_bytes(0, 7) == 0
     assert lib.specdec_gumbel_draft(None, 1, 1, 1, 8, p, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_gumbel_draft(p, 1, 1, 1, 0, p, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_gumbel_noise(1, 1, 1, 8, None, None) == sd.ERR_INVALID_ARG
