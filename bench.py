@@ -49,8 +49,8 @@ DEFAULT_WORKLOAD = "chain_b256_v128256"
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from
-# one ncu capture of the benchmarked workload, keyed by the sha256 of the kernel source
-# it was taken on; reported as null once the source differs.
+# one ncu capture of the benchmarked workload, keyed by the sha256 of that kernel's source
+# files (KERNEL_SOURCES) it was taken on; reported as null once they differ.
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
     "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
@@ -59,9 +59,20 @@ NCU_TRAFFIC = {
 }
 
 
-def kernel_source_sha() -> str:
+# The translation unit of each profiled kernel and the headers it includes.
+KERNEL_SOURCES = {
+    "chain_seq": ("chain_seq.cu", "specdec_device.cuh", "specdec_internal.h"),
+    "chain_stats": ("chain_stream.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
+}
+
+
+def kernel_source_sha(kernel: str | None = None) -> str:
+    """sha256 (16 hex digits) of a kernel's source files, or of every CUDA source."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "speculative_decoding_token_temperature_gb300" / "csrc").glob("*")):
+    csrc = ROOT / "speculative_decoding_token_temperature_gb300" / "csrc"
+    files = ([csrc / f for f in KERNEL_SOURCES[kernel]] if kernel in KERNEL_SOURCES else
+             sorted(p for p in csrc.iterdir() if p.suffix in (".cu", ".cuh", ".h")))
+    for p in files:
         h.update(p.read_bytes())
     return h.hexdigest()[:16]
 
@@ -605,7 +616,7 @@ def main():
         kname, alg_bytes = "chain_stats", rows * V * esize   # every logits row read once
     k_ms, k_n = per_kernel[kname]
     achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kname)
     traffic = NCU_TRAFFIC.get(kname, {})
     traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
     # bytes one whole call must move (the same left-to-right count for either chain
