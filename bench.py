@@ -54,8 +54,10 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
     "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
-    # profiles/chain_seq_b256_v128256.md: 320.67 MB read + 3.24 MB written (batch seed 0)
-    "chain_seq": {"bytes": 323_909_120, "src_sha": "392be0e2941a591a"},
+    # profiles/chain_seq_b256_v128256.md: 320.22 MB read + 3.26 MB written (batch seed 0)
+    "chain_seq": {"bytes": 323_471_616, "src_sha": "84a44dd5ad4a2df5"},
+    # profiles/block_row_b256_v128256.md: 1445.93 MB read + 5.20 MB written (batch seed 0)
+    "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b"},
 }
 
 
@@ -63,6 +65,7 @@ NCU_TRAFFIC = {
 KERNEL_SOURCES = {
     "chain_seq": ("chain_seq.cu", "specdec_device.cuh", "specdec_internal.h"),
     "chain_stats": ("chain_stream.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
+    "block_fused": ("block_fused.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
 }
 
 
