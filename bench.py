@@ -80,6 +80,27 @@ def kernel_source_sha(kernel: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
+def replica_round(rank: int, s: int) -> int:
+    """The workload round (seed) of batch s on rank `rank`: replicas verify different data."""
+    return 100 * rank + s
+
+
+def max_over_ranks(elapsed_ms: float, dist=None, device="cpu") -> float:
+    """The timed interval of the whole job: the maximum over ranks (after the barriers that
+    bracket the timed region).  dist: torch.distributed or None for one process."""
+    if dist is None:
+        return float(elapsed_ms)
+    import torch
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def job_value(units_per_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's units (weak scaling) over the slowest rank's time."""
+    return units_per_step * world / (ms_per_step / 1e3)
+
+
 def measured_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -272,7 +293,7 @@ def run_kv_compact(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     _build.ensure_built()
     sd.load_library()
-    x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 100 * rank, dev)
+    x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, replica_round(rank, 0), dev)
     walk = sd.verify_tree_recursive(*(x[k] for k in ("logits", "draft_probs", "node_tokens", "parents",
                                                      "temperatures", "uniforms")), D)
     cache = torch.zeros(B, KV_PREFIX + N, KV_SLOT_BYTES // 2, dtype=torch.bfloat16, device=dev)
@@ -379,7 +400,8 @@ def run_tree_rr(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     _build.ensure_built()
     sd.load_library()
-    sets = [workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 100 * rank + s, dev) for s in range(args.sets)]
+    sets = [workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, replica_round(rank, s), dev)
+            for s in range(args.sets)]
     outs = [{"tokens": torch.empty(B, D + 1, dtype=torch.int32, device=dev),
              "path": torch.empty(B, D, dtype=torch.int32, device=dev),
              "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
@@ -410,11 +432,7 @@ def run_tree_rr(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     ms_per_step = elapsed_ms / args.steps
     with sd.KernelTimer(max_launches=2 * args.steps + 16) as kt:
         torch.cuda.synchronize()
@@ -446,7 +464,7 @@ def run_tree_rr(args, rank, world, local_rank):
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
     achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
-    line = dict(base, value=rows * world / (ms_per_step / 1e3), ms_per_step=ms_per_step, dtype="f32", config=dict(
+    line = dict(base, value=job_value(rows, world, ms_per_step), ms_per_step=ms_per_step, dtype="f32", config=dict(
         cfg, parallelism=f"replicas x{world}", l2=f"{args.sets} seeded batches rotated (inputs smaller than L2)"),
         roofline={"kernel": "tree_rr", "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
@@ -515,7 +533,7 @@ def main():
     B, g, V, dtype = workload_shape(args.workload)
     esize = 2 if dtype == "bf16" else 4
     rows = B * (g + 1)
-    sets = [workloads.chain_workload(args.workload, 100 * rank + s, dev) for s in range(args.sets)]
+    sets = [workloads.chain_workload(args.workload, replica_round(rank, s), dev) for s in range(args.sets)]
     keys = ("logits", "draft_probs", "draft_tokens", "temperatures", "uniforms")
     outs = [{"tokens": torch.empty(B, g + 1, dtype=torch.int32, device=dev),
              "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
@@ -572,13 +590,9 @@ def main():
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = rows * world / (ms_per_step / 1e3)
+    value = job_value(rows, world, ms_per_step)
 
     # Per-kernel durations: the same K steps again with every library launch bracketed
     # by CUDA events on the launching stream.
