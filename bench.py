@@ -12,6 +12,9 @@ tests up to the first rejection, residual/bonus draw).
 
 --rule block times block verification (specdec_verify_block: the draft judged jointly,
 every row and q row read) on the same workload instead of the chain rule.
+--rule tree times the Medusa candidate-tree walk (specdec_verify_tree) on
+tree_b32_n64_v32000 (the Medusa sparse tree of 64 nodes, half the sequences greedy); rows
+are B*(N+1) candidate rows per call.
 --rule tree_recursive times sampled tree verification by recursive rejection
 (specdec_verify_tree_recursive) on tree_rr_b32_n64_v32000 (the Medusa sparse tree's
 topology, tokens drafted i.i.d. per node); rows are B*(N+1) candidate rows per call.
@@ -267,6 +270,7 @@ def run_reference(args, rank):
 
 
 TREE_RR_WORKLOAD = "tree_rr_b32_n64_v32000"
+TREE_WORKLOAD = "tree_b32_n64_v32000"
 KV_SLOT_BYTES = 128 * 1024  # one cache slot: 32 layers x 8 KV heads x 128 x (K, V) x bf16
 KV_PREFIX = 64
 
@@ -340,29 +344,48 @@ def run_kv_compact(args, rank, world, local_rank):
 
 
 def run_tree_rr(args, rank, world, local_rank):
-    """Sampled tree verification by recursive rejection: the same timing contract."""
+    """Token-tree verification on the Medusa sparse tree's topology: the recursive-rejection
+    walk (rule tree_recursive, every node drafted i.i.d. from q) or the Medusa walk (rule
+    tree: sample from the target at each node, descend on a matching child).  The same
+    timing contract as the chain rule; rows are B*(N+1) candidate rows per call."""
     import numpy as np
     import torch
     import workloads
     from oracle import specdec_oracle as so  # the tree topology and the CPU baseline only
 
-    w = workloads.TREE_RR_WORKLOADS[TREE_RR_WORKLOAD]
+    medusa = args.rule == "tree"
+    name = TREE_WORKLOAD if medusa else TREE_RR_WORKLOAD
+    w = (workloads.TREE_WORKLOADS if medusa else workloads.TREE_RR_WORKLOADS)[name]
     B, V, D = w["B"], w["V"], w["depth"]
-    parents, _, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
+    parents, paths, _ = so.medusa_sparse_tree(workloads.medusa_workload_accuracies(), 64)
     N = len(parents)
     rows = B * (N + 1)
-    keys = ("logits", "draft_probs", "node_tokens", "parents", "temperatures", "uniforms")
+    keys = (("logits", "node_tokens", "parents", "temperatures", "uniforms") if medusa else
+            ("logits", "draft_probs", "node_tokens", "parents", "temperatures", "uniforms"))
+    kernel = "tree_walk" if medusa else "tree_rr"
     base = {"metric": METRIC, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
-    cfg = {"workload": TREE_RR_WORKLOAD, "rule": "tree_recursive", "B": B, "N": N, "V": V, "max_depth": D,
-           "logits_dtype": w["dtype"], "draft_probs_dtype": "fp32"}
+    cfg = {"workload": name, "rule": args.rule, "B": B, "N": N, "V": V, "max_depth": D,
+           "logits_dtype": w["dtype"]}
+    if not medusa:
+        cfg["draft_probs_dtype"] = "fp32"
+
+    def make(round_idx, device):
+        if medusa:
+            return workloads.tree_workload(name, parents, paths, round_idx, device)
+        return workloads.tree_rr_workload(name, parents, round_idx, device)
 
     def oracle_rate(x, seconds, max_seqs):
         L = x["logits"].float().numpy() if w["dtype"] == "bf16" else x["logits"].numpy()
-        q, t, T, u = (x[k].numpy() for k in ("draft_probs", "node_tokens", "temperatures", "uniforms"))
+        t, T, u = (x[k].numpy() for k in ("node_tokens", "temperatures", "uniforms"))
+        q = None if medusa else x["draft_probs"].numpy()
         n, t0 = 0, time.perf_counter()
         while n < max_seqs:
-            so.verify_tree_rr_sequence(L[n % B], q[n % B], t[n % B], parents, float(T[n % B]), u[n % B], D)
+            i = n % B
+            if medusa:
+                so.verify_tree_sequence(L[i], t[i], parents, float(T[i]), u[i], D)
+            else:
+                so.verify_tree_rr_sequence(L[i], q[i], t[i], parents, float(T[i]), u[i], D)
             n += 1
             if time.perf_counter() - t0 >= seconds:
                 break
@@ -373,7 +396,7 @@ def run_tree_rr(args, rank, world, local_rank):
         if rank != 0:
             return 0
         torch.set_num_threads(1)
-        x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, 0, "cpu")
+        x = make(0, "cpu")
         per_step = args.ref_sequences
         for _ in range(args.warmup):
             oracle_rate(x, 1e9, per_step)
@@ -385,7 +408,7 @@ def run_tree_rr(args, rank, world, local_rank):
         line = dict(base, impl="reference", value=value, ms_per_step=dt * 1e3, dtype="f64",
                     config=dict(cfg, step_sample_sequences=per_step),
                     cpu_baseline={"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": f"{per_step} sequences of {TREE_RR_WORKLOAD} per step"},
+                                  "sample": f"{per_step} sequences of {name} per step"},
                     e2e={"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
         print(json.dumps(line), flush=True)
         return 0
@@ -400,17 +423,18 @@ def run_tree_rr(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     _build.ensure_built()
     sd.load_library()
-    sets = [workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, replica_round(rank, s), dev)
-            for s in range(args.sets)]
+    sets = [make(replica_round(rank, s), dev) for s in range(args.sets)]
     outs = [{"tokens": torch.empty(B, D + 1, dtype=torch.int32, device=dev),
              "path": torch.empty(B, D, dtype=torch.int32, device=dev),
              "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
              "status": torch.empty(B, dtype=torch.int32, device=dev)} for _ in sets]
     stream = torch.cuda.current_stream(dev)
 
+    verify = sd.verify_tree if medusa else sd.verify_tree_recursive
+
     def step(i):
         x = sets[i % len(sets)]
-        sd.verify_tree_recursive(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=stream)
+        verify(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -440,9 +464,9 @@ def run_tree_rr(args, rank, world, local_rank):
             step(i)
         torch.cuda.synchronize()
         per_kernel = kt.read()
-    k_ms, k_n = per_kernel["tree_rr"]
+    k_ms, k_n = per_kernel[kernel]
     # a lower bound on the bytes the walk must read: every visited node's logits row once,
-    # and the q row of every node where the walk ended with children (all rejected)
+    # and (recursive rejection) the q row of every node where the walk ended with children
     es = 2 if w["dtype"] == "bf16" else 4
     has_kids = np.zeros(N + 1, dtype=bool)
     for j, a in enumerate(parents):
@@ -457,7 +481,7 @@ def run_tree_rr(args, rank, world, local_rank):
                 continue
             tot += (J[b] + 1) * V * es
             last = 0 if J[b] == 0 else 1 + int(path[b][J[b] - 1])
-            if has_kids[last]:
+            if has_kids[last] and not medusa:
                 tot += V * 4
         alg.append(tot)
     alg_bytes = float(np.mean(alg))
@@ -466,7 +490,7 @@ def run_tree_rr(args, rank, world, local_rank):
     achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
     line = dict(base, value=job_value(rows, world, ms_per_step), ms_per_step=ms_per_step, dtype="f32", config=dict(
         cfg, parallelism=f"replicas x{world}", l2=f"{args.sets} seeded batches rotated (inputs smaller than L2)"),
-        roofline={"kernel": "tree_rr", "bound": "latency", "achieved": achieved,
+        roofline={"kernel": kernel, "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
                   "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,
                   "traffic": None},
@@ -499,7 +523,8 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--rule", choices=["chain", "block", "tree_recursive", "gumbel", "chain_varlen", "kv_compact"],
+    ap.add_argument("--rule", choices=["chain", "block", "tree", "tree_recursive", "gumbel", "chain_varlen",
+                                       "kv_compact"],
                     default="chain")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -508,7 +533,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.rule == "tree_recursive":
+    if args.rule in ("tree", "tree_recursive"):
         return run_tree_rr(args, rank, world, local_rank)
     if args.rule == "kv_compact":
         return run_kv_compact(args, rank, world, local_rank)

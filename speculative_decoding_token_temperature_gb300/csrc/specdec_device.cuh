@@ -81,6 +81,44 @@ template <int VEC> __device__ __forceinline__ void load_q(const float* p, int64_
   }
 }
 
+// Row reads from global memory (read-only path) or from the rows staged in shared memory.
+template <typename T, int VEC, bool SMEM> struct RowAccess {
+  static __device__ __forceinline__ void vec(const T* p, int64_t k, float (&v)[VEC]) {
+    if constexpr (!SMEM || VEC == 1) {
+      VecLoad<T, VEC>::load(p, k, v);
+    } else if constexpr (sizeof(T) == 2) {
+      const uint4 w = *reinterpret_cast<const uint4*>(p + k);
+      v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+      v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    } else {
+      const float4 w = *reinterpret_cast<const float4*>(p + k);
+      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    }
+  }
+  static __device__ __forceinline__ float one(const T* p, int64_t k) {
+    if constexpr (!SMEM) return Elem<T>::load(p, k);
+    else if constexpr (sizeof(T) == 2) return __uint_as_float(static_cast<uint32_t>(p[k]) << 16);
+    else return p[k];
+  }
+  static __device__ __forceinline__ void qvec(const float* p, int64_t k, float (&v)[VEC]) {
+    if constexpr (!SMEM) {
+      load_q<VEC>(p, k, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VEC; j += 4) {
+        const float4 w = *reinterpret_cast<const float4*>(p + k + j);
+        v[j] = w.x; v[j + 1] = w.y; v[j + 2] = w.z; v[j + 3] = w.w;
+      }
+    }
+  }
+  static __device__ __forceinline__ float qone(const float* p, int64_t k) {
+    if constexpr (!SMEM) return __ldg(p + k);
+    else return p[k];
+  }
+};
+
+constexpr int kStageCopy = 32768;  // bytes per bulk copy when staging a row
+
 // ---------------------------------------------------------------------------------
 // Block reductions and scans (NT threads, fixed order => deterministic)
 // ---------------------------------------------------------------------------------

@@ -30,43 +30,6 @@ namespace specdec {
 
 namespace {
 
-// Row reads from global memory (read-only path) or from the rows staged in shared memory.
-template <typename T, int VEC, bool SMEM> struct RowAccess {
-  static __device__ __forceinline__ void vec(const T* p, int64_t k, float (&v)[VEC]) {
-    if constexpr (!SMEM || VEC == 1) {
-      VecLoad<T, VEC>::load(p, k, v);
-    } else if constexpr (sizeof(T) == 2) {
-      const uint4 w = *reinterpret_cast<const uint4*>(p + k);
-      v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-      v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-    } else {
-      const float4 w = *reinterpret_cast<const float4*>(p + k);
-      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
-    }
-  }
-  static __device__ __forceinline__ float one(const T* p, int64_t k) {
-    if constexpr (!SMEM) return Elem<T>::load(p, k);
-    else if constexpr (sizeof(T) == 2) return __uint_as_float(static_cast<uint32_t>(p[k]) << 16);
-    else return p[k];
-  }
-  static __device__ __forceinline__ void qvec(const float* p, int64_t k, float (&v)[VEC]) {
-    if constexpr (!SMEM) {
-      load_q<VEC>(p, k, v);
-    } else {
-#pragma unroll
-      for (int j = 0; j < VEC; j += 4) {
-        const float4 w = *reinterpret_cast<const float4*>(p + k + j);
-        v[j] = w.x; v[j + 1] = w.y; v[j + 2] = w.z; v[j + 3] = w.w;
-      }
-    }
-  }
-  static __device__ __forceinline__ float qone(const float* p, int64_t k) {
-    if constexpr (!SMEM) return __ldg(p + k);
-    else return p[k];
-  }
-};
-
-constexpr int kStageCopy = 32768;  // bytes per bulk copy when staging a row
 
 template <typename T, int VEC, int NT, bool STAGED>
 __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
@@ -88,6 +51,29 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
   const float* ub = P.u + static_cast<int64_t>(b) * (N + 1);
   int32_t* out_t = P.out_tokens + static_cast<int64_t>(b) * (D + 1);
   int32_t* out_p = P.out_path + static_cast<int64_t>(b) * D;
+  auto row_off = [&](int node) { return (static_cast<int64_t>(b) * (N + 1) + (node < 0 ? 0 : 1 + node)) * V; };
+  auto issue_rows = [&](int node, bool with_q) {  // one thread: the node's rows into the stage
+    fence_proxy_async_smem();
+    const int64_t roff = row_off(node);
+    const char* lsrc = reinterpret_cast<const char*>(static_cast<const T*>(P.logits) + roff);
+    const char* qsrc = reinterpret_cast<const char*>(P.q + roff);
+    const uint32_t lb = static_cast<uint32_t>(static_cast<int64_t>(V) * sizeof(T));
+    const uint32_t qb = with_q ? static_cast<uint32_t>(V) * 4u : 0u;
+    mbar_expect_tx(&sbar, lb + qb);
+    for (uint32_t o = 0; o < lb; o += kStageCopy)
+      bulk_copy_g2s(stage + o, lsrc + o, min(static_cast<uint32_t>(kStageCopy), lb - o), &sbar);
+    for (uint32_t o = 0; o < qb; o += kStageCopy)
+      bulk_copy_g2s(stage + lbytes + o, qsrc + o, min(static_cast<uint32_t>(kStageCopy), qb - o), &sbar);
+  };
+  if constexpr (STAGED) {
+    // The root's rows are read by every walk that passes validation; in a valid tree node 0
+    // is a child of the root, so its q row is needed whenever N > 0 and the walk samples.
+    if (tid == 0) {
+      mbar_init(&sbar, 1);
+      mbar_fence_init();
+      issue_rows(-1, N > 0 && !greedy);
+    }
+  }
 
   // Validate the tree, the tokens, the temperature and (sampled) every uniform.
   int st = 0;
@@ -118,43 +104,29 @@ __global__ void __launch_bounds__(NT) tree_rr_kernel(const TreeParams P) {
   }
   st = Block<NT>::or_int(st, sh_i);
 
-  if constexpr (STAGED) {
-    if (tid == 0) {
-      mbar_init(&sbar, 1);
-      mbar_fence_init();
-    }
-    __syncthreads();
-  }
   uint32_t sphase = 0;
+  if constexpr (STAGED) {  // the root copies land before the CTA reads the stage or exits
+    if (Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i)) st |= SPECDEC_STATUS_TIMEOUT;
+    sphase ^= 1u;
+  }
   int node = -1, d = 0;
   if (!(st & SPECDEC_STATUS_ERROR_MASK)) {
     for (;;) {
-      const int row = (node < 0) ? 0 : 1 + node;
-      const int64_t roff = (static_cast<int64_t>(b) * (N + 1) + row) * V;
+      const int64_t roff = row_off(node);
       const T* lrow = static_cast<const T*>(P.logits) + roff;
       const float* qrow = P.q + roff;
       if constexpr (STAGED) {  // bring the node's rows into shared memory (q only if it has children)
-        int kids = 0;
-        for (int j = tid; j < N; j += NT) kids |= (__ldg(P.parents + j) == node) ? 1 : 0;
-        kids = Block<NT>::or_int(kids, sh_i);  // also orders every earlier read of the stage
-        if (tid == 0) {
-          fence_proxy_async_smem();
-          const uint32_t lb = static_cast<uint32_t>(static_cast<int64_t>(V) * sizeof(T));
-          const uint32_t qb = (kids && !greedy) ? static_cast<uint32_t>(V) * 4u : 0u;
-          mbar_expect_tx(&sbar, lb + qb);
-          for (uint32_t o = 0; o < lb; o += kStageCopy)
-            bulk_copy_g2s(stage + o, reinterpret_cast<const char*>(lrow) + o, min(static_cast<uint32_t>(kStageCopy), lb - o),
-                          &sbar);
-          for (uint32_t o = 0; o < qb; o += kStageCopy)
-            bulk_copy_g2s(stage + lbytes + o, reinterpret_cast<const char*>(qrow) + o,
-                          min(static_cast<uint32_t>(kStageCopy), qb - o), &sbar);
+        if (node >= 0) {
+          int kids = 0;
+          for (int j = tid; j < N; j += NT) kids |= (__ldg(P.parents + j) == node) ? 1 : 0;
+          kids = Block<NT>::or_int(kids, sh_i);  // also orders every earlier read of the stage
+          if (tid == 0) issue_rows(node, kids && !greedy);
+          if (Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i)) {  // uniform decision
+            st |= SPECDEC_STATUS_TIMEOUT;
+            break;
+          }
+          sphase ^= 1u;
         }
-        const int gave_up = Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i);  // uniform decision
-        if (gave_up) {
-          st |= SPECDEC_STATUS_TIMEOUT;
-          break;
-        }
-        sphase ^= 1u;
         lrow = reinterpret_cast<const T*>(stage);
         qrow = reinterpret_cast<const float*>(stage + lbytes);
       }
