@@ -104,6 +104,36 @@ def job_value(units_per_step: float, world: int, ms_per_step: float) -> float:
     return units_per_step * world / (ms_per_step / 1e3)
 
 
+def graph_timed(step, steps: int, dev, dist=None):
+    """Capture `steps` calls of step(i, stream) into one CUDA graph and time one replay with
+    CUDA events on the replay stream (barriers and synchronisation on both sides).  For
+    launch-bound rules, whose kernels finish sooner than the host issues the next call,
+    this measures the device work of exactly `steps` steps.  Returns milliseconds."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(steps):
+                step(i, side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    g.replay()  # untimed: first replay uploads the graph
+    torch.cuda.synchronize()
+    run = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(run)
+    g.replay()
+    ev1.record(run)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return ev0.elapsed_time(ev1)
+
+
 def measured_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -273,6 +303,7 @@ TREE_RR_WORKLOAD = "tree_rr_b32_n64_v32000"
 TREE_WORKLOAD = "tree_b32_n64_v32000"
 KV_SLOT_BYTES = 128 * 1024  # one cache slot: 32 layers x 8 KV heads x 128 x (K, V) x bf16
 KV_PREFIX = 64
+KV_ROTATE = 24  # tree-slot windows rotated between steps (about 24 x 10 MB moved, over L2)
 
 
 def run_kv_compact(args, rank, world, local_rank):
@@ -300,12 +331,14 @@ def run_kv_compact(args, rank, world, local_rank):
     x = workloads.tree_rr_workload(TREE_RR_WORKLOAD, parents, replica_round(rank, 0), dev)
     walk = sd.verify_tree_recursive(*(x[k] for k in ("logits", "draft_probs", "node_tokens", "parents",
                                                      "temperatures", "uniforms")), D)
-    cache = torch.zeros(B, KV_PREFIX + N, KV_SLOT_BYTES // 2, dtype=torch.bfloat16, device=dev)
-    prefix = torch.full((B,), KV_PREFIX, dtype=torch.int32, device=dev)
+    # Step i compacts the tree slots that follow prefix KV_PREFIX + (i mod KV_ROTATE) * (N + 1):
+    # the slots the steps touch add up to well over L2, so no step finds its rows there.
+    cache = torch.zeros(B, KV_PREFIX + KV_ROTATE * (N + 1), KV_SLOT_BYTES // 2, dtype=torch.bfloat16, device=dev)
+    prefixes = [torch.full((B,), KV_PREFIX + r * (N + 1), dtype=torch.int32, device=dev) for r in range(KV_ROTATE)]
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        sd.compact_kv(cache, prefix, walk["path"], walk["num_accepted"], stream=stream)
+    def step(i, st=stream):
+        sd.compact_kv(cache, prefixes[i % KV_ROTATE], walk["path"], walk["num_accepted"], stream=st)
 
     for i in range(args.warmup):
         step(i)
@@ -318,15 +351,17 @@ def run_kv_compact(args, rank, world, local_rank):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
+    with ClockSampler(local_rank, uuid) as clocks:  # one short kernel per step: timed as a CUDA graph
+        elapsed = graph_timed(step, args.steps, dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank, uuid) as clocks:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
+    ms = elapsed / args.steps
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
     gbs = moved / (ms / 1e3) / 1e9
@@ -334,7 +369,9 @@ def run_kv_compact(args, rank, world, local_rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": TREE_RR_WORKLOAD, "rule": "kv_compact", "B": B, "N": N,
-                       "slot_bytes": KV_SLOT_BYTES, "prefix": KV_PREFIX, "moves_per_step": moves},
+                       "slot_bytes": KV_SLOT_BYTES, "prefix": KV_PREFIX, "moves_per_step": moves,
+                       "l2": f"{KV_ROTATE} slot windows rotated between steps (touched bytes larger than L2)",
+                       "launch": f"CUDA graph of the {args.steps} steps; eager Python calls: {eager_ms * 1e3:.1f} us per step"},
             "roofline": {"kernel": "kv_compact", "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "algorithmic_bytes_per_launch": moved, "traffic": None},
             "gpu_launches": args.steps, "clocks": clocks.summary(), "kernel_src_sha": kernel_source_sha()}
@@ -432,9 +469,9 @@ def run_tree_rr(args, rank, world, local_rank):
 
     verify = sd.verify_tree if medusa else sd.verify_tree_recursive
 
-    def step(i):
+    def step(i, st=stream):
         x = sets[i % len(sets)]
-        verify(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=stream)
+        verify(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=st)
 
     for i in range(args.warmup):
         step(i)
@@ -444,26 +481,20 @@ def run_tree_rr(args, rank, world, local_rank):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # One kernel per step, shorter than the Python call that issues it: the K steps are
+    # captured into a CUDA graph and its replay is timed.
     with ClockSampler(local_rank, uuid) as clocks:
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+        elapsed_ms = max_over_ranks(graph_timed(step, args.steps, dev, dist), dist, dev)
     ms_per_step = elapsed_ms / args.steps
-    with sd.KernelTimer(max_launches=2 * args.steps + 16) as kt:
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            step(i)
-        torch.cuda.synchronize()
-        per_kernel = kt.read()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
+    per_kernel = {kernel: (elapsed_ms, args.steps)}
     k_ms, k_n = per_kernel[kernel]
     # a lower bound on the bytes the walk must read: every visited node's logits row once,
     # and (recursive rejection) the q row of every node where the walk ended with children
@@ -489,7 +520,8 @@ def run_tree_rr(args, rank, world, local_rank):
     peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
     achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
     line = dict(base, value=job_value(rows, world, ms_per_step), ms_per_step=ms_per_step, dtype="f32", config=dict(
-        cfg, parallelism=f"replicas x{world}", l2=f"{args.sets} seeded batches rotated (inputs smaller than L2)"),
+        cfg, parallelism=f"replicas x{world}", l2=f"{args.sets} seeded batches rotated (inputs larger than L2)",
+        launch=f"CUDA graph of the {args.steps} steps; eager Python calls: {eager_ms * 1e3:.1f} us per step"),
         roofline={"kernel": kernel, "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
                   "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,

@@ -409,11 +409,13 @@ __device__ __forceinline__ void st_async_16(uint32_t remote_addr, const float4& 
       : "memory");
 }
 // Wait for a phase completed by other CTAs' st.async writes (acquire at cluster scope),
-// bounded like mbar_wait.
+// bounded like mbar_wait.  It polls with the non-blocking test_wait: a thread suspended in
+// try_wait was measured to resume several microseconds after such a phase completed, which
+// on a chain of dependent exchanges costs more than the polling.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -421,13 +423,29 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = global_timer_ns();  // one loop shape for every lane (measured faster)
   for (;;) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (global_timer_ns() - t0 > kMaxWaitNs) return false;
   }
 }
+// Plain 32-bit loads and stores of (possibly another CTA's) shared memory, addressed by
+// cluster_map; ordered with respect to other CTAs by cluster_sync_all().
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Split cluster barrier without memory ordering: every thread arrives, then waits.  After
+// mbarrier initialisation (fence.mbarrier_init by the initialising thread) this makes the
+// barriers usable by the other CTAs' bulk copies and st.async.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 // Every thread of every CTA in the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");

@@ -167,6 +167,10 @@ struct TreeParams {
   int32_t* out_status;
 };
 
+// The Medusa walk with rows split across a cluster of C CTAs: the cluster size for B
+// sequences of V-entry rows (0 when no size fits: 16-byte rows needed), and its launch.
+int tree_walk_cluster_size(int B, int V, specdec_dtype ldt);
+cudaError_t launch_tree_walk_cluster(const TreeParams& P, specdec_dtype ldt, int C, cudaStream_t stream);
 cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector_path,
                              cudaStream_t stream);
 // Accepted-branch KV compaction (contiguous or paged caches).

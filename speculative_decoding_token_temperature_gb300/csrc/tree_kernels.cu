@@ -6,10 +6,9 @@
 // total mass of 2^((l - max) * log2(e) / T) and scans the row in index order for the
 // smallest k with C_k > u_d * S (inverse CDF of softmax(l / T)).  If a child of the node
 // carries the drawn token (lowest node index on duplicates) the walk descends; otherwise
-// the drawn token ends the walk.  Only the rows on the walk are read.  When a row fits in
-// shared memory (V = 32000: 64 KB bf16, 128 KB fp32) it is staged there by bulk copies as
-// the walk reaches its node (the root row's copy is issued before the inputs are
-// validated), so the three passes read shared memory and only the copy waits on HBM.
+// the drawn token ends the walk.  Only the rows on the walk are read.  This one-CTA walk
+// over global memory serves rows that are not 16-byte aligned or too long to stage; the
+// others take the cluster walk of tree_walk_cluster.cu.
 //
 // Mask (SD 20.5, box "Token tree and tree attention"): node i sees every prefix column,
 // itself and its ancestors; position id P + depth(i).
@@ -23,10 +22,8 @@ namespace specdec {
 
 namespace {
 
-template <typename T, int VEC, int NT, bool STAGED>
+template <typename T, int VEC, int NT>
 __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
-  extern __shared__ __align__(128) unsigned char stage[];
-  __shared__ __align__(8) uint64_t sbar;
   __shared__ float sh_f[32];
   __shared__ int sh_i[32];
   __shared__ double sh_d[32];
@@ -40,25 +37,6 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
   const int32_t* toks = P.node_tokens + static_cast<int64_t>(b) * N;
   int32_t* out_t = P.out_tokens + static_cast<int64_t>(b) * (D + 1);
   int32_t* out_p = P.out_path + static_cast<int64_t>(b) * D;
-  using A = RowAccess<T, VEC, STAGED>;
-  const uint32_t row_bytes = static_cast<uint32_t>(static_cast<int64_t>(V) * sizeof(T));
-  auto row_ptr = [&](int node) {
-    return static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * (N + 1) + (node < 0 ? 0 : 1 + node)) * V;
-  };
-  auto issue_row = [&](int node) {  // one thread: copy the node's row into the stage
-    fence_proxy_async_smem();
-    mbar_expect_tx(&sbar, row_bytes);
-    const char* src = reinterpret_cast<const char*>(row_ptr(node));
-    for (uint32_t o = 0; o < row_bytes; o += kStageCopy)
-      bulk_copy_g2s(stage + o, src + o, min(static_cast<uint32_t>(kStageCopy), row_bytes - o), &sbar);
-  };
-  if constexpr (STAGED) {
-    if (tid == 0) {  // the root row is read by every walk that passes validation
-      mbar_init(&sbar, 1);
-      mbar_fence_init();
-      issue_row(-1);
-    }
-  }
 
   // Validate the tree, the tokens, the temperature and the uniforms.
   int st = 0;
@@ -89,32 +67,18 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
   }
   st = Block<NT>::or_int(st, sh_i);
 
-  uint32_t sphase = 0;
-  if constexpr (STAGED) {  // the root copy lands before the CTA reads the stage or exits
-    if (Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i)) st |= SPECDEC_STATUS_TIMEOUT;
-    sphase ^= 1u;
-  }
   int node = -1, d = 0;
   if (!(st & SPECDEC_STATUS_ERROR_MASK)) {
     for (;;) {
-      const T* lrow = STAGED ? reinterpret_cast<const T*>(stage) : row_ptr(node);
-      if constexpr (STAGED) {
-        if (node >= 0) {  // every read of the previous row ended at the child search's barrier
-          if (tid == 0) issue_row(node);
-          if (Block<NT>::or_int(mbar_wait(&sbar, sphase) ? 0 : 1, sh_i)) {  // uniform decision
-            st |= SPECDEC_STATUS_TIMEOUT;
-            break;
-          }
-          sphase ^= 1u;
-        }
-      }
+      const int row = (node < 0) ? 0 : 1 + node;
+      const T* lrow = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * (N + 1) + row) * V;
       // pass 1: maximum and its lowest index (each thread walks its vectors in index order)
       float best = -kInf;
       int bidx = INT_MAX;
       bool nan = false;
       for (int k = tid * VEC; k < V; k += NT * VEC) {
         float v[VEC];
-        A::vec(lrow, k, v);
+        VecLoad<T, VEC>::load(lrow, k, v);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           nan |= (v[e] != v[e]);
@@ -136,7 +100,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
         float tot = 0.f;
         for (int k = tid * VEC; k < V; k += NT * VEC) {
           float v[VEC];
-          A::vec(lrow, k, v);
+          VecLoad<T, VEC>::load(lrow, k, v);
           float a = 0.f;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) a += ex2((v[e] - m) * c);
@@ -154,7 +118,7 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
           float a = 0.f;
           if (k < V) {
             float v[VEC];
-            A::vec(lrow, k, v);
+            VecLoad<T, VEC>::load(lrow, k, v);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               w[e] = ex2((v[e] - m) * c);
@@ -215,25 +179,9 @@ __global__ void __launch_bounds__(NT) tree_walk_kernel(const TreeParams P) {
   }
 }
 
-template <typename T, int VEC, bool STAGED>
+template <typename T, int VEC>
 cudaError_t launch_walk_t(const TreeParams& P, cudaStream_t stream) {
-  int smem = 0;
-  if constexpr (STAGED) {
-    smem = static_cast<int>(static_cast<int64_t>(P.V) * static_cast<int64_t>(sizeof(T)));
-    static unsigned long long configured = 0;
-    int dev = 0;
-    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured & bit)) {
-      if (cudaError_t e = cudaFuncSetAttribute(tree_walk_kernel<T, VEC, kTreeThreads, true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTreeStageBytes);
-          e != cudaSuccess)
-        return e;
-      configured |= bit;
-    }
-  }
-  return launch_kernel(tree_walk_kernel<T, VEC, kTreeThreads, STAGED>, dim3(P.B), dim3(kTreeThreads),
-                       static_cast<size_t>(smem), stream, 0, P);
+  return launch_kernel(tree_walk_kernel<T, VEC, kTreeThreads>, dim3(P.B), dim3(kTreeThreads), 0, stream, 0, P);
 }
 
 __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restrict__ parents, int N,
@@ -286,17 +234,14 @@ __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restric
 
 cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector_path,
                              cudaStream_t stream) {
-  if (vector_path) {  // 16-byte rows: staged in shared memory when one fits
-    const int64_t need = static_cast<int64_t>(P.V) * (ldt == SPECDEC_BF16 ? 2 : 4);
-    if (need <= kTreeStageBytes) {
-      if (ldt == SPECDEC_BF16) return launch_walk_t<uint16_t, 8, true>(P, stream);
-      return launch_walk_t<float, 4, true>(P, stream);
-    }
-    if (ldt == SPECDEC_BF16) return launch_walk_t<uint16_t, 8, false>(P, stream);
-    return launch_walk_t<float, 4, false>(P, stream);
+  if (vector_path) {
+    if (const int C = tree_walk_cluster_size(P.B, P.V, ldt); C > 0)
+      return launch_tree_walk_cluster(P, ldt, C, stream);
+    if (ldt == SPECDEC_BF16) return launch_walk_t<uint16_t, 8>(P, stream);
+    return launch_walk_t<float, 4>(P, stream);
   }
-  if (ldt == SPECDEC_BF16) return launch_walk_t<uint16_t, 1, false>(P, stream);
-  return launch_walk_t<float, 1, false>(P, stream);
+  if (ldt == SPECDEC_BF16) return launch_walk_t<uint16_t, 1>(P, stream);
+  return launch_walk_t<float, 1>(P, stream);
 }
 
 cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* mask,

@@ -80,6 +80,50 @@ def test_tree_b32_n64_v32000(sd, medusa64):
     assert stats["accepted"] > 0
 
 
+@pytest.mark.parametrize("C", ["1", "2", "4", "8"])
+@pytest.mark.parametrize("V,dtype", [(32008, "bf16"), (20004, "fp32"), (64, "bf16")])
+def test_tree_cluster_sizes(sd, medusa64, monkeypatch, C, V, dtype):
+    """Rows split across clusters of 1, 2, 4 and 8 CTAs (a short last slice at V = 32008
+    and 20004; at V = 64 each CTA of an 8-CTA cluster holds a single 16-byte vector).
+    Spiked logits (1 N(0,1), +10 on child tokens) make most walks descend several levels."""
+    parents, paths = medusa64
+    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    for seed in range(3):
+        x = workloads.make_tree_inputs(12, V, parents, paths, depth=4, seed=100 * seed + V % 97, device=DEV,
+                                       dtype=dtype, top=min(10, V), scale=1.0, spike=10.0,
+                                       temps="half_greedy:0.7")
+        out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+        _check_tree(out, x, 4, stats)
+    assert stats["accepted"] >= stats["sequences"]  # walks descend on average at least once
+    assert stats["flagged"] <= 1
+
+
+def test_tree_v128256_rows_split(sd, medusa64):
+    """A 128256-entry vocabulary (256 KB bf16 rows, staged as four 64 KB slices)."""
+    parents, paths = medusa64
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    x = workloads.make_tree_inputs(16, 128256, parents, paths, depth=4, seed=9, device=DEV, dtype="bf16",
+                                   scale=1.0, spike=12.0, temps="half_greedy:0.9")
+    out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+    _check_tree(out, x, 4, stats)
+    assert stats["accepted"] > 0 and stats["flagged"] <= 1
+
+
+def test_tree_deep_walks_b32(sd, medusa64):
+    """tree_b32_n64_v32000's shapes with logits whose spikes dominate, so walks reach the
+    deepest levels (the stated workload's spikes rarely win, and its walks stop at the root)."""
+    parents, paths = medusa64
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    for r in range(6):
+        x = workloads.make_tree_inputs(32, 32000, parents, paths, depth=4, seed=500 + r, device=DEV,
+                                       scale=1.0, spike=10.0)
+        out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+        _check_tree(out, x, 4, stats)
+    assert stats["accepted"] >= 1.5 * stats["sequences"]
+    assert stats["flagged"] <= 1
+
+
 @pytest.mark.parametrize("V,dtype", [(32000, "bf16"), (1001, "fp32"), (4096, "fp32"), (37, "bf16")])
 def test_tree_shapes_and_edges(sd, medusa64, V, dtype):
     parents, paths = medusa64
