@@ -7,27 +7,29 @@
 // the latency of one visit times the rows visited.  A cluster of C CTAs (C in 1, 2, 4, 8)
 // serves one sequence: CTA r stages the contiguous slice [r * slice, (r + 1) * slice) of
 // every visited row in its shared memory with bulk copies, and per row
-//   sweep    one pass over the slice: its maximum and lowest index (a 64-bit order key)
-//            and, sampled, its mass sum 2^((l - m_t) c) relative to each thread's running
-//            maximum m_t (rescaled as the maximum grows), combined over warps  -> mail A
+//   slice    its maximum and lowest index (a 64-bit order key) and, sampled, its mass
+//            sum 2^((l - m_t) c) relative to each thread's maximum m_t, combined over
+//            warps by rescaling to the warp maximum                           -> mail A
 //   decide   from every slice's key (and mass, rescaled to the row maximum m): the row's
 //            status, the greedy argmax, or the slice and warp chunk holding u * S
 //   draw     (sampled) the warp owning u * S scans its chunk in index order; the token
 //            goes to every CTA                                                  -> mail C
-// Mail is a 16- or 32-byte message from every CTA pushed into every member's shared memory
+// Mail is a 16-byte message from every CTA pushed into every member's shared memory
 // with st.async, completing transaction bytes on the receiver's mbarrier (no cluster-wide
 // barrier per exchange).  Every exchange is all-to-all (in mail C the CTAs that did not
 // draw send an empty message), and two mailbox parities alternate: a CTA sends into a
 // parity only after it received every member's message of the exchange in between, which
 // each member sends only after it received and read the parity's previous messages.
 // Every CTA reaches the same decisions from the same messages, so the walk stays uniform
-// across the cluster.  Cross-warp and cross-CTA masses are fp32 pairs (hi + lo) kept by
-// error-free sums (Knuth's TwoSum): fp64 arithmetic is slow on this part and this path is
-// a chain of dependent steps.  Waiting lanes enter their polling loop converged (a warp
+// across the cluster.  Masses are fp32 throughout (fp64 arithmetic is slow on this part
+// and this path is a chain of dependent steps): a prefix carries at most a few dozen
+// roundings, a relative error of a few 1e-6 at worst, below the 1e-5 band in which a
+// draw's boundary is treated as a tie.  Waiting lanes enter their polling loop converged (a warp
 // whose lanes wait while another lane still has to send was measured to stall for
 // microseconds).  The inputs (tree, tokens, temperature, uniforms) are validated in the
 // background of the walk and the walk's result is discarded when they fail, so validation
-// loads do not delay the first row.
+// loads do not delay the first row; trees of up to kWalkWarpSearch nodes are copied to
+// shared memory for the child searches.
 // Within a slice each warp owns a contiguous chunk, read by its lanes as consecutive
 // 16-byte vectors; index order inside a chunk is (iteration, lane, element).
 
@@ -46,43 +48,12 @@ constexpr int kWalkMaxCluster = 8;
 constexpr int kWalkWarpSearch = 512;  // trees up to this many nodes: one warp finds the child
 constexpr unsigned kFull = 0xffffffffu;
 
-// ---- fp32 pairs: value = hi + lo, |lo| <= ulp(hi) / 2 --------------------------------
-struct F2 {
-  float hi, lo;
-};
-__device__ __forceinline__ F2 two_sum(float a, float b) {  // a + b exactly, as a pair
-  const float s = a + b;
-  const float bb = s - a;
-  return {s, (a - (s - bb)) + (b - bb)};
-}
-__device__ __forceinline__ F2 f2_add(F2 x, F2 y) {
-  const F2 s = two_sum(x.hi, y.hi);
-  const float e = s.lo + (x.lo + y.lo);
-  const float hi = s.hi + e;
-  return {hi, e - (hi - s.hi)};
-}
-__device__ __forceinline__ F2 f2_scale(F2 x, float u) {  // x * u; the product error by fma
-  const float p = x.hi * u;
-  const float e = fmaf(x.lo, u, fmaf(x.hi, u, -p));
-  const float hi = p + e;
-  return {hi, e - (hi - p)};
-}
-__device__ __forceinline__ float f2_diff(F2 x, F2 y) {  // x - y, rounded to fp32
-  const F2 d = two_sum(x.hi, -y.hi);
-  return d.hi + (d.lo + (x.lo - y.lo));
-}
-__device__ __forceinline__ F2 f2_shfl_up(F2 x, int o) {
-  return {__shfl_up_sync(kFull, x.hi, o), __shfl_up_sync(kFull, x.lo, o)};
-}
-__device__ __forceinline__ F2 f2_shfl(F2 x, int src) {
-  return {__shfl_sync(kFull, x.hi, src), __shfl_sync(kFull, x.lo, src)};
-}
-// Inclusive prefix over lanes 0..width-1 in lane order (a fixed tree of f2_add; width a
+// Inclusive prefix over lanes 0..width-1 in lane order (a fixed tree of fp32 adds; width a
 // power of two, lanes at or above it keep their own value).
-__device__ __forceinline__ F2 f2_lane_scan(F2 x, int lane, int width) {
+__device__ __forceinline__ float lane_scan(float x, int lane, int width) {
   for (int o = 1; o < width; o <<= 1) {
-    const F2 n = f2_shfl_up(x, o);
-    if (lane >= o) x = f2_add(n, x);
+    const float n = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += n;
   }
   return x;
 }
@@ -122,42 +93,40 @@ __device__ __forceinline__ void stage_vec(const T* p, int k, float (&v)[16 / siz
 }
 
 struct WalkShared {
-  uint4 slot[2][kWalkMaxCluster][2];  // mailbox: one message (16 or 32 bytes) per member, by parity
+  uint4 slot[2][kWalkMaxCluster];  // mailbox: one 16-byte message per member, by parity
   uint64_t xbar[2];                // mailbox barriers, by parity
   uint64_t sbar;                   // stage barrier
   unsigned long long key[32];      // pass 1: per-warp keys
   float wsum[32];                  // sampled: per-warp masses relative to the warp maximum
   int wlast[32];                   // sampled: per-warp largest index of a finite logit
   float u[kMaxTreeDepth + 1];      // this sequence's uniforms
-  F2 target, wbase;                // the inverse-CDF point; mass before the owner warp's chunk
+  int2 tree[kWalkWarpSearch];      // (parent, token) of every node, when N <= kWalkWarpSearch
+  float target, wbase;             // the inverse-CDF point; mass before the owner warp's chunk
   float m;                         // row maximum
   int z, owner, ow, lastg, next, y;
   int rs_a, rs_b, rs_y;             // row status after mail A, mail B and the draw
 };
 
-// One thread: this CTA's message of `nv` 16-byte words to every member, arming the local
-// barrier for all of them.
-__device__ __forceinline__ void mail_send(WalkShared& sh, int par, uint32_t C, uint32_t rank, const uint4* msg,
-                                          int nv) {
-  mbar_expect_tx(&sh.xbar[par], C * 16u * static_cast<uint32_t>(nv));
+// One thread: this CTA's 16-byte message to every member, arming the local barrier for
+// all of them.
+__device__ __forceinline__ void mail_send(WalkShared& sh, int par, uint32_t C, uint32_t rank, uint4 msg) {
+  mbar_expect_tx(&sh.xbar[par], C * 16u);
+  const uint32_t sa = smem_addr(&sh.slot[par][rank]);
   const uint32_t ba = smem_addr(&sh.xbar[par]);
-  for (int v = 0; v < nv; ++v) {
-    const uint32_t sa = smem_addr(&sh.slot[par][rank][v]);
-    const float4 w = make_float4(__uint_as_float(msg[v].x), __uint_as_float(msg[v].y), __uint_as_float(msg[v].z),
-                                 __uint_as_float(msg[v].w));
-    for (uint32_t r = 0; r < C; ++r) st_async_16(cluster_map(sa, r), w, cluster_map(ba, r));
-  }
+  const float4 w = make_float4(__uint_as_float(msg.x), __uint_as_float(msg.y), __uint_as_float(msg.z),
+                               __uint_as_float(msg.w));
+  for (uint32_t r = 0; r < C; ++r) st_async_16(cluster_map(sa, r), w, cluster_map(ba, r));
 }
 
-// Warp: the lowest-index child of `node` carrying token y (INT_MAX: none).
-__device__ __forceinline__ int warp_find_child(const int32_t* __restrict__ parents, const int32_t* __restrict__ toks,
-                                               int N, int node, int y, int lane) {
+// Warp: the lowest-index child of `node` carrying token y (INT_MAX: none), from the
+// (parent, token) pairs held in shared memory.
+__device__ __forceinline__ int warp_find_child(const int2* tree, int N, int node, int y, int lane) {
   int child = INT_MAX;
-  for (int j = lane; j < N; j += 32)
-    if (__ldg(parents + j) == node && __ldg(toks + j) == y) child = min(child, j);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) child = min(child, __shfl_xor_sync(kFull, child, o));
-  return child;
+  for (int j = lane; j < N; j += 32) {
+    const int2 pt = tree[j];
+    if (pt.x == node && pt.y == y) child = min(child, j);
+  }
+  return __reduce_min_sync(kFull, child);
 }
 
 template <typename T, int NT>
@@ -214,6 +183,7 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
     if (!(a >= -1 && a < j)) vst |= SPECDEC_STATUS_BAD_TREE;
     const int t = __ldg(toks + j);
     if (t < 0 || t >= V) vst |= SPECDEC_STATUS_BAD_TOKEN;
+    if (warp_search) sh.tree[j] = make_int2(a, t);
     int x = j, cnt = 0;  // nodes on the root path of j (bounded walk)
     while (x >= 0 && x < N && cnt <= D) { ++cnt; x = __ldg(P.parents + x); }
     if (cnt > D) vst |= SPECDEC_STATUS_BAD_TREE;
@@ -229,9 +199,9 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
 
   int node = -1, d = 0, st_rows = 0;
   for (;;) {
-    // ---- one sweep over the slice: maximum and its lowest index (the order key), and for
-    // a sampled row the mass sum 2^((l - m_t) c) relative to the thread's running maximum
-    // m_t, rescaled whenever the maximum grows ------------------------------------------
+    // ---- the slice: maximum and its lowest index (the order key), and for a sampled row
+    // the mass sum 2^((l - m_t) c) relative to each thread's maximum m_t (a second read of
+    // the thread's elements in shared memory) ---------------------------------------------
     const bool landed = mbar_wait(&sh.sbar, sphase);
     if (landed) {
       sphase ^= 1u;
@@ -241,35 +211,26 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
     int bidx = INT_MAX, lastf = -1;
     bool nan = false;
     if (landed) {
-      if (greedy) {
-        for (int k = w0 + lane * VEC; k < w1; k += SPAN) {  // each thread visits its indices in order
-          float v[VEC];
-          stage_vec<T>(stage, k, v);
+      for (int k = w0 + lane * VEC; k < w1; k += SPAN) {  // each thread visits its indices in order
+        float v[VEC];
+        stage_vec<T>(stage, k, v);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            nan |= (v[e] != v[e]);
-            if (v[e] > best) { best = v[e]; bidx = s0 + k + e; }
-          }
+        for (int e = 0; e < VEC; ++e) {
+          nan |= (v[e] != v[e]);
+          if (v[e] > best) { best = v[e]; bidx = s0 + k + e; }
         }
-      } else {
+      }
+      if (!greedy && best > -kInf)  // the thread's mass relative to its maximum (shared memory again)
         for (int k = w0 + lane * VEC; k < w1; k += SPAN) {
           float v[VEC];
           stage_vec<T>(stage, k, v);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float x = v[e];
-            nan |= (x != x);
-            if (x > best) {
-              s = fmaf(s, ex2((best - x) * c), 1.f);
-              best = x;
-              bidx = s0 + k + e;
-            } else if (x > -kInf) {
-              s += ex2((x - best) * c);
+          for (int e = 0; e < VEC; ++e)
+            if (v[e] > -kInf) {
+              s += ex2((v[e] - best) * c);
+              lastf = s0 + k + e;
             }
-            if (x > -kInf) lastf = s0 + k + e;
-          }
         }
-      }
     }
     const unsigned long long wkey = warp_max_key(landed ? order_key(best, bidx, nan) : kKeyTimeout);
     if (!greedy) {  // the warp's mass relative to the warp maximum
@@ -293,33 +254,30 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
       const unsigned long long ckey = warp_max_key(kw);
       const float mr = key_value(ckey);  // this slice's maximum
       int lp = -1;
-      F2 pre{0.f, 0.f};  // sampled: mass through warp `lane`'s chunk, relative to mr
+      float pre = 0.f;  // sampled: mass through warp `lane`'s chunk, relative to mr
       float sw = 0.f;
       if (!greedy) {
         const float kv = key_value(kw);
         sw = (lane < WARPS && kv > -kInf) ? sh.wsum[lane] * ex2((kv - mr) * c) : 0.f;
-        pre = f2_lane_scan(F2{sw, 0.f}, lane, WARPS);
+        pre = lane_scan(sw, lane, WARPS);
         lp = __reduce_max_sync(kFull, lane < WARPS ? sh.wlast[lane] : -1);
       }
-      const F2 mass = f2_shfl(pre, WARPS - 1);
+      const float mass = __shfl_sync(kFull, pre, WARPS - 1);
       if (lane == 0) {
-        const uint4 msg[2] = {make_uint4(static_cast<uint32_t>(ckey), static_cast<uint32_t>(ckey >> 32),
-                                         __float_as_uint(mass.hi), __float_as_uint(mass.lo)),
-                              make_uint4(static_cast<uint32_t>(lp), 0u, 0u, 0u)};
-        mail_send(sh, par, C, rank, msg, greedy ? 1 : 2);
+        const uint4 msg = make_uint4(static_cast<uint32_t>(ckey), static_cast<uint32_t>(ckey >> 32),
+                                     __float_as_uint(mass), static_cast<uint32_t>(lp));
+        mail_send(sh, par, C, rank, msg);
       }
       __syncwarp();
       const bool ok = !__any_sync(kFull, !mbar_wait_cluster(&sh.xbar[par], (xk >> 1) & 1u));
       unsigned long long kr = 0ull;
-      F2 sr{0.f, 0.f};
+      float sr = 0.f;
       int lr = -1;
       if (lane < static_cast<int>(C)) {
-        const uint4 a = sh.slot[par][lane][0];
+        const uint4 a = sh.slot[par][lane];
         kr = (static_cast<unsigned long long>(a.y) << 32) | a.x;
-        if (!greedy) {
-          sr = F2{__uint_as_float(a.z), __uint_as_float(a.w)};
-          lr = static_cast<int>(sh.slot[par][lane][1].x);
-        }
+        sr = __uint_as_float(a.z);
+        lr = static_cast<int>(a.w);
       }
       const unsigned long long K = warp_max_key(kr);
       const float m = key_value(K);
@@ -329,7 +287,7 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
       else if (m == -kInf) rs = SPECDEC_STATUS_EMPTY_ROW;
       if (rs == 0 && greedy && warp_search) {  // the greedy token is the argmax: descend now
         const int y = key_index(K);
-        const int child = warp_find_child(P.parents, toks, N, node, y, lane);
+        const int child = warp_find_child(sh.tree, N, node, y, lane);
         if (lane == 0) {
           const bool down = child != INT_MAX && d < D;
           if (rank == 0) {
@@ -349,22 +307,21 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
         lr = __reduce_max_sync(kFull, lr);
         const float mk = key_value(kr);
         const float f = (lane < static_cast<int>(C) && mk > -kInf) ? ex2((mk - m) * c) : 0.f;
-        const F2 incl = f2_lane_scan(f2_scale(sr, f), lane, static_cast<int>(C));  // mass through slice `lane`
-        const F2 target = f2_scale(f2_shfl(incl, static_cast<int>(C) - 1), sh.u[d]);
-        const unsigned hit = __ballot_sync(kFull, lane < static_cast<int>(C) && f2_diff(incl, target) > 0.f);
+        const float incl = lane_scan(sr * f, lane, static_cast<int>(C));  // mass through slice `lane`
+        const float target = __shfl_sync(kFull, incl, static_cast<int>(C) - 1) * sh.u[d];
+        const unsigned hit = __ballot_sync(kFull, lane < static_cast<int>(C) && incl > target);
         const int owner = hit ? __ffs(hit) - 1 : -1;
-        const F2 before = f2_shfl(incl, owner > 0 ? owner - 1 : 0);
-        const F2 obase = owner > 0 ? before : F2{0.f, 0.f};
+        const float before = __shfl_sync(kFull, incl, owner > 0 ? owner - 1 : 0);
+        const float obase = owner > 0 ? before : 0.f;
         int ow = -1;
-        F2 wb{0.f, 0.f};
+        float wb = 0.f;
         if (owner == static_cast<int>(rank)) {
           const float fme = ex2((mr - m) * c);
-          const F2 cum = f2_add(obase, f2_scale(pre, fme));
-          const unsigned h2 = __ballot_sync(kFull, lane < WARPS && f2_diff(cum, target) > 0.f);
+          const unsigned h2 = __ballot_sync(kFull, lane < WARPS && obase + pre * fme > target);
           const unsigned pos = __ballot_sync(kFull, lane < WARPS && sw > 0.f);
           ow = h2 ? __ffs(h2) - 1 : (pos ? 31 - __clz(pos) : 0);  // past the end only by rounding
-          const F2 prev = f2_shfl(pre, ow > 0 ? ow - 1 : 0);
-          wb = ow > 0 ? f2_add(obase, f2_scale(prev, fme)) : obase;
+          const float prev = __shfl_sync(kFull, pre, ow > 0 ? ow - 1 : 0);
+          wb = ow > 0 ? obase + prev * fme : obase;
         }
         if (lane == 0) {
           sh.owner = owner;
@@ -401,8 +358,8 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
       const int owner = sh.owner;
       const int par = static_cast<int>(xk & 1u);
       if (owner == static_cast<int>(rank) && warp == sh.ow) {
-        const F2 target = sh.target;
-        F2 base = sh.wbase;
+        const float target = sh.target;
+        float base = sh.wbase;
         int yy = -1, wl = -1;
         for (int k0 = w0; k0 < w1; k0 += SPAN) {
           const int k = k0 + lane * VEC;
@@ -427,7 +384,7 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
             const float t = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += t;
           }
-          const float rem = f2_diff(target, base);  // mass still to pass at this tile's start
+          const float rem = target - base;  // mass still to pass at this tile's start
           const unsigned hit = __ballot_sync(kFull, incl > rem);
           if (hit) {
             const int first = __ffs(hit) - 1;
@@ -446,25 +403,25 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
             yy = __shfl_sync(kFull, yy, first);
             break;
           }
-          base = f2_add(base, F2{__shfl_sync(kFull, incl, 31), 0.f});
+          base += __shfl_sync(kFull, incl, 31);
         }
         wl = __reduce_max_sync(kFull, wl);
         if (yy < 0) yy = wl;  // the chunk ended before the point by rounding
         if (yy < 0) yy = sh.lastg;
         if (lane == 0) {
           const uint4 msg = make_uint4(static_cast<uint32_t>(yy), 1u, 0u, 0u);
-          mail_send(sh, par, C, rank, &msg, 1);
+          mail_send(sh, par, C, rank, msg);
         }
       }
       if (owner != static_cast<int>(rank) && tid == 0) {  // an empty message keeps mail C all-to-all
         const uint4 msg = make_uint4(0u, 0u, 0u, 0u);
-        mail_send(sh, par, C, rank, &msg, 1);
+        mail_send(sh, par, C, rank, msg);
       }
       if (warp == 0) {
         __syncwarp();  // the waiting loop starts converged
         const bool ok = !__any_sync(kFull, !mbar_wait_cluster(&sh.xbar[par], (xk >> 1) & 1u));
         if (!ok) ry = SPECDEC_STATUS_TIMEOUT;
-        else y = (owner >= 0) ? static_cast<int>(sh.slot[par][owner][0].x) : sh.lastg;
+        else y = (owner >= 0) ? static_cast<int>(sh.slot[par][owner].x) : sh.lastg;
       }
       ++xk;
     }
@@ -473,7 +430,7 @@ __global__ void __launch_bounds__(NT, 2) tree_walk_cluster_kernel(const TreePara
     int child = -1;
     if (warp_search) {
       if (warp == 0) {
-        const int ch = ry ? INT_MAX : warp_find_child(P.parents, toks, N, node, y, lane);
+        const int ch = ry ? INT_MAX : warp_find_child(sh.tree, N, node, y, lane);
         const bool down = !ry && ch != INT_MAX && d < D;
         if (lane == 0) {
           if (!ry && rank == 0) {
