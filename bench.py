@@ -61,6 +61,8 @@ NCU_TRAFFIC = {
     "chain_seq": {"bytes": 323_471_616, "src_sha": "84a44dd5ad4a2df5"},
     # profiles/block_row_b256_v128256.md: 1445.93 MB read + 5.20 MB written (batch seed 0)
     "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b"},
+    # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
+    "tree_walk": {"bytes": 2_302_976, "src_sha": "b6b0b125e0082802"},
 }
 
 
@@ -69,6 +71,7 @@ KERNEL_SOURCES = {
     "chain_seq": ("chain_seq.cu", "specdec_device.cuh", "specdec_internal.h"),
     "chain_stats": ("chain_stream.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
     "block_fused": ("block_fused.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
+    "tree_walk": ("tree_walk_cluster.cu", "specdec_device.cuh", "specdec_internal.h"),
 }
 
 
@@ -525,7 +528,8 @@ def run_tree_rr(args, rank, world, local_rank):
         roofline={"kernel": kernel, "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
                   "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,
-                  "traffic": None},
+                  "traffic": (NCU_TRAFFIC[kernel]["bytes"] if kernel in NCU_TRAFFIC and
+                              NCU_TRAFFIC[kernel]["src_sha"] == kernel_source_sha(kernel) else None)},
         kernels_ms_per_launch={k: v[0] / v[1] for k, v in per_kernel.items() if v[1]},
         gpu_launches=int(round(sum(v[1] for v in per_kernel.values()))),
         mean_accepted=float(np.mean([o["num_accepted"].float().mean().item() for o in outs])),
