@@ -71,10 +71,10 @@ __device__ __forceinline__ int warp_max_int(int v) {
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ double warp_incl_scan(double v, int lane) {
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
+    const float n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
   return v;
@@ -448,20 +448,20 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
   }
 }
 
-// fp64 scan of this member's chunk masses (first warp): each lane sums a contiguous run
+// fp32 scan of this member's chunk masses (first warp): each lane sums a contiguous run
 // of chunks.  The search repeats exactly this arithmetic, so the member's total and the
 // search's running prefixes agree to the bit.
 struct LocalScan {
   int c0, c1;
-  double mine, incl, total;
+  float mine, incl, total;
 };
 __device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int lane) {
   LocalScan s;
   const int cpl = (n + 31) / 32;
   s.c0 = min(lane * cpl, n);
   s.c1 = min(s.c0 + cpl, n);
-  s.mine = 0.0;
-  for (int q = s.c0; q < s.c1; ++q) s.mine += static_cast<double>(mass[q]);
+  s.mine = 0.f;
+  for (int q = s.c0; q < s.c1; ++q) s.mine += mass[q];
   s.incl = warp_incl_scan(s.mine, lane);
   s.total = __shfl_sync(0xffffffffu, s.incl, 31);
   return s;
@@ -472,16 +472,16 @@ __device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int la
 // `target`, then the element inside it.  If rounding leaves no such element, the last
 // positive-weight element of the part is taken.
 template <typename T>
-__device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, double base, double target,
+__device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, float base, float target,
                             float mJ, float c, float invZ, bool no_q, const float* mass, int lane) {
   using GL = typename Group<T>::L;
   constexpr int GPL = kSeqDrawChunk / 4 / 32;
   const LocalScan s = local_scan(mass, n, lane);
   int cstar = -1, lastpos = -1;
-  double cbase = 0.0, prelast = 0.0, pre = base + (s.incl - s.mine);
+  float cbase = 0.f, prelast = 0.f, pre = base + (s.incl - s.mine);
   for (int q = s.c0; q < s.c1; ++q) {
-    const double w = static_cast<double>(mass[q]);
-    if (w > 0.0) { lastpos = q; prelast = pre; }
+    const float w = mass[q];
+    if (w > 0.f) { lastpos = q; prelast = pre; }
     if (cstar < 0 && pre + w > target) { cstar = q; cbase = pre; }
     pre += w;
   }
@@ -499,7 +499,7 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
   const int k0 = (d0 + cstar) * kSeqDrawChunk;
   const int ng = min(kSeqDrawChunk, V - k0) / 4;
   float w[GPL][4], gsum[GPL];
-  double lane_tot = 0.0;
+  float lane_tot = 0.f;
 #pragma unroll
   for (int j = 0; j < GPL; ++j) {
     const int g = lane * GPL + j;
@@ -510,7 +510,7 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
       const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
       const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
       gsum[j] = group_weights<T>(lw, q4, -__fmul_rn(mJ, c), c, invZ, no_q, w[j]);
-      lane_tot += static_cast<double>(gsum[j]);
+      lane_tot += gsum[j];
     }
   }
   int last_pos = -1;
@@ -519,27 +519,27 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (w[j][e] > 0.f) last_pos = k0 + 4 * (lane * GPL + j) + e;
-  const double gincl = warp_incl_scan(lane_tot, lane);
+  const float gincl = warp_incl_scan(lane_tot, lane);
   const unsigned ghit = __ballot_sync(0xffffffffu, cbase + gincl > target);
   int y = -1;
   if (ghit) {
     const int fl = __ffs(ghit) - 1;
     if (lane == fl) {
-      double p2 = cbase + (gincl - lane_tot);
+      float p2 = cbase + (gincl - lane_tot);
 #pragma unroll
       for (int j = 0; j < GPL; ++j) {
-        if (y < 0 && p2 + static_cast<double>(gsum[j]) > target) {
+        if (y < 0 && p2 + gsum[j] > target) {
           float run = 0.f;
           int lastp = -1;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             run += w[j][e];
             if (w[j][e] > 0.f) lastp = k0 + 4 * (lane * GPL + j) + e;
-            if (y < 0 && p2 + static_cast<double>(run) > target) y = k0 + 4 * (lane * GPL + j) + e;
+            if (y < 0 && p2 + run > target) y = k0 + 4 * (lane * GPL + j) + e;
           }
           if (y < 0) y = lastp;
         }
-        p2 += static_cast<double>(gsum[j]);
+        p2 += gsum[j];
       }
     }
     y = __shfl_sync(0xffffffffu, y, fl);
@@ -548,18 +548,12 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
   return y;
 }
 
-// A member's draw total (fp64), a flag and the leader's unclaimed sequence as one 16-byte
+// A member's draw total (fp32), a flag and the leader's unclaimed sequence as one 16-byte
 // exchange payload.
-__device__ __forceinline__ float4 pack_total(double t, int flag, int bn) {
-  const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(t));
-  return make_float4(__uint_as_float(static_cast<uint32_t>(bits)), __uint_as_float(static_cast<uint32_t>(bits >> 32)),
-                     __int_as_float(flag), __int_as_float(bn));
+__device__ __forceinline__ float4 pack_total(float t, int flag, int bn) {
+  return make_float4(t, 0.f, __int_as_float(flag), __int_as_float(bn));
 }
-__device__ __forceinline__ double unpack_total(const float4& v) {
-  const unsigned long long bits = static_cast<unsigned long long>(__float_as_uint(v.x)) |
-                                  (static_cast<unsigned long long>(__float_as_uint(v.y)) << 32);
-  return __longlong_as_double(static_cast<long long>(bits));
-}
+__device__ __forceinline__ float unpack_total(const float4& v) { return v.x; }
 
 // ---------------------------------------------------------------------------------
 // The kernel
@@ -671,7 +665,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   // a drawn token still to be found by this member's first warp (at the next task's start)
   bool srch = false;
   int s_b = 0, s_J = 0, s_par = 0;
-  double s_base = 0.0, s_target = 0.0;
+  float s_base = 0.f, s_target = 0.f;
   float s_m = 0.f, s_c = 0.f, s_invZ = 1.f;
   bool s_noq = true;
 
@@ -816,7 +810,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         if (lane == 0) gs.mass[par][cd - d0] = sr;
       }
       const bool qbad = group_any(group, !(qmx < kInf) || qmn < 0.f);  // also: every chunk mass is in place
-      double tot = 0.0;
+      float tot = 0.f;
       if (gwarp == 0) tot = local_scan(gs.mass[par], d1 - d0, lane).total;
       mine = pack_total(tot, qbad ? 1 : 0, 0);
     }
@@ -925,7 +919,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       }
     } else {  // the members' totals of the drawn row
       J = ri;
-      double S = 0.0;
+      float S = 0.f;
       bool anybad = false;
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
@@ -935,7 +929,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       if (kind == kTaskDraw && anybad) {
         st = SPECDEC_STATUS_BAD_PROB;
         done = failed = true;
-      } else if (kind == kTaskDraw && !(S > 0.0)) {
+      } else if (kind == kTaskDraw && !(S > 0.f)) {
         // zero total residual (possible only through rounding): draw from p itself
         nxt_local = true;
         nxt = cur;
@@ -943,14 +937,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         nxt.warn = warn | (SPECDEC_STATUS_ZERO_RESIDUAL >> 8);
       } else {
         // the member whose part holds u * S (else the last member with mass) finds y
-        const double target = static_cast<double>(g[4]) * S;
+        const float target = g[4] * S;
         int rstar = -1, rlast = 0;
-        double base = 0.0, run = 0.0, baselast = 0.0;
+        float base = 0.f, run = 0.f, baselast = 0.f;
 #pragma unroll
         for (int r = 0; r < kC; ++r) {
-          const double tt = unpack_total(gs.slot[xp][r]);
-          if (tt > 0.0) { rlast = r; baselast = run; }
-          if (rstar < 0 && tt > 0.0 && run + tt > target) { rstar = r; base = run; }
+          const float tt = unpack_total(gs.slot[xp][r]);
+          if (tt > 0.f) { rlast = r; baselast = run; }
+          if (rstar < 0 && tt > 0.f && run + tt > target) { rstar = r; base = run; }
           run += tt;
         }
         if (rstar < 0) { rstar = rlast; base = baselast; }
