@@ -119,6 +119,28 @@ template <typename T, int VEC, bool SMEM> struct RowAccess {
 
 constexpr int kStageCopy = 32768;  // bytes per bulk copy when staging a row
 
+// Order keys of (value, index): a larger key is a larger value, then a smaller index.
+// A NaN anywhere gives the canonical NaN's key, above +inf; all ones marks a copy that
+// timed out.  -0 is folded into +0 so that equal values tie on their index.
+constexpr unsigned long long kKeyTimeout = ~0ull;
+__device__ __forceinline__ unsigned long long order_key(float v, int idx, bool nan) {
+  uint32_t u = nan ? 0x7fc00000u : __float_as_uint(v + 0.f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ float key_value(unsigned long long k) {
+  const uint32_t o = static_cast<uint32_t>(k >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ int key_index(unsigned long long k) {
+  return static_cast<int>(~static_cast<uint32_t>(k));
+}
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {  // two redux.sync
+  const unsigned hi = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(k >> 32));
+  const unsigned lo = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(k >> 32) == hi ? static_cast<unsigned>(k) : 0u);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
 // ---------------------------------------------------------------------------------
 // Block reductions and scans (NT threads, fixed order => deterministic)
 // ---------------------------------------------------------------------------------
