@@ -57,12 +57,14 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
     "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
-    # profiles/chain_seq_b256_v128256.md: 320.22 MB read + 3.26 MB written (batch seed 0)
-    "chain_seq": {"bytes": 323_471_616, "src_sha": "84a44dd5ad4a2df5"},
+    # profiles/chain_seq_b256_v128256.md: 320.42 MB read + 3.32 MB written (batch seed 0)
+    "chain_seq": {"bytes": 323_735_040, "src_sha": "7f6cc8d70765ec89"},
     # profiles/block_row_b256_v128256.md: 1445.93 MB read + 5.20 MB written (batch seed 0)
     "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b"},
     # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
-    "tree_walk": {"bytes": 2_302_976, "src_sha": "b6b0b125e0082802"},
+    "tree_walk": {"bytes": 2_302_720, "src_sha": "00db4cb54f9e827b"},
+    # profiles/tree_rr_b32_n64_v32000.md: 17.87 MB read, 0 written (batch seed 0)
+    "tree_rr": {"bytes": 17_865_728, "src_sha": "1bd299588a42f14d"},
 }
 
 
@@ -72,6 +74,7 @@ KERNEL_SOURCES = {
     "chain_stats": ("chain_stream.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
     "block_fused": ("block_fused.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
     "tree_walk": ("tree_walk_cluster.cu", "specdec_device.cuh", "specdec_internal.h"),
+    "tree_rr": ("tree_rr.cu", "specdec_device.cuh", "specdec_internal.h"),
 }
 
 
