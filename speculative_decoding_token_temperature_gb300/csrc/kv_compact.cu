@@ -8,9 +8,10 @@
 //
 // A path climbs the tree (path[d] >= d, strictly increasing), so a move never reads a slot
 // that an earlier move wrote; it may read the slot a later move writes (path [1, 2] reads
-// slot 1 before filling it), so the moves of one sequence run depth by depth with a CTA
-// barrier between them.  Grid: (row chunks, sequences); each CTA moves its byte range of
-// the row at every depth.  Contiguous caches address slot s of sequence b at
+// slot 1 before filling it).  Every thread moves the same byte offsets at every depth, so
+// it loads a batch of depths into registers before it stores any of them: the loads of a
+// batch are in flight together, and no read can see a later move's write.  Grid: (row
+// chunks, sequences); each CTA moves its byte range of the row at every depth.  Contiguous caches address slot s of sequence b at
 // base + b * seq_stride + s * slot_stride; paged caches at base + block_table[b][s / bs] *
 // block_stride + (s % bs) * slot_stride.
 
@@ -56,31 +57,55 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(const KvCom
     }
     return P.base + static_cast<int64_t>(b) * P.seq_stride + static_cast<int64_t>(s) * P.slot_stride;
   };
-  for (int d = 0; d < J; ++d) {
-    const int s = __ldg(path + d);
-    if (s != d) {
-      const char* src = slot(P0 + s);
-      char* dst = slot(P0 + d);
-      if (vec16) {
-        constexpr int U = 4;
-        for (int64_t o = lo + 16 * static_cast<int64_t>(threadIdx.x); o < hi; o += 16 * U * kCompactThreads) {
-          uint4 v[U];
+  constexpr int kBatch = 4;  // depths whose loads are in flight together
+  for (int d0 = 0; d0 < J; d0 += kBatch) {
+    const int nd = min(kBatch, J - d0);
+    if (vec16) {
+      constexpr int U = 4;  // 16-byte vectors per thread per depth: 256 threads x 64 B = the 16 KB chunk
+      static_assert(U * 16 * kCompactThreads == kCompactChunk, "one pass covers the chunk");
+      const int64_t o0 = lo + 16 * static_cast<int64_t>(threadIdx.x);
+      uint4 v[kBatch][U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int64_t oo = o + 16 * static_cast<int64_t>(u) * kCompactThreads;
-            if (oo < hi) v[u] = *reinterpret_cast<const uint4*>(src + oo);
-          }
+      for (int i = 0; i < kBatch; ++i) {
+        if (i < nd) {
+          const int d = d0 + i, s = __ldg(path + d);
+          if (s != d) {
+            const char* src = slot(P0 + s);
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int64_t oo = o + 16 * static_cast<int64_t>(u) * kCompactThreads;
-            if (oo < hi) *reinterpret_cast<uint4*>(dst + oo) = v[u];
+            for (int u = 0; u < U; ++u) {
+              const int64_t oo = o0 + 16 * static_cast<int64_t>(u) * kCompactThreads;
+              if (oo < hi) v[i][u] = *reinterpret_cast<const uint4*>(src + oo);
+            }
           }
         }
-      } else {
-        for (int64_t o = lo + threadIdx.x; o < hi; o += kCompactThreads) dst[o] = src[o];
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (i < nd) {
+          const int d = d0 + i, s = __ldg(path + d);
+          if (s != d) {
+            char* dst = slot(P0 + d);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int64_t oo = o0 + 16 * static_cast<int64_t>(u) * kCompactThreads;
+              if (oo < hi) *reinterpret_cast<uint4*>(dst + oo) = v[i][u];
+            }
+          }
+        }
+      }
+    } else {
+      for (int64_t o = lo + threadIdx.x; o < hi; o += kCompactThreads) {
+        char v[kBatch];
+        for (int i = 0; i < nd; ++i) {
+          const int d = d0 + i, s = __ldg(path + d);
+          v[i] = s != d ? slot(P0 + s)[o] : 0;
+        }
+        for (int i = 0; i < nd; ++i) {
+          const int d = d0 + i, s = __ldg(path + d);
+          if (s != d) slot(P0 + d)[o] = v[i];
+        }
       }
     }
-    __syncthreads();  // every read of this depth is done before the next depth writes
   }
 }
 
