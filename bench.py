@@ -52,19 +52,22 @@ DEFAULT_WORKLOAD = "chain_b256_v128256"
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from
-# one ncu capture of the benchmarked workload, keyed by the sha256 of that kernel's source
-# files (KERNEL_SOURCES) it was taken on; reported as null once they differ.
+# one ncu capture of one workload and rule, keyed by the sha256 of that kernel's source
+# files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
+# as null once the sources differ.
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
-    "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf"},
+    "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf", "workload": "chain_b256_v128256", "rule": "chain"},
     # profiles/chain_seq_b256_v128256.md: 320.42 MB read + 3.32 MB written (batch seed 0)
-    "chain_seq": {"bytes": 323_735_040, "src_sha": "7f6cc8d70765ec89"},
+    "chain_seq": {"bytes": 323_735_040, "src_sha": "7f6cc8d70765ec89", "workload": "chain_b256_v128256", "rule": "chain"},
     # profiles/block_row_b256_v128256.md: 1445.93 MB read + 5.20 MB written (batch seed 0)
-    "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b"},
+    "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b", "workload": "chain_b256_v128256",
+                    "rule": "block"},
     # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
-    "tree_walk": {"bytes": 2_302_720, "src_sha": "00db4cb54f9e827b"},
+    "tree_walk": {"bytes": 2_302_720, "src_sha": "00db4cb54f9e827b", "workload": "tree_b32_n64_v32000", "rule": "tree"},
     # profiles/tree_rr_b32_n64_v32000.md: 17.87 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_865_728, "src_sha": "1bd299588a42f14d"},
+    "tree_rr": {"bytes": 17_865_728, "src_sha": "1bd299588a42f14d", "workload": "tree_rr_b32_n64_v32000",
+                "rule": "tree_recursive"},
 }
 
 
@@ -87,6 +90,14 @@ def kernel_source_sha(kernel: str | None = None) -> str:
     for p in files:
         h.update(p.read_bytes())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, rule: str):
+    """ncu traffic per launch recorded for this kernel, workload and rule, or None."""
+    t = NCU_TRAFFIC.get(kernel)
+    if not t or t["workload"] != workload or t["rule"] != rule or t["src_sha"] != kernel_source_sha(kernel):
+        return None
+    return t["bytes"]
 
 
 def replica_round(rank: int, s: int) -> int:
@@ -531,8 +542,7 @@ def run_tree_rr(args, rank, world, local_rank):
         roofline={"kernel": kernel, "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
                   "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,
-                  "traffic": (NCU_TRAFFIC[kernel]["bytes"] if kernel in NCU_TRAFFIC and
-                              NCU_TRAFFIC[kernel]["src_sha"] == kernel_source_sha(kernel) else None)},
+                  "traffic": recorded_traffic(kernel, name, args.rule)},
         kernels_ms_per_launch={k: v[0] / v[1] for k, v in per_kernel.items() if v[1]},
         gpu_launches=int(round(sum(v[1] for v in per_kernel.values()))),
         mean_accepted=float(np.mean([o["num_accepted"].float().mean().item() for o in outs])),
@@ -697,9 +707,7 @@ def main():
         kname, alg_bytes = "chain_stats", rows * V * esize   # every logits row read once
     k_ms, k_n = per_kernel[kname]
     achieved = alg_bytes / (k_ms / k_n / 1e3) / 1e9 if k_n else None
-    sha = kernel_source_sha(kname)
-    traffic = NCU_TRAFFIC.get(kname, {})
-    traffic_val = traffic.get("bytes") if traffic.get("src_sha") == sha else None
+    traffic_val = recorded_traffic(kname, args.workload, args.rule)
     # bytes one whole call must move (the same left-to-right count for either chain
     # kernel set; every row and q row for the block rule)
     call_bytes = seq_bytes
@@ -721,7 +729,7 @@ def main():
         "gpu_launches": int(round(launches_per_step * args.steps)) * (2 * ((g + 2) // 2) if args.rule == "gumbel" else 1),
         "mean_accepted": statistics.mean(accepted),
         "clocks": clocks.summary(),
-        "kernel_src_sha": sha,
+        "kernel_src_sha": kernel_source_sha(kname),
     }
 
     if not args.no_e2e:
