@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
   // (s_more: more remain beyond the list).
   auto list_kids = [=](int node, int after) {
     int n = 0;
+    bool full = false;  // the list filled up: children may remain after its last entry
     for (int j0 = after + 1; j0 < N; j0 += 32) {
       const int j = j0 + lane;
       const bool is = j < N && __ldg(P.parents + j) == node;
@@ -96,11 +97,14 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
       const int pos = n + __popc(bal & ((1u << lane) - 1u));
       if (is && pos < kRRKids) s_kids[pos] = j;
       n += __popc(bal);
-      if (n >= kRRKids) break;
+      if (n >= kRRKids) {
+        full = true;
+        break;
+      }
     }
     if (lane == 0) {
       s_nkids = min(n, kRRKids);
-      s_more = n > kRRKids ? 1 : 0;
+      s_more = full ? 1 : 0;
     }
   };
   if constexpr (STAGED) {

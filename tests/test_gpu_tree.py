@@ -110,6 +110,23 @@ def test_tree_v128256_rows_split(sd, medusa64):
     assert stats["accepted"] > 0 and stats["flagged"] <= 1
 
 
+def test_tree_large_tree_block_child_search(sd):
+    """A 4680-node tree (4 heads x top-8, every path): more nodes than one warp searches, so
+    the cluster walk finds children with the whole CTA; spiked logits make walks descend."""
+    from fractions import Fraction
+    acc = [[Fraction(1, 2 + i + k).limit_denominator(1000) for i in range(8)] for k in range(4)]
+    parents, paths, _ = so.medusa_sparse_tree(acc, 10 ** 6)
+    assert len(parents) == 4680
+    stats = {"sequences": 0, "flagged": 0, "accepted": 0}
+    for seed, dtype in ((1, "bf16"), (2, "fp32")):
+        x = workloads.make_tree_inputs(4, 2048, parents, paths, depth=4, seed=seed, device=DEV, dtype=dtype,
+                                       top=8, scale=1.0, spike=10.0)
+        out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
+        _check_tree(out, x, 4, stats)
+    assert stats["accepted"] >= stats["sequences"]
+    assert stats["flagged"] <= 1
+
+
 def test_tree_deep_walks_b32(sd, medusa64):
     """tree_b32_n64_v32000's shapes with logits whose spikes dominate, so walks reach the
     deepest levels (the stated workload's spikes rarely win, and its walks stop at the root)."""

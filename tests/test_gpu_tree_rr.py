@@ -157,6 +157,20 @@ def test_tree_rr_shapes(sd, parents, V, dtype):
     rep.finish()
 
 
+def test_tree_rr_star_tree_more_children_than_the_list(sd):
+    """600 children at the root (the kernel lists 256 at a time) and a few grandchildren:
+    walks that reject many children refill the list; the drafter is far from the target so
+    rejections are common."""
+    from oracle import specdec_oracle as so
+    parents = [-1] * 600 + [0, 0, 5, 599]
+    rep = Report("tree_rr star, 600 children")
+    for seed, dtype in ((1, "fp32"), (2, "bf16")):
+        x = workloads.make_tree_rr_inputs(4, 512, parents, depth=2, seed=seed, device=DEV, dtype=dtype,
+                                          scale=2.0, n_spikes=3, spike=3.0, noise=3.0, temps="const:1.0")
+        check_walks(rep, x, _run(sd, x, 2), 2)
+    rep.finish()
+
+
 def test_tree_rr_errors_follow_the_walk(sd):
     from oracle import specdec_oracle as so
     parents = [-1, -1, 0, 0]
