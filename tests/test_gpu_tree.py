@@ -179,6 +179,43 @@ def test_tree_degenerate(sd):
     assert (out["num_accepted"].cpu()[[0, 1, 4, 5]] == 0).all()
 
 
+@pytest.mark.parametrize("C", ["1", "4"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_tree_degenerate_cluster_walk(sd, monkeypatch, C, dtype):
+    """The input errors of test_tree_degenerate on 16-byte rows (the cluster walk), plus
+    errors in rows the walk reaches only after descending, and in rows it never reads."""
+    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    V, D = 1024, 3
+    parents = torch.tensor([-1, -1, 0, 0, 2], dtype=torch.int32, device=DEV)
+    B = 10
+    g = torch.Generator(device=DEV).manual_seed(3)
+    logits = torch.randn(B, 6, V, generator=g, device=DEV)
+    toks = torch.randint(0, V, (B, 5), generator=g, device=DEV, dtype=torch.int32)
+    for b in range(B):  # spike the first child's token in every row, so walks descend
+        for row, node in ((0, 0), (1, 2), (3, 4)):
+            logits[b, row, int(toks[b, node])] += 12.0
+    toks[0, 0] = toks[0, 1] = int(torch.argmax(logits[0, 0]))      # duplicate siblings
+    toks[1, 3] = V + 1                                               # bad token
+    logits[2, 0, 4] = float("nan")                                   # bad root row
+    logits[5, 1, 7] = float("nan")                                   # bad row of node 0 (reached by descent)
+    logits[6, 2, :] = float("-inf")                                  # node 1's row: never reached
+    logits[7, 1, :] = float("-inf")                                  # node 0's row empty
+    logits[8, 5, 9] = float("inf")                                   # a leaf's row: never read
+    T = torch.tensor([0.0, 0.5, 0.5, 0.5, 0.0, 0.9, 0.7, 0.0, 0.6, float("nan")], device=DEV)
+    u = torch.rand(B, D + 1, generator=g, device=DEV)
+    u[3, 2] = 1.5                                                    # bad uniform
+    if dtype == "bf16":
+        logits = logits.to(torch.bfloat16)
+    out = sd.verify_tree(logits, toks, parents, T, u, D)
+    x = {"logits": logits, "node_tokens": toks, "parents": parents, "temperatures": T, "uniforms": u}
+    _check_tree(out, x, D, {"sequences": 0, "flagged": 0, "accepted": 0})
+    out = sd.verify_tree(logits, toks, parents, T, u[:, :3].contiguous(), 2)  # too deep for max_depth 2
+    assert (out["status"].cpu() & so.STATUS_BAD_TREE).all()
+    bad = torch.tensor([-1, 1, 0, 0, 2], dtype=torch.int32, device=DEV)
+    out = sd.verify_tree(logits, toks, bad, T, u, D)
+    assert (out["status"].cpu() & so.STATUS_BAD_TREE).all()
+
+
 def test_mask_worked_example(sd):
     fx = read_fixture("tree_mask_6node.txt")
     parents = torch.tensor([int(v) for v in fx["parents"]], dtype=torch.int32, device=DEV)
