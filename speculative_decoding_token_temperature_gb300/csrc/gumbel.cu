@@ -27,7 +27,8 @@
 // Entries that cannot win are skipped: u <= 1 - 2^-24 bounds G <= 24, so once some entry
 // has score L, any entry with a_i + 24.25 < L is out of the race.  Each part of a row first
 // finds its largest a and scores that entry (L), then races only its entries within 24.25
-// of L.
+// of L; of those, an entry whose noise bound -log2(1 - u) (from -ln u >= 1 - u) cannot
+// lift it to L is dropped before its noise is computed.
 //
 // verify: rows are evaluated left to right in waves of two rows of every sequence still
 //         open, each row split across CTAs (parts); a decision kernel merges the parts,
@@ -84,6 +85,15 @@ __device__ __forceinline__ float neg_log2_xi(float u) {
   const float y2 = y * y;
   const float s = fmaf(y2, fmaf(y2, fmaf(y2, fmaf(y2, 1.f / 9.f, 1.f / 7.f), 1.f / 5.f), 1.f / 3.f), 1.f);
   return -lg2_approx(-2.f * y * s);                                // xi = -ln(1 + x) = -2 atanh(y)
+}
+
+// Since -ln u >= 1 - u, G = -log2(-ln u) <= -log2(1 - u) (1 - u is exact in float32).  An
+// entry whose a - log2(1 - u) stays below the top entry's score s_top cannot win or tie:
+// one base-2 logarithm rejects most entries before the noise itself is computed.  The
+// slack covers lg2.approx's error and that of the computed G (below 4e-6).
+constexpr float kBoundSlack = 1e-3f;
+__device__ __forceinline__ bool cannot_reach(float a, float u, float s_top) {
+  return a - lg2_approx(1.f - u) + kBoundSlack < s_top;
 }
 
 struct Best {
@@ -223,7 +233,8 @@ __device__ Partial race_part(const T* row, int V, int part, int parts, bool gree
   const int jt = top.i >> 2;
   const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), k, b, 0u), key0, key1);
   const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
-  const float cut = __fsub_rn(__fmul_rn(top.s, c), -neg_log2_xi(uniform_of(xts[top.i & 3]))) - kNoiseMax;
+  const float score_top = __fsub_rn(__fmul_rn(top.s, c), -neg_log2_xi(uniform_of(xts[top.i & 3])));
+  const float cut = score_top - kNoiseMax;
   Best best;
   best.s = -kInf;
   best.i = INT_MAX;
@@ -236,8 +247,12 @@ __device__ Partial race_part(const T* row, int V, int part, int parts, bool gree
     const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), k, b, 0u), key0, key1);
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (a[e] >= cut) take(best, __fsub_rn(a[e], -neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
+    for (int e = 0; e < 4; ++e) {
+      if (!(a[e] >= cut)) continue;
+      const float u = uniform_of(xs[e]);
+      if (cannot_reach(a[e], u, score_top)) continue;
+      take(best, __fsub_rn(a[e], -neg_log2_xi(u)), 4 * j + e);
+    }
   });
   block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
   out.best = best.s;
@@ -355,7 +370,8 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
                                             static_cast<uint32_t>(b), 0u),
                                  key0, key1);
   const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
-  const float cut = __fadd_rn(log2f(top.s), neg_log2_xi(uniform_of(xts[top.i & 3]))) - kNoiseMax;
+  const float score_top = __fadd_rn(log2f(top.s), neg_log2_xi(uniform_of(xts[top.i & 3])));
+  const float cut = score_top - kNoiseMax;
   Best best;
   best.s = -kInf;
   best.i = INT_MAX;
@@ -369,8 +385,12 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
                                   key0, key1);
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (a[e] >= cut) take(best, __fadd_rn(a[e], neg_log2_xi(uniform_of(xs[e]))), 4 * j + e);
+    for (int e = 0; e < 4; ++e) {
+      if (!(a[e] >= cut)) continue;
+      const float u = uniform_of(xs[e]);
+      if (cannot_reach(a[e], u, score_top)) continue;
+      take(best, __fadd_rn(a[e], neg_log2_xi(u)), 4 * j + e);
+    }
   });
   block_best<kGumbelThreads>(best, unused, sh_b, sh_m);
   if (threadIdx.x == 0) out[row] = best.i;
