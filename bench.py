@@ -56,17 +56,17 @@ FALLBACK_HBM_GBS = 6800.0
 # files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
 # as null once the sources differ.
 NCU_TRAFFIC = {
-    # profiles/chain_stream_b256_v128256.md: 525.38 MB read + 4.59 MB written
-    "chain_stats": {"bytes": 529_971_456, "src_sha": "81b1747f6de05fcf", "workload": "chain_b256_v128256", "rule": "chain"},
+    # profiles/chain_stream_b256_v128256.md: 525.40 MB read + 4.51 MB written (SPECDEC_CHAIN_SCAN=1)
+    "chain_stats": {"bytes": 529_910_016, "src_sha": "581fddc45ff69850", "workload": "chain_b256_v128256", "rule": "chain"},
     # profiles/chain_seq_b256_v128256.md: 320.42 MB read + 3.32 MB written (batch seed 0)
     "chain_seq": {"bytes": 323_735_040, "src_sha": "7f6cc8d70765ec89", "workload": "chain_b256_v128256", "rule": "chain"},
-    # profiles/block_row_b256_v128256.md: 1445.93 MB read + 5.20 MB written (batch seed 0)
-    "block_fused": {"bytes": 1_451_124_000, "src_sha": "7e21bc173361194b", "workload": "chain_b256_v128256",
+    # profiles/block_row_b256_v128256.md: 1445.92 MB read + 5.02 MB written (batch seed 0)
+    "block_fused": {"bytes": 1_450_931_456, "src_sha": "2b98aa7b8ff33093", "workload": "chain_b256_v128256",
                     "rule": "block"},
     # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
     "tree_walk": {"bytes": 2_302_720, "src_sha": "00db4cb54f9e827b", "workload": "tree_b32_n64_v32000", "rule": "tree"},
     # profiles/tree_rr_b32_n64_v32000.md: 17.87 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_865_728, "src_sha": "1bd299588a42f14d", "workload": "tree_rr_b32_n64_v32000",
+    "tree_rr": {"bytes": 17_869_312, "src_sha": "bc37a4ac319d4cb3", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
 
