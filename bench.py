@@ -77,7 +77,7 @@ KERNEL_SOURCES = {
     "chain_stats": ("chain_stream.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
     "block_fused": ("block_fused.cu", "stream_common.cuh", "specdec_device.cuh", "specdec_internal.h"),
     "tree_walk": ("tree_walk_cluster.cu", "specdec_device.cuh", "specdec_internal.h"),
-    "tree_rr": ("tree_rr.cu", "specdec_device.cuh", "specdec_internal.h"),
+    "tree_rr": ("tree_rr_cluster.cu", "specdec_device.cuh", "specdec_internal.h"),
 }
 
 

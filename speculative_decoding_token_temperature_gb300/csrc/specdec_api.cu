@@ -482,7 +482,10 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
   const bool vec = rows_vectorizable(logits, V, elem_size(ldt)) && rows_vectorizable(draft_probs, V, 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope prof(SPECDEC_KERNEL_TREE_RR, s);
-  if (cudaError_t e = launch_tree_rr(P, ldt, vec, s); e != cudaSuccess) return fail_cuda("tree recursive-rejection kernel", e);
+  // 16-byte rows: each row split across a cluster (tree_rr_cluster.cu); else one CTA per sequence
+  const int C = vec ? tree_rr_cluster_size(B, V, ldt) : 0;
+  cudaError_t e = C > 0 ? launch_tree_rr_cluster(P, ldt, C, s) : launch_tree_rr(P, ldt, vec, s);
+  if (e != cudaSuccess) return fail_cuda("tree recursive-rejection kernel", e);
   return SPECDEC_OK;
 }
 

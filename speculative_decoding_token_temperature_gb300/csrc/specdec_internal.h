@@ -189,6 +189,10 @@ struct KvCompactParams {
 cudaError_t launch_kv_compact(const KvCompactParams& P, cudaStream_t stream);
 
 // Sampled tree verification by recursive rejection at every node.
+// Recursive rejection with rows split across a cluster of C CTAs: the cluster size for B
+// sequences of V-entry rows (0 when no size fits: 16-byte rows needed), and its launch.
+int tree_rr_cluster_size(int B, int V, specdec_dtype ldt);
+cudaError_t launch_tree_rr_cluster(const TreeParams& P, specdec_dtype ldt, int C, cudaStream_t stream);
 cudaError_t launch_tree_rr(const TreeParams& P, specdec_dtype ldt, bool vector_path, cudaStream_t stream);
 // Gumbel-coupled verification and the drafter's shared-noise sampler (Philox noise).
 struct GumbelParams {

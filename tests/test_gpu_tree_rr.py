@@ -157,6 +157,20 @@ def test_tree_rr_shapes(sd, parents, V, dtype):
     rep.finish()
 
 
+@pytest.mark.parametrize("C", ["1", "2", "4", "8"])
+@pytest.mark.parametrize("V,dtype", [(32008, "bf16"), (4096, "fp32"), (20004, "fp32"), (64, "bf16")])
+def test_tree_rr_cluster_sizes(sd, medusa_parents, monkeypatch, C, V, dtype):
+    """Rows split across clusters of 1, 2, 4 and 8 CTAs (sizes whose slices would not fit
+    or would be empty fall back to the default); short last slices at 32008 and 20004."""
+    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    rep = Report(f"tree_rr cluster {C} V={V} {dtype}")
+    for seed in range(3):
+        x = workloads.make_tree_rr_inputs(8, V, medusa_parents, depth=4, seed=40 + seed, device=DEV, dtype=dtype,
+                                          scale=2.0, n_spikes=4, spike=4.0, noise=1.0, temps="uniform:0.0:1.5")
+        check_walks(rep, x, _run(sd, x, 4), 4)
+    rep.finish()
+
+
 def test_tree_rr_star_tree_more_children_than_the_list(sd):
     """600 children at the root (the kernel lists 256 at a time) and a few grandchildren:
     walks that reject many children refill the list; the drafter is far from the target so
