@@ -65,8 +65,8 @@ NCU_TRAFFIC = {
                     "rule": "block"},
     # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
     "tree_walk": {"bytes": 2_302_720, "src_sha": "00db4cb54f9e827b", "workload": "tree_b32_n64_v32000", "rule": "tree"},
-    # profiles/tree_rr_b32_n64_v32000.md: 17.87 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_869_312, "src_sha": "bc37a4ac319d4cb3", "workload": "tree_rr_b32_n64_v32000",
+    # profiles/tree_rr_b32_n64_v32000.md: 17.88 MB read, 0 written (batch seed 0)
+    "tree_rr": {"bytes": 17_875_200, "src_sha": "34d395f8655c4269", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
 
