@@ -622,7 +622,8 @@ def main():
             x["gammas"] = torch.randint(0, g + 1, (B,), generator=gen, dtype=torch.int32).to(dev)
 
         def verify(logits, draft_probs, draft_tokens, temperatures, uniforms, out=None, stream=None, _sets=sets):
-            gm = next(x["gammas"] for x in _sets if x["logits"] is logits)
+            # (host copies of the first batch in the end-to-end pass use its counts)
+            gm = next((x["gammas"] for x in _sets if x["logits"] is logits), _sets[0]["gammas"])
             return sd.verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniforms, gm, out=out,
                                           stream=stream)
         rows = float(np.mean([float((x["gammas"] + 1).sum()) for x in sets]))
@@ -736,6 +737,15 @@ def main():
         host = {k: sets[0][k].cpu().pin_memory() for k in keys}
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
+        rows_in_place = args.rule in ("chain", "chain_varlen") and per_kernel.get("chain_seq", (0.0, 0))[1] > 0
+        if rows_in_place:
+            # The chain calls leave pinned logits and draft probabilities where they are
+            # and the kernel reads the rows the round needs over the host link: count the
+            # other inputs' copies plus those rows (rows 0..J and q row J of this batch).
+            o0, gc0 = outs[0], gcap[0]
+            read0 = float((torch.minimum(o0["num_accepted"], gc0) + 1).float().sum()) * V * esize
+            read0 += float((o0["num_accepted"] < gc0).float().sum()) * V * 4
+            h2d = sum(host[k].numel() * host[k].element_size() for k in keys[2:]) + int(read0)
         for _ in range(2):
             verify(*(host[k] for k in keys))
         torch.cuda.synchronize()
@@ -749,6 +759,8 @@ def main():
         assert res["tokens"].device.type == "cpu"
         line["e2e"] = {"value": rows * world / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        if rows_in_place:
+            line["e2e"]["host_rows"] = "read in place from pinned host memory (rows 0..J, q row J)"
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x0 = {k: sets[0][k].cpu() for k in keys}

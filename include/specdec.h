@@ -100,6 +100,13 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
  * and status bits describe rows 0..J plus uniforms[b, g] and q row J where the draw
  * uses them.  A non-finite temperature is an error whatever the rows hold.
  * Sizes: B >= 1, g >= 1, V >= 1, V < 2^31.
+ * Host-resident rows: logits and draft_probs may be pinned host memory (cudaHostAlloc, or
+ * registered with cudaHostRegister, mapped at its own address).  The left-to-right kernel
+ * then reads only the rows the round needs, straight over the host link (no copy of the
+ * whole batch); this needs 16-byte aligned rows, g + 1 <= 32 and V <= 2,097,152, else
+ * SPECDEC_ERR_UNSUPPORTED.  Pageable host memory gives SPECDEC_ERR_INVALID_ARG.  The
+ * other inputs, the outputs and the workspace are device memory.  The same holds for
+ * specdec_verify_greedy and specdec_verify_chain_varlen.
  */
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
 

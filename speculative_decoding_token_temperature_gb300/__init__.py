@@ -179,6 +179,14 @@ class _HostRoundTrip:
             return t
         return t.to(self.device, non_blocking=True)
 
+    def rows(self, t):
+        """The logits and draft-probability rows of the chain calls: pinned host tensors stay
+        on the host (the library reads the rows it needs over the host link), others are
+        copied like every other input."""
+        if t is None or not self.on_host or (t.is_pinned() and t.is_contiguous()):
+            return t
+        return t.to(self.device, non_blocking=True)
+
     def to_host(self, t):
         if t is None or not self.on_host:
             return t
@@ -193,10 +201,11 @@ def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
     temperatures [B] fp32; uniforms [B, g+1] fp32.  Returns a dict with tokens
     [B, g+1] int32 (-1 padded), num_accepted [B] int32, p_draft [B, g] fp32 (if
     requested) and status [B] int32.  Host tensors are copied to the current device and
-    the results copied back.
+    the results copied back, except pinned host logits and draft_probs: the library reads
+    the rows the round needs from them in place, over the host link.
     """
     return _verify_round("specdec_verify_chain", "specdec_chain_workspace_bytes", logits, draft_probs,
-                         draft_tokens, temperatures, uniforms, out, with_p_draft, stream)
+                         draft_tokens, temperatures, uniforms, out, with_p_draft, stream, rows_on_host=True)
 
 
 def verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniforms, gammas, *, out=None,
@@ -215,7 +224,7 @@ def verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniform
                                                    wsb, s_)
 
     return _verify_round(_Entry(), "specdec_chain_workspace_bytes", logits, draft_probs, draft_tokens,
-                         temperatures, uniforms, out, with_p_draft, stream)
+                         temperatures, uniforms, out, with_p_draft, stream, rows_on_host=True)
 
 
 def verify_block(logits, draft_probs, draft_tokens, temperatures, uniforms, *, out=None,
@@ -227,22 +236,23 @@ def verify_block(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
 
 
 def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, temperatures, uniforms,
-                  out, with_p_draft, stream) -> dict:
+                  out, with_p_draft, stream, rows_on_host: bool = False) -> dict:
     lib = load_library()
     rt = _HostRoundTrip([logits])
-    logits, draft_probs, draft_tokens, temperatures, uniforms = (
-        rt.to_device(t) for t in (logits, draft_probs, draft_tokens, temperatures, uniforms))
+    rows = rt.rows if rows_on_host else rt.to_device
+    logits, draft_probs = rows(logits), rows(draft_probs)
+    draft_tokens, temperatures, uniforms = (rt.to_device(t) for t in (draft_tokens, temperatures, uniforms))
     if logits.dim() != 3:
         raise ValueError("logits must be [B, g+1, V]")
     B, g1, V = logits.shape
     g = g1 - 1
-    dev = logits.device
+    dev = rt.device
     code = _dtype_code(logits)
-    _need(draft_probs, "draft_probs", torch.float32, (B, g, V), dev)
+    _need(draft_probs, "draft_probs", torch.float32, (B, g, V), draft_probs.device if rt.on_host else dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
     _need(temperatures, "temperatures", torch.float32, (B,), dev)
     _need(uniforms, "uniforms", torch.float32, (B, g1), dev)
-    _need(logits, "logits", None, (B, g1, V), dev)
+    _need(logits, "logits", None, (B, g1, V), logits.device if rt.on_host else dev)
     if out is None:
         out = {
             "tokens": torch.empty(B, g1, dtype=torch.int32, device=dev),
@@ -254,11 +264,19 @@ def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, 
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     ws, wsb = _workspace(int(getattr(lib, ws_entry)(B, g, V, code)), dev, s.cuda_stream)
     fn = getattr(lib, entry) if isinstance(entry, str) else entry
-    rc = fn(
-        _ptr(logits), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperatures),
-        _ptr(uniforms), B, g, V, _ptr(out["tokens"]), _ptr(out["num_accepted"]),
-        _ptr(out.get("p_draft")), _ptr(out.get("status")), _ptr(ws), wsb,
-        ctypes.c_void_p(s.cuda_stream))
+
+    def call(lg, qp):
+        return fn(
+            _ptr(lg), code, _ptr(qp), _ptr(draft_tokens), _ptr(temperatures),
+            _ptr(uniforms), B, g, V, _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+            _ptr(out.get("p_draft")), _ptr(out.get("status")), _ptr(ws), wsb,
+            ctypes.c_void_p(s.cuda_stream))
+
+    rc = call(logits, draft_probs)
+    if rc == ERR_UNSUPPORTED and rt.on_host and (logits.device.type == "cpu" or draft_probs.device.type == "cpu"):
+        # rows the kernel cannot read in place (unaligned rows, sizes beyond the
+        # left-to-right kernel): copy them like the other inputs
+        rc = call(rt.to_device(logits), rt.to_device(draft_probs))
     _check(rc, entry if isinstance(entry, str) else "specdec_verify_chain_varlen")
     return {k: rt.to_host(v) for k, v in out.items()}
 
@@ -267,13 +285,13 @@ def verify_greedy(logits, draft_tokens, *, out=None, stream=None) -> dict:
     """Greedy verification (specdec_verify_greedy): tokens, num_accepted, status."""
     lib = load_library()
     rt = _HostRoundTrip([logits])
-    logits, draft_tokens = rt.to_device(logits), rt.to_device(draft_tokens)
+    logits, draft_tokens = rt.rows(logits), rt.to_device(draft_tokens)
     B, g1, V = logits.shape
     g = g1 - 1
-    dev = logits.device
+    dev = rt.device
     code = _dtype_code(logits)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
-    _need(logits, "logits", None, (B, g1, V), dev)
+    _need(logits, "logits", None, (B, g1, V), logits.device if rt.on_host else dev)
     if out is None:
         out = {
             "tokens": torch.empty(B, g1, dtype=torch.int32, device=dev),
@@ -282,10 +300,15 @@ def verify_greedy(logits, draft_tokens, *, out=None, stream=None) -> dict:
         }
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     ws, wsb = _workspace(int(lib.specdec_greedy_workspace_bytes(B, g, V, code)), dev, s.cuda_stream)
-    rc = lib.specdec_verify_greedy(_ptr(logits), code, _ptr(draft_tokens), B, g, V,
-                                   _ptr(out["tokens"]), _ptr(out["num_accepted"]),
-                                   _ptr(out.get("status")), _ptr(ws), wsb,
-                                   ctypes.c_void_p(s.cuda_stream))
+    def call(lg):
+        return lib.specdec_verify_greedy(_ptr(lg), code, _ptr(draft_tokens), B, g, V,
+                                         _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                         _ptr(out.get("status")), _ptr(ws), wsb,
+                                         ctypes.c_void_p(s.cuda_stream))
+
+    rc = call(logits)
+    if rc == ERR_UNSUPPORTED and logits.device.type == "cpu":  # rows the kernel cannot read in place
+        rc = call(rt.to_device(logits))
     _check(rc, "specdec_verify_greedy")
     return {k: rt.to_host(v) for k, v in out.items()}
 

@@ -26,6 +26,11 @@
 // A team follows its sequence's chain row after row.  When the chain ends, the team
 // takes new work from two ticket queues: sequence starts first, then queued draws.  So
 // every chain starts early, and the draws fill the machine behind the chains.
+//
+// The logits and draft probabilities may also sit in pinned host memory (kHost): the
+// kernel then reads them over the host link itself, only the rows the round needs, with
+// per-lane 16-byte cp.async copies into the same stages (bulk copies are kept to device
+// memory) and plain loads for single elements.
 
 #include <climits>
 
@@ -45,6 +50,29 @@ static_assert(kSeqWarps % kSeqGroups == 0, "groups must split the warps evenly")
 static_assert(kC >= 1 && kC <= 8, "portable cluster sizes only");
 
 __device__ __forceinline__ bool is_greedy(float T) { return !(T >= SPECDEC_GREEDY_TEMPERATURE); }
+
+// Loads of the logits and q rows: through the read-only path from device memory, plain
+// global loads (cached in L2 only) when the rows may sit in host memory.
+template <bool kHost, typename X>
+__device__ __forceinline__ X load_in(const X* p) {
+  if constexpr (kHost) return __ldcg(p);
+  else return __ldg(p);
+}
+template <bool kHost, typename T>
+__device__ __forceinline__ float load_elem(const T* row, int64_t k) {
+  if constexpr (sizeof(T) == 2) return __uint_as_float(static_cast<uint32_t>(load_in<kHost>(row + k)) << 16);
+  else return load_in<kHost>(row + k);
+}
+
+// One 16-byte asynchronous copy of global (or mapped host) memory into shared memory, and
+// the arrival of this thread on an mbarrier once all its earlier such copies have landed
+// (the barrier counts one arrival per copying thread).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 
 // Barrier over the threads of one group (named barriers 1.., 0 stays __syncthreads).
 __device__ __forceinline__ void group_sync(int group) {
@@ -214,15 +242,26 @@ struct Pipe {
   __device__ __forceinline__ unsigned char* stage(uint32_t i) { return buf + (i % kSeqStages) * kSeqChunkBytes; }
   __device__ __forceinline__ uint64_t* sbar(uint32_t i) { return bar + (i % kSeqStages); }
   __device__ __forceinline__ uint32_t in_flight() const { return issued - k; }
-  // Issue one copy group (one or two copies) into the next stage.  The fence orders this
-  // warp's earlier reads of that stage (completed by a __syncwarp) before the copy.
-  __device__ __forceinline__ void issue(const void* a, uint32_t na, const void* b, uint32_t nb, int off_b) {
+  // Issue one copy group (one or two copies) into the next stage: bulk copies by one lane,
+  // or (kHost) 16-byte copies by every lane, each of which then arrives on the stage's
+  // barrier.  The fence orders this warp's earlier reads of that stage (completed by a
+  // __syncwarp) before the copy.
+  template <bool kHost>
+  __device__ __forceinline__ void issue(const void* a, uint32_t na, const void* b, uint32_t nb, int off_b, int lane) {
     uint64_t* br = sbar(issued);
     unsigned char* dst = stage(issued);
-    fence_proxy_async_smem();
-    mbar_expect_tx(br, na + nb);
-    bulk_copy_g2s(dst, a, na, br);
-    if (nb) bulk_copy_g2s(dst + off_b, b, nb, br);
+    if constexpr (kHost) {
+      const char* ca = static_cast<const char*>(a);
+      const char* cb = static_cast<const char*>(b);
+      for (uint32_t o = 16u * lane; o < na; o += 512u) cp_async_16(dst + o, ca + o);
+      for (uint32_t o = 16u * lane; o < nb; o += 512u) cp_async_16(dst + off_b + o, cb + o);
+      cp_async_arrive(br);
+    } else if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_expect_tx(br, na + nb);
+      bulk_copy_g2s(dst, a, na, br);
+      if (nb) bulk_copy_g2s(dst + off_b, b, nb, br);
+    }
   }
   __device__ __forceinline__ bool wait() { return mbar_wait(sbar(k), (k / kSeqStages) & 1u); }
 };
@@ -353,21 +392,21 @@ struct Task {
   int lo = 0, hi = 0, n = 0;
 };
 
-template <typename T>
+template <typename T, bool kHost>
 __device__ __forceinline__ void issue_job(Pipe& pp, const Task& t, int j, int gwarp, int lane, int V,
                                           int64_t row_bytes) {
   constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
-  if (lane == 0) {
+  if (kHost || lane == 0) {
     const int ch = t.lo + gwarp + j * kWarpsPerGroup;
     if (t.kind == kTaskRow) {
       const uint32_t nb = static_cast<uint32_t>(
           min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes));
-      pp.issue(t.src + static_cast<int64_t>(ch) * kSeqChunkBytes, nb, nullptr, 0, 0);
+      pp.issue<kHost>(t.src + static_cast<int64_t>(ch) * kSeqChunkBytes, nb, nullptr, 0, 0, lane);
     } else {
       const int n = min(kSeqDrawChunk, V - ch * kSeqDrawChunk);
       const int64_t off = static_cast<int64_t>(ch) * kSeqDrawChunk;
-      pp.issue(t.src + off * static_cast<int64_t>(sizeof(T)), static_cast<uint32_t>(n) * sizeof(T),
-               t.q ? t.q + off : nullptr, t.q ? static_cast<uint32_t>(n) * 4u : 0u, LB);
+      pp.issue<kHost>(t.src + off * static_cast<int64_t>(sizeof(T)), static_cast<uint32_t>(n) * sizeof(T),
+                      t.q ? t.q + off : nullptr, t.q ? static_cast<uint32_t>(n) * 4u : 0u, LB, lane);
     }
   }
   ++pp.issued;
@@ -471,7 +510,7 @@ __device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int la
 // chunk whose running mass (from `base`, the mass of all earlier members) first exceeds
 // `target`, then the element inside it.  If rounding leaves no such element, the last
 // positive-weight element of the part is taken.
-template <typename T>
+template <typename T, bool kHost>
 __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, float base, float target,
                             float mJ, float c, float invZ, bool no_q, const float* mass, int lane) {
   using GL = typename Group<T>::L;
@@ -507,8 +546,8 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
 #pragma unroll
     for (int e = 0; e < 4; ++e) w[j][e] = 0.f;
     if (g < ng) {
-      const GL lw = __ldg(reinterpret_cast<const GL*>(lrow + k0) + g);
-      const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(qrow + k0) + g);
+      const GL lw = load_in<kHost>(reinterpret_cast<const GL*>(lrow + k0) + g);
+      const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : load_in<kHost>(reinterpret_cast<const float4*>(qrow + k0) + g);
       gsum[j] = group_weights<T>(lw, q4, -__fmul_rn(mJ, c), c, invZ, no_q, w[j]);
       lane_tot += gsum[j];
     }
@@ -558,7 +597,7 @@ __device__ __forceinline__ float unpack_total(const float4& v) { return v.x; }
 // ---------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool kHost>
 __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const ChainParams P) {
   using GL = typename Group<T>::L;
   constexpr int VPL = kSeqChunkBytes / 16 / 32;
@@ -583,7 +622,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   const bool first = gwarp == 0 && lane == 0;  // this member's first thread
   const bool leader = tm.rank == 0 && first;   // the team's first thread
   if (lane == 0) {
-    for (int s = 0; s < kSeqStages; ++s) mbar_init(&pp.bar[s], 1);
+    for (int s = 0; s < kSeqStages; ++s) mbar_init(&pp.bar[s], kHost ? 32 : 1);
     if (gwarp == 0) {
       mbar_init(&gs.xbar[0], 1);
       mbar_init(&gs.xbar[1], 1);
@@ -676,7 +715,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     if (srch && gwarp == 0) {
       const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
       const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
-      const int y = local_search<T>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
+      const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
                                     gs.mass[s_par], lane);
       if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
     }
@@ -707,8 +746,8 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       if (first && !g2) {
         g2 = true;
         if (at_draft && !P.greedy_only && gx >= 0 && gx < V) {
-          glx = Elem<T>::load(reinterpret_cast<const T*>(tc.src), gx);
-          gqx = __ldg(P.q + (static_cast<int64_t>(b) * P.gamma + ri) * V + gx);
+          glx = load_elem<kHost>(reinterpret_cast<const T*>(tc.src), gx);
+          gqx = load_in<kHost>(P.q + (static_cast<int64_t>(b) * P.gamma + ri) * V + gx);
         }
       }
     };
@@ -716,9 +755,9 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     // This task's copies: kSeqStages in flight, one more as each stage is read.
     int ci = 0;
     auto refill = [&]() {
-      if (pp.ok && ci < tc.n) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+      if (pp.ok && ci < tc.n) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
     };
-    while (pp.ok && ci < tc.n && pp.in_flight() < kSeqStages) issue_job<T>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+    while (pp.ok && ci < tc.n && pp.in_flight() < kSeqStages) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
     float4 mine;
     if (kind == kTaskRow) {
@@ -986,7 +1025,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   if (srch && gwarp == 0 && tm.ok) {
     const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
     const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
-    const int y = local_search<T>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
+    const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
                                   gs.mass[s_par], lane);
     if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
   }
@@ -998,7 +1037,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   cluster_sync_all();
 }
 
-template <typename T>
+template <typename T, bool kHost>
 cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
   constexpr int smem = kSeqWarps * kSeqStages * kSeqChunkBytes;
   static unsigned long long configured = 0;
@@ -1018,12 +1057,12 @@ cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (!(configured & bit)) {
-    if (cudaError_t e = cudaFuncSetAttribute(chain_seq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaError_t e = cudaFuncSetAttribute(chain_seq_kernel<T, kHost>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         e != cudaSuccess)
       return e;
     cfg.gridDim = dim3(static_cast<unsigned>(kC * device_sm_count()));
     int n = 0;
-    if (cudaError_t e = cudaOccupancyMaxActiveClusters(&n, chain_seq_kernel<T>, &cfg); e != cudaSuccess) return e;
+    if (cudaError_t e = cudaOccupancyMaxActiveClusters(&n, chain_seq_kernel<T, kHost>, &cfg); e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_clusters[dev & 63] = n;
     configured |= bit;
@@ -1031,14 +1070,18 @@ cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
   const int want = (P.B + kSeqGroups - 1) / kSeqGroups;
   const int clusters = min(max_clusters[dev & 63], want);
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kC));
-  return cudaLaunchKernelEx(&cfg, chain_seq_kernel<T>, P);
+  return cudaLaunchKernelEx(&cfg, chain_seq_kernel<T, kHost>, P);
 }
 
 }  // namespace
 
 cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
-  if (ldt == SPECDEC_BF16) return launch_typed<uint16_t>(P, stream);
-  return launch_typed<float>(P, stream);
+  if (P.host_inputs) {
+    if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, true>(P, stream);
+    return launch_typed<float, true>(P, stream);
+  }
+  if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, false>(P, stream);
+  return launch_typed<float, false>(P, stream);
 }
 
 }  // namespace specdec

@@ -195,6 +195,25 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   if (gammas && !(stream_path && V <= kSeqMaxV))  // per-sequence counts: left-to-right kernel only
     return fail(SPECDEC_ERR_UNSUPPORTED, "per-sequence draft counts need 16-byte rows, g + 1 <= 32");
   if (workspace_bytes < chain_ws_bytes(B, g, V, ldt)) return SPECDEC_ERR_WORKSPACE;
+  // logits and q in pinned host memory: the left-to-right kernel reads the rows it needs
+  // over the host link; pageable host memory is refused (the first check that asks the
+  // CUDA runtime)
+  bool host_in = false;
+  for (const void* p : {logits, greedy_only ? nullptr : static_cast<const void*>(q)}) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes a{};
+    if (cudaError_t e = cudaPointerGetAttributes(&a, p); e != cudaSuccess) return fail_cuda("pointer attributes", e);
+    if (a.type == cudaMemoryTypeUnregistered)
+      return fail(SPECDEC_ERR_INVALID_ARG, "host logits and draft probabilities must be pinned (cudaHostAlloc, cudaHostRegister)");
+    if (a.type == cudaMemoryTypeHost) {
+      if (a.devicePointer != p) return fail(SPECDEC_ERR_UNSUPPORTED, "host memory not mapped at its own address");
+      host_in = true;
+    }
+  }
+  if (host_in && !(stream_path && (gammas || use_left_to_right()) && V <= kSeqMaxV))
+    return fail(SPECDEC_ERR_UNSUPPORTED,
+                "host-resident logits or draft probabilities need the left-to-right kernel: 16-byte rows, g + 1 <= 32, "
+                "V <= 2,097,152");
 
   ChainParams P{};
   P.logits = logits;
@@ -223,6 +242,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
     return fail_cuda("clearing the workspace counters", e);
   if (stream_path && (gammas || use_left_to_right()) && V <= kSeqMaxV) {
     P.grid_stats = device_sm_count();
+    P.host_inputs = host_in ? 1 : 0;
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
     if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);
     return SPECDEC_OK;

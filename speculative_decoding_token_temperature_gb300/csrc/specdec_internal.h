@@ -100,6 +100,7 @@ struct ChainParams {
   int nseg;              // segments per row
   int seg;               // elements per segment
   int greedy_only;
+  int host_inputs;       // left-to-right kernel: logits and q may sit in pinned host memory
   int nch;               // streaming path: 4 KB chunks per logits row
   int nchd;              // streaming path: draw chunks per row
   int grid_stats, grid_draw;
