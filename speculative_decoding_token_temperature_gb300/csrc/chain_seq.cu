@@ -46,6 +46,11 @@ constexpr float kNaN = __builtin_nanf("");
 constexpr int kWarpsPerGroup = kSeqWarps / kSeqGroups;
 constexpr int kGroupThreads = kWarpsPerGroup * 32;
 constexpr int kC = kSeqCluster;
+// Copies a warp keeps in flight for a draw task (a row task keeps kSeqStages).  While both
+// stream, the rows -- the chains, which are the critical path -- get the larger share of
+// the bandwidth; the draws fill in behind them.
+constexpr int kSeqDrawStages = 2;
+static_assert(kSeqDrawStages >= 1 && kSeqDrawStages <= kSeqStages, "draw copies use the row stages");
 static_assert(kSeqWarps % kSeqGroups == 0, "groups must split the warps evenly");
 static_assert(kC >= 1 && kC <= 8, "portable cluster sizes only");
 
@@ -752,12 +757,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       }
     };
 
-    // This task's copies: kSeqStages in flight, one more as each stage is read.
+    // This task's copies: kSeqStages in flight for a row (kSeqDrawStages for a draw), one
+    // more as each stage is read.
     int ci = 0;
     auto refill = [&]() {
       if (pp.ok && ci < tc.n) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
     };
-    while (pp.ok && ci < tc.n && pp.in_flight() < kSeqStages) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+    const uint32_t depth = kind == kTaskRow ? kSeqStages : kSeqDrawStages;
+    while (pp.ok && ci < tc.n && pp.in_flight() < depth) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
     float4 mine;
     if (kind == kTaskRow) {
