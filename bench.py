@@ -58,8 +58,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/chain_stream_b256_v128256.md: 525.37 MB read + 4.25 MB written (SPECDEC_CHAIN_SCAN=1)
     "chain_stats": {"bytes": 529_620_480, "src_sha": "e4f192c1e6151e13", "workload": "chain_b256_v128256", "rule": "chain"},
-    # profiles/chain_seq_b256_v128256.md: 320.87 MB read + 3.00 MB written (batch seed 0)
-    "chain_seq": {"bytes": 323_870_208, "src_sha": "557e8eac163fe22b", "workload": "chain_b256_v128256", "rule": "chain"},
+    # profiles/chain_seq_b256_v128256.md: 320.69 MB read + 3.28 MB written (batch seed 0)
+    "chain_seq": {"bytes": 323_976_192, "src_sha": "d901c79203301ed0", "workload": "chain_b256_v128256", "rule": "chain"},
     # profiles/block_row_b256_v128256.md: 1446.00 MB read + 5.02 MB written (batch seed 0)
     "block_fused": {"bytes": 1_451_024_640, "src_sha": "9909774bce867764", "workload": "chain_b256_v128256",
                     "rule": "block"},

@@ -48,7 +48,8 @@ constexpr int kGroupThreads = kWarpsPerGroup * 32;
 constexpr int kC = kSeqCluster;
 // Copies a warp keeps in flight for a draw task (a row task keeps kSeqStages).  While both
 // stream, the rows -- the chains, which are the critical path -- get the larger share of
-// the bandwidth; the draws fill in behind them.
+// the bandwidth; the draws fill in behind them.  A draw taken while other teams wait for
+// work (the machine has bandwidth to spare) keeps kSeqStages too.
 constexpr int kSeqDrawStages = 2;
 static_assert(kSeqDrawStages >= 1 && kSeqDrawStages <= kSeqStages, "draw copies use the row stages");
 static_assert(kSeqWarps % kSeqGroups == 0, "groups must split the warps evenly");
@@ -281,6 +282,7 @@ enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3 };
 struct Entry {
   int b, row, kind, warn;
   float m, Z, T;
+  int deep = 0;  // a draw taken while teams wait for work: all kSeqStages copies in flight
 };
 __device__ __forceinline__ void pack_entry(const Entry& e, float4& e0, float4& e1) {
   e0 = make_float4(__int_as_float(e.b), __int_as_float(e.row | (e.kind << 8) | (e.warn << 16)), e.m, e.Z);
@@ -296,6 +298,7 @@ __device__ __forceinline__ Entry unpack_entry(const float4& e0, const float4& e1
   e.m = e0.z;
   e.Z = e0.w;
   e.T = e1.x;
+  e.deep = __float_as_int(e1.y);
   return e;
 }
 
@@ -357,6 +360,9 @@ __device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, floa
       const float4* ent = q.ring_draws + 2 * static_cast<int64_t>(d);
       e0 = __ldcg(ent);
       e1 = __ldcg(ent + 1);
+      // teams waiting for work: the machine has bandwidth to spare, stream the draw deep
+      const int idle = static_cast<int>(ld_relaxed(q.draw_ticket) - ld_relaxed(q.pub_draws));
+      e1.y = __int_as_float(idle > 0 ? 1 : 0);
       return 1;
     }
     if (ld_relaxed(q.finished) >= static_cast<unsigned>(q.B)) return -1;
@@ -763,7 +769,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     auto refill = [&]() {
       if (pp.ok && ci < tc.n) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
     };
-    const uint32_t depth = kind == kTaskRow ? kSeqStages : kSeqDrawStages;
+    const uint32_t depth = (kind == kTaskRow || cur.deep) ? kSeqStages : kSeqDrawStages;
     while (pp.ok && ci < tc.n && pp.in_flight() < depth) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
     float4 mine;
