@@ -13,11 +13,11 @@ Sources (cited by page title and section throughout):
 
 Every floating-point input is widened exactly to float64 (bf16 and fp32 values are
 exactly representable) and all arithmetic is float64.  Readings taken where the pages
-are silent or disagree are marked READING and listed in the design doc.
+are silent or disagree are marked READING.
 
-Parity status: every public function here is pinned by ``tests/test_oracle_pins.py``
-(worked examples, closed forms, identities and exact integration over the uniforms);
-none is "parity unpinned".
+Parity status: every public function here is pinned (``tests/test_oracle_*.py``: worked
+examples, closed forms, identities, exact integration over the uniforms, and the Philox
+generator's published known-answer vectors); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -169,7 +169,8 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
     Returns a dict: tokens [gamma+1] (-1 padded), J, status, p_draft [gamma] (p_i(x_i),
     NaN where unevaluated), q_draft [gamma], margins [gamma] (|u_i - p_i(x_i)/q_i(x_i)|,
     the distance of the test to its decision boundary), and for a sampled draw 'y_u'
-    (u * S) plus, when want_cdf, 'cdf' and 'S' of the weights the draw used.
+    (u * S) plus, when want_cdf, 'cdf' and 'S' of the weights the draw used and 'pcdf',
+    the CDF of p_J itself.
     """
     logits = np.asarray(logits)
     g1, V = logits.shape
@@ -273,6 +274,7 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
     if want_cdf:
         out["cdf"] = C
         out["S"] = S
+        out["pcdf"] = np.cumsum(p[J])  # the target row's own CDF (the zero-residual fallback)
     return out
 
 
@@ -358,7 +360,8 @@ def verify_block_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
 
     Returns tokens [gamma+1] (-1 padded), J (= n), status, p_draft [gamma] (p_k(x_k)),
     w [gamma+1], survival [gamma+1], margins [gamma] (|u[k-1] - survival_k| for k =
-    1..gamma), and for a sampled draw 'y_u' plus, when want_cdf, 'cdf' and 'S'.
+    1..gamma), and for a sampled draw 'y_u' plus, when want_cdf, 'cdf', 'S' and 'pcdf'
+    (the CDF of p_n itself).
     """
     logits = np.asarray(logits)
     g1, V = logits.shape
@@ -445,6 +448,7 @@ def verify_block_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
     if want_cdf:
         out["cdf"] = C
         out["S"] = S
+        out["pcdf"] = np.cumsum(p[n])  # the target row's own CDF (the zero-residual fallback)
     return out
 
 
@@ -477,7 +481,7 @@ def verify_block(logits, q, drafts, T, u) -> dict:
 # race is run in log2 units, score_i = a_i - log2(xi_i) with xi_i = -ln(u_i) = -log1p(u_i - 1)
 # (argmax(a_i / ln 2 + g_i) with g = -ln(xi) is the same argmax), a_i = l_i * log2(e) / T
 # for the target and log2(q_i) for the drafter; ties go to the lowest index.  The scores
-# are formed in float32, the precision the pages' code computes in.
+# are float64 from the float32 uniforms.
 # ---------------------------------------------------------------------------------
 LOG2E = 1.0 / np.log(2.0)
 PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
@@ -517,16 +521,17 @@ def gumbel_uniforms(seed: int, b, k, V: int) -> np.ndarray:
     return ((x >> np.uint32(9)).astype(np.float32) + np.float32(0.5)) * np.float32(2.0 ** -23)
 
 
-def gumbel_scores(a32, u32) -> np.ndarray:
-    """The race in log2 units, float32: a - log2(xi), xi = -log1p(u - 1)."""
-    a32 = np.asarray(a32, dtype=np.float32)
-    u32 = np.asarray(u32, dtype=np.float32)
-    with np.errstate(divide="ignore"):
-        xi = -np.log1p(u32 - np.float32(1.0))
-        return a32 - np.log2(xi)
+def gumbel_scores(a, u32) -> np.ndarray:
+    """The race in log2 units, in float64: a - log2(xi), xi = -ln(u), from the float32
+    uniforms u (widened exactly) and the scores' first terms a (float64)."""
+    a = np.asarray(a, dtype=np.float64)
+    u = np.asarray(u32, dtype=np.float32).astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        xi = -np.log1p(u - 1.0)
+        return a - np.log2(xi)
 
 
-def _lowest_argmax32(s) -> int:
+def _lowest_argmax_score(s) -> int:
     """Lowest index of the largest score; a NaN score (a NaN or negative q) never wins;
     -1 when no score is a number."""
     s = np.asarray(s)
@@ -547,23 +552,23 @@ def gumbel_draft_sequence(q, seed: int, b: int) -> dict:
     q = widen(q)
     gamma, V = q.shape
     u = gumbel_uniforms(seed, b, np.arange(gamma), V)
-    with np.errstate(divide="ignore"):
-        a = np.log2(q.astype(np.float32))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        a = np.log2(q)
     drafts, gaps = [], []
     for kk in range(gamma):
         s = gumbel_scores(a[kk], u[kk])
-        drafts.append(_lowest_argmax32(s))
+        drafts.append(_lowest_argmax_score(s))
         gaps.append(_top2_gap(s))
     return {"drafts": np.array(drafts, dtype=np.int64), "gaps": np.array(gaps)}
 
 
 def gumbel_target_token(logits_row, T: float, seed: int, b: int, k: int) -> tuple[int, float]:
     """The target's Gumbel-max sample at row k: argmax_i (l_i * c - log2 xi_i), c =
-    log2(e) / T in float32; returns (token, top-two score gap)."""
-    c = np.float32(np.float32(LOG2E) / np.float32(T))
-    a = np.asarray(logits_row, dtype=np.float32) * c
+    log2(e) / T, in float64; returns (token, top-two score gap)."""
+    c = LOG2E / float(T)
+    a = widen(logits_row) * c
     s = gumbel_scores(a, gumbel_uniforms(seed, b, k, len(a)))
-    return _lowest_argmax32(s), _top2_gap(s)
+    return _lowest_argmax_score(s), _top2_gap(s)
 
 
 def verify_gumbel_sequence(logits, drafts, T: float, seed: int, b: int) -> dict:

@@ -145,3 +145,53 @@ def test_target_sample_follows_softmax_at_temperature():
     toks = np.array([so.gumbel_target_token(logits, T, 21, b, 2)[0] for b in range(n)])
     counts = np.bincount(toks, minlength=len(logits))
     assert stats.chisquare(counts, so.target_distribution(logits, T) * n).pvalue > 1e-4
+
+
+def _kat_vectors():
+    from pathlib import Path
+    rows = []
+    for line in (Path(__file__).resolve().parent / "golden" / "philox4x32_10_kat.txt").read_text().splitlines():
+        line = line.strip()
+        if line.startswith("kat ="):
+            w = [int(t, 16) for t in line.split("=", 1)[1].split()]
+            rows.append((w[:4], w[4:6], w[6:10]))
+    assert len(rows) == 3
+    return rows
+
+
+def test_philox_matches_the_published_known_answers():
+    """Philox4x32-10 against the generator's published known-answer vectors (Random123,
+    Salmon et al., SC 2011): counter, key -> four output words, bit for bit."""
+    for ctr, key, want in _kat_vectors():
+        got = [int(x) for x in so.philox4x32_10(*ctr, *key)]
+        assert got == want, ([hex(v) for v in got], [hex(v) for v in want])
+
+
+def _philox_variant(ctr, key, *, swap_hilo=False, bump_first=False, swap_mult=False, rounds=10,
+                    swap_key_words=False):
+    """Philox4x32 with one plausible mistake planted (the KAT test must reject each)."""
+    M = (0xD2511F53, 0xCD9E8D57)
+    W = (0x9E3779B9, 0xBB67AE85)
+    m0, m1 = (M[1], M[0]) if swap_mult else M
+    c = list(ctr)
+    k0, k1 = (key[1], key[0]) if swap_key_words else key
+    for r in range(rounds):
+        if r or bump_first:
+            k0, k1 = (k0 + W[0]) & 0xFFFFFFFF, (k1 + W[1]) & 0xFFFFFFFF
+        p0, p1 = m0 * c[0], m1 * c[2]
+        hi0, lo0, hi1, lo1 = p0 >> 32, p0 & 0xFFFFFFFF, p1 >> 32, p1 & 0xFFFFFFFF
+        if swap_hilo:
+            hi0, lo0, hi1, lo1 = lo0, hi0, lo1, hi1
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+    return c
+
+
+@pytest.mark.parametrize("mistake", [dict(swap_hilo=True), dict(bump_first=True), dict(swap_mult=True),
+                                     dict(rounds=7), dict(swap_key_words=True)])
+def test_planted_philox_mistakes_fail_the_known_answers(mistake):
+    kats = _kat_vectors()
+    # the unmodified variant reproduces every vector (the variant itself is faithful) ...
+    for ctr, key, want in kats:
+        assert _philox_variant(ctr, key) == want
+    # ... and each planted mistake misses at least one of them
+    assert any(_philox_variant(ctr, key, **mistake) != want for ctr, key, want in kats)
