@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import workloads
-from parity import ParityReport, check_chain, run_oracle_chain
+from parity import ParityReport, assert_flag_budget, check_chain, run_oracle_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -55,46 +55,45 @@ def _run_and_check(sd, report, x, sample=None, workers=None):
     return out
 
 
-def _finish(report, max_flag_fraction=None):
+def _finish(report, budget=True):
+    """No hard failure; on a measured workload (budget) the stated flag bound as well."""
     path = os.environ.get("SPECDEC_PARITY_REPORT")
     if path:
         with open(path, "a") as f:
             f.write(json.dumps(dict(report.summary(), rule="block")) + "\n")
     assert not report.failures, report.failures[:10]
-    if max_flag_fraction is not None:
-        assert report.flagged <= max(1, max_flag_fraction * report.rows), report.summary()
+    if budget:
+        assert_flag_budget(report.flagged, report.rows, report.summary())
 
 
 def test_block_b1_v1000_all_rounds(sd):
     rep = ParityReport("block chain_b1_v1000 (100 rounds)")
     for r in range(100):
         _run_and_check(sd, rep, workloads.chain_workload("chain_b1_v1000", r, DEV), workers=1)
-    _finish(rep, 1e-4)
+    _finish(rep)
 
 
 def test_block_b64_v32000_all_rounds(sd):
     rep = ParityReport("block chain_b64_v32000 (40 rounds)")
     for r in range(40):
         _run_and_check(sd, rep, workloads.chain_workload("chain_b64_v32000", r, DEV))
-    _finish(rep, 1e-4)
+    _finish(rep)
 
 
-def test_block_b256_v128256_full_size_sampled(sd):
-    """Full-size launches; every sequence of the first round, 64 of the second."""
-    rep = ParityReport("block chain_b256_v128256 (2 rounds, full size)")
-    g = np.random.default_rng(2)
+def test_block_b256_v128256_full_rounds(sd):
+    """Two full-size launches, every sequence checked."""
+    rep = ParityReport("block chain_b256_v128256 (2 full rounds)")
     for r in range(2):
         x = workloads.chain_workload("chain_b256_v128256", r, DEV)
-        sample = None if r == 0 else np.sort(g.choice(256, 64, replace=False))
-        _run_and_check(sd, rep, x, sample=sample)
+        _run_and_check(sd, rep, x)
         del x
     _finish(rep)
 
 
-def test_block_b512_v152064_fp32_sampled(sd):
-    rep = ParityReport("block chain_b512_v152064 (1 round, 96 sequences)")
+def test_block_b512_v152064_fp32_full_round(sd):
+    rep = ParityReport("block chain_b512_v152064 (1 full round)")
     x = workloads.chain_workload("chain_b512_v152064", 0, DEV)
-    _run_and_check(sd, rep, x, sample=np.sort(np.random.default_rng(3).choice(512, 96, replace=False)))
+    _run_and_check(sd, rep, x)
     del x
     torch.cuda.empty_cache()
     _finish(rep)
@@ -112,7 +111,7 @@ def test_block_ragged_shapes(sd, B, gamma, V, dtype):
                                         recipe="spikes", scale=2.0, n_spikes=min(3, V), spike=4.0,
                                         noise=0.7, temps="uniform:0.0:1.5")
         _run_and_check(sd, rep, x, workers=1)
-    _finish(rep)
+    _finish(rep, budget=False)  # a few dozen rows per shape: flags reported, not bounded
 
 
 def test_block_unsupported_layouts_are_refused(sd):

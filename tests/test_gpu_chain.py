@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import workloads
-from parity import FLAG_TOL, ParityReport, check_chain, run_oracle_chain
+from parity import FLAG_TOL, ParityReport, assert_flag_budget, check_chain, run_oracle_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -46,53 +46,54 @@ def _record(report):
             f.write(json.dumps(report.summary()) + "\n")
 
 
-def _finish(report, max_flag_fraction=None):
+def _finish(report, budget=True):
+    """No hard failure; on a measured workload (budget) the stated flag bound as well."""
     _record(report)
     assert not report.failures, report.failures[:10]
-    if max_flag_fraction is not None:
-        assert report.flagged <= max(1, max_flag_fraction * report.rows), report.summary()
+    if budget:
+        assert_flag_budget(report.flagged, report.rows, report.summary())
 
 
 def test_chain_b1_v1000_all_rounds(sd):
     rep = ParityReport("chain_b1_v1000 (100 rounds)")
     for r in range(100):
         _run_and_check(sd, rep, workloads.chain_workload("chain_b1_v1000", r, DEV), workers=1)
-    _finish(rep, 1e-4)
+    _finish(rep)
 
 
 def test_chain_b64_v32000_all_rounds(sd):
     rep = ParityReport("chain_b64_v32000 (100 rounds)")
     for r in range(100):
         _run_and_check(sd, rep, workloads.chain_workload("chain_b64_v32000", r, DEV))
-    _finish(rep, 1e-4)
+    _finish(rep)
 
 
-def test_chain_b256_v128256_full_size_sampled(sd):
-    """Full-size launches of the benchmarked workload; the oracle checks 64 sequences per
-    round (every sequence in the first round)."""
-    rep = ParityReport("chain_b256_v128256 (3 rounds, full size)")
-    g = np.random.default_rng(0)
-    for r in range(3):
+def test_chain_b256_v128256_full_rounds(sd):
+    """Five full-size launches of the benchmarked workload, every sequence checked: 10,240
+    rows, enough for the 1e-4 bound on flagged rows to be measurable (it allows one)."""
+    rep = ParityReport("chain_b256_v128256 (5 full rounds)")
+    for r in range(5):
         x = workloads.chain_workload("chain_b256_v128256", r, DEV)
-        sample = None if r == 0 else np.sort(g.choice(256, 64, replace=False))
-        _run_and_check(sd, rep, x, sample=sample)
+        _run_and_check(sd, rep, x)
         del x
     _finish(rep)
 
 
-def test_chain_b256_v128256_sigma075_sampled(sd):
-    rep = ParityReport("chain_b256_v128256_s075 (1 round, 128 sequences)")
-    x = workloads.chain_workload("chain_b256_v128256_s075", 0, DEV)
-    _run_and_check(sd, rep, x, sample=np.arange(0, 256, 2))
+def test_chain_b256_v128256_sigma075_full_rounds(sd):
+    rep = ParityReport("chain_b256_v128256_s075 (5 full rounds)")
+    for r in range(5):
+        x = workloads.chain_workload("chain_b256_v128256_s075", r, DEV)
+        _run_and_check(sd, rep, x)
+        del x
     _finish(rep)
 
 
-def test_chain_b512_v152064_full_size_sampled(sd):
-    rep = ParityReport("chain_b512_v152064 (2 rounds, full size, 96 sequences each)")
-    g = np.random.default_rng(1)
-    for r in range(2):
+def test_chain_b512_v152064_full_rounds(sd):
+    """Three full-size launches of the B=512 fp32 workload, every sequence checked."""
+    rep = ParityReport("chain_b512_v152064 (3 full rounds)")
+    for r in range(3):
         x = workloads.chain_workload("chain_b512_v152064", r, DEV)
-        _run_and_check(sd, rep, x, sample=np.sort(g.choice(512, 96, replace=False)))
+        _run_and_check(sd, rep, x)
         del x
         torch.cuda.empty_cache()
     _finish(rep)
@@ -110,7 +111,7 @@ def test_chain_ragged_shapes(sd, B, gamma, V, dtype):
                                         recipe="spikes", scale=2.0, n_spikes=min(3, V), spike=4.0,
                                         noise=0.7, temps="uniform:0.0:1.5")
         _run_and_check(sd, rep, x, workers=1)
-    _finish(rep)
+    _finish(rep, budget=False)  # a few dozen rows per shape: flags reported, not bounded
 
 
 def test_greedy_call_matches_oracle(sd):

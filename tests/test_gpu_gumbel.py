@@ -2,8 +2,8 @@
 against the oracle (Art of Guessing, "Gumbel coupling"), through the C ABI.
 
 Both sides regenerate the same Philox4x32-10 noise, so every uniform is bit-identical;
-the scores are float32 on both sides, but the logarithms come from different math
-libraries, so two entries whose scores lie within GAP_TOL of each other may swap.  Rules:
+the oracle forms the scores in float64 and the kernels in float32, so two entries whose
+scores lie within GAP_TOL of each other may swap.  Rules:
 status bits and greedy rows bit-exact; a sampled token (draft or target) may differ only
 where the oracle's top-two score gap at that row is below GAP_TOL (flagged); the round
 then follows from the tokens.
@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import workloads
+from parity import assert_flag_budget
 
 pytestmark = pytest.mark.gpu
 
@@ -65,7 +66,7 @@ def check_rounds(rep, L, drafts, T, seed, gpu, idx):
     for b in idx:
         o = so.verify_gumbel_sequence(L[b], drafts[b], float(T[b]), seed, b)
         rep.seqs += 1
-        rep.rows += max(o["J"], 0) + 1
+        rep.rows += len(o["tokens"])  # gamma + 1 rows per sequence, as in the chain rule
         if int(g_s[b]) != o["status"]:
             rep.fail(f"seq {b}: status gpu {int(g_s[b])} oracle {o['status']}")
             continue
@@ -111,13 +112,13 @@ def test_gumbel_round_shapes(sd, B, gamma, V, dtype):
     assert rep.flagged <= 1
 
 
-def test_gumbel_b256_v128256_full_size_sampled(sd):
-    """A full-size launch; the oracle drafts and checks 24 sampled sequences, the GPU
-    drafter the rest."""
-    rep = Report("gumbel chain_b256_v128256 (1 round, 24 sequences)")
+def test_gumbel_b256_v128256_full_round(sd):
+    """A full-size launch; the oracle drafts and checks every sequence (the drafts the GPU
+    verifies are the oracle's), and at most 1e-4 of the rows may be flagged."""
+    rep = Report("gumbel chain_b256_v128256 (1 full round)")
     x = workloads.chain_workload("chain_b256_v128256", 0, DEV)
     seed = 2024
-    idx = sorted(np.random.default_rng(0).choice(256, 24, replace=False).tolist())
+    idx = list(range(256))
     q = x["draft_probs"]
     od = oracle_drafts({b: _np(q[b]) for b in idx}, seed, idx)
     drafts = sd.gumbel_draft(q, seed).clone()
@@ -131,6 +132,7 @@ def test_gumbel_b256_v128256_full_size_sampled(sd):
     check_rounds(rep, Lfull, {b: od[b]["drafts"] for b in idx}, T, seed, out, idx)
     rep.finish()
     assert rep.accepted > 0
+    assert_flag_budget(rep.flagged, rep.rows, (rep.flagged, rep.rows))
 
 
 def test_gumbel_errors_follow_the_rows_read(sd):
@@ -200,3 +202,17 @@ def test_gumbel_deterministic(sd):
     for k in a:
         assert torch.equal(a[k], b[k])
     assert torch.equal(d, sd.gumbel_draft(x["draft_probs"], 3))
+
+
+def test_noise_at_the_zero_known_answer(sd):
+    """Counter (0, 0, 0, 0) under key (0, 0) is the first published Philox4x32-10
+    known-answer vector (Random123, Salmon et al., SC 2011): seed 0, sequence 0, row 0,
+    entries 0..3 of the library's noise come from those four words."""
+    from pathlib import Path
+    line = next(l for l in (Path(__file__).resolve().parent / "golden" / "philox4x32_10_kat.txt")
+                .read_text().splitlines() if l.startswith("kat = 00000000 00000000 00000000 00000000 00000000 00000000"))
+    words = np.array([int(t, 16) for t in line.split("=", 1)[1].split()[6:10]], dtype=np.float64)
+    u = (np.floor(words / 512.0) + 0.5) * 2.0 ** -23
+    want = -np.log2(-np.log1p(u - 1.0))
+    g = _np(sd.gumbel_noise(0, 1, 1, 4, device=DEV)).reshape(-1)
+    assert np.max(np.abs(g - want)) < 4e-6, (g, want)

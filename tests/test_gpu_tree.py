@@ -9,7 +9,7 @@ import torch
 import workloads
 from golden import read_fixture
 from oracle import specdec_oracle as so
-from parity import FLAG_TOL
+from parity import FLAG_TOL, assert_flag_budget
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -67,7 +67,7 @@ def _check_tree(gpu, x, D, stats):
 def test_tree_b32_n64_v32000(sd, medusa64):
     parents, paths = medusa64
     stats = {"sequences": 0, "flagged": 0, "accepted": 0}
-    for r in range(25):
+    for r in range(100):
         x = workloads.tree_workload("tree_b32_n64_v32000", parents, paths, r, DEV)
         out = sd.verify_tree(x["logits"], x["node_tokens"], x["parents"], x["temperatures"], x["uniforms"], 4)
         torch.cuda.synchronize()
@@ -75,8 +75,8 @@ def test_tree_b32_n64_v32000(sd, medusa64):
     path = os.environ.get("SPECDEC_PARITY_REPORT")
     if path:
         with open(path, "a") as f:
-            f.write(json.dumps({"workload": "tree_b32_n64_v32000 (25 rounds)", **stats}) + "\n")
-    assert stats["flagged"] <= max(1, 1e-4 * stats["sequences"] * 5)
+            f.write(json.dumps({"workload": "tree_b32_n64_v32000 (100 rounds)", **stats}) + "\n")
+    assert_flag_budget(stats["flagged"], stats["sequences"] * 5, stats)  # up to D + 1 = 5 draws a walk
     assert stats["accepted"] > 0
 
 

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads
-from parity import ParityReport, check_chain, run_oracle_chain
+from parity import ParityReport, assert_flag_budget, check_chain, run_oracle_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -48,14 +48,15 @@ def _run_and_check(sd, rep, x, gammas, sample=None, workers=None):
     return out
 
 
-def _finish(rep, max_flag_fraction=None):
+def _finish(rep, budget=True):
+    """No hard failure; on a measured workload (budget) the stated flag bound as well."""
     path = os.environ.get("SPECDEC_PARITY_REPORT")
     if path:
         with open(path, "a") as f:
             f.write(json.dumps(dict(rep.summary(), rule="varlen")) + "\n")
     assert not rep.failures, rep.failures[:10]
-    if max_flag_fraction is not None:
-        assert rep.flagged <= max(1, max_flag_fraction * rep.rows), rep.summary()
+    if budget:
+        assert_flag_budget(rep.flagged, rep.rows, rep.summary())
 
 
 def test_varlen_b64_v32000_rounds(sd):
@@ -63,13 +64,13 @@ def test_varlen_b64_v32000_rounds(sd):
     for r in range(30):
         x = workloads.chain_workload("chain_b64_v32000", r, DEV)
         _run_and_check(sd, rep, x, _gammas(64, 4, r))
-    _finish(rep, 1e-4)
+    _finish(rep)
 
 
-def test_varlen_b256_v128256_full_size_sampled(sd):
-    rep = ParityReport("varlen chain_b256_v128256 (1 round, 64 sequences)")
+def test_varlen_b256_v128256_full_round(sd):
+    rep = ParityReport("varlen chain_b256_v128256 (1 full round)")
     x = workloads.chain_workload("chain_b256_v128256", 1, DEV)
-    _run_and_check(sd, rep, x, _gammas(256, 7, 9), sample=np.sort(np.random.default_rng(4).choice(256, 64, False)))
+    _run_and_check(sd, rep, x, _gammas(256, 7, 9))
     _finish(rep)
 
 
@@ -80,7 +81,7 @@ def test_varlen_shapes(sd, B, gamma, V, dtype):
         x = workloads.make_chain_inputs(B, gamma, V, dtype, seed=seed, device=DEV, recipe="spikes", scale=2.0,
                                         n_spikes=3, spike=4.0, noise=0.7, temps="uniform:0.0:1.5")
         _run_and_check(sd, rep, x, _gammas(B, gamma, 100 + seed), workers=1)
-    _finish(rep)
+    _finish(rep, budget=False)  # a few dozen rows per shape: flags reported, not bounded
 
 
 def test_full_counts_equal_the_chain_call(sd):
