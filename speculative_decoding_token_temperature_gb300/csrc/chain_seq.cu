@@ -33,6 +33,7 @@
 // memory) and plain loads for single elements.
 
 #include <climits>
+#include <type_traits>
 
 #include "specdec_device.cuh"
 #include "specdec_internal.h"
@@ -46,12 +47,6 @@ constexpr float kNaN = __builtin_nanf("");
 constexpr int kWarpsPerGroup = kSeqWarps / kSeqGroups;
 constexpr int kGroupThreads = kWarpsPerGroup * 32;
 constexpr int kC = kSeqCluster;
-// Copies a warp keeps in flight for a draw task (a row task keeps kSeqStages).  While both
-// stream, the rows -- the chains, which are the critical path -- get the larger share of
-// the bandwidth; the draws fill in behind them.  A draw taken while other teams wait for
-// work (the machine has bandwidth to spare) keeps kSeqStages too.
-constexpr int kSeqDrawStages = 2;
-static_assert(kSeqDrawStages >= 1 && kSeqDrawStages <= kSeqStages, "draw copies use the row stages");
 static_assert(kSeqWarps % kSeqGroups == 0, "groups must split the warps evenly");
 static_assert(kC >= 1 && kC <= 8, "portable cluster sizes only");
 
@@ -95,20 +90,15 @@ __device__ __forceinline__ bool group_any(int group, bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ int warp_max_int(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
   return v;
@@ -164,29 +154,58 @@ template <> struct Group<float> {
   }
 };
 
-// Residual (or target) weights of 4 consecutive elements and their fp32 running sum in
-// index order; the chunk masses and the final scan both use it.  nmc = -rnd(m_J * c);
-// with q == 0 (the bonus row, or a zero residual) the weights are p itself.
+// Geometry of a draw task's copies: kElems elements of the drawn row per copy (logits at
+// the stage's start, q at kLB), in kStages stages of kSeqDrawStageBytes that reuse a warp's
+// row stages; each lane takes kGPL groups of 4 elements of a copy.
+template <typename T> struct DrawGeo {
+  static constexpr int kElems = sizeof(T) == 2 ? kSeqDrawElemsBf16 : kSeqDrawElemsF32;
+  static constexpr int kLB = kElems * static_cast<int>(sizeof(T));
+  static constexpr int kStages = kSeqStages * kSeqChunkBytes / kSeqDrawStageBytes;
+  static constexpr int kGPL = kElems / 4 / 32;
+  static_assert(kElems * (static_cast<int>(sizeof(T)) + 4) == kSeqDrawStageBytes, "logits and q fill a stage");
+  static_assert(kStages >= 2, "two draw copies in flight per warp");
+  static_assert(kElems % 128 == 0 && kLB % 16 == 0, "whole groups per lane, 16-byte copies");
+};
+
+// max(p - q, 0) with p = e * invZ, in one rounding (a saturating fused multiply-add; for a
+// draft probability q >= 0 and p <= 1 the clamp at 1 never binds).
+__device__ __forceinline__ float resid(float e, float invZ, float q) {
+  float w;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(w) : "f"(e), "f"(invZ), "f"(-q));
+  return w;
+}
+// Three-input minimum (NaN ignored) and NaN-propagating maximum.
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float y;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Residual (or target) weights w of 4 consecutive elements: w_k = max(p_k - q_k, 0), p_k =
+// 2^(l_k c - rnd(m_J c)) / Z (nmc = -rnd(m_J c)); q == 0 (the bonus row, or a zero
+// residual) leaves p itself.  Returns the group's mass (w0 + w2) + (w1 + w3); the chunk
+// masses and the final search both take this sum.
 template <typename T>
 __device__ __forceinline__ float group_weights(const typename Group<T>::L& lw, const float4& q4, float nmc,
-                                               float c, float invZ, bool no_q, float (&w)[4]) {
+                                               float c, float invZ, float (&w)[4]) {
   float l[4];
   Group<T>::unpack(lw, l);
-  const unsigned long long c2 = f2pack(c, c), nmc2 = f2pack(nmc, nmc), niz2 = f2pack(-invZ, -invZ);
-  const unsigned long long q01 = no_q ? 0ull : f2pack(q4.x, q4.y), q23 = no_q ? 0ull : f2pack(q4.z, q4.w);
-  float acc = 0.f;
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    float y0, y1;
-    f2unpack(f2fma(f2pack(l[2 * p], l[2 * p + 1]), c2, nmc2), y0, y1);
-    float r0, r1;  // q - p
-    f2unpack(f2fma(f2pack(ex2(y0), ex2(y1)), niz2, p == 0 ? q01 : q23), r0, r1);
-    w[2 * p] = fmaxf(-r0, 0.f);
-    w[2 * p + 1] = fmaxf(-r1, 0.f);
-    acc += w[2 * p];
-    acc += w[2 * p + 1];
-  }
-  return acc;
+  const unsigned long long c2 = f2pack(c, c), nmc2 = f2pack(nmc, nmc);
+  float y0, y1, y2, y3;
+  f2unpack(f2fma(f2pack(l[0], l[1]), c2, nmc2), y0, y1);
+  f2unpack(f2fma(f2pack(l[2], l[3]), c2, nmc2), y2, y3);
+  w[0] = resid(ex2(y0), invZ, q4.x);
+  w[1] = resid(ex2(y1), invZ, q4.y);
+  w[2] = resid(ex2(y2), invZ, q4.z);
+  w[3] = resid(ex2(y3), invZ, q4.w);
+  float s0, s1;
+  f2unpack(f2add(f2pack(w[0], w[1]), f2pack(w[2], w[3])), s0, s1);
+  return s0 + s1;
 }
 
 // Shared state of one group (one team member).  Its layout is the same in every CTA, so
@@ -197,9 +216,10 @@ struct GroupShared {
   float4 mbox[2][2];            // the next task's 32-byte entry, by task parity
   uint64_t mbar_box[2];         // their mbarriers
   RowSum wsum[kWarpsPerGroup];  // per-warp row summaries
+  float4 ahead;                 // a row's statistics computed ahead, as read from the workspace
   // per task parity: draft token bits, its logit, its q, u_i, u_gamma, input error bits
   float gq[2][8];
-  float mass[2][kSeqMaxDrawChunks];  // draw: mass per chunk of this member's part, by task parity
+  long long mass[2][kSeqMaxDrawChunks];  // draw: mass per chunk of this member's part (fixed point), by task parity
 };
 
 // This group's side of a team: its member index and the exchange sequence number.
@@ -237,16 +257,28 @@ __device__ int exchange(GroupShared& gs, Team& tm, const float4& mine, int group
   return par;
 }
 
-// One warp's bulk-copy pipeline: kSeqStages stages of kSeqChunkBytes in shared memory.
-// `k` counts completed stages and `issued` issued ones, over the kernel's lifetime.
+// One warp's bulk-copy pipeline in its kSeqStages * kSeqChunkBytes of shared memory: a
+// row task cuts it into kSeqStages stages of kSeqChunkBytes, a draw task into
+// DrawGeo<T>::kStages stages of kSeqDrawStageBytes.  Stage s completes on barrier s.  A
+// task consumes every copy it issues, so the pipe is empty between tasks and each task
+// starts its stages at 0 (begin()); `phase` keeps every barrier's parity across tasks.
 struct Pipe {
   unsigned char* buf;
   uint64_t* bar;
-  uint32_t k = 0, issued = 0;
+  uint32_t k = 0, issued = 0;  // copies consumed and issued by the current task
+  uint32_t phase = 0;          // bit s: parity of barrier s's next phase
+  uint32_t si = 0, sk = 0;     // stages of the next copy to issue and to consume
+  uint32_t nst = kSeqStages, sbytes = kSeqChunkBytes;
   bool ok = true;  // false once a bounded wait gave up
 
-  __device__ __forceinline__ unsigned char* stage(uint32_t i) { return buf + (i % kSeqStages) * kSeqChunkBytes; }
-  __device__ __forceinline__ uint64_t* sbar(uint32_t i) { return bar + (i % kSeqStages); }
+  __device__ __forceinline__ void begin(uint32_t stages, uint32_t stage_bytes) {
+    nst = stages;
+    sbytes = stage_bytes;
+    k = issued = 0;
+    si = sk = 0;
+  }
+  __device__ __forceinline__ unsigned char* stage(uint32_t s) { return buf + s * sbytes; }
+  __device__ __forceinline__ unsigned char* cur() { return stage(sk); }
   __device__ __forceinline__ uint32_t in_flight() const { return issued - k; }
   // Issue one copy group (one or two copies) into the next stage: bulk copies by one lane,
   // or (kHost) 16-byte copies by every lane, each of which then arrives on the stage's
@@ -254,8 +286,8 @@ struct Pipe {
   // __syncwarp) before the copy.
   template <bool kHost>
   __device__ __forceinline__ void issue(const void* a, uint32_t na, const void* b, uint32_t nb, int off_b, int lane) {
-    uint64_t* br = sbar(issued);
-    unsigned char* dst = stage(issued);
+    uint64_t* br = bar + si;
+    unsigned char* dst = stage(si);
     if constexpr (kHost) {
       const char* ca = static_cast<const char*>(a);
       const char* cb = static_cast<const char*>(b);
@@ -268,11 +300,21 @@ struct Pipe {
       bulk_copy_g2s(dst, a, na, br);
       if (nb) bulk_copy_g2s(dst + off_b, b, nb, br);
     }
+    si = (si + 1 == nst) ? 0u : si + 1;
+    ++issued;
   }
-  __device__ __forceinline__ bool wait() { return mbar_wait(sbar(k), (k / kSeqStages) & 1u); }
+  // Wait for the oldest copy in flight; consume() then releases its stage.
+  __device__ __forceinline__ bool wait() { return mbar_wait(bar + sk, (phase >> sk) & 1u); }
+  __device__ __forceinline__ void consume() {
+    phase ^= 1u << sk;
+    sk = (sk + 1 == nst) ? 0u : sk + 1;
+    ++k;
+  }
 };
 
-enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3 };
+// kTaskAhead: the statistics of a row that its chain's team will reach later, computed
+// by a team that would otherwise wait for work and left in the workspace for the chain.
+enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3, kTaskAhead = 4 };
 
 // A task entry: 32 bytes, in the global rings and in a team's mailbox.
 //   e0 = (sequence b (-1: no more work), row | kind << 8 | warnings << 16, m, Z)
@@ -282,7 +324,6 @@ enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3 };
 struct Entry {
   int b, row, kind, warn;
   float m, Z, T;
-  int deep = 0;  // a draw taken while teams wait for work: all kSeqStages copies in flight
 };
 __device__ __forceinline__ void pack_entry(const Entry& e, float4& e0, float4& e1) {
   e0 = make_float4(__int_as_float(e.b), __int_as_float(e.row | (e.kind << 8) | (e.warn << 16)), e.m, e.Z);
@@ -298,7 +339,6 @@ __device__ __forceinline__ Entry unpack_entry(const float4& e0, const float4& e1
   e.m = e0.z;
   e.Z = e0.w;
   e.T = e1.x;
-  e.deep = __float_as_int(e1.y);
   return e;
 }
 
@@ -326,14 +366,18 @@ struct Queue {
   unsigned *start_ticket, *pub_draws, *draw_ticket, *finished;
   int* ready_draws;
   float4* ring_draws;
-  int B;
+  int B, cap;
 };
 constexpr int kDrawTag = 1 << 30;
 
-__device__ __forceinline__ int take_ticket(const Queue& q) {
-  if (ld_relaxed(q.start_ticket) < static_cast<unsigned>(q.B)) {
-    const unsigned s = atomicAdd(q.start_ticket, 1u);
+// A ticket for the team's next task.  `pre` is a start ticket the leader already took
+// (UINT_MAX: none); once a start ticket comes back past the last sequence, the team
+// (starts_left false) takes only draw tickets.
+__device__ __forceinline__ int take_ticket(const Queue& q, unsigned pre, bool& starts_left) {
+  if (starts_left) {
+    const unsigned s = pre != UINT_MAX ? pre : atomicAdd(q.start_ticket, 1u);
     if (s < static_cast<unsigned>(q.B)) return static_cast<int>(s);
+    starts_left = false;
   }
   return kDrawTag | static_cast<int>(atomicAdd(q.draw_ticket, 1u));
 }
@@ -356,13 +400,10 @@ __device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, floa
   const int d = tk & ~kDrawTag;
   uint64_t t0 = 0;
   for (;;) {
-    if (d < 2 * q.B && ld_acquire(q.ready_draws + d) != 0) {
+    if (d < q.cap && ld_acquire(q.ready_draws + d) != 0) {
       const float4* ent = q.ring_draws + 2 * static_cast<int64_t>(d);
       e0 = __ldcg(ent);
       e1 = __ldcg(ent + 1);
-      // teams waiting for work: the machine has bandwidth to spare, stream the draw deep
-      const int idle = static_cast<int>(ld_relaxed(q.draw_ticket) - ld_relaxed(q.pub_draws));
-      e1.y = __int_as_float(idle > 0 ? 1 : 0);
       return 1;
     }
     if (ld_relaxed(q.finished) >= static_cast<unsigned>(q.B)) return -1;
@@ -382,6 +423,30 @@ __device__ void publish_draw(const Queue& q, const Entry& e) {
   st_release(q.ready_draws + k, 1);
 }
 
+// Rows lo..hi of sequence b for teams that wait for work (one entry each, published in one
+// batch).  The chain's team waits for their statistics instead of streaming them itself.
+__device__ void publish_ahead(const Queue& q, int b, int lo, int hi, float T) {
+  const unsigned k0 = atomicAdd(q.pub_draws, static_cast<unsigned>(hi - lo + 1));
+  for (int r = lo; r <= hi; ++r) {
+    const unsigned k = k0 + static_cast<unsigned>(r - lo);
+    if (k >= static_cast<unsigned>(q.cap)) break;  // cannot happen: each row is published at most once
+    Entry e;
+    e.b = b;
+    e.row = r;
+    e.kind = kTaskAhead;
+    e.warn = 0;
+    e.m = 0.f;
+    e.Z = 1.f;
+    e.T = T;
+    float4 e0, e1;
+    pack_entry(e, e0, e1);
+    float4* ent = q.ring_draws + 2 * static_cast<int64_t>(k);
+    __stcg(ent, e0);
+    __stcg(ent + 1, e1);
+    st_release(q.ready_draws + k, 1);
+  }
+}
+
 // The team leader hands a task entry to every member's mailbox of the given parity.
 __device__ __forceinline__ void send_entry(GroupShared& gs, int par, const float4& e0, const float4& e1) {
   const uint32_t sa = smem_addr(&gs.mbox[par][0]);
@@ -394,8 +459,9 @@ __device__ __forceinline__ void send_entry(GroupShared& gs, int par, const float
 }
 
 // This member's copies of one task: the logits row (or drawn row) and, for a residual
-// draw, the q row; the member's chunk range [lo, hi) (4 KB chunks for a row, 512-element
-// chunks for a draw); this warp's jobs are the chunks lo + gwarp, lo + gwarp + W, ...
+// draw, the q row; the member's chunk range [lo, hi) (4 KB chunks for a row,
+// DrawGeo<T>::kElems-element chunks for a draw); this warp's jobs are the chunks
+// lo + gwarp, lo + gwarp + W, ...
 struct Task {
   int kind = 0;
   const char* src = nullptr;
@@ -406,21 +472,18 @@ struct Task {
 template <typename T, bool kHost>
 __device__ __forceinline__ void issue_job(Pipe& pp, const Task& t, int j, int gwarp, int lane, int V,
                                           int64_t row_bytes) {
-  constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
-  if (kHost || lane == 0) {
-    const int ch = t.lo + gwarp + j * kWarpsPerGroup;
-    if (t.kind == kTaskRow) {
-      const uint32_t nb = static_cast<uint32_t>(
-          min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes));
-      pp.issue<kHost>(t.src + static_cast<int64_t>(ch) * kSeqChunkBytes, nb, nullptr, 0, 0, lane);
-    } else {
-      const int n = min(kSeqDrawChunk, V - ch * kSeqDrawChunk);
-      const int64_t off = static_cast<int64_t>(ch) * kSeqDrawChunk;
-      pp.issue<kHost>(t.src + off * static_cast<int64_t>(sizeof(T)), static_cast<uint32_t>(n) * sizeof(T),
-                      t.q ? t.q + off : nullptr, t.q ? static_cast<uint32_t>(n) * 4u : 0u, LB, lane);
-    }
+  using DG = DrawGeo<T>;
+  const int ch = t.lo + gwarp + j * kWarpsPerGroup;
+  if (t.kind == kTaskRow) {
+    const uint32_t nb = static_cast<uint32_t>(
+        min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes));
+    pp.issue<kHost>(t.src + static_cast<int64_t>(ch) * kSeqChunkBytes, nb, nullptr, 0, 0, lane);
+  } else {
+    const int n = min(DG::kElems, V - ch * DG::kElems);
+    const int64_t off = static_cast<int64_t>(ch) * DG::kElems;
+    pp.issue<kHost>(t.src + off * static_cast<int64_t>(sizeof(T)), static_cast<uint32_t>(n) * sizeof(T),
+                    t.q ? t.q + off : nullptr, t.q ? static_cast<uint32_t>(n) * 4u : 0u, DG::kLB, lane);
   }
-  ++pp.issued;
 }
 
 // One 4 KB chunk of a row into this lane's running (max, sum, argmax).
@@ -430,12 +493,15 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
   constexpr int VEC = Vec<T>::n;
   constexpr int VPL = kSeqChunkBytes / 16 / 32;
   constexpr int EPC = kSeqChunkBytes / static_cast<int>(sizeof(T));
-  // chunk maximum of this lane
+  // chunk maximum of this lane (bf16: per 16-byte vector first, kept for the argmax search)
   float mt;
+  uint32_t mv[VPL];
   if constexpr (sizeof(T) == 2) {
-    uint32_t mm = kNegInfBf16x2;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) mm = bf2max(bf2max(mm, w[j].x), bf2max(bf2max(w[j].y, w[j].z), w[j].w));
+    for (int j = 0; j < VPL; ++j) mv[j] = bf2max(bf2max(w[j].x, w[j].y), bf2max(w[j].z, w[j].w));
+    uint32_t mm = mv[0];
+#pragma unroll
+    for (int j = 1; j < VPL; ++j) mm = bf2max(mm, mv[j]);
     mt = max_nan(bf16_lo(mm), bf16_hi(mm));
   } else {
     mt = -kInf;
@@ -445,18 +511,47 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
                                max_nan(__uint_as_float(w[j].z), __uint_as_float(w[j].w))));
   }
   if (greedy) {
-    // strictly larger maximum: locate its first index in this chunk (earlier chunks keep ties)
+    // strictly larger maximum: locate its first index in this chunk (earlier chunks keep
+    // ties).  Entries past the row's end hold -inf and never equal a larger maximum; a
+    // NaN maximum matches nothing (the row is an input error).
     if (mt > ml || (mt != mt && ml == ml)) {
       int idx = INT_MAX;
+      if (sizeof(T) == 2 && mt != 0.f) {
+        // bf16: mt is one of the lane's values, so match its 16-bit pattern (zero is left to
+        // the comparison below, where -0 and +0 are equal): the first 16-byte vector whose
+        // per-vector maximum holds it, then the first half-word inside that vector
+        const uint32_t p16 = __float_as_uint(mt) >> 16, pat = p16 | (p16 << 16);
+        auto zero_half = [](uint32_t x) { return (x - 0x00010001u) & ~x & 0x80008000u; };
+        int jv = VPL;
+        uint4 hv = w[VPL - 1];
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+        for (int j = VPL - 1; j >= 0; --j) {
+          if (zero_half(mv[j] ^ pat)) {
+            jv = j;
+            hv = w[j];
+          }
+        }
+        if (jv < VPL) {
+          const uint32_t ww[4] = {hv.x, hv.y, hv.z, hv.w};
+          int e = VEC;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          float v;
-          if constexpr (sizeof(T) == 2) v = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
-          else v = __uint_as_float(ww[e]);
-          if (idx == INT_MAX && v == mt && lane + 32 * j < nv) idx = ch * EPC + (lane + 32 * j) * VEC + e;
+          for (int q = 3; q >= 0; --q) {
+            const uint32_t z = zero_half(ww[q] ^ pat);  // the lowest set half is exact
+            if (z) e = 2 * q + ((z & 0x8000u) ? 0 : 1);
+          }
+          if (e < VEC) idx = ch * EPC + (lane + 32 * jv) * VEC + e;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            float v;
+            if constexpr (sizeof(T) == 2) v = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
+            else v = __uint_as_float(ww[e]);
+            if (idx == INT_MAX && v == mt) idx = ch * EPC + (lane + 32 * j) * VEC + e;
+          }
         }
       }
       ml = mt;
@@ -498,21 +593,51 @@ __device__ __forceinline__ void row_chunk(const uint4 (&w)[kSeqChunkBytes / 512]
   }
 }
 
-// fp32 scan of this member's chunk masses (first warp): each lane sums a contiguous run
-// of chunks.  The search repeats exactly this arithmetic, so the member's total and the
+// The draw's running masses are exact sums in 64-bit fixed point, units of 2^-52 (every
+// weight and mass is at most about 1): fp32 running sums would round at a few 1e-8 of S,
+// and move draws whose uniform falls that close to a boundary of the CDF.  fx() is the one
+// rounding, of each lane's fp32 sum of its weights in a chunk (mass pass) or of each
+// weight (search) into these units.
+__device__ __forceinline__ long long fx(float x) {
+  // x >= 0 (weights and masses): x = m * 2^(e - 150) is m * 2^(e - 98) units, from the bits
+  // with integer shifts (values below 2^-29 are truncated to whole units)
+  const uint32_t b = __float_as_uint(x);
+  const int e = static_cast<int>(b >> 23);
+  const unsigned long long m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  const int sh = (e ? e : 1) - 98;
+  if (sh >= 0) return static_cast<long long>(m << sh);
+  return sh > -64 ? static_cast<long long>(m >> -sh) : 0;
+}
+// u * S exactly, floored to the units (u in [0, 1) from its fp32 bits): for integer C,
+// C > floor(u * S) holds exactly when C > u * S.
+__device__ __forceinline__ long long fx_target(float u, long long S) {
+  if (!(u > 0.f) || S <= 0) return 0;
+  const uint32_t ub = __float_as_uint(u);
+  const int e = static_cast<int>(ub >> 23);                 // biased exponent (u < 1: e <= 126)
+  const unsigned long long m = e ? ((ub & 0x7FFFFFu) | 0x800000u) : (ub & 0x7FFFFFu);
+  const int sh = 150 - (e ? e : 1);                          // u = m * 2^-sh, sh >= 24
+  const unsigned long long us = static_cast<unsigned long long>(S);
+  const unsigned long long lo = us * m, hi = __umul64hi(us, m);
+  if (sh >= 128) return 0;
+  if (sh >= 64) return static_cast<long long>(hi >> (sh - 64));
+  return static_cast<long long>((lo >> sh) | (hi << (64 - sh)));
+}
+
+// Scan of this member's chunk masses (first warp): each lane sums a contiguous run of
+// chunks.  The search repeats exactly this arithmetic, so the member's total and the
 // search's running prefixes agree to the bit.
 struct LocalScan {
   int c0, c1;
-  float mine, incl, total;
+  long long mine, incl, total;
 };
-__device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int lane) {
+__device__ __forceinline__ LocalScan local_scan(const long long* mass, int n, int lane) {
   LocalScan s;
   const int cpl = (n + 31) / 32;
   s.c0 = min(lane * cpl, n);
   s.c1 = min(s.c0 + cpl, n);
-  s.mine = 0.f;
+  s.mine = 0;
   for (int q = s.c0; q < s.c1; ++q) s.mine += mass[q];
-  s.incl = warp_incl_scan(s.mine, lane);
+  s.incl = warp_incl_scan_ll(s.mine, lane);
   s.total = __shfl_sync(0xffffffffu, s.incl, 31);
   return s;
 }
@@ -522,16 +647,17 @@ __device__ __forceinline__ LocalScan local_scan(const float* mass, int n, int la
 // `target`, then the element inside it.  If rounding leaves no such element, the last
 // positive-weight element of the part is taken.
 template <typename T, bool kHost>
-__device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, float base, float target,
-                            float mJ, float c, float invZ, bool no_q, const float* mass, int lane) {
+__device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int n, long long base, long long target,
+                            float mJ, float c, float invZ, bool no_q, const long long* mass, int lane) {
   using GL = typename Group<T>::L;
-  constexpr int GPL = kSeqDrawChunk / 4 / 32;
+  constexpr int GPL = DrawGeo<T>::kGPL;
+  constexpr int CH = DrawGeo<T>::kElems;
   const LocalScan s = local_scan(mass, n, lane);
   int cstar = -1, lastpos = -1;
-  float cbase = 0.f, prelast = 0.f, pre = base + (s.incl - s.mine);
+  long long cbase = 0, prelast = 0, pre = base + (s.incl - s.mine);
   for (int q = s.c0; q < s.c1; ++q) {
-    const float w = mass[q];
-    if (w > 0.f) { lastpos = q; prelast = pre; }
+    const long long w = mass[q];
+    if (w > 0) { lastpos = q; prelast = pre; }
     if (cstar < 0 && pre + w > target) { cstar = q; cbase = pre; }
     pre += w;
   }
@@ -546,20 +672,23 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
     cstar = best < 0 ? 0 : best;
     cbase = owner ? __shfl_sync(0xffffffffu, prelast, __ffs(owner) - 1) : base;
   }
-  const int k0 = (d0 + cstar) * kSeqDrawChunk;
-  const int ng = min(kSeqDrawChunk, V - k0) / 4;
-  float w[GPL][4], gsum[GPL];
-  float lane_tot = 0.f;
+  const int k0 = (d0 + cstar) * CH;
+  const int ng = min(CH, V - k0) / 4;
+  float w[GPL][4];
+  long long gsum[GPL];  // a group's mass: the sum of its weights' units
+  long long lane_tot = 0;
 #pragma unroll
   for (int j = 0; j < GPL; ++j) {
     const int g = lane * GPL + j;
-    gsum[j] = 0.f;
+    gsum[j] = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) w[j][e] = 0.f;
     if (g < ng) {
       const GL lw = load_in<kHost>(reinterpret_cast<const GL*>(lrow + k0) + g);
       const float4 q4 = no_q ? make_float4(0.f, 0.f, 0.f, 0.f) : load_in<kHost>(reinterpret_cast<const float4*>(qrow + k0) + g);
-      gsum[j] = group_weights<T>(lw, q4, -__fmul_rn(mJ, c), c, invZ, no_q, w[j]);
+      group_weights<T>(lw, q4, -__fmul_rn(mJ, c), c, invZ, w[j]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) gsum[j] += fx(w[j][e]);
       lane_tot += gsum[j];
     }
   }
@@ -569,21 +698,21 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (w[j][e] > 0.f) last_pos = k0 + 4 * (lane * GPL + j) + e;
-  const float gincl = warp_incl_scan(lane_tot, lane);
+  const long long gincl = warp_incl_scan_ll(lane_tot, lane);
   const unsigned ghit = __ballot_sync(0xffffffffu, cbase + gincl > target);
   int y = -1;
   if (ghit) {
     const int fl = __ffs(ghit) - 1;
     if (lane == fl) {
-      float p2 = cbase + (gincl - lane_tot);
+      long long p2 = cbase + (gincl - lane_tot);
 #pragma unroll
       for (int j = 0; j < GPL; ++j) {
         if (y < 0 && p2 + gsum[j] > target) {
-          float run = 0.f;
+          long long run = 0;
           int lastp = -1;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            run += w[j][e];
+            run += fx(w[j][e]);
             if (w[j][e] > 0.f) lastp = k0 + 4 * (lane * GPL + j) + e;
             if (y < 0 && p2 + run > target) y = k0 + 4 * (lane * GPL + j) + e;
           }
@@ -598,12 +727,15 @@ __device__ int local_search(const T* lrow, const float* qrow, int V, int d0, int
   return y;
 }
 
-// A member's draw total (fp32), a flag and the leader's unclaimed sequence as one 16-byte
-// exchange payload.
-__device__ __forceinline__ float4 pack_total(float t, int flag, int bn) {
-  return make_float4(t, 0.f, __int_as_float(flag), __int_as_float(bn));
+// A member's draw total (fixed point, as two words) and a bad-probability flag as one
+// 16-byte exchange payload.
+__device__ __forceinline__ float4 pack_total(long long t, int flag) {
+  return make_float4(__int_as_float(static_cast<int>(t)), __int_as_float(static_cast<int>(t >> 32)),
+                     __int_as_float(flag), 0.f);
 }
-__device__ __forceinline__ float unpack_total(const float4& v) { return v.x; }
+__device__ __forceinline__ long long unpack_total(const float4& v) {
+  return (static_cast<long long>(__float_as_int(v.y)) << 32) | static_cast<unsigned>(__float_as_int(v.x));
+}
 
 // ---------------------------------------------------------------------------------
 // The kernel
@@ -612,8 +744,7 @@ template <typename T, bool kHost>
 __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const ChainParams P) {
   using GL = typename Group<T>::L;
   constexpr int VPL = kSeqChunkBytes / 16 / 32;
-  constexpr int GPL = kSeqDrawChunk / 4 / 32;
-  constexpr int LB = kSeqDrawChunk * static_cast<int>(sizeof(T));
+  constexpr int GPL = DrawGeo<T>::kGPL;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kSeqWarps][kSeqStages];
   __shared__ GroupShared gshared[kSeqGroups];
@@ -649,7 +780,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   const int V = P.V;
   const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(T);
   const int nch = static_cast<int>((row_bytes + kSeqChunkBytes - 1) / kSeqChunkBytes);
-  const int nchd = (V + kSeqDrawChunk - 1) / kSeqDrawChunk;
+  const int nchd = (V + DrawGeo<T>::kElems - 1) / DrawGeo<T>::kElems;
   const int c0 = static_cast<int>(static_cast<int64_t>(nch) * tm.rank / kC);
   const int c1 = static_cast<int>(static_cast<int64_t>(nch) * (tm.rank + 1) / kC);
   const int d0 = static_cast<int>(static_cast<int64_t>(nchd) * tm.rank / kC);
@@ -663,17 +794,18 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   qu.ready_draws = P.ws.ready;
   qu.ring_draws = P.ws.ring;
   qu.B = P.B;
+  qu.cap = P.ws.ring_cap;
 
   // drafts to verify for sequence b: gamma, or its own count (the bonus row is row gb)
   auto gamma_of = [&](int b) { return P.gammas ? __ldg(P.gammas + b) : P.gamma; };
   auto make_task = [&](const Entry& e) {
     Task t;
-    t.kind = e.kind;
+    t.kind = e.kind == kTaskAhead ? kTaskRow : e.kind;
     t.src = logits + (static_cast<int64_t>(e.b) * R + e.row) * row_bytes;
     t.q = (e.kind == kTaskDraw && e.row < gamma_of(e.b)) ? P.q + (static_cast<int64_t>(e.b) * P.gamma + e.row) * V
                                                           : nullptr;
-    t.lo = (e.kind == kTaskRow) ? c0 : d0;
-    t.hi = (e.kind == kTaskRow) ? c1 : d1;
+    t.lo = (t.kind == kTaskRow) ? c0 : d0;
+    t.hi = (t.kind == kTaskRow) ? c1 : d1;
     t.n = (t.hi > t.lo + gwarp) ? (t.hi - t.lo - gwarp + kWarpsPerGroup - 1) / kWarpsPerGroup : 0;
     return t;
   };
@@ -689,11 +821,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   // every member (expect 32 bytes) and filled by one send from the team's leader, who
   // takes a ticket and waits until its entry exists.
   uint32_t mb = 0;
+  bool starts_left = true;  // (leader) start tickets may remain
+  unsigned pre_ticket = UINT_MAX;  // (leader) a start ticket taken while publishing a draw
   auto take_box = [&]() {
     if (first) mbar_expect_tx(&gs.mbar_box[mb & 1u], 32);
     if (leader) {
       float4 e0, e1 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int r = resolve_ticket(P, qu, take_ticket(qu), e0, e1);
+      const int r = resolve_ticket(P, qu, take_ticket(qu, pre_ticket, starts_left), e0, e1);
+      pre_ticket = UINT_MAX;
       if (r < 0) {
         if (r == -2) atomicOr(P.ws.error, 8u);
         e0 = no_more();
@@ -712,10 +847,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
 
   Entry cur = take_box();
   uint32_t t = 0;  // tasks done by this team
-  // a drawn token still to be found by this member's first warp (at the next task's start)
+  // rows ahead_lo..ahead_hi of the team's current chain went to teams that waited for work
+  int ahead_lo = INT_MAX, ahead_hi = -1;
+  // every start ticket is taken (as the leader last reported it; every thread holds it)
+  bool starts_gone = false;
+  // a drawn token for this member to find (its second warp, while the team takes a ticket)
   bool srch = false;
   int s_b = 0, s_J = 0, s_par = 0;
-  float s_base = 0.f, s_target = 0.f;
+  long long s_base = 0, s_target = 0;
   float s_m = 0.f, s_c = 0.f, s_invZ = 1.f;
   bool s_noq = true;
 
@@ -723,20 +862,15 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     const int par = static_cast<int>(t & 1u);
     // the previous task's draw, if this member holds u * S (its masses stay put until the
     // barrier at the end of this task's chunks)
-    if (srch && gwarp == 0) {
-      const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
-      const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
-      const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
-                                    gs.mass[s_par], lane);
-      if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
-    }
-    srch = false;
 
     const int b = cur.b, ri = cur.row, kind = cur.kind;
     const float Tc = cur.T;
     const bool greedy = P.greedy_only || is_greedy(Tc);
     const float c = greedy ? 0.f : kLog2e / Tc;
-    const Task tc = make_task(cur);
+    // a row of this chain whose statistics another team computes: read, not streamed
+    const bool ahead_row = kind == kTaskRow && ri >= ahead_lo && ri <= ahead_hi;
+    Task tc = make_task(cur);
+    if (ahead_row) tc.n = 0;
     const int gb = gamma_of(b);
     const bool gbad = gb < 0 || gb > P.gamma;  // a count of drafts out of range
 
@@ -753,6 +887,13 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         if (!gbad) gug = __ldg(P.u + static_cast<int64_t>(b) * R + gb);
       }
     }
+    // teams waiting for work, seen by the leader as its row starts (sent with its summary)
+    unsigned w_dt = 0, w_pd = 0, w_st = 0;
+    if (leader && kind == kTaskRow && !ahead_row) {
+      w_dt = ld_relaxed(qu.draw_ticket);
+      w_pd = ld_relaxed(qu.pub_draws);
+      w_st = ld_relaxed(qu.start_ticket);
+    }
     auto gather2 = [&]() {
       if (first && !g2) {
         g2 = true;
@@ -763,17 +904,35 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       }
     };
 
-    // This task's copies: kSeqStages in flight for a row (kSeqDrawStages for a draw), one
-    // more as each stage is read.
+    // This task's copies: a copy in every stage (kSeqStages of 4 KB for a row, two of 6 KB
+    // for a draw), one more as each stage is read.
     int ci = 0;
     auto refill = [&]() {
       if (pp.ok && ci < tc.n) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
     };
-    const uint32_t depth = (kind == kTaskRow || cur.deep) ? kSeqStages : kSeqDrawStages;
-    while (pp.ok && ci < tc.n && pp.in_flight() < depth) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+    if (tc.kind == kTaskRow) pp.begin(kSeqStages, kSeqChunkBytes);
+    else pp.begin(DrawGeo<T>::kStages, kSeqDrawStageBytes);
+    while (pp.ok && ci < tc.n && pp.in_flight() < pp.nst) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
-    float4 mine;
-    if (kind == kTaskRow) {
+    float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool ahead_fail = false;
+    if (ahead_row) {
+      // the statistics another team left in the workspace (each member reads them)
+      gather2();
+      if (first) {
+        const int64_t hk = static_cast<int64_t>(b) * R + ri;
+        uint64_t t0 = 0;
+        bool got = true;
+        while (ld_acquire(P.ws.help_ready + hk) == 0) {
+          if (t0 == 0) t0 = global_timer_ns();
+          else if (global_timer_ns() - t0 > kMaxWaitNs) { got = false; break; }
+          __nanosleep(64);
+        }
+        if (got) gs.ahead = __ldcg(P.ws.help + hk);
+        else atomicOr(P.ws.error, 16u);
+        ahead_fail = !got;
+      }
+    } else if (tc.kind == kTaskRow) {
       float ml = -kInf, Zl = 0.f;
       int zl = INT_MAX;
       for (int j = 0; j < tc.n && pp.ok; ++j) {
@@ -785,22 +944,18 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         const int ch = c0 + gwarp + j * kWarpsPerGroup;
         const int nv = static_cast<int>(
             min(static_cast<int64_t>(kSeqChunkBytes), row_bytes - static_cast<int64_t>(ch) * kSeqChunkBytes) / 16);
-        const uint4* vb = reinterpret_cast<const uint4*>(pp.stage(pp.k));
+        const uint4* vb = reinterpret_cast<const uint4*>(pp.cur());
         uint4 w[VPL];
+        if (nv == VPL * 32) {  // a whole chunk
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          const int e = lane + 32 * v;
-          if (e < nv) {
-            w[v] = vb[e];
-          } else if constexpr (sizeof(T) == 2) {
-            w[v] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
-          } else {
-            const uint32_t nf = __float_as_uint(-kInf);
-            w[v] = make_uint4(nf, nf, nf, nf);
-          }
+          for (int v = 0; v < VPL; ++v) w[v] = vb[lane + 32 * v];
+        } else {  // the row's last chunk: -inf past its end
+          constexpr uint32_t nf = sizeof(T) == 2 ? kNegInfBf16x2 : 0xFF800000u;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) w[v] = (lane + 32 * v < nv) ? vb[lane + 32 * v] : make_uint4(nf, nf, nf, nf);
         }
         __syncwarp();
-        ++pp.k;
+        pp.consume();
         refill();
         row_chunk<T>(w, nv, ch, greedy, c, lane, ml, Zl, zl);
         gather2();
@@ -821,50 +976,75 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         if (lane < kWarpsPerGroup) s = gs.wsum[lane];
         s = warp_merge(s, c);
       }
-      mine = make_float4(s.m, s.Z, __int_as_float(s.z), 0.f);
+      // the leader's view of the queues: teams waiting for work, and whether start tickets
+      // may remain (bit 30)
+      const int idle = static_cast<int>(w_dt - w_pd);
+      const bool starts_remain = leader && w_st < static_cast<unsigned>(P.B);
+      const int qv = min(max(idle, 0), (1 << 30) - 1) | (starts_remain ? (1 << 30) : 0);
+      mine = make_float4(s.m, s.Z, __int_as_float(s.z), __int_as_float(qv));
     } else {
       const float nmc = -__fmul_rn(cur.m, c), invZ = 1.f / cur.Z;
-      const bool with_q = tc.q != nullptr;
       float qmx = 0.f, qmn = 0.f;
-      for (int j = 0; j < tc.n && pp.ok; ++j) {
-        if (!pp.wait()) {
-          if (lane == 0) atomicOr(P.ws.error, 1u);
-          pp.ok = false;
-          break;
-        }
-        const int cd = d0 + gwarp + j * kWarpsPerGroup;
-        const int ng = min(kSeqDrawChunk, V - cd * kSeqDrawChunk) / 4;
-        const unsigned char* sbuf = pp.stage(pp.k);
-        GL lw[GPL];
-        float4 qv[GPL];
-#pragma unroll
-        for (int v = 0; v < GPL; ++v) {
-          const int g = lane + 32 * v;
-          if (g < ng) {
-            lw[v] = reinterpret_cast<const GL*>(sbuf)[g];
-            qv[v] = with_q ? reinterpret_cast<const float4*>(sbuf + LB)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+      // the chunks of the drawn row, with or without a q row (the bonus row, or a draw
+      // from p after a zero residual)
+      auto chunks = [&](auto with_q_t) {
+        constexpr bool kWithQ = decltype(with_q_t)::value;
+        using DG = DrawGeo<T>;
+        for (int j = 0; j < tc.n && pp.ok; ++j) {
+          if (!pp.wait()) {
+            if (lane == 0) atomicOr(P.ws.error, 1u);
+            pp.ok = false;
+            break;
           }
-        }
-        __syncwarp();
-        ++pp.k;
-        refill();
-        float sr = 0.f;
+          const int cd = d0 + gwarp + j * kWarpsPerGroup;
+          const int ng = min(DG::kElems, V - cd * DG::kElems) / 4;  // groups of 4 in this chunk
+          const GL* lb = reinterpret_cast<const GL*>(pp.cur());
+          const float4* qb = reinterpret_cast<const float4*>(pp.cur() + DG::kLB);
+          GL lw[GPL];
+          float4 qv[GPL];
+          if (ng == DG::kElems / 4) {  // a whole chunk
 #pragma unroll
-        for (int v = 0; v < GPL; ++v) {
-          if (lane + 32 * v < ng) {
+            for (int v = 0; v < GPL; ++v) {
+              lw[v] = lb[lane + 32 * v];
+              qv[v] = kWithQ ? qb[lane + 32 * v] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          } else {  // the row's last chunk: -inf logits (zero weight) past its end
+#pragma unroll
+            for (int v = 0; v < GPL; ++v) {
+              const bool in = lane + 32 * v < ng;
+              if constexpr (sizeof(T) == 2) lw[v] = in ? lb[lane + 32 * v] : GL{kNegInfBf16x2, kNegInfBf16x2};
+              else lw[v] = in ? lb[lane + 32 * v] : GL{0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u};
+              qv[v] = (kWithQ && in) ? qb[lane + 32 * v] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          __syncwarp();
+          pp.consume();
+          refill();
+          float sr = 0.f;
+#pragma unroll
+          for (int v = 0; v < GPL; ++v) {
             float w4[4];
-            sr += group_weights<T>(lw[v], qv[v], nmc, c, invZ, !with_q, w4);
-            qmx = max_nan(qmx, max_nan(max_nan(qv[v].x, qv[v].y), max_nan(qv[v].z, qv[v].w)));
-            qmn = fminf(qmn, fminf(fminf(qv[v].x, qv[v].y), fminf(qv[v].z, qv[v].w)));
+            sr += group_weights<T>(lw[v], qv[v], nmc, c, invZ, w4);
+            if constexpr (kWithQ) {
+              qmx = max3_nan(qmx, qv[v].x, qv[v].y);
+              qmx = max3_nan(qmx, qv[v].z, qv[v].w);
+              qmn = min3(qmn, qv[v].x, qv[v].y);
+              qmn = min3(qmn, qv[v].z, qv[v].w);
+            }
           }
+          // the chunk's mass: the lanes' fp32 sums, added exactly in fixed point
+          long long sx = fx(sr);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+          if (lane == 0) gs.mass[par][cd - d0] = sx;
         }
-        sr = warp_sum(sr);
-        if (lane == 0) gs.mass[par][cd - d0] = sr;
-      }
+      };
+      if (tc.q != nullptr) chunks(std::true_type{});
+      else chunks(std::false_type{});
       const bool qbad = group_any(group, !(qmx < kInf) || qmn < 0.f);  // also: every chunk mass is in place
-      float tot = 0.f;
+      long long tot = 0;
       if (gwarp == 0) tot = local_scan(gs.mass[par], d1 - d0, lane).total;
-      mine = pack_total(tot, qbad ? 1 : 0, 0);
+      mine = pack_total(tot, qbad ? 1 : 0);
     }
     if (first) {  // this task's inputs for the decision
       int err = 0;
@@ -885,23 +1065,33 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       g[5] = __int_as_float(err);
     }
     __syncwarp();
-    const int xp = exchange(gs, tm, mine, group, gwarp, lane, P.ws.error);
+    int xp = 0;
+    if (!ahead_row) {
+      xp = exchange(gs, tm, mine, group, gwarp, lane, P.ws.error);
+    } else if (group_any(group, ahead_fail)) {  // (also makes gs.ahead visible to the group)
+      tm.ok = false;  // the bounded wait for the statistics gave up
+    }
 
     // The decision, taken by every thread on the same inputs.
+    if (kind == kTaskRow && !ahead_row) starts_gone = !(__float_as_int(gs.slot[xp][0].w) & (1 << 30));
     const float* g = gs.gq[par];
     int warn = cur.warn;  // status bits above the error byte, >> 8
     bool done = false, failed = false, drawn = false;
     int J = -1, y = -1, st = 0;
     bool nxt_local = false;  // the next task stays with this team (next row, second draw pass)
     Entry nxt = cur;
-    if (kind == kTaskRow) {
-      RowSum rs;
-      {
-        const float4 s0 = gs.slot[xp][0];
-        rs.m = s0.x;
-        rs.Z = s0.y;
-        rs.z = __float_as_int(s0.z);
-      }
+    // a row's statistics: the members' summaries merged in member order, or those read
+    // from the workspace for a row computed ahead
+    RowSum rs;
+    if (ahead_row) {
+      rs.m = gs.ahead.x;
+      rs.Z = gs.ahead.y;
+      rs.z = __float_as_int(gs.ahead.z);
+    } else if (kind == kTaskRow || kind == kTaskAhead) {
+      const float4 s0 = gs.slot[xp][0];
+      rs.m = s0.x;
+      rs.Z = s0.y;
+      rs.z = __float_as_int(s0.z);
 #pragma unroll
       for (int r = 1; r < kC; ++r) {
         const float4 sr = gs.slot[xp][r];
@@ -911,6 +1101,15 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         o.z = __float_as_int(sr.z);
         rs = merge(rs, o, c);
       }
+    }
+    if (kind == kTaskAhead) {
+      // left for the chain's team, which waits on the flag
+      if (leader) {
+        const int64_t hk = static_cast<int64_t>(b) * R + ri;
+        __stcg(P.ws.help + hk, make_float4(rs.m, rs.Z, __int_as_float(rs.z), 0.f));
+        st_release(P.ws.help_ready + hk, 1);
+      }
+    } else if (kind == kTaskRow) {
       int err = 0;
       if (gbad) err = SPECDEC_STATUS_BAD_TOKEN;
       else if (!P.greedy_only && !(Tc - Tc == 0.f)) err = SPECDEC_STATUS_BAD_TEMPERATURE;
@@ -948,6 +1147,15 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
           nxt.m = 0.f;
           nxt.Z = 1.f;
           nxt.T = Tc;
+          // Teams wait for work: hand them this chain's later rows (from ri + 2; this team
+          // goes on with ri + 1), one row per waiting team.
+          const int idle = ahead_row ? 0 : (__float_as_int(gs.slot[xp][0].w) & ((1 << 30) - 1));
+          const int lo = max(ri + 2, ahead_hi + 1), hi = min(gb, ri + 1 + idle);
+          if (idle > 0 && lo <= hi) {
+            if (leader) publish_ahead(qu, b, lo, hi, Tc);
+            ahead_lo = lo;
+            ahead_hi = hi;
+          }
         } else {  // rejection at ri, or row gamma: the extra token comes from row ri
           J = ri;
           if (greedy) {
@@ -957,7 +1165,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
             st = SPECDEC_STATUS_BAD_UNIFORM;
             done = failed = true;
           } else {
-            Entry e;  // the draw goes to the queue; any team may take it
+            Entry e;
             e.b = b;
             e.row = ri;
             e.kind = kTaskDraw;
@@ -965,13 +1173,23 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
             e.m = rs.m;
             e.Z = rs.Z;
             e.T = Tc;
-            if (leader) publish_draw(qu, e);
+            if (starts_gone) {
+              // no sequence waits to start: this team draws now, while row J is in L2
+              nxt_local = true;
+              nxt = e;
+            } else if (leader) {
+              // the draw goes to the queue (any team may take it) so that this team starts
+              // the next sequence; that start ticket's atomic goes out beside the
+              // publication's
+              if (starts_left) pre_ticket = atomicAdd(qu.start_ticket, 1u);
+              publish_draw(qu, e);
+            }
           }
         }
       }
     } else {  // the members' totals of the drawn row
       J = ri;
-      float S = 0.f;
+      long long S = 0;
       bool anybad = false;
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
@@ -981,7 +1199,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       if (kind == kTaskDraw && anybad) {
         st = SPECDEC_STATUS_BAD_PROB;
         done = failed = true;
-      } else if (kind == kTaskDraw && !(S > 0.f)) {
+      } else if (kind == kTaskDraw && !(S > 0)) {
         // zero total residual (possible only through rounding): draw from p itself
         nxt_local = true;
         nxt = cur;
@@ -989,14 +1207,14 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         nxt.warn = warn | (SPECDEC_STATUS_ZERO_RESIDUAL >> 8);
       } else {
         // the member whose part holds u * S (else the last member with mass) finds y
-        const float target = g[4] * S;
+        const long long target = fx_target(g[4], S);
         int rstar = -1, rlast = 0;
-        float base = 0.f, run = 0.f, baselast = 0.f;
+        long long base = 0, run = 0, baselast = 0;
 #pragma unroll
         for (int r = 0; r < kC; ++r) {
-          const float tt = unpack_total(gs.slot[xp][r]);
-          if (tt > 0.f) { rlast = r; baselast = run; }
-          if (rstar < 0 && tt > 0.f && run + tt > target) { rstar = r; base = run; }
+          const long long tt = unpack_total(gs.slot[xp][r]);
+          if (tt > 0) { rlast = r; baselast = run; }
+          if (rstar < 0 && tt > 0 && run + tt > target) { rstar = r; base = run; }
           run += tt;
         }
         if (rstar < 0) { rstar = rlast; base = baselast; }
@@ -1030,22 +1248,29 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         atomicAdd(qu.finished, 1u);
       }
     }
+    // A draw ends its chain, so the team takes a ticket next: the member holding u * S
+    // finds the drawn token with its second warp meanwhile (the leader, in the first warp,
+    // fetches the ticket).
+    if (srch && gwarp == 1) {
+      const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
+      const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
+      const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
+                                           gs.mass[s_par], lane);
+      if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
+    }
+    srch = false;
     // the next task: this sequence's next step, or new work through the mailbox
+    if (!nxt_local) {
+      ahead_lo = INT_MAX;
+      ahead_hi = -1;
+    }
     cur = nxt_local ? nxt : take_box();
     ++t;
-  }
-  // a draw found in the last task
-  if (srch && gwarp == 0 && tm.ok) {
-    const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
-    const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
-    const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
-                                  gs.mass[s_par], lane);
-    if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
   }
   // Copies still in flight (left by a bounded wait that gave up): wait for them, bounded,
   // before the CTA exits.
   if (lane == 0)
-    for (; pp.k < pp.issued; ++pp.k) mbar_wait(pp.sbar(pp.k), (pp.k / kSeqStages) & 1u);
+    for (; pp.k < pp.issued; pp.consume()) mbar_wait(pp.bar + pp.sk, (pp.phase >> pp.sk) & 1u);
   // No CTA leaves while another member may still write into its shared memory.
   cluster_sync_all();
 }

@@ -116,14 +116,18 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   }
   // queue entries of the left-to-right kernel (streaming layout only)
   const int64_t n_entries = path == 2 ? static_cast<int64_t>(B) * g + 2 * static_cast<int64_t>(B) : 0;
-  // (the streaming layout also keeps a bad-draft-probability flag per sequence)
+  // (the streaming layout also keeps a bad-draft-probability flag per sequence and, for
+  // the left-to-right kernel, a ready flag per row for statistics computed ahead)
+  const int64_t n_help = path == 2 ? rows : 0;
   const int64_t n_counters = path == 3 ? 0
-                                        : std::max<int64_t>(2 * static_cast<int64_t>(B), n_entries + (path == 2 ? B : 0));
+                                        : std::max<int64_t>(2 * static_cast<int64_t>(B),
+                                                            n_entries + (path == 2 ? B : 0) + n_help);
   size_t off = 0;
   const size_t o_error = off;    off += kAlign;
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * static_cast<size_t>(n_counters));
   const size_t counters_end = off;
   const size_t o_ring = off;     off += round_up(2 * sizeof(float4) * static_cast<size_t>(n_entries));
+  const size_t o_help = off;     off += round_up(sizeof(float4) * static_cast<size_t>(n_help));
   const size_t o_seq = off;      off += round_up(sizeof(SeqState) * static_cast<size_t>(B));
   const size_t o_list = off;     off += round_up(sizeof(DrawEntry) * static_cast<size_t>(n_drawn));
   const size_t o_brows = off;    off += block ? round_up(sizeof(float4) * static_cast<size_t>(rows)) : 0;
@@ -144,6 +148,9 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->ready = reinterpret_cast<int*>(p + o_counters);
     ws->ring = reinterpret_cast<float4*>(p + o_ring);
     ws->qbad = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries : nullptr;
+    ws->help_ready = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries + B : nullptr;
+    ws->help = path == 2 ? reinterpret_cast<float4*>(p + o_help) : nullptr;
+    ws->ring_cap = static_cast<int>(n_entries);
     ws->block_rows = block ? reinterpret_cast<float4*>(p + o_brows) : nullptr;
 
   }
@@ -192,7 +199,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   const int64_t nseg = (static_cast<int64_t>(V) + seg - 1) / seg;
   const int64_t items = static_cast<int64_t>(B) * (g + 1) * nseg;
   if (items > INT32_MAX || nseg > 65535 || B > 65535) return SPECDEC_ERR_UNSUPPORTED;
-  if (gammas && !(stream_path && V <= kSeqMaxV))  // per-sequence counts: left-to-right kernel only
+  if (gammas && !(stream_path && V <= seq_max_v(ldt)))  // per-sequence counts: left-to-right kernel only
     return fail(SPECDEC_ERR_UNSUPPORTED, "per-sequence draft counts need 16-byte rows, g + 1 <= 32");
   if (workspace_bytes < chain_ws_bytes(B, g, V, ldt)) return SPECDEC_ERR_WORKSPACE;
   // logits and q in pinned host memory: the left-to-right kernel reads the rows it needs
@@ -210,10 +217,10 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
       host_in = true;
     }
   }
-  if (host_in && !(stream_path && (gammas || use_left_to_right()) && V <= kSeqMaxV))
+  if (host_in && !(stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt)))
     return fail(SPECDEC_ERR_UNSUPPORTED,
                 "host-resident logits or draft probabilities need the left-to-right kernel: 16-byte rows, g + 1 <= 32, "
-                "V <= 2,097,152");
+                "V <= 1,048,576 (bf16) or 786,432 (fp32)");
 
   ChainParams P{};
   P.logits = logits;
@@ -240,7 +247,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   // always written before they are read.
   if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
     return fail_cuda("clearing the workspace counters", e);
-  if (stream_path && (gammas || use_left_to_right()) && V <= kSeqMaxV) {
+  if (stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt)) {
     P.grid_stats = device_sm_count();
     P.host_inputs = host_in ? 1 : 0;
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);

@@ -43,10 +43,13 @@ struct ChainWorkspace {
   int* qbad;             // [B]: a bad draft probability met by the mass pass; cleared per call
   float4* block_rows;    // [B*(g+1)]: block verification's (m, Z, w_k, w_k / Z) per row
 
-  // left-to-right kernel: task queues (rows first, then draws)
-  unsigned* queue;       // [5]: rows published, rows claimed, draws published, draws claimed, sequences finished
-  int* ready;            // [B*g + 2B]: entry published (rows ring, then draws ring); cleared per call
-  float4* ring;          // [2 * (B*g + 2B)]: 32-byte task entries (rows ring, then draws ring)
+  // left-to-right kernel: the task queues and the statistics of rows computed ahead
+  unsigned* queue;       // [4]: starts taken, entries published, entries claimed, sequences finished
+  int* ready;            // [ring_cap]: entry published; cleared per call
+  float4* ring;          // [2 * ring_cap]: 32-byte task entries (draws and rows computed ahead)
+  int ring_cap;          // B*g + 2B
+  float4* help;          // [B*(g+1)]: (m, Z, argmax bits, 0) of a row computed ahead for its chain
+  int* help_ready;       // [B*(g+1)]: that row's statistics are in place; cleared per call
 };
 
 // Streaming (bulk-copy) path geometry.
@@ -85,9 +88,18 @@ constexpr int kSeqGroups = 2;
 constexpr int kSeqCluster = 2;
 constexpr int kSeqStages = 3;
 constexpr int kSeqChunkBytes = 4096;
-constexpr int kSeqDrawChunk = 512;        // drawn-row elements per copy (logits + q fit 4 KB)
-constexpr int kSeqMaxDrawChunks = 1024;   // chunk masses of one member's part of the drawn row
-constexpr int64_t kSeqMaxV = static_cast<int64_t>(kSeqDrawChunk) * kSeqMaxDrawChunks * kSeqCluster;
+// A draw task copies logits and q of the drawn row in 6 KB stages, two per warp in the
+// warp's three 4 KB row stages: 1024 elements (2 KB of bf16 logits + 4 KB of q) or 768
+// (3 KB of fp32 logits + 3 KB of q) per copy.
+constexpr int kSeqDrawStageBytes = 6144;
+constexpr int kSeqDrawElemsBf16 = 1024;
+constexpr int kSeqDrawElemsF32 = 768;
+constexpr int kSeqMaxDrawChunks = 512;    // chunk masses of one member's part of the drawn row
+// Largest V the left-to-right kernel takes (its chunk-mass table in shared memory).
+constexpr int64_t seq_max_v(specdec_dtype ldt) {
+  return static_cast<int64_t>(ldt == SPECDEC_BF16 ? kSeqDrawElemsBf16 : kSeqDrawElemsF32) * kSeqMaxDrawChunks *
+         kSeqCluster;
+}
 
 struct ChainParams {
   const void* logits;
