@@ -61,7 +61,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
 #define SPECDEC_STATUS_BAD_UNIFORM 16       /* uniform outside [0, 1) on a sampled sequence   */
 #define SPECDEC_STATUS_BAD_TREE 32          /* parent not in [-1, i), or tree deeper than D   */
 #define SPECDEC_STATUS_BAD_TEMPERATURE 64   /* temperature NaN or infinite                    */
-#define SPECDEC_STATUS_TIMEOUT 128          /* a bounded wait inside a kernel gave up (internal) */
+#define SPECDEC_STATUS_TIMEOUT 128          /* a bounded wait inside a kernel gave up: not finished */
 #define SPECDEC_STATUS_ERROR_MASK 0xFF
 #define SPECDEC_STATUS_ZERO_Q 256           /* warning: q_i(x_i) == 0; accepted iff p_i(x_i) > 0 */
 #define SPECDEC_STATUS_ZERO_RESIDUAL 512    /* warning: residual mass 0 after rounding; drew from p */
@@ -103,10 +103,14 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
  * Host-resident rows: logits and draft_probs may be pinned host memory (cudaHostAlloc, or
  * registered with cudaHostRegister, mapped at its own address).  The left-to-right kernel
  * then reads only the rows the round needs, straight over the host link (no copy of the
- * whole batch); this needs 16-byte aligned rows, g + 1 <= 32 and V <= 2,097,152, else
- * SPECDEC_ERR_UNSUPPORTED.  Pageable host memory gives SPECDEC_ERR_INVALID_ARG.  The
- * other inputs, the outputs and the workspace are device memory.  The same holds for
- * specdec_verify_greedy and specdec_verify_chain_varlen.
+ * whole batch); this needs 16-byte aligned rows, g + 1 <= 32 and V <= 1,048,576 (bf16) or
+ * 786,432 (fp32), else SPECDEC_ERR_UNSUPPORTED.  Pageable host memory gives
+ * SPECDEC_ERR_INVALID_ARG, and so does a device pointer on a device other than the current
+ * one.  The other inputs, the outputs and the workspace are device memory.  The same holds
+ * for specdec_verify_greedy and specdec_verify_chain_varlen.
+ * Bounded waits: the left-to-right kernel's waits on its queues and copies give up after a
+ * bound (one second); a sequence the kernel could not finish then comes back with
+ * SPECDEC_STATUS_TIMEOUT, num_accepted -1 and tokens -1 (out_p_draft NaN).
  */
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
 
@@ -128,8 +132,8 @@ int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* dra
  * past J, out_p_draft NaN past J.  A count outside [0, g] gives SPECDEC_STATUS_BAD_TOKEN.
  * Exactness needs each count chosen without looking at the drafts it decides on (the
  * page's non-anticipating requirement, box "Trimming a draft can break exactness"); the
- * verifier cannot check it.  Needs 16-byte aligned rows, g + 1 <= 32 and V <= 2,097,152
- * (the left-to-right kernel), else SPECDEC_ERR_UNSUPPORTED.  Workspace:
+ * verifier cannot check it.  Needs 16-byte aligned rows, g + 1 <= 32 and V <= 1,048,576 (bf16)
+ * or 786,432 (fp32) (the left-to-right kernel), else SPECDEC_ERR_UNSUPPORTED.  Workspace:
  * specdec_chain_workspace_bytes.
  */
 int specdec_verify_chain_varlen(const void* logits, specdec_dtype ldt, const float* draft_probs,
@@ -388,6 +392,8 @@ int specdec_profile_stop(void);
  *
  *   - Set-up: the first call on each device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture begins.
+ *     The address is kept per device and primary context: after a device reset
+ *     (cudaDeviceReset) the next call looks it up again.
  *   - Limit: a shape whose specdec_chain_workspace_bytes() exceeds
  *     SPECDEC_NOALLOC_SCRATCH_BYTES is rejected with SPECDEC_ERR_TOO_LARGE (nothing is
  *     launched; specdec_last_error() gives the sizes).  16 MiB covers, e.g., B=512, g=8,
@@ -405,6 +411,34 @@ int specdec_verify_chain_noalloc(const void* logits, specdec_dtype ldt, const fl
                                  const float* uniforms, int B, int g, int V, int32_t* out_tokens,
                                  int32_t* out_num_accepted, float* out_p_draft, int32_t* out_status,
                                  void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Test hooks (the library's own tests and sweeps; not for production use).
+ *
+ * Process-global settings read by the calls issued after them (not thread-safe; set them
+ * while no call is being issued).  Every hook defaults to 0, the production behaviour.
+ *   SPECDEC_HOOK_CHAIN_ALL_ROWS    1: chain and greedy calls whose rows the left-to-right
+ *                                  kernel takes run the all-rows streaming kernels instead
+ *   SPECDEC_HOOK_BLOCK_TWO_PASS    1: block verification runs the statistics and mass
+ *                                  kernels instead of the one-launch kernel
+ *   SPECDEC_HOOK_TREE_CLUSTER      1, 2, 4 or 8: the tree walks' cluster size (where it fits)
+ *   SPECDEC_HOOK_CHAIN_DROP_DRAWS  1: the left-to-right kernel never marks a queued draw
+ *                                  as published, so the teams that take its ticket wait
+ *                                  until the queue wait gives up (the sequences it belongs
+ *                                  to come back with SPECDEC_STATUS_TIMEOUT)
+ *   SPECDEC_HOOK_QUEUE_WAIT_US     >= 1: the left-to-right kernel's bound on waits for
+ *                                  queued work, in microseconds (0: one second)
+ * Returns SPECDEC_OK, or SPECDEC_ERR_INVALID_ARG for an unknown hook or value.
+ */
+#define SPECDEC_HOOK_CHAIN_ALL_ROWS 0
+#define SPECDEC_HOOK_BLOCK_TWO_PASS 1
+#define SPECDEC_HOOK_TREE_CLUSTER 2
+#define SPECDEC_HOOK_CHAIN_DROP_DRAWS 3
+#define SPECDEC_HOOK_QUEUE_WAIT_US 4
+#define SPECDEC_NUM_HOOKS 5
+
+int specdec_set_test_hook(int hook, int value);
+int specdec_get_test_hook(int hook);
 
 /* Library version string, e.g. "0.1.0". */
 const char* specdec_version(void);

@@ -22,6 +22,10 @@ __all__ = [
 
 F32, BF16 = 0, 1
 GREEDY_TEMPERATURE = 1e-3
+STATUS_TIMEOUT = 128
+
+# Test hooks of the library (specdec_set_test_hook): the library's own tests and sweeps.
+HOOK_CHAIN_ALL_ROWS, HOOK_BLOCK_TWO_PASS, HOOK_TREE_CLUSTER, HOOK_CHAIN_DROP_DRAWS, HOOK_QUEUE_WAIT_US = range(5)
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
 _ERR_NAMES = {1: "invalid argument", 2: "unsupported size", 3: "CUDA launch error",
@@ -110,6 +114,10 @@ def load_library():
     lib.specdec_version.restype = ctypes.c_char_p
     lib.specdec_last_error.argtypes = []
     lib.specdec_last_error.restype = ctypes.c_char_p
+    lib.specdec_set_test_hook.argtypes = [i32, i32]
+    lib.specdec_set_test_hook.restype = i32
+    lib.specdec_get_test_hook.argtypes = [i32]
+    lib.specdec_get_test_hook.restype = i32
     _LIB = lib
     return lib
 
@@ -160,6 +168,33 @@ def _workspace(nbytes: int, device, stream_handle: int):
         ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
         _WORKSPACES[key] = ws
     return ws, ws.numel()
+
+
+def set_test_hook(hook: int, value: int) -> None:
+    """Set one of the library's test hooks (HOOK_*; 0 restores the production behaviour)."""
+    _check(load_library().specdec_set_test_hook(int(hook), int(value)), "specdec_set_test_hook")
+
+
+def get_test_hook(hook: int) -> int:
+    return int(load_library().specdec_get_test_hook(int(hook)))
+
+
+class test_hooks:
+    """Context manager: the given hooks set for the block, their previous values restored."""
+
+    def __init__(self, **hooks):
+        self.hooks = {globals()["HOOK_" + k.upper()]: int(v) for k, v in hooks.items()}
+        self.saved = {}
+
+    def __enter__(self):
+        for h, v in self.hooks.items():
+            self.saved[h] = get_test_hook(h)
+            set_test_hook(h, v)
+        return self
+
+    def __exit__(self, *exc):
+        for h, v in self.saved.items():
+            set_test_hook(h, v)
 
 
 def chain_workspace_bytes(B: int, gamma: int, V: int, dtype=torch.bfloat16) -> int:

@@ -408,19 +408,21 @@ __device__ int resolve_ticket(const ChainParams& P, const Queue& q, int tk, floa
     }
     if (ld_relaxed(q.finished) >= static_cast<unsigned>(q.B)) return -1;
     if (t0 == 0) t0 = global_timer_ns();
-    else if (global_timer_ns() - t0 > kMaxWaitNs) return -2;
+    else if (global_timer_ns() - t0 > P.queue_wait_ns) return -2;
     __nanosleep(128);
   }
 }
 
-__device__ void publish_draw(const Queue& q, const Entry& e) {
+// (drop: the test hook that loses the publication, so that whoever takes the ticket waits
+// until its bound gives up)
+__device__ void publish_draw(const Queue& q, const Entry& e, bool drop) {
   float4 e0, e1;
   pack_entry(e, e0, e1);
   const unsigned k = atomicAdd(q.pub_draws, 1u);
   float4* ent = q.ring_draws + 2 * static_cast<int64_t>(k);
   __stcg(ent, e0);
   __stcg(ent + 1, e1);
-  st_release(q.ready_draws + k, 1);
+  if (!drop) st_release(q.ready_draws + k, 1);
 }
 
 // Rows lo..hi of sequence b for teams that wait for work (one entry each, published in one
@@ -809,10 +811,11 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     t.n = (t.hi > t.lo + gwarp) ? (t.hi - t.lo - gwarp + kWarpsPerGroup - 1) / kWarpsPerGroup : 0;
     return t;
   };
-  auto no_more = []() {
+  // The entry that ends a team's work: b = -1, or -2 when its wait for work gave up.
+  auto no_more = [](int code) {
     float4 e0, e1;
     Entry e{};
-    e.b = -1;
+    e.b = code;
     pack_entry(e, e0, e1);
     return e0;
   };
@@ -831,7 +834,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       pre_ticket = UINT_MAX;
       if (r < 0) {
         if (r == -2) atomicOr(P.ws.error, 8u);
-        e0 = no_more();
+        e0 = no_more(r == -2 ? -2 : -1);
       }
       send_entry(gs, static_cast<int>(mb & 1u), e0, e1);
     }
@@ -849,8 +852,9 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   uint32_t t = 0;  // tasks done by this team
   // rows ahead_lo..ahead_hi of the team's current chain went to teams that waited for work
   int ahead_lo = INT_MAX, ahead_hi = -1;
-  // every start ticket is taken (as the leader last reported it; every thread holds it)
-  bool starts_gone = false;
+  // every start ticket is taken, and teams wait for work (as the leader last reported the
+  // queues; every thread holds both)
+  bool starts_gone = false, teams_wait = false;
   // a drawn token for this member to find (its second warp, while the team takes a ticket)
   bool srch = false;
   int s_b = 0, s_J = 0, s_par = 0;
@@ -912,7 +916,11 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     };
     if (tc.kind == kTaskRow) pp.begin(kSeqStages, kSeqChunkBytes);
     else pp.begin(DrawGeo<T>::kStages, kSeqDrawStageBytes);
-    while (pp.ok && ci < tc.n && pp.in_flight() < pp.nst) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
+    // While every team is busy, a draw keeps one copy in flight per warp (rows keep a copy
+    // in every stage), so the rows -- the chains, the critical path -- get the larger share
+    // of the bandwidth; once teams wait for work, every stage.
+    const uint32_t depth = (tc.kind == kTaskRow || teams_wait) ? pp.nst : 1u;
+    while (pp.ok && ci < tc.n && pp.in_flight() < depth) issue_job<T, kHost>(pp, tc, ci++, gwarp, lane, V, row_bytes);
 
     float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
     bool ahead_fail = false;
@@ -981,7 +989,9 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       const int idle = static_cast<int>(w_dt - w_pd);
       const bool starts_remain = leader && w_st < static_cast<unsigned>(P.B);
       const int qv = min(max(idle, 0), (1 << 30) - 1) | (starts_remain ? (1 << 30) : 0);
-      mine = make_float4(s.m, s.Z, __int_as_float(s.z), __int_as_float(qv));
+      // bit 31: a copy wait of this member gave up (its summary is incomplete)
+      const bool lost = group_any(group, !pp.ok);
+      mine = make_float4(s.m, s.Z, __int_as_float(s.z), __int_as_float(qv | (lost ? INT_MIN : 0)));
     } else {
       const float nmc = -__fmul_rn(cur.m, c), invZ = 1.f / cur.Z;
       float qmx = 0.f, qmn = 0.f;
@@ -1044,7 +1054,8 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       const bool qbad = group_any(group, !(qmx < kInf) || qmn < 0.f);  // also: every chunk mass is in place
       long long tot = 0;
       if (gwarp == 0) tot = local_scan(gs.mass[par], d1 - d0, lane).total;
-      mine = pack_total(tot, qbad ? 1 : 0);
+      const bool lost = group_any(group, !pp.ok);  // a copy wait of this member gave up
+      mine = pack_total(tot, (qbad ? 1 : 0) | (lost ? 2 : 0));
     }
     if (first) {  // this task's inputs for the decision
       int err = 0;
@@ -1072,8 +1083,27 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       tm.ok = false;  // the bounded wait for the statistics gave up
     }
 
+    // A copy wait of either member gave up (the task's data are incomplete), or a wait on
+    // the exchange or on a row computed ahead did: the team stops here, writing nothing
+    // for this sequence; the kernel's last CTA reports it as timed out.
+    bool lost = !tm.ok;
+    if (!ahead_row && (kind == kTaskRow || kind == kTaskAhead)) {
+#pragma unroll
+      for (int r = 0; r < kC; ++r) lost |= __float_as_int(gs.slot[xp][r].w) < 0;
+    } else if (!ahead_row) {
+#pragma unroll
+      for (int r = 0; r < kC; ++r) lost |= (__float_as_int(gs.slot[xp][r].z) & 2) != 0;
+    }
+    if (lost) {
+      tm.ok = false;
+      break;
+    }
+
     // The decision, taken by every thread on the same inputs.
-    if (kind == kTaskRow && !ahead_row) starts_gone = !(__float_as_int(gs.slot[xp][0].w) & (1 << 30));
+    if (kind == kTaskRow && !ahead_row) {
+      starts_gone = !(__float_as_int(gs.slot[xp][0].w) & (1 << 30));
+      teams_wait = (__float_as_int(gs.slot[xp][0].w) & ((1 << 30) - 1)) > 0;
+    }
     const float* g = gs.gq[par];
     int warn = cur.warn;  // status bits above the error byte, >> 8
     bool done = false, failed = false, drawn = false;
@@ -1182,7 +1212,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
               // the next sequence; that start ticket's atomic goes out beside the
               // publication's
               if (starts_left) pre_ticket = atomicAdd(qu.start_ticket, 1u);
-              publish_draw(qu, e);
+              publish_draw(qu, e, P.drop_draws != 0);
             }
           }
         }
@@ -1194,7 +1224,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
         S += unpack_total(gs.slot[xp][r]);
-        anybad |= __float_as_int(gs.slot[xp][r].z) != 0;
+        anybad |= (__float_as_int(gs.slot[xp][r].z) & 1) != 0;
       }
       if (kind == kTaskDraw && anybad) {
         st = SPECDEC_STATUS_BAD_PROB;
@@ -1245,6 +1275,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       if (lane == 0) {
         P.out_J[b] = Jo;
         if (P.out_status) P.out_status[b] = st | (warn << 8);
+        if (!drawn) __stcg(P.ws.seq_done + b, 1);  // (a drawn token: once it is written)
         atomicAdd(qu.finished, 1u);
       }
     }
@@ -1256,7 +1287,10 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
       const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
                                            gs.mass[s_par], lane);
-      if (lane == 0) P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
+      if (lane == 0) {
+        P.out_tokens[static_cast<int64_t>(s_b) * R + s_J] = y;
+        __stcg(P.ws.seq_done + s_b, 1);
+      }
     }
     srch = false;
     // the next task: this sequence's next step, or new work through the mailbox
@@ -1271,8 +1305,30 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   // before the CTA exits.
   if (lane == 0)
     for (; pp.k < pp.issued; pp.consume()) mbar_wait(pp.bar + pp.sk, (pp.phase >> pp.sk) & 1u);
+  // A team whose wait gave up stopped with work left: sequences it (or the teams whose
+  // work it was waiting for) did not finish.  Once every team has stopped this way -- then
+  // no team is working -- the last one marks each sequence without its done flag as timed
+  // out (J = -1, tokens -1, p_draft NaN).  Teams that ran out of work normally skip this.
+  const bool abnormal = !tm.ok || cur.b == -2;
+
   // No CTA leaves while another member may still write into its shared memory.
   cluster_sync_all();
+
+  if (abnormal && leader) {
+    __threadfence();  // this team's outputs and done flags (its members: the cluster barrier)
+    const unsigned teams = (gridDim.x / kC) * kSeqGroups;
+    if (atomicAdd(P.ws.exit_count, 1u) == teams - 1) {
+      __threadfence();
+      for (int b = 0; b < P.B; ++b) {
+        if (ld_acquire(P.ws.seq_done + b) != 0) continue;
+        for (int i = 0; i < R; ++i) P.out_tokens[static_cast<int64_t>(b) * R + i] = -1;
+        if (P.out_p_draft)
+          for (int i = 0; i < P.gamma; ++i) P.out_p_draft[static_cast<int64_t>(b) * P.gamma + i] = kNaN;
+        P.out_J[b] = -1;
+        if (P.out_status) P.out_status[b] = SPECDEC_STATUS_TIMEOUT;
+      }
+    }
+  }
 }
 
 template <typename T, bool kHost>

@@ -1,5 +1,6 @@
 // C-ABI entry points: argument validation, workspace layout, launches, kernel timing.
 
+#include <atomic>
 #include <cstdint>
 #include <algorithm>
 #include <mutex>
@@ -14,6 +15,11 @@
 #include "specdec_internal.h"
 
 namespace specdec {
+
+// Test hooks (specdec_set_test_hook): process-global, 0 = production behaviour.
+std::atomic<int> g_test_hooks[SPECDEC_NUM_HOOKS];
+int test_hook(int hook) { return (hook >= 0 && hook < SPECDEC_NUM_HOOKS) ? g_test_hooks[hook].load() : 0; }
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -32,22 +38,12 @@ bool rows_vectorizable(const void* base, int64_t V, size_t esize) {
 }
 
 // Aligned rows take the left-to-right kernel, which reads rows only up to the first
-// rejection, unless SPECDEC_CHAIN_SCAN=1 selects the kernels that scan every row first.
-bool use_left_to_right() {
-  static const bool v = [] {
-    const char* e = std::getenv("SPECDEC_CHAIN_SCAN");
-    return !(e && e[0] == '1');
-  }();
-  return v;
-}
+// rejection; the all-rows kernels serve them only under the test hook.
+bool use_left_to_right() { return test_hook(SPECDEC_HOOK_CHAIN_ALL_ROWS) == 0; }
 
-// Block verification runs as one launch that reads every row once, unless
-// SPECDEC_BLOCK_TWO_PASS=1 selects the statistics and mass kernels of the streaming path
-// (read at every call).
-bool block_two_pass() {
-  const char* e = std::getenv("SPECDEC_BLOCK_TWO_PASS");
-  return e && e[0] == '1';
-}
+// Block verification runs as one launch that reads every row once; the statistics and
+// mass kernels of the streaming path serve it only under the test hook.
+bool block_two_pass() { return test_hook(SPECDEC_HOOK_BLOCK_TWO_PASS) != 0; }
 
 // ---- last error (per host thread) -----------------------------------------------------
 thread_local char g_last_error[256] = "no error";
@@ -119,9 +115,10 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
   // (the streaming layout also keeps a bad-draft-probability flag per sequence and, for
   // the left-to-right kernel, a ready flag per row for statistics computed ahead)
   const int64_t n_help = path == 2 ? rows : 0;
+  const int64_t n_done = path == 2 ? B : 0;  // left-to-right kernel: sequence finished
   const int64_t n_counters = path == 3 ? 0
                                         : std::max<int64_t>(2 * static_cast<int64_t>(B),
-                                                            n_entries + (path == 2 ? B : 0) + n_help);
+                                                            n_entries + (path == 2 ? B : 0) + n_help + n_done);
   size_t off = 0;
   const size_t o_error = off;    off += kAlign;
   const size_t o_counters = off; off += round_up(sizeof(unsigned) * static_cast<size_t>(n_counters));
@@ -149,6 +146,8 @@ size_t chain_workspace_layout(int B, int g, int V, specdec_dtype ldt, int path, 
     ws->ring = reinterpret_cast<float4*>(p + o_ring);
     ws->qbad = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries : nullptr;
     ws->help_ready = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries + B : nullptr;
+    ws->seq_done = path == 2 ? reinterpret_cast<int*>(p + o_counters) + n_entries + B + n_help : nullptr;
+    ws->exit_count = reinterpret_cast<unsigned*>(p + o_error) + 6;
     ws->help = path == 2 ? reinterpret_cast<float4*>(p + o_help) : nullptr;
     ws->ring_cap = static_cast<int>(n_entries);
     ws->block_rows = block ? reinterpret_cast<float4*>(p + o_brows) : nullptr;
@@ -212,6 +211,12 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
     if (cudaError_t e = cudaPointerGetAttributes(&a, p); e != cudaSuccess) return fail_cuda("pointer attributes", e);
     if (a.type == cudaMemoryTypeUnregistered)
       return fail(SPECDEC_ERR_INVALID_ARG, "host logits and draft probabilities must be pinned (cudaHostAlloc, cudaHostRegister)");
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+      int cur = 0;
+      if (cudaError_t e = cudaGetDevice(&cur); e != cudaSuccess) return fail_cuda("querying the current device", e);
+      if (a.device != cur)
+        return fail(SPECDEC_ERR_INVALID_ARG, "logits or draft probabilities on a device other than the current one");
+    }
     if (a.type == cudaMemoryTypeHost) {
       if (a.devicePointer != p) return fail(SPECDEC_ERR_UNSUPPORTED, "host memory not mapped at its own address");
       host_in = true;
@@ -250,6 +255,9 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   if (stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt)) {
     P.grid_stats = device_sm_count();
     P.host_inputs = host_in ? 1 : 0;
+    P.drop_draws = test_hook(SPECDEC_HOOK_CHAIN_DROP_DRAWS) ? 1 : 0;
+    const int wait_us = test_hook(SPECDEC_HOOK_QUEUE_WAIT_US);
+    P.queue_wait_ns = wait_us > 0 ? static_cast<unsigned long long>(wait_us) * 1000ull : 1000000000ull;
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
     if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);
     return SPECDEC_OK;
@@ -296,25 +304,52 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
 // ---- built-in scratch for specdec_verify_chain_noalloc ---------------------------------
 // One fixed array in device memory; every GPU that loads the library holds it until the
 // process exits.  Host code must not pass the symbol itself to a kernel: its address in
-// host code is a host-side stand-in.  The device address is looked up once per device.
+// host code is a host-side stand-in.  The device address is looked up once per device and
+// context: a device reset (cudaDeviceReset) makes a new primary context, which loads the
+// module again, possibly at another address.
 constexpr size_t kNoAllocScratchBytes = SPECDEC_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up on first use).
+// The driver's cuCtxGetCurrent (through the runtime's entry-point lookup, so the library
+// needs no link to the driver library), or null where it is not available.
+using CtxGetCurrent = int (*)(void**);
+CtxGetCurrent ctx_get_current() {
+  static const CtxGetCurrent fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrent>(nullptr);
+    return reinterpret_cast<CtxGetCurrent>(f);
+  }();
+  return fn;
+}
+
+// Device address of the scratch array on the current device and context (looked up on the
+// first use on each, and on every use where the context cannot be queried).
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return fail_cuda("querying the current device", e);
   if (dev < 0 || dev >= kMaxDevices) return fail(SPECDEC_ERR_UNSUPPORTED, "device index beyond the scratch table");
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  void* ctx = nullptr;
+  const CtxGetCurrent get = ctx_get_current();
+  const bool known = get != nullptr && get(&ctx) == 0 && ctx != nullptr;
+  if (!known || g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch); e != cudaSuccess)
       return fail_cuda("looking up the built-in scratch array", e);
+    if (!known) {  // cudaGetSymbolAddress made the context current: ask again
+      ctx = nullptr;
+      if (get == nullptr || get(&ctx) != 0) ctx = nullptr;
+    }
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return SPECDEC_OK;
@@ -677,7 +712,21 @@ int specdec_profile_stop(void) {
   return SPECDEC_OK;
 }
 
-const char* specdec_version(void) { return "0.1.0"; }
+const char* specdec_version(void) { return "0.2.0"; }
+
+int specdec_set_test_hook(int hook, int value) {
+  if (hook < 0 || hook >= SPECDEC_NUM_HOOKS) return SPECDEC_ERR_INVALID_ARG;
+  if (value < 0) return SPECDEC_ERR_INVALID_ARG;
+  if (hook == SPECDEC_HOOK_TREE_CLUSTER && !(value == 0 || value == 1 || value == 2 || value == 4 || value == 8))
+    return SPECDEC_ERR_INVALID_ARG;
+  if ((hook == SPECDEC_HOOK_CHAIN_ALL_ROWS || hook == SPECDEC_HOOK_BLOCK_TWO_PASS ||
+       hook == SPECDEC_HOOK_CHAIN_DROP_DRAWS) && value > 1)
+    return SPECDEC_ERR_INVALID_ARG;
+  g_test_hooks[hook].store(value);
+  return SPECDEC_OK;
+}
+
+int specdec_get_test_hook(int hook) { return test_hook(hook); }
 
 const char* specdec_last_error(void) { return g_last_error; }
 

@@ -9,6 +9,9 @@
 
 namespace specdec {
 
+// The value of a test hook (SPECDEC_HOOK_*, specdec_set_test_hook); 0 = production.
+int test_hook(int hook);
+
 constexpr int kChainThreads = 256;
 constexpr int kChainVectorsPerThread = 8;    // 16-byte vectors per thread per segment
 constexpr int kScalarElemsPerThread = 32;    // elements per thread per segment (scalar path)
@@ -50,6 +53,8 @@ struct ChainWorkspace {
   int ring_cap;          // B*g + 2B
   float4* help;          // [B*(g+1)]: (m, Z, argmax bits, 0) of a row computed ahead for its chain
   int* help_ready;       // [B*(g+1)]: that row's statistics are in place; cleared per call
+  int* seq_done;         // [B]: the sequence's outputs are written; cleared per call
+  unsigned* exit_count;  // [1]: CTAs that finished; cleared per call
 };
 
 // Streaming (bulk-copy) path geometry.
@@ -113,6 +118,8 @@ struct ChainParams {
   int seg;               // elements per segment
   int greedy_only;
   int host_inputs;       // left-to-right kernel: logits and q may sit in pinned host memory
+  int drop_draws;        // left-to-right kernel, test hook: queued draws are never marked published
+  unsigned long long queue_wait_ns;  // left-to-right kernel: bound on waits for queued work
   int nch;               // streaming path: 4 KB chunks per logits row
   int nchd;              // streaming path: draw chunks per row
   int grid_stats, grid_draw;

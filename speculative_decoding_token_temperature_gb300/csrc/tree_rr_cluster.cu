@@ -29,7 +29,6 @@
 // (the walk starts after); the root's copies are issued before validation.
 
 #include <climits>
-#include <cstdlib>
 
 #include "specdec_device.cuh"
 #include "specdec_internal.h"
@@ -590,8 +589,7 @@ cudaError_t launch_rr_cluster_t(const TreeParams& P, int C, int slice, cudaStrea
 
 int tree_rr_cluster_size(int B, int V, specdec_dtype ldt) {
   const int es = ldt == SPECDEC_BF16 ? 2 : 4;
-  if (const char* env = std::getenv("SPECDEC_TREE_CLUSTER")) {  // a fixed size, for sweeps
-    const int C = std::atoi(env);
+  if (const int C = test_hook(SPECDEC_HOOK_TREE_CLUSTER)) {  // a fixed size (test hook)
     if ((C == 1 || C == 2 || C == 4 || C == 8) && rr_slice(V, es, C) > 0) return C;
   }
   int best = 0;

@@ -34,7 +34,6 @@
 // 16-byte vectors; index order inside a chunk is (iteration, lane, element).
 
 #include <climits>
-#include <cstdlib>
 
 #include "specdec_device.cuh"
 #include "specdec_internal.h"
@@ -531,8 +530,7 @@ cudaError_t launch_cluster_t(const TreeParams& P, int C, int slice, cudaStream_t
 
 int tree_walk_cluster_size(int B, int V, specdec_dtype ldt) {
   const int es = ldt == SPECDEC_BF16 ? 2 : 4;
-  if (const char* env = std::getenv("SPECDEC_TREE_CLUSTER")) {  // a fixed size, for sweeps
-    const int C = std::atoi(env);
+  if (const int C = test_hook(SPECDEC_HOOK_TREE_CLUSTER)) {  // a fixed size (test hook)
     if ((C == 1 || C == 2 || C == 4 || C == 8) && walk_slice(V, es, C) > 0) return C;
   }
   int best = 0;

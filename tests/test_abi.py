@@ -137,3 +137,20 @@ def test_binding_marshalling_errors_without_gpu(built_library):
         sd._need(t, "x", torch.float32, (3, 2), t.device)
     with pytest.raises(ValueError):
         sd._need(t.t(), "x", torch.float32, (3, 2), t.device)
+
+
+def test_test_hooks_are_validated_and_default_to_production(built_library):
+    import speculative_decoding_token_temperature_gb300 as sd
+    lib = sd.load_library()
+    for h in range(5):
+        assert lib.specdec_get_test_hook(h) == 0
+    assert lib.specdec_set_test_hook(99, 1) == sd.ERR_INVALID_ARG
+    assert lib.specdec_set_test_hook(-1, 0) == sd.ERR_INVALID_ARG
+    assert lib.specdec_set_test_hook(sd.HOOK_TREE_CLUSTER, 3) == sd.ERR_INVALID_ARG
+    assert lib.specdec_set_test_hook(sd.HOOK_CHAIN_ALL_ROWS, 2) == sd.ERR_INVALID_ARG
+    assert lib.specdec_set_test_hook(sd.HOOK_QUEUE_WAIT_US, -5) == sd.ERR_INVALID_ARG
+    with sd.test_hooks(tree_cluster=4, queue_wait_us=250):
+        assert lib.specdec_get_test_hook(sd.HOOK_TREE_CLUSTER) == 4
+        assert lib.specdec_get_test_hook(sd.HOOK_QUEUE_WAIT_US) == 250
+    assert lib.specdec_get_test_hook(sd.HOOK_TREE_CLUSTER) == 0
+    assert lib.specdec_get_test_hook(sd.HOOK_QUEUE_WAIT_US) == 0

@@ -26,15 +26,11 @@ def sd(built_library):
 
 
 @pytest.fixture(params=["one_launch", "two_pass"], autouse=True)
-def block_path(request, monkeypatch):
+def block_path(request, sd):
     """Every test runs on both implementations: the single launch that reads each row
-    once (default) and the statistics + mass kernels (SPECDEC_BLOCK_TWO_PASS=1, read by
-    the library at every call)."""
-    if request.param == "two_pass":
-        monkeypatch.setenv("SPECDEC_BLOCK_TWO_PASS", "1")
-    else:
-        monkeypatch.delenv("SPECDEC_BLOCK_TWO_PASS", raising=False)
-    return request.param
+    once (default) and the statistics + mass kernels (the library's test hook)."""
+    with sd.test_hooks(block_two_pass=int(request.param == "two_pass")):
+        yield request.param
 
 
 def _np(t):
@@ -44,7 +40,8 @@ def _np(t):
 
 
 def _run_and_check(sd, report, x, sample=None, workers=None):
-    report.name = report.name.split(" [")[0] + f" [{os.environ.get('SPECDEC_BLOCK_TWO_PASS') and 'two_pass' or 'one_launch'}]"
+    path = "two_pass" if sd.get_test_hook(sd.HOOK_BLOCK_TWO_PASS) else "one_launch"
+    report.name = report.name.split(" [")[0] + f" [{path}]"
     out = sd.verify_block(*(x[k] for k in KEYS))
     torch.cuda.synchronize()
     idx = slice(None) if sample is None else sample

@@ -11,6 +11,7 @@ import pytest
 import scipy.stats
 import torch
 
+from golden import read_fixture
 from oracle import specdec_oracle as so
 
 pytestmark = pytest.mark.gpu
@@ -39,8 +40,8 @@ def _chi2(counts, probs):
 
 @pytest.mark.parametrize("dtype,V", [("fp32", 6), ("bf16", 6), ("fp32", 8), ("bf16", 8)])
 def test_chain_output_law(sd, dtype, V):
-    """V = 6 rows are not 16-byte aligned (scalar-load kernels); V = 8 rows take the
-    streaming bulk-copy kernels."""
+    """V = 6 rows are not 16-byte aligned (scalar-load kernels); V = 8 rows (32 bytes in
+    fp32, 16 in bf16) take the left-to-right kernel."""
     gamma, T = 3, 0.8
     rng = np.random.default_rng(21)
     logits = rng.standard_normal((gamma + 1, V)) * 1.5
@@ -107,3 +108,100 @@ def test_tree_first_token_law(sd):
         second_after_node0 += torch.bincount(tok[via0, 1], minlength=V).cpu().numpy()
     assert _chi2(first, p0) > 1e-3
     assert _chi2(second_after_node0, p1) > 1e-3
+
+
+def _bigram_round(sd, LP, QQ, ctx, g):
+    """One verification round (gamma = 1) of the toy bigram model from contexts ctx: the
+    drafter proposes d ~ q(. | ctx); target rows p(. | ctx) and p(. | d)."""
+    n = ctx.numel()
+    d = torch.multinomial(QQ[ctx], 1, generator=g).view(n)
+    L = torch.stack([LP[ctx], LP[d]], 1).contiguous()
+    Q = QQ[ctx].unsqueeze(1).contiguous()
+    u = torch.rand(n, 2, generator=g, device=DEV)
+    out = sd.verify_chain(L, Q, d.view(n, 1).to(torch.int32), torch.ones(n, device=DEV), u)
+    assert (out["status"] == 0).all()
+    return out["tokens"].long(), out["num_accepted"].long()
+
+
+@pytest.mark.parametrize("V", [6, 8])
+def test_bigram_two_token_joint_law(sd, V):
+    """SD 20.5, "A broken sampler looks healthy on a speed dashboard": a toy bigram target
+    and drafter over V tokens; rounds of gamma = 1 from a start token until every sequence
+    has emitted two tokens; the joint law of (first, second) must be p(a | s) p(b | a) over
+    all V^2 cells (chi-square; V = 6: the page's 36 cells, rows of 24 bytes for the
+    scalar-load kernels; V = 8: 32-byte rows for the left-to-right kernel).  The
+    resample-from-p mistake (the extra token after a rejection drawn from p instead of the
+    residual), planted on the host in a copy of the outputs, must fail the same test."""
+    s0 = 3
+    rng = np.random.default_rng(11)
+    P = rng.dirichlet(np.ones(V) * 1.2, size=V)
+    Qd = rng.dirichlet(np.ones(V) * 1.2, size=V)
+    LP = torch.tensor(np.log(P), dtype=torch.float32, device=DEV)
+    QQ = torch.tensor(Qd, dtype=torch.float32, device=DEV)
+    Pw = np.stack([so.target_distribution(LP[c].double().cpu().numpy(), 1.0) for c in range(V)])
+    PW = torch.tensor(Pw, dtype=torch.float64, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(17)
+    good, bad = np.zeros(V * V), np.zeros(V * V)
+    for _ in range(ROUNDS // BATCH):
+        ctx = torch.full((BATCH,), s0, dtype=torch.long, device=DEV)
+        tok, J = _bigram_round(sd, LP, QQ, ctx, g)
+        first, second = tok[:, 0], torch.where(J == 1, tok[:, 1], torch.full_like(J, -1))
+        need = J == 0
+        tok2, J2 = _bigram_round(sd, LP, QQ, first[need], g)
+        second[need] = tok2[:, 0]
+        good += torch.bincount(first * V + second, minlength=V * V).cpu().numpy()
+        # the planted mistake: after a rejection the extra token comes from p, not the residual
+        bf = torch.where(need, torch.multinomial(PW[ctx].float(), 1, generator=g).view(-1), first)
+        bs = second.clone()
+        rej2 = J2 == 0
+        idx = torch.nonzero(need).view(-1)
+        bs[idx[rej2]] = torch.multinomial(PW[first[need][rej2]].float(), 1, generator=g).view(-1)
+        bad += torch.bincount(bf * V + bs, minlength=V * V).cpu().numpy()
+    joint = (Pw[s0][:, None] * Pw).reshape(-1)
+    assert _chi2(good, joint) > 1e-3
+    assert _chi2(bad, joint) < 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_accepted_length_iid_worked_example(sd, dtype):
+    """SD 20.5, "How many tokens a round produces, and the speedup": the worked example's
+    p and q (box "The rule by hand, three tokens") at every position, alpha = 0.7, gamma = 4:
+    E[J + 1] = (1 - 0.7^5) / 0.3 = 2.77310 within 4 standard errors over 10^6 rounds, and J
+    follows the capped geometric law.  The vocabulary is padded with zero-probability
+    tokens (logit -inf, q = 0) to 16-byte rows, so the left-to-right kernel runs."""
+    fx = read_fixture("worked_example_3token.txt")
+    p = np.array([float(v) for v in fx["p"]])
+    q = np.array([float(v) for v in fx["q"]])
+    gamma, V = 4, (4 if dtype == "fp32" else 8)
+    lrow = np.full(V, -np.inf)
+    lrow[:3] = np.log(p)
+    qrow = np.zeros(V)
+    qrow[:3] = q
+    lt = torch.tensor(lrow, dtype=torch.float32)
+    if dtype == "bf16":
+        lt = lt.to(torch.bfloat16)
+    pw = so.target_distribution(lt.double().numpy(), 1.0)
+    qt = torch.tensor(qrow, dtype=torch.float32)
+    alpha = so.acceptance_rate(pw, qt.double().numpy())
+    if dtype == "fp32":
+        assert abs(alpha - 0.7) < 1e-6  # the page's alpha (bf16 logits round p slightly)
+    L = lt.to(DEV).view(1, 1, V).expand(BATCH, gamma + 1, V).contiguous()
+    Q = qt.to(DEV).view(1, 1, V).expand(BATCH, gamma, V).contiguous()
+    Tt = torch.ones(BATCH, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(29)
+    hist = np.zeros(gamma + 1)
+    for _ in range(ROUNDS // BATCH):
+        d = torch.multinomial(Q.view(-1, V), 1, replacement=True, generator=g).view(BATCH, gamma).to(torch.int32)
+        u = torch.rand(BATCH, gamma + 1, generator=g, device=DEV)
+        out = sd.verify_chain(L, Q, d, Tt, u)
+        assert (out["status"] == 0).all()
+        hist += torch.bincount(out["num_accepted"].long(), minlength=gamma + 1).cpu().numpy()
+    law = np.array([alpha ** i * (1 - alpha) for i in range(gamma)] + [alpha ** gamma])
+    n = hist.sum()
+    mean = float((hist * np.arange(1, gamma + 2)).sum() / n)
+    sd_ = float(np.sqrt((law * (np.arange(1, gamma + 2) - (law * np.arange(1, gamma + 2)).sum()) ** 2).sum()))
+    expect = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(mean - expect) < 4 * sd_ / np.sqrt(n), (mean, expect)
+    if dtype == "fp32":
+        assert abs(expect - 2.77310) < 1e-5
+    assert _chi2(hist, law) > 1e-3

@@ -82,12 +82,12 @@ def test_tree_b32_n64_v32000(sd, medusa64):
 
 @pytest.mark.parametrize("C", ["1", "2", "4", "8"])
 @pytest.mark.parametrize("V,dtype", [(32008, "bf16"), (20004, "fp32"), (64, "bf16")])
-def test_tree_cluster_sizes(sd, medusa64, monkeypatch, C, V, dtype):
+def test_tree_cluster_sizes(sd, medusa64, hooks, C, V, dtype):
     """Rows split across clusters of 1, 2, 4 and 8 CTAs (a short last slice at V = 32008
     and 20004; at V = 64 each CTA of an 8-CTA cluster holds a single 16-byte vector).
     Spiked logits (1 N(0,1), +10 on child tokens) make most walks descend several levels."""
     parents, paths = medusa64
-    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    hooks(tree_cluster=int(C))
     stats = {"sequences": 0, "flagged": 0, "accepted": 0}
     for seed in range(3):
         x = workloads.make_tree_inputs(12, V, parents, paths, depth=4, seed=100 * seed + V % 97, device=DEV,
@@ -181,10 +181,10 @@ def test_tree_degenerate(sd):
 
 @pytest.mark.parametrize("C", ["1", "4"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_tree_degenerate_cluster_walk(sd, monkeypatch, C, dtype):
+def test_tree_degenerate_cluster_walk(sd, hooks, C, dtype):
     """The input errors of test_tree_degenerate on 16-byte rows (the cluster walk), plus
     errors in rows the walk reaches only after descending, and in rows it never reads."""
-    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    hooks(tree_cluster=int(C))
     V, D = 1024, 3
     parents = torch.tensor([-1, -1, 0, 0, 2], dtype=torch.int32, device=DEV)
     B = 10

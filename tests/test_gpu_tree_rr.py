@@ -159,10 +159,10 @@ def test_tree_rr_shapes(sd, parents, V, dtype):
 
 @pytest.mark.parametrize("C", ["1", "2", "4", "8"])
 @pytest.mark.parametrize("V,dtype", [(32008, "bf16"), (4096, "fp32"), (20004, "fp32"), (64, "bf16")])
-def test_tree_rr_cluster_sizes(sd, medusa_parents, monkeypatch, C, V, dtype):
+def test_tree_rr_cluster_sizes(sd, medusa_parents, hooks, C, V, dtype):
     """Rows split across clusters of 1, 2, 4 and 8 CTAs (sizes whose slices would not fit
     or would be empty fall back to the default); short last slices at 32008 and 20004."""
-    monkeypatch.setenv("SPECDEC_TREE_CLUSTER", C)
+    hooks(tree_cluster=int(C))
     rep = Report(f"tree_rr cluster {C} V={V} {dtype}")
     for seed in range(3):
         x = workloads.make_tree_rr_inputs(8, V, medusa_parents, depth=4, seed=40 + seed, device=DEV, dtype=dtype,
