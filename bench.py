@@ -56,16 +56,16 @@ FALLBACK_HBM_GBS = 6800.0
 # files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
 # as null once the sources differ.
 NCU_TRAFFIC = {
-    # profiles/chain_stream_b256_v128256.md: 525.37 MB read + 4.25 MB written (SPECDEC_CHAIN_SCAN=1)
+    # all-rows chain kernels (the test hook): 525.37 MB read + 4.25 MB written
     "chain_stats": {"bytes": 529_620_480, "src_sha": "e4f192c1e6151e13", "workload": "chain_b256_v128256", "rule": "chain"},
-    # profiles/chain_seq_b256_v128256.md: 320.69 MB read + 3.28 MB written (batch seed 0)
+    # left-to-right chain kernel: 320.69 MB read + 3.28 MB written (batch seed 0)
     "chain_seq": {"bytes": 323_976_192, "src_sha": "d901c79203301ed0", "workload": "chain_b256_v128256", "rule": "chain"},
-    # profiles/block_row_b256_v128256.md: 1446.00 MB read + 5.02 MB written (batch seed 0)
+    # one-launch block kernel: 1446.00 MB read + 5.02 MB written (batch seed 0)
     "block_fused": {"bytes": 1_451_024_640, "src_sha": "9909774bce867764", "workload": "chain_b256_v128256",
                     "rule": "block"},
-    # profiles/tree_walk_cluster_b32_n64_v32000.md: 2.30 MB read, 0 written (batch seed 0)
+    # Medusa walk on a cluster: 2.30 MB read, 0 written (batch seed 0)
     "tree_walk": {"bytes": 2_303_744, "src_sha": "50961ac4861b7cee", "workload": "tree_b32_n64_v32000", "rule": "tree"},
-    # profiles/tree_rr_b32_n64_v32000.md: 17.88 MB read, 0 written (batch seed 0)
+    # recursive rejection on a cluster: 17.88 MB read, 0 written (batch seed 0)
     "tree_rr": {"bytes": 17_878_528, "src_sha": "d3385b1d084f98dd", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
@@ -277,6 +277,58 @@ def cpu_oracle_rate(inputs_cpu: dict, target_seconds: float, max_seqs: int | Non
             break
     dt = time.perf_counter() - t0
     return n * g1 / dt, n, dt
+
+
+_ORACLE_WORKER = {}
+
+
+def _oracle_worker_init(folder: str, rule: str):
+    import numpy as np
+    sys.path.insert(0, str(ROOT))
+    for k in ("L", "q", "d", "T", "u"):
+        _ORACLE_WORKER[k] = np.load(os.path.join(folder, k + ".npy"), mmap_mode="r")
+    _ORACLE_WORKER["verify"] = oracle_rule(rule)
+
+
+def _oracle_worker_run(job):
+    """Worker w of n: sequences w, w + n, ... of the batch (cycling) for `seconds`."""
+    import numpy as np
+    w, n, seconds = job
+    W = _ORACLE_WORKER
+    B = W["u"].shape[0]
+    done, i, t0 = 0, w, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        b = i % B
+        W["verify"](np.asarray(W["L"][b]), np.asarray(W["q"][b]), np.asarray(W["d"][b]), float(W["T"][b]),
+                    np.asarray(W["u"][b]))
+        done += 1
+        i += n
+    return done
+
+
+def cpu_oracle_rate_all_cores(inputs_cpu: dict, target_seconds: float, rule: str = "chain"):
+    """The same oracle, one process per host core (a spawn-started pool over memory-mapped
+    inputs: this process holds a CUDA context), sequences split round-robin, for about
+    target_seconds; returns (rows/s, sequences, seconds, processes)."""
+    import multiprocessing as mp
+    import tempfile
+    import numpy as np
+    n = os.cpu_count() or 1
+    L = inputs_cpu["logits"]
+    L = L.float().numpy() if str(L.dtype) == "torch.bfloat16" else L.numpy()
+    arrays = {"L": L, "q": inputs_cpu["draft_probs"].numpy(), "d": inputs_cpu["draft_tokens"].numpy(),
+              "T": inputs_cpu["temperatures"].numpy(), "u": inputs_cpu["uniforms"].numpy()}
+    g1 = arrays["u"].shape[1]
+    with tempfile.TemporaryDirectory() as folder:
+        for k, v in arrays.items():
+            np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(v))
+        with mp.get_context("spawn").Pool(n, initializer=_oracle_worker_init, initargs=(folder, rule)) as pool:
+            pool.map(_oracle_worker_run, [(w, n, 0.05) for w in range(n)])  # workers up and warm
+            t0 = time.perf_counter()
+            done = pool.map(_oracle_worker_run, [(w, n, target_seconds) for w in range(n)])
+            dt = time.perf_counter() - t0
+    nseq = int(sum(done))
+    return nseq * g1 / dt, nseq, dt, n
 
 
 def run_reference(args, rank):
@@ -770,6 +822,11 @@ def main():
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{nseq} sequences ({nseq * (g + 1)} rows; {nseq / B:.1f} passes over the "
                                           f"{B} sequences of one batch), {secs:.1f} s"}
+        prate, pseq, psecs, procs = cpu_oracle_rate_all_cores(x0, args.cpu_seconds / 2, rule=args.rule)
+        line["cpu_baseline"]["all_cores"] = {
+            "value": prate, "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"{pseq} sequences of the same batch ({pseq * (g + 1)} rows), one process per host core "
+                      f"(os.cpu_count() = {procs}), {psecs:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
