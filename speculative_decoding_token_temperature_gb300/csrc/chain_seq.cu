@@ -777,6 +777,9 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   }
   // Every member's barriers exist before any member writes into another's shared memory.
   cluster_sync_all();
+  // The workspace counters are cleared by the kernel launched just before this one, which
+  // lets this launch start early (programmatic dependent launch): wait for it here.
+  grid_dependency_wait();
 
   const int R = P.gamma + 1;
   const int V = P.V;
@@ -1331,8 +1334,17 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   }
 }
 
+// Clears the workspace's counter block (counters, flags and queue words that must start at
+// zero) for the left-to-right kernel launched right after it, and lets that launch begin
+// at once: its set-up overlaps this kernel, and it waits for this kernel before it uses
+// the counters.
+__global__ void __launch_bounds__(256) seq_clear_kernel(uint4* p, size_t n) {
+  grid_launch_dependents();
+  for (size_t i = threadIdx.x; i < n; i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 template <typename T, bool kHost>
-cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
+cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream, bool pdl) {
   constexpr int smem = kSeqWarps * kSeqStages * kSeqChunkBytes;
   static unsigned long long configured = 0;
   static int max_clusters[64] = {};
@@ -1343,11 +1355,13 @@ cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
   cfg.blockDim = dim3(kSeqWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (!(configured & bit)) {
@@ -1364,18 +1378,24 @@ cudaError_t launch_typed(const ChainParams& P, cudaStream_t stream) {
   const int want = (P.B + kSeqGroups - 1) / kSeqGroups;
   const int clusters = min(max_clusters[dev & 63], want);
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kC));
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, chain_seq_kernel<T, kHost>, P);
 }
 
 }  // namespace
 
-cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream) {
+cudaError_t launch_chain_seq_clear(const ChainParams& P, cudaStream_t stream) {
+  return launch_kernel(seq_clear_kernel, dim3(1), dim3(256), 0, stream, 0, reinterpret_cast<uint4*>(P.ws.error),
+                       P.counter_bytes / 16);
+}
+
+cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream, bool pdl) {
   if (P.host_inputs) {
-    if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, true>(P, stream);
-    return launch_typed<float, true>(P, stream);
+    if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, true>(P, stream, pdl);
+    return launch_typed<float, true>(P, stream, pdl);
   }
-  if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, false>(P, stream);
-  return launch_typed<float, false>(P, stream);
+  if (ldt == SPECDEC_BF16) return launch_typed<uint16_t, false>(P, stream, pdl);
+  return launch_typed<float, false>(P, stream, pdl);
 }
 
 }  // namespace specdec

@@ -248,18 +248,25 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   const int path = stream_path ? 2 : (vec ? 1 : 0);
   size_t counter_bytes = 0;
   chain_workspace_layout(B, g, V, ldt, path, workspace, &P.ws, &counter_bytes);
-  // Arrival counters and the draw list count must start at zero; other regions are
-  // always written before they are read.
-  if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
-    return fail_cuda("clearing the workspace counters", e);
-  if (stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt)) {
+  // Arrival counters, queue words and flags must start at zero; other regions are always
+  // written before they are read.  The left-to-right kernel's launch clears them itself
+  // (a clearing kernel it overlaps); the other paths clear them here.
+  const bool left_to_right = stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt);
+  if (!left_to_right)
+    if (cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, s); e != cudaSuccess)
+      return fail_cuda("clearing the workspace counters", e);
+  if (left_to_right) {
+    P.counter_bytes = counter_bytes;
     P.grid_stats = device_sm_count();
     P.host_inputs = host_in ? 1 : 0;
     P.drop_draws = test_hook(SPECDEC_HOOK_CHAIN_DROP_DRAWS) ? 1 : 0;
     const int wait_us = test_hook(SPECDEC_HOOK_QUEUE_WAIT_US);
     P.queue_wait_ns = wait_us > 0 ? static_cast<unsigned long long>(wait_us) * 1000ull : 1000000000ull;
+    if (cudaError_t e = launch_chain_seq_clear(P, s); e != cudaSuccess) return fail_cuda("clearing the workspace counters", e);
+    // (kernel timing brackets the kernel alone with events: no early start then)
     ProfScope prof(SPECDEC_KERNEL_CHAIN_SEQ, s);
-    if (cudaError_t e = launch_chain_seq(P, ldt, s); e != cudaSuccess) return fail_cuda("left-to-right kernel", e);
+    if (cudaError_t e = launch_chain_seq(P, ldt, s, !prof.active); e != cudaSuccess)
+      return fail_cuda("left-to-right kernel", e);
     return SPECDEC_OK;
   }
   if (stream_path) {

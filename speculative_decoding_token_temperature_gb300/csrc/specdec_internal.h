@@ -120,6 +120,7 @@ struct ChainParams {
   int host_inputs;       // left-to-right kernel: logits and q may sit in pinned host memory
   int drop_draws;        // left-to-right kernel, test hook: queued draws are never marked published
   unsigned long long queue_wait_ns;  // left-to-right kernel: bound on waits for queued work
+  size_t counter_bytes;  // left-to-right kernel: the counter block at the workspace's start (cleared per call)
   int nch;               // streaming path: 4 KB chunks per logits row
   int nchd;              // streaming path: draw chunks per row
   int grid_stats, grid_draw;
@@ -165,8 +166,11 @@ cudaError_t launch_block_finish(const ChainParams& P, specdec_dtype ldt, cudaStr
 cudaError_t launch_block_fused(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
 bool block_fused_fits(int g, int V, specdec_dtype ldt);
 int device_sm_count();
-// Left-to-right chain verification reading rows only up to the first rejection.
-cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream);
+// Left-to-right chain verification reading rows only up to the first rejection: the kernel
+// that clears its counter block, then the kernel itself, which (pdl) may start while the
+// clearing kernel runs.
+cudaError_t launch_chain_seq_clear(const ChainParams& P, cudaStream_t stream);
+cudaError_t launch_chain_seq(const ChainParams& P, specdec_dtype ldt, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_chain_stats(const ChainParams& P, specdec_dtype ldt, bool vector_path,
                                cudaStream_t stream);
