@@ -56,17 +56,17 @@ FALLBACK_HBM_GBS = 6800.0
 # files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
 # as null once the sources differ.
 NCU_TRAFFIC = {
-    # all-rows chain kernels (the test hook): 525.37 MB read + 4.25 MB written
-    "chain_stats": {"bytes": 529_620_480, "src_sha": "e4f192c1e6151e13", "workload": "chain_b256_v128256", "rule": "chain"},
-    # left-to-right chain kernel: 320.69 MB read + 3.28 MB written (batch seed 0)
-    "chain_seq": {"bytes": 323_976_192, "src_sha": "d901c79203301ed0", "workload": "chain_b256_v128256", "rule": "chain"},
-    # one-launch block kernel: 1446.00 MB read + 5.02 MB written (batch seed 0)
-    "block_fused": {"bytes": 1_451_024_640, "src_sha": "9909774bce867764", "workload": "chain_b256_v128256",
+    # all-rows chain kernels (the test hook): 525.37 MB read + 4.53 MB written
+    "chain_stats": {"bytes": 529_893_888, "src_sha": "9f4f6cfafe3e2cb6", "workload": "chain_b256_v128256", "rule": "chain"},
+    # left-to-right chain kernel: 310.61 MB read + 5.61 MB written (batch seed 0)
+    "chain_seq": {"bytes": 316_219_648, "src_sha": "da2ec18b71139cd4", "workload": "chain_b256_v128256", "rule": "chain"},
+    # one-launch block kernel: 1445.90 MB read + 4.97 MB written (batch seed 0)
+    "block_fused": {"bytes": 1_450_869_760, "src_sha": "4827fd93253ec87d", "workload": "chain_b256_v128256",
                     "rule": "block"},
     # Medusa walk on a cluster: 2.30 MB read, 0 written (batch seed 0)
-    "tree_walk": {"bytes": 2_303_744, "src_sha": "50961ac4861b7cee", "workload": "tree_b32_n64_v32000", "rule": "tree"},
+    "tree_walk": {"bytes": 2_304_000, "src_sha": "34061ec3e192e131", "workload": "tree_b32_n64_v32000", "rule": "tree"},
     # recursive rejection on a cluster: 17.88 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_878_528, "src_sha": "d3385b1d084f98dd", "workload": "tree_rr_b32_n64_v32000",
+    "tree_rr": {"bytes": 17_878_784, "src_sha": "cf3cf10bf8a50ae2", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
 
@@ -626,6 +626,9 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-rows", action="store_true",
+                    help="chain rules: the all-rows streaming kernels instead of the left-to-right kernel "
+                         "(the library's test hook; for comparison)")
     ap.add_argument("--rule", choices=["chain", "block", "tree", "tree_recursive", "gumbel", "chain_varlen",
                                        "kv_compact"],
                     default="chain")
@@ -657,6 +660,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     _build.ensure_built()
     sd.load_library()
+    if args.all_rows:
+        sd.set_test_hook(sd.HOOK_CHAIN_ALL_ROWS, 1)
 
     B, g, V, dtype = workload_shape(args.workload)
     esize = 2 if dtype == "bf16" else 4
@@ -772,7 +777,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "rule": args.rule, "B": B, "gamma": g, "V": V,
                    "logits_dtype": dtype, "draft_probs_dtype": "fp32", "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2, {args.sets} seeded batches rotated"},
+                   "l2": f"inputs larger than L2, {args.sets} seeded batches rotated",
+                   **({"path": "all-rows kernels (library test hook)"} if args.all_rows else {})},
         "hbm_gbs_call": call_bytes / (ms_per_step / 1e3) / 1e9,
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
@@ -781,7 +787,9 @@ def main():
         "rows_read_per_step": rows_read,
         "kernels_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items() if v[1]},
         # the Gumbel call is one timed scope of 2 launches per wave of two rows
-        "gpu_launches": int(round(launches_per_step * args.steps)) * (2 * ((g + 2) // 2) if args.rule == "gumbel" else 1),
+        # (a left-to-right call also launches the one-block kernel that clears its counters)
+        "gpu_launches": int(round(launches_per_step * args.steps)) * (2 * ((g + 2) // 2) if args.rule == "gumbel" else 1)
+                        + (args.steps if kname == "chain_seq" else 0),
         "mean_accepted": statistics.mean(accepted),
         "clocks": clocks.summary(),
         "kernel_src_sha": kernel_source_sha(kname),
