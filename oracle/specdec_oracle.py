@@ -727,7 +727,7 @@ def verify_tree_sequence(logits, node_tokens, parents, T: float, u, max_depth: i
 
 
 def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_depth: int,
-                            want_cdf: bool = False) -> dict:
+                            want_cdf: bool = False, without_replacement: bool = False) -> dict:
     """Sampled verification of a token tree by recursive rejection, for one sequence.
 
     SD 20.5, box "Recursive rejection at a node with several children" (the multi-step
@@ -754,6 +754,17 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
     does; then, in walk order, the logits row of every visited node, q(s) of every tried
     child, and the whole q row of a node at its first rejection (when the residual needs
     it).  An error gives n_accepted -1 and -1 outputs.
+
+    without_replacement: Sequoia's variant (Chen et al.; SD 20.5, the paragraph after the
+    box's proof): a node's children were drawn without replacement, so each try has its
+    own draft distribution q_i -- q with the tokens of the children already rejected at the
+    node set to zero, renormalised -- used both in the test (u * q_i(s_i) < R_i(s_i)) and
+    in the residual (R_{i+1} = max(0, R_i - q_i) normalised).  READINGS: q_1 = q as given
+    (as everywhere else) and q_i = q / Z_i off the rejected tokens with
+    Z_i = 1 - sum of q at them (the renormaliser of a q that sums to 1); when Z_i <= 0
+    (q's mass is used up) q_i is zero, so the try follows the q(s) = 0 rule and a rejection
+    leaves R_i as it is; children drawn without replacement carry distinct tokens, so two
+    children of one node with the same token are an input error (BAD_TREE).
 
     Returns tokens [max_depth+1] (-1 padded), path [max_depth], n_accepted, status,
     margins [N] (|u[1+j] - R(s_j)/q(s_j)| for every tried child j, inf otherwise) and,
@@ -784,6 +795,12 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
     for t in node_tokens:
         if not (0 <= t < V):
             status |= STATUS_BAD_TOKEN
+    if without_replacement and not status & STATUS_BAD_TREE:
+        seen = set()
+        for j in range(n):
+            if (parents[j], node_tokens[j]) in seen:
+                status |= STATUS_BAD_TREE
+            seen.add((parents[j], node_tokens[j]))
     if not greedy and not np.all((u >= 0.0) & (u < 1.0)):
         status |= STATUS_BAD_UNIFORM
     if status & STATUS_ERROR_MASK:
@@ -812,11 +829,14 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
             qn = widen(q[row]) if children else None
             q_checked = False
             child = None
+            rejected, Zi = [], 1.0  # without replacement: tokens rejected here, q's mass left
             for j in children:
                 s = node_tokens[j]
                 qs = qn[s]
                 if not (np.isfinite(qs) and qs >= 0.0):
                     return fail(STATUS_BAD_PROB)
+                if without_replacement:  # q_i(s): children are distinct, so s is not rejected yet
+                    qs = qs / Zi if Zi > 0.0 else 0.0
                 if qs == 0.0:
                     status |= STATUS_ZERO_Q
                     out["margins"][j] = np.inf
@@ -831,7 +851,16 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
                     if not np.all(np.isfinite(qn) & (qn >= 0.0)):
                         return fail(STATUS_BAD_PROB)
                     q_checked = True
-                r = np.maximum(R - qn, 0.0)
+                if without_replacement:
+                    qi = np.zeros_like(qn)
+                    if Zi > 0.0:
+                        qi = qn / Zi
+                        qi[rejected] = 0.0
+                    rejected.append(s)
+                    Zi -= qn[s]
+                else:
+                    qi = qn
+                r = np.maximum(R - qi, 0.0)
                 if r.sum() > 0.0:
                     R = r / r.sum()
                 else:
@@ -852,10 +881,12 @@ def verify_tree_rr_sequence(logits, q, node_tokens, parents, T: float, u, max_de
     return out
 
 
-def verify_tree_rr(logits, q, node_tokens, parents, T, u, max_depth: int) -> dict:
+def verify_tree_rr(logits, q, node_tokens, parents, T, u, max_depth: int,
+                   without_replacement: bool = False) -> dict:
     """Batched recursive-rejection tree verification: a loop of verify_tree_rr_sequence."""
     B = np.asarray(logits).shape[0]
-    res = [verify_tree_rr_sequence(logits[b], q[b], node_tokens[b], parents, float(T[b]), u[b], max_depth)
+    res = [verify_tree_rr_sequence(logits[b], q[b], node_tokens[b], parents, float(T[b]), u[b], max_depth,
+                                   without_replacement=without_replacement)
            for b in range(B)]
     return {
         "tokens": np.stack([r["tokens"] for r in res]),
