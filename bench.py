@@ -475,13 +475,15 @@ def run_tree_rr(args, rank, world, local_rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
     cfg = {"workload": name, "rule": args.rule, "B": B, "N": N, "V": V, "max_depth": D,
            "logits_dtype": w["dtype"]}
+    wor = bool(getattr(args, "without_replacement", False)) and not medusa
     if not medusa:
         cfg["draft_probs_dtype"] = "fp32"
+        cfg["children"] = "drawn without replacement" if wor else "drafted i.i.d."
 
     def make(round_idx, device):
         if medusa:
             return workloads.tree_workload(name, parents, paths, round_idx, device)
-        return workloads.tree_rr_workload(name, parents, round_idx, device)
+        return workloads.tree_rr_workload(name, parents, round_idx, device, without_replacement=wor)
 
     def oracle_rate(x, seconds, max_seqs):
         L = x["logits"].float().numpy() if w["dtype"] == "bf16" else x["logits"].numpy()
@@ -493,7 +495,8 @@ def run_tree_rr(args, rank, world, local_rank):
             if medusa:
                 so.verify_tree_sequence(L[i], t[i], parents, float(T[i]), u[i], D)
             else:
-                so.verify_tree_rr_sequence(L[i], q[i], t[i], parents, float(T[i]), u[i], D)
+                so.verify_tree_rr_sequence(L[i], q[i], t[i], parents, float(T[i]), u[i], D,
+                                           without_replacement=wor)
             n += 1
             if time.perf_counter() - t0 >= seconds:
                 break
@@ -539,10 +542,11 @@ def run_tree_rr(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     verify = sd.verify_tree if medusa else sd.verify_tree_recursive
+    flags = {} if medusa else {"without_replacement": wor}
 
     def step(i, st=stream):
         x = sets[i % len(sets)]
-        verify(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=st)
+        verify(*(x[k] for k in keys), D, out=outs[i % len(sets)], stream=st, **flags)
 
     for i in range(args.warmup):
         step(i)
@@ -596,7 +600,7 @@ def run_tree_rr(args, rank, world, local_rank):
         roofline={"kernel": kernel, "bound": "latency", "achieved": achieved,
                   "peak": peak, "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback", "unit": "GB/s",
                   "frac": (achieved / peak) if achieved else None, "algorithmic_bytes_per_launch": alg_bytes,
-                  "traffic": recorded_traffic(kernel, name, args.rule)},
+                  "traffic": recorded_traffic(kernel, name, args.rule + ("_without_replacement" if wor else ""))},
         kernels_ms_per_launch={k: v[0] / v[1] for k, v in per_kernel.items() if v[1]},
         gpu_launches=int(round(sum(v[1] for v in per_kernel.values()))),
         mean_accepted=float(np.mean([o["num_accepted"].float().mean().item() for o in outs])),
@@ -629,6 +633,8 @@ def main():
     ap.add_argument("--all-rows", action="store_true",
                     help="chain rules: the all-rows streaming kernels instead of the left-to-right kernel "
                          "(the library's test hook; for comparison)")
+    ap.add_argument("--without-replacement", action="store_true",
+                    help="rule tree_recursive: every node's children drawn without replacement (Sequoia)")
     ap.add_argument("--rule", choices=["chain", "block", "tree", "tree_recursive", "gumbel", "chain_varlen",
                                        "kv_compact"],
                     default="chain")

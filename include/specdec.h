@@ -252,11 +252,22 @@ int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* no
  *                            (a residual summed to 0 after rounding; R_i is kept).
  * max_depth D bounds the number of nodes on any root path.  N >= 0, 1 <= D <= 64.  No
  * workspace is needed (specdec_tree_workspace_bytes applies and returns 0).
+ *
+ * flags: 0, or SPECDEC_TREE_WITHOUT_REPLACEMENT -- the children of every node were drawn
+ * without replacement (Sequoia, Chen et al.; SD 20.5, the paragraph after the box's
+ * proof): try i uses q_i, q with the tokens of the children already rejected at the node
+ * set to zero and renormalised by Z_i = 1 - (q at those tokens), in the test
+ * (u * q_i(s_i) < R_i(s_i)) and in the residual (R_{i+1} = (R_i - q_i)+ normalised).
+ * When Z_i <= 0 (q's mass is used up) q_i is zero: the try follows the ZERO_Q rule and a
+ * rejection leaves R_i.  Children drawn without replacement carry distinct tokens, so
+ * two children of one node with the same token are an input error (BAD_TREE).  Other
+ * flag bits: SPECDEC_ERR_INVALID_ARG.
  */
+#define SPECDEC_TREE_WITHOUT_REPLACEMENT 1
 int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const float* draft_probs,
                                   const int32_t* node_tokens, const int32_t* parents,
                                   const float* temperatures, const float* uniforms, int B, int N, int V,
-                                  int max_depth, int32_t* out_tokens, int32_t* out_path,
+                                  int max_depth, int flags, int32_t* out_tokens, int32_t* out_path,
                                   int32_t* out_num_accepted, int32_t* out_status, void* stream);
 
 /* ------------------------------------------------------------------------------------

@@ -23,6 +23,7 @@ __all__ = [
 F32, BF16 = 0, 1
 GREEDY_TEMPERATURE = 1e-3
 STATUS_TIMEOUT = 128
+TREE_WITHOUT_REPLACEMENT = 1  # specdec_verify_tree_recursive: children drawn without replacement
 
 # Test hooks of the library (specdec_set_test_hook): the library's own tests and sweeps.
 HOOK_CHAIN_ALL_ROWS, HOOK_BLOCK_TWO_PASS, HOOK_TREE_CLUSTER, HOOK_CHAIN_DROP_DRAWS, HOOK_QUEUE_WAIT_US = range(5)
@@ -88,7 +89,7 @@ def load_library():
     lib.specdec_verify_greedy.restype = i32
     lib.specdec_verify_tree.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.specdec_verify_tree.restype = i32
-    lib.specdec_verify_tree_recursive.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.specdec_verify_tree_recursive.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.specdec_verify_tree_recursive.restype = i32
     u64 = ctypes.c_uint64
     lib.specdec_gumbel_workspace_bytes.argtypes = [i32, i32]
@@ -385,13 +386,15 @@ def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth:
 
 
 def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperatures, uniforms, max_depth: int, *,
-                          out=None, stream=None) -> dict:
+                          without_replacement: bool = False, out=None, stream=None) -> dict:
     """Sampled tree verification by recursive rejection (specdec_verify_tree_recursive).
 
     logits [B, N+1, V] bf16/fp32; draft_probs [B, N+1, V] fp32 (row 0: the root's children
     were drafted from it, row 1+i: node i's children); node_tokens [B, N] int32; parents
     [N] int32; temperatures [B]; uniforms [B, N+1] (slot 1+j tests node j, slot 0 the final
-    draw).  Returns tokens [B, D+1], path [B, D], num_accepted [B], status [B]."""
+    draw).  without_replacement: every node's children were drawn without replacement
+    (SPECDEC_TREE_WITHOUT_REPLACEMENT).  Returns tokens [B, D+1], path [B, D],
+    num_accepted [B], status [B]."""
     lib = load_library()
     rt = _HostRoundTrip([logits])
     logits, draft_probs, node_tokens, parents, temperatures, uniforms = (
@@ -417,6 +420,7 @@ def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperature
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     rc = lib.specdec_verify_tree_recursive(_ptr(logits), code, _ptr(draft_probs), _ptr(node_tokens), _ptr(parents),
                                            _ptr(temperatures), _ptr(uniforms), B, N, V, D,
+                                           TREE_WITHOUT_REPLACEMENT if without_replacement else 0,
                                            _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["num_accepted"]),
                                            _ptr(out.get("status")), ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_tree_recursive")

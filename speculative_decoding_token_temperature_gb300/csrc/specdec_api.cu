@@ -525,10 +525,11 @@ int specdec_verify_tree(const void* logits, specdec_dtype ldt, const int32_t* no
 int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const float* draft_probs,
                                   const int32_t* node_tokens, const int32_t* parents,
                                   const float* temperatures, const float* uniforms, int B, int N, int V,
-                                  int max_depth, int32_t* out_tokens, int32_t* out_path,
+                                  int max_depth, int flags, int32_t* out_tokens, int32_t* out_path,
                                   int32_t* out_num_accepted, int32_t* out_status, void* stream) {
   if (!valid_dtype(ldt)) return fail(SPECDEC_ERR_INVALID_ARG, "unknown logits dtype");
   if (B <= 0 || N < 0 || V <= 0 || max_depth < 1) return fail(SPECDEC_ERR_INVALID_ARG, "bad sizes");
+  if (flags & ~SPECDEC_TREE_WITHOUT_REPLACEMENT) return fail(SPECDEC_ERR_INVALID_ARG, "unknown flag bits");
   if (!logits || !draft_probs || !temperatures || !uniforms || !out_tokens || !out_path || !out_num_accepted)
     return fail(SPECDEC_ERR_INVALID_ARG, "a required pointer is null");
   if (N > 0 && (!node_tokens || !parents)) return fail(SPECDEC_ERR_INVALID_ARG, "node tokens and parents needed");
@@ -548,6 +549,7 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
   P.out_path = out_path;
   P.out_J = out_num_accepted;
   P.out_status = out_status;
+  P.wor = (flags & SPECDEC_TREE_WITHOUT_REPLACEMENT) ? 1 : 0;
   const bool vec = rows_vectorizable(logits, V, elem_size(ldt)) && rows_vectorizable(draft_probs, V, 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope prof(SPECDEC_KERNEL_TREE_RR, s);
@@ -719,7 +721,7 @@ int specdec_profile_stop(void) {
   return SPECDEC_OK;
 }
 
-const char* specdec_version(void) { return "0.2.0"; }
+const char* specdec_version(void) { return "0.3.0"; }
 
 int specdec_set_test_hook(int hook, int value) {
   if (hook < 0 || hook >= SPECDEC_NUM_HOOKS) return SPECDEC_ERR_INVALID_ARG;

@@ -483,6 +483,50 @@ __device__ __forceinline__ void grid_launch_dependents() {
 
 namespace specdec {
 
+// Token trees whose children were drawn without replacement: SPECDEC_STATUS_BAD_TREE if
+// an earlier node (index below j) has node j's parent and token, else 0 -- from (parent,
+// token) pairs staged in shared memory, or from global memory with loads going out eight
+// pairs at a time.
+__device__ __forceinline__ int sibling_repeats_staged(const int* vp, const int* vt, int j) {
+  const int a = vp[j], t = vt[j];
+  int bad = 0;
+#pragma unroll 8
+  for (int i = 0; i < j; ++i) bad |= (vp[i] == a && vt[i] == t) ? 1 : 0;
+  return bad ? SPECDEC_STATUS_BAD_TREE : 0;
+}
+__device__ __forceinline__ int sibling_repeats(const int32_t* parents, const int32_t* toks, int j, int a, int t) {
+  int bad = 0, i = 0;
+  for (; i + 8 <= j; i += 8) {
+    int pa[8], tk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      pa[e] = __ldg(parents + i + e);
+      tk[e] = __ldg(toks + i + e);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bad |= (pa[e] == a && tk[e] == t) ? 1 : 0;
+  }
+  for (; i < j; ++i) bad |= (__ldg(parents + i) == a && __ldg(toks + i) == t) ? 1 : 0;
+  return bad ? SPECDEC_STATUS_BAD_TREE : 0;
+}
+
+// q's mass left at a tree node whose children were drawn without replacement,
+// Z = 1 - (q at the children rejected so far), as an unevaluated sum hi + lo of two
+// floats: each subtraction is exact (Knuth's two-sum), so Z keeps its accuracy however
+// small it gets, with fp32 adds only.
+struct MassLeft {
+  float hi = 1.f, lo = 0.f;
+  __device__ __forceinline__ void sub(float x) {
+    const float s = __fsub_rn(hi, x);
+    const float bv = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(-x, bv));
+    const float l = __fadd_rn(lo, err);
+    hi = __fadd_rn(s, l);
+    lo = __fsub_rn(l, __fsub_rn(hi, s));
+  }
+  __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+};
+
 // Kernel launch that returns its own error (no reliance on cudaGetLastError, which would
 // also report unrelated earlier errors of the calling thread).  pdl != 0 lets the kernel
 // start while the previous kernel in the stream finishes (programmatic dependent launch);

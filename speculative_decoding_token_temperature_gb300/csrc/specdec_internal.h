@@ -189,6 +189,7 @@ struct TreeParams {
   int32_t* out_path;
   int32_t* out_J;
   int32_t* out_status;
+  int wor;  // recursive rejection: children drawn without replacement
 };
 
 // The Medusa walk with rows split across a cluster of C CTAs: the cluster size for B

@@ -23,6 +23,12 @@
 // part and this path is a chain of dependent steps): a prefix carries at most a few dozen
 // roundings, a few 1e-6 relative, below the 1e-5 band in which the parity rule treats a
 // boundary as a tie; totals and prefixes are summed in the same warp order, so they agree.
+// Children drawn without replacement (P.wor; Sequoia): try i tests against q_i, q with the
+// rejected siblings' tokens zeroed and renormalised by Z_i = 1 - (q at them).  The residual
+// form stays (p - a q)+ / S with the raw q: (R_i - q_i)+ = (p - (a + S / Z_i) q)+ / S at
+// every token not yet rejected, and a rejected token already has p - a q < 0 (it was
+// rejected because R_i(s) < q_i(s)), so a_{i+1} = a_i + S_i / Z_i.  Z_i is kept in fp64 (a
+// few subtractions per node).  When Z_i <= 0, q_i is zero: the ZERO_Q test, no pass.
 // Only the rows the walk visits are read.  When a node's logits and q rows fit in shared
 // memory (V = 32000 bf16: 64 KB + 128 KB), they are staged there by bulk copies as the walk
 // reaches the node, and every pass reads shared memory instead of making a round trip to
@@ -47,6 +53,7 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
   static_assert(WARPS <= 32, "one lane per warp in the cross-warp steps");
   extern __shared__ __align__(128) unsigned char stage[];
   __shared__ int sh_i[32];
+  __shared__ int s_vp[NT], s_vt[NT];  // validation without replacement: (parent, token) per node
   __shared__ unsigned long long s_key[32];
   __shared__ float s_wz[32];     // per-warp mass of the current pass
   __shared__ float s_dw[32];     // per-warp mass of the weights the draw uses
@@ -124,6 +131,16 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
     if (!(a >= -1 && a < j)) st |= SPECDEC_STATUS_BAD_TREE;
     const int t = __ldg(toks + j);
     if (t < 0 || t >= V) st |= SPECDEC_STATUS_BAD_TOKEN;
+    if (P.wor && N <= NT) {  // (parent, token) pairs for the repeated-sibling check below
+      s_vp[j] = a;
+      s_vt[j] = t;
+    } else if (P.wor) {
+      st |= sibling_repeats(P.parents, toks, j, a, t);
+    }
+  }
+  if (P.wor && N <= NT) {
+    __syncthreads();
+    if (tid < N) st |= sibling_repeats_staged(s_vp, s_vt, tid);
   }
   st = Block<NT>::or_int(st, sh_i);
   if (!(st & SPECDEC_STATUS_BAD_TREE)) {
@@ -248,6 +265,7 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
         const float Z = s_Z, invZ = 1.f / Z;
         // the current residual is (p - a q)+ / S
         float a = 0.f, S = 1.f;
+        MassLeft zq;  // without replacement: q's mass left at this node
         bool q_checked = false;
         int ki = 0, par = 0;
         for (;;) {
@@ -262,10 +280,13 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
           }
           const int j = s_kids[ki++];
           const int s = __ldg(toks + j);
-          const float qs = A::qone(qrow, s);
-          if (!(qs >= 0.f && qs < kInf)) { st |= SPECDEC_STATUS_BAD_PROB; break; }
+          const float qraw = A::qone(qrow, s);
+          if (!(qraw >= 0.f && qraw < kInf)) { st |= SPECDEC_STATUS_BAD_PROB; break; }
+          // this try's q(s): as given, or q_i(s) without replacement
+          const float zv = zq.value();
+          const float qs = !P.wor ? qraw : (zv > 0.f ? qraw / zv : 0.f);
           const float ps = ex2((A::one(lrow, s) - m) * c) * invZ;
-          const float Rs = fmaxf(ps - a * qs, 0.f) / S;
+          const float Rs = fmaxf(ps - a * qraw, 0.f) / S;
           bool accept;
           if (qs == 0.f) {
             st |= SPECDEC_STATUS_ZERO_Q;
@@ -274,8 +295,12 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_kernel(const TreeParams P) {
             accept = __ldg(ub + 1 + j) * qs < Rs;
           }
           if (accept) { child = j; break; }
-          // rejected: S' = sum (p - (a + S) q)+, and the q row is read whole
-          const float an = a + S;
+          if (P.wor) {
+            zq.sub(qraw);
+            if (!(zv > 0.f)) continue;  // q_i = 0: the residual stays R_i
+          }
+          // rejected: S' = sum (p - (a + S / Z_i) q)+, and the q row is read whole
+          const float an = a + (P.wor ? S / zv : S);
           float rt = 0.f;
           int qbad = 0;
           for (int k = w0 + lane * VEC; k < w1; k += SPAN) {

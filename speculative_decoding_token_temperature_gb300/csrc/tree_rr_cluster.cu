@@ -8,7 +8,10 @@
 // extra token is drawn from the last R by inverse CDF and the walk ends.  Every residual is
 // (p - a q)+ / S for a scalar a (a_1 = 0, S_1 = 1; a rejection gives a <- a + S and
 // S <- sum (p - a q)+), so a test needs only p(s_i) and q(s_i), and a rejection costs one
-// pass over the node's logits and q rows.
+// pass over the node's logits and q rows.  Children drawn without replacement (P.wor;
+// Sequoia) test against q_i = q off the rejected siblings' tokens, renormalised by
+// Z_i = 1 - (q at them); the residual keeps its form with the raw q and a <- a + S / Z_i
+// (a rejected token already has p - a q < 0); Z_i in fp64; Z_i <= 0: q_i = 0, no pass.
 //
 // A cluster of C CTAs serves one sequence (as the Medusa walk of tree_walk_cluster.cu):
 // CTA r stages the contiguous slice r of the visited node's logits row (and q row, when
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
   extern __shared__ __align__(128) unsigned char stage[];
   __shared__ RRShared sh;
   __shared__ int sh_i[32];
+  __shared__ int s_vp[NT], s_vt[NT];  // validation without replacement: (parent, token) per node
   const T* sl = reinterpret_cast<const T*>(stage);                 // this slice of the logits row
   const float* sq = reinterpret_cast<const float*>(stage + qoff);  // this slice of the q row
   const uint32_t C = cluster_size(), rank = cluster_rank();
@@ -189,6 +193,12 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
     if (!(a >= -1 && a < j)) st |= SPECDEC_STATUS_BAD_TREE;
     const int t = __ldg(toks + j);
     if (t < 0 || t >= V) st |= SPECDEC_STATUS_BAD_TOKEN;
+    if (P.wor && N <= NT) {  // (parent, token) pairs for the repeated-sibling check below
+      s_vp[j] = a;
+      s_vt[j] = t;
+    } else if (P.wor) {
+      st |= sibling_repeats(P.parents, toks, j, a, t);
+    }
     int x = j, cnt = 0;  // nodes on the root path of j (bounded walk)
     while (x >= 0 && x < N && cnt <= D) { ++cnt; x = __ldg(P.parents + x); }
     if (cnt > D) st |= SPECDEC_STATUS_BAD_TREE;
@@ -199,6 +209,10 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
       if (!(uu >= 0.f && uu < 1.f)) st |= SPECDEC_STATUS_BAD_UNIFORM;
     }
   if (tid == 0 && !(Tb - Tb == 0.f)) st |= SPECDEC_STATUS_BAD_TEMPERATURE;
+  if (P.wor && N <= NT) {
+    __syncthreads();
+    if (tid < N) st |= sibling_repeats_staged(s_vp, s_vt, tid);
+  }
   st = Block<NT>::or_int(st, sh_i);
   cluster_wait();
 
@@ -315,6 +329,7 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
       } else {
         const float Z = sh.Z, invZ = 1.f / Z;
         float a = 0.f, S = 1.f;  // the current residual is (p - a q)+ / S
+        MassLeft zq;             // without replacement: q's mass left at this node
         bool q_checked = false;
         int ki = 0, par = 0;
         for (;;) {
@@ -328,11 +343,14 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
             continue;
           }
           const int j = sh.kids[ki];
-          const float lj = sh.kl[ki], qs = sh.kq[ki];
+          const float lj = sh.kl[ki], qraw = sh.kq[ki];
           ++ki;
-          if (!(qs >= 0.f && qs < kInf)) { st |= SPECDEC_STATUS_BAD_PROB; break; }
+          if (!(qraw >= 0.f && qraw < kInf)) { st |= SPECDEC_STATUS_BAD_PROB; break; }
+          // this try's q(s): as given, or q_i(s) without replacement
+          const float zv = zq.value();
+          const float qs = !P.wor ? qraw : (zv > 0.f ? qraw / zv : 0.f);
           const float ps = ex2((lj - m) * c) * invZ;
-          const float Rs = fmaxf(ps - a * qs, 0.f) / S;
+          const float Rs = fmaxf(ps - a * qraw, 0.f) / S;
           bool accept;
           if (qs == 0.f) {
             st |= SPECDEC_STATUS_ZERO_Q;
@@ -341,8 +359,12 @@ __global__ void __launch_bounds__(NT, 2) tree_rr_cluster_kernel(const TreeParams
             accept = __ldg(ub + 1 + j) * qs < Rs;
           }
           if (accept) { child = j; break; }
-          // rejected: the slice's part of S' = sum (p - (a + S) q)+ (and the q check)
-          const float an = a + S;
+          if (P.wor) {
+            zq.sub(qraw);
+            if (!(zv > 0.f)) continue;  // q_i = 0: the residual stays R_i
+          }
+          // rejected: the slice's part of S' = sum (p - (a + S / Z_i) q)+ (and the q check)
+          const float an = a + (P.wor ? S / zv : S);
           float rt = 0.f;
           int qbad = 0;
           for (int k = w0 + lane * VEC; k < w1; k += SPAN) {

@@ -99,10 +99,12 @@ def test_host_validation_rejects_before_launch(built_library):
     assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 1, 1, 8, p, p, None, None, ws, 1, None) == sd.ERR_WORKSPACE
     assert lib.specdec_verify_block(p, sd.BF16, p, p, p, p, 0, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
     # recursive-rejection tree walk: null q, bad depth
-    assert lib.specdec_verify_tree_recursive(p, sd.BF16, None, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
-    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
-    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 65, p, p, p, None, None) == sd.ERR_UNSUPPORTED
-    assert lib.specdec_verify_tree_recursive(p, 5, p, p, p, p, p, 1, 2, 8, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, None, p, p, p, p, 1, 2, 8, 2, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 0, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 65, 0, p, p, p, None, None) == sd.ERR_UNSUPPORTED
+    assert lib.specdec_verify_tree_recursive(p, 5, p, p, p, p, p, 1, 2, 8, 2, 0, p, p, p, None, None) == sd.ERR_INVALID_ARG
+    # flag bits other than SPECDEC_TREE_WITHOUT_REPLACEMENT
+    assert lib.specdec_verify_tree_recursive(p, sd.BF16, p, p, p, p, p, 1, 2, 8, 2, 2, p, p, p, None, None) == sd.ERR_INVALID_ARG
     # per-sequence draft counts: null counts; unaligned rows (V = 4 bf16) are refused
     assert lib.specdec_verify_chain_varlen(p, sd.BF16, p, p, p, p, None, 1, 1, 8, p, p, None, None, ws, 4096, None) == sd.ERR_INVALID_ARG
     assert lib.specdec_verify_chain_varlen(p, sd.BF16, p, p, p, p, p, 1, 1, 4, p, p, None, None, ws, 4096, None) == sd.ERR_UNSUPPORTED

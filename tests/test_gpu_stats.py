@@ -205,3 +205,42 @@ def test_accepted_length_iid_worked_example(sd, dtype):
     if dtype == "fp32":
         assert abs(expect - 2.77310) < 1e-5
     assert _chi2(hist, law) > 1e-3
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_tree_without_replacement_first_token_law(sd, dtype):
+    """SD 20.5, the paragraph after the proof of "Recursive rejection at a node with
+    several children" (Sequoia): with a node's children drawn without replacement, each
+    rejected token zeroed in q and q renormalised, the emitted token still follows p.
+    Three children at the root, drawn without replacement from q, 10^6 walks: the first
+    token's law is p (chi-square); the i.i.d. rule applied to the same children is not
+    (its error here is 0.05 on two tokens, found exactly in the oracle's pins)."""
+    V, k = 8, 3
+    p4 = np.array([0.10, 0.40, 0.30, 0.20])
+    q4 = np.array([0.40, 0.30, 0.20, 0.10])
+    lrow = np.full(V, -np.inf)
+    lrow[:4] = np.log(p4)
+    qrow = np.zeros(V)
+    qrow[:4] = q4
+    lt = torch.tensor(lrow, dtype=torch.float32)
+    if dtype == "bf16":
+        lt = lt.to(torch.bfloat16)
+    pw = so.target_distribution(lt.double().numpy(), 1.0)
+    L = lt.to(DEV).view(1, 1, V).expand(BATCH, k + 1, V).contiguous()
+    Q = torch.tensor(qrow, dtype=torch.float32, device=DEV).view(1, 1, V).expand(BATCH, k + 1, V).contiguous()
+    parents = torch.full((k,), -1, dtype=torch.int32, device=DEV)
+    T = torch.ones(BATCH, device=DEV)
+    qdraw = torch.tensor(qrow, dtype=torch.float64).view(1, V).expand(BATCH, V).contiguous()
+    g_cpu = torch.Generator().manual_seed(31)  # sequential draws without replacement, in draw order
+    g = torch.Generator(device=DEV).manual_seed(37)
+    good, bad = np.zeros(V), np.zeros(V)
+    for _ in range(ROUNDS // BATCH):
+        toks = torch.multinomial(qdraw, k, replacement=False, generator=g_cpu).to(torch.int32).to(DEV)
+        u = torch.rand(BATCH, k + 1, generator=g, device=DEV)
+        out = sd.verify_tree_recursive(L, Q, toks, parents, T, u, 1, without_replacement=True)
+        assert (out["status"] & 0xFF == 0).all()
+        good += torch.bincount(out["tokens"][:, 0].long(), minlength=V).cpu().numpy()
+        iid = sd.verify_tree_recursive(L, Q, toks, parents, T, u, 1)
+        bad += torch.bincount(iid["tokens"][:, 0].long(), minlength=V).cpu().numpy()
+    assert _chi2(good, pw) > 1e-3
+    assert _chi2(bad, pw) < 1e-6

@@ -195,14 +195,18 @@ def make_tree_inputs(B: int, V: int, parents, paths, *, depth: int, seed: int = 
 
 def make_tree_rr_inputs(B: int, V: int, parents, *, depth: int, seed: int = 0, device="cpu",
                         dtype: str = "bf16", recipe: str = "spikes", scale: float = 4.0, n_spikes: int = 8,
-                        spike: float = 8.0, noise=1.0, temps: str = "const:1.0") -> dict:
+                        spike: float = 8.0, noise=1.0, temps: str = "const:1.0",
+                        without_replacement: bool = False) -> dict:
     """Seeded inputs for sampled tree verification with per-node drafting distributions.
 
     Target logits per node (row 0: the root), a drafter that sees the target logits plus
     Gaussian noise (q = softmax((l + noise) / T), one-hot at its argmax for a greedy
     sequence), and every node's token drawn from its parent's q row, independently for
-    siblings.  Returns logits [B, N+1, V], draft_probs [B, N+1, V] fp32, node_tokens
-    [B, N] int32, parents [N] int32, temperatures [B], uniforms [B, N+1].
+    siblings -- or, with without_replacement, a node's children drawn in index order
+    without replacement from its q row (distinct tokens; a greedy sequence's one-hot row
+    gets a small floor first, since its walk does not use q).  Returns logits [B, N+1, V],
+    draft_probs [B, N+1, V] fp32, node_tokens [B, N] int32, parents [N] int32,
+    temperatures [B], uniforms [B, N+1].
     """
     g = _gen(device, seed)
     N = len(parents)
@@ -225,7 +229,14 @@ def make_tree_rr_inputs(B: int, V: int, parents, *, depth: int, seed: int = 0, d
         q[greedy] = hot
     del d
     parent_row = torch.tensor([0 if a < 0 else 1 + a for a in parents], dtype=torch.long, device=device)
-    if N:
+    if N and without_replacement:
+        node_tokens = torch.zeros(B, N, dtype=torch.long, device=device)
+        for a in sorted(set(parents)):
+            kids = [j for j in range(N) if parents[j] == a]
+            qa = q[:, 0 if a < 0 else 1 + a, :]
+            qa = torch.where(greedy.view(B, 1), qa + 1e-6, qa)
+            node_tokens[:, kids] = torch.multinomial(qa, len(kids), replacement=False, generator=g)
+    elif N:
         qp = q[:, parent_row, :].reshape(B * N, V)
         node_tokens = torch.multinomial(qp, 1, generator=g).view(B, N)
     else:
@@ -242,11 +253,13 @@ def make_tree_rr_inputs(B: int, V: int, parents, *, depth: int, seed: int = 0, d
     }
 
 
-def tree_rr_workload(name: str, parents, round_idx: int = 0, device="cpu") -> dict:
+def tree_rr_workload(name: str, parents, round_idx: int = 0, device="cpu",
+                     without_replacement: bool = False) -> dict:
     w = dict(TREE_RR_WORKLOADS[name])
     number = w.pop("number")
     return make_tree_rr_inputs(w.pop("B"), w.pop("V"), parents, depth=w.pop("depth"),
-                               seed=seed_for(number, round_idx), device=device, **w)
+                               seed=seed_for(number, round_idx), device=device,
+                               without_replacement=without_replacement, **w)
 
 
 def tree_workload(name: str, parents, paths, round_idx: int = 0, device="cpu") -> dict:
