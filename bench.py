@@ -56,17 +56,17 @@ FALLBACK_HBM_GBS = 6800.0
 # files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
 # as null once the sources differ.
 NCU_TRAFFIC = {
-    # all-rows chain kernels (the test hook): 525.37 MB read + 4.53 MB written
-    "chain_stats": {"bytes": 529_893_888, "src_sha": "9f4f6cfafe3e2cb6", "workload": "chain_b256_v128256", "rule": "chain"},
-    # left-to-right chain kernel: 310.61 MB read + 5.61 MB written (batch seed 0)
-    "chain_seq": {"bytes": 316_219_648, "src_sha": "da2ec18b71139cd4", "workload": "chain_b256_v128256", "rule": "chain"},
-    # one-launch block kernel: 1445.90 MB read + 4.97 MB written (batch seed 0)
-    "block_fused": {"bytes": 1_450_869_760, "src_sha": "4827fd93253ec87d", "workload": "chain_b256_v128256",
+    # all-rows chain kernels (the test hook): 525.37 MB read + 4.48 MB written
+    "chain_stats": {"bytes": 529_844_736, "src_sha": "94193918dae374cb", "workload": "chain_b256_v128256", "rule": "chain"},
+    # left-to-right chain kernel: 311.45 MB read + 5.22 MB written (batch seed 0)
+    "chain_seq": {"bytes": 316_666_624, "src_sha": "2310c8c574e15f6b", "workload": "chain_b256_v128256", "rule": "chain"},
+    # one-launch block kernel: 1446.09 MB read + 4.72 MB written (batch seed 0)
+    "block_fused": {"bytes": 1_450_804_480, "src_sha": "6b3ef2c8d20866f8", "workload": "chain_b256_v128256",
                     "rule": "block"},
     # Medusa walk on a cluster: 2.30 MB read, 0 written (batch seed 0)
-    "tree_walk": {"bytes": 2_304_000, "src_sha": "34061ec3e192e131", "workload": "tree_b32_n64_v32000", "rule": "tree"},
+    "tree_walk": {"bytes": 2_304_256, "src_sha": "2829f64e6a972a75", "workload": "tree_b32_n64_v32000", "rule": "tree"},
     # recursive rejection on a cluster: 17.88 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_878_784, "src_sha": "cf3cf10bf8a50ae2", "workload": "tree_rr_b32_n64_v32000",
+    "tree_rr": {"bytes": 17_883_648, "src_sha": "51a76a1993c3b0a7", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
 
