@@ -50,22 +50,43 @@ namespace {
 constexpr int kGumbelThreads = 512;
 constexpr int kGumbelMaxParts = 16;  // CTAs per row at most
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
+// Philox4x32-10's round keys, (k0, k1) of rounds 0..9: the key bumped by the Weyl
+// constants before every round but the first.  Built on the host once per call and
+// passed as a kernel parameter, so each round reads its keys from the constant bank.
+struct PhiloxKeys {
+  uint32_t k[20];
+};
+PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys ks;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
   for (int r = 0; r < 10; ++r) {
     if (r) {
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    ks.k[2 * r] = k0;
+    ks.k[2 * r + 1] = k1;
+  }
+  return ks;
+}
+
+// One Philox4x32-10 block (Salmon et al., SC 2011): ten rounds of two 32x32 -> 64-bit
+// products, their halves crossed with the other two words and the round keys.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& ks) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ ks.k[2 * r], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ ks.k[2 * r + 1], static_cast<uint32_t>(p0));
   }
   return c;
 }
 
+// u = ((x >> 9) + 1/2) 2^-23, built from the bits: 1 + (x >> 9) 2^-23 is the float with
+// those 23 mantissa bits, and subtracting 1 - 2^-24 from it is exact (Sterbenz).
 __device__ __forceinline__ float uniform_of(uint32_t x) {
-  return (static_cast<float>(x >> 9) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
+  return __fsub_rn(__uint_as_float(0x3F800000u | (x >> 9)), 0.99999994039535522f);
 }
 
 constexpr float kLog2Log2e = 0.52876637294489777f;  // log2(log2(e))
@@ -210,17 +231,26 @@ struct Partial {
 
 template <typename T, bool VEC>
 __device__ Partial race_part(const T* row, int V, int part, int parts, bool greedy, float c, uint32_t k, uint32_t b,
-                             uint32_t key0, uint32_t key1, Best* sh_b, float* sh_m) {
+                             const PhiloxKeys& ks, Best* sh_b, float* sh_m) {
   Best top;
   top.s = -kInf;
   top.i = INT_MAX;
   float mx = -kInf;
+  // the part's largest logit by group (entries past V are -inf): the group of the first
+  // strict maximum, then its lowest entry holding it
   for_groups<T, VEC, kGumbelThreads>(row, V, part, parts, [&](int j, const float (&v)[4]) {
     mx = max_nan(mx, max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])));
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (4 * j + e < V) take(top, v[e], 4 * j + e);
+    take(top, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), j);
   });
+  if (top.i != INT_MAX) {
+    const int j = top.i;
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = 4 * j + e < V ? Elem<T>::load(row, 4 * j + e) : -kInf;
+    int e = 0;
+    while (e < 3 && !(v[e] == top.s)) ++e;
+    top.i = 4 * j + e;
+  }
   block_best<kGumbelThreads>(top, mx, sh_b, sh_m);
   Partial out;
   out.mx = mx;
@@ -231,7 +261,7 @@ __device__ Partial race_part(const T* row, int V, int part, int parts, bool gree
     return out;
   }
   const int jt = top.i >> 2;
-  const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), k, b, 0u), key0, key1);
+  const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), k, b, 0u), ks);
   const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
   const float score_top = __fsub_rn(__fmul_rn(top.s, c), -neg_log2_xi(uniform_of(xts[top.i & 3])));
   const float cut = score_top - kNoiseMax;
@@ -244,7 +274,7 @@ __device__ Partial race_part(const T* row, int V, int part, int parts, bool gree
 #pragma unroll
     for (int e = 0; e < 4; ++e) a[e] = (4 * j + e < V) ? __fmul_rn(v[e], c) : -kInf;
     if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
-    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), k, b, 0u), key0, key1);
+    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), k, b, 0u), ks);
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -269,20 +299,25 @@ __device__ __forceinline__ const Partial* partials_of(const GumbelParams& P, int
 }
 
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_wave_kernel(const GumbelParams P, int wave) {
+__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_wave_kernel(const GumbelParams P, int wave,
+                                                                     const __grid_constant__ PhiloxKeys ks) {
   __shared__ Best sh_b[kGumbelThreads / 32];
   __shared__ float sh_m[kGumbelThreads / 32];
   const int part = blockIdx.x % P.parts;
   const int r = (blockIdx.x / P.parts) % kWaveRows;
   const int b = blockIdx.x / (P.parts * kWaveRows);
   const int k = wave * kWaveRows + r;
+  // Launched early behind the previous decision (programmatic dependent launch): let the
+  // next kernel start early too, then wait for the decisions this wave reads.
+  grid_launch_dependents();
+  grid_dependency_wait();
   if (k > P.G || __ldcg(P.state + b) != 0) return;  // past the last row, or the round is decided
   const float Tb = __ldg(P.temps + b);
   const bool greedy = !(Tb >= SPECDEC_GREEDY_TEMPERATURE);
   const float c = greedy ? 1.f : kLog2e / Tb;
   const T* row = static_cast<const T*>(P.logits) + (static_cast<int64_t>(b) * (P.G + 1) + k) * P.V;
   const Partial out = race_part<T, VEC>(row, P.V, part, P.parts, greedy, c, static_cast<uint32_t>(k),
-                                        static_cast<uint32_t>(b), P.key0, P.key1, sh_b, sh_m);
+                                        static_cast<uint32_t>(b), ks, sh_b, sh_m);
   if (threadIdx.x == 0)
     reinterpret_cast<Partial*>(P.partials)[(static_cast<int64_t>(b) * kWaveRows + r) * P.parts + part] = out;
 }
@@ -290,6 +325,8 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_wave_kernel(const Gu
 // One thread per sequence: merge the parts of the wave's rows in order and decide.
 __global__ void __launch_bounds__(128) gumbel_decide_kernel(const GumbelParams P, int wave) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  grid_launch_dependents();
+  grid_dependency_wait();  // the wave's parts
   if (b >= P.B || P.state[b] != 0) return;
   const int R = P.G + 1;
   const float Tb = __ldg(P.temps + b);
@@ -342,9 +379,9 @@ __global__ void __launch_bounds__(128) gumbel_decide_kernel(const GumbelParams P
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const float* __restrict__ q, uint32_t key0,
-                                                                      uint32_t key1, int G, int V,
-                                                                      int32_t* __restrict__ out) {
+__global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const float* __restrict__ q,
+                                                                      const __grid_constant__ PhiloxKeys ks, int G,
+                                                                      int V, int32_t* __restrict__ out) {
   __shared__ Best sh_b[kGumbelThreads / 32];
   __shared__ float sh_m[kGumbelThreads / 32];
   const int row = blockIdx.x;  // b * G + k
@@ -368,7 +405,7 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
   const int jt = top.i >> 2;
   const uint4 xt = philox4x32_10(make_uint4(static_cast<uint32_t>(jt), static_cast<uint32_t>(k),
                                             static_cast<uint32_t>(b), 0u),
-                                 key0, key1);
+                                 ks);
   const uint32_t xts[4] = {xt.x, xt.y, xt.z, xt.w};
   const float score_top = __fadd_rn(log2f(top.s), neg_log2_xi(uniform_of(xts[top.i & 3])));
   const float cut = score_top - kNoiseMax;
@@ -382,7 +419,7 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
     if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) < cut) return;
     const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
                                              static_cast<uint32_t>(b), 0u),
-                                  key0, key1);
+                                  ks);
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -397,8 +434,8 @@ __global__ void __launch_bounds__(kGumbelThreads, 2) gumbel_draft_kernel(const f
 }
 
 // The shared noise itself: out[(b * R + k) * V + i] = G of entry i, row k, sequence b.
-__global__ void __launch_bounds__(256) gumbel_noise_kernel(uint32_t key0, uint32_t key1, int B, int R, int V,
-                                                           float* __restrict__ out) {
+__global__ void __launch_bounds__(256) gumbel_noise_kernel(const __grid_constant__ PhiloxKeys ks, int B, int R,
+                                                           int V, float* __restrict__ out) {
   const int ng = (V + 3) / 4;
   const int64_t total = static_cast<int64_t>(B) * R * ng;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
@@ -408,7 +445,7 @@ __global__ void __launch_bounds__(256) gumbel_noise_kernel(uint32_t key0, uint32
     const int k = static_cast<int>(rowi % R), b = static_cast<int>(rowi / R);
     const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(k),
                                              static_cast<uint32_t>(b), 0u),
-                                  key0, key1);
+                                  ks);
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -422,32 +459,52 @@ cudaError_t launch_gumbel_noise(uint64_t seed, int B, int R, int V, float* out, 
   const int64_t total = static_cast<int64_t>(B) * R * ((V + 3) / 4);
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 8);
   return launch_kernel(gumbel_noise_kernel, dim3(static_cast<unsigned>(std::max<int64_t>(blocks, 1))), dim3(256), 0,
-                       stream, 0, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), B, R, V, out);
+                       stream, 0, philox_keys(seed), B, R, V, out);
 }
 
 cudaError_t launch_gumbel_verify(const GumbelParams& P, specdec_dtype ldt, bool vec, cudaStream_t stream) {
   const int waves = (P.G + 1 + kWaveRows - 1) / kWaveRows;
   const dim3 grid(static_cast<unsigned>(P.B) * kWaveRows * static_cast<unsigned>(P.parts)), block(kGumbelThreads);
   const dim3 dgrid((P.B + 127) / 128), dblock(128);
+  const PhiloxKeys ks = philox_keys(static_cast<uint64_t>(P.key0) | (static_cast<uint64_t>(P.key1) << 32));
+  // Every launch after the first starts while its predecessor finishes (programmatic
+  // dependent launch); each kernel waits for its predecessor's results before reading them.
   for (int w = 0; w < waves; ++w) {
     cudaError_t e;
+    const int pdl = w > 0 ? 1 : 0;
     if (ldt == SPECDEC_BF16)
-      e = vec ? launch_kernel(gumbel_wave_kernel<uint16_t, true>, grid, block, 0, stream, 0, P, w)
-              : launch_kernel(gumbel_wave_kernel<uint16_t, false>, grid, block, 0, stream, 0, P, w);
+      e = vec ? launch_kernel(gumbel_wave_kernel<uint16_t, true>, grid, block, 0, stream, pdl, P, w, ks)
+              : launch_kernel(gumbel_wave_kernel<uint16_t, false>, grid, block, 0, stream, pdl, P, w, ks);
     else
-      e = vec ? launch_kernel(gumbel_wave_kernel<float, true>, grid, block, 0, stream, 0, P, w)
-              : launch_kernel(gumbel_wave_kernel<float, false>, grid, block, 0, stream, 0, P, w);
+      e = vec ? launch_kernel(gumbel_wave_kernel<float, true>, grid, block, 0, stream, pdl, P, w, ks)
+              : launch_kernel(gumbel_wave_kernel<float, false>, grid, block, 0, stream, pdl, P, w, ks);
     if (e != cudaSuccess) return e;
-    if ((e = launch_kernel(gumbel_decide_kernel, dgrid, dblock, 0, stream, 0, P, w)) != cudaSuccess) return e;
+    if ((e = launch_kernel(gumbel_decide_kernel, dgrid, dblock, 0, stream, 1, P, w)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 int gumbel_parts(int B) {
-  // about four CTAs per SM in the first wave (two resident at a time)
-  const int want = 4 * device_sm_count();
-  const int parts = (want + B * kWaveRows - 1) / (B * kWaveRows);
-  return parts < 1 ? 1 : (parts > kGumbelMaxParts ? kGumbelMaxParts : parts);
+  // At least about four CTAs per SM in the first wave (two resident at a time), and of
+  // the part counts up to twice that, the one whose last round of resident CTAs is the
+  // fullest (fewest SMs idle at the end of the wave).
+  const int slots = 2 * device_sm_count();
+  const int rows = B * kWaveRows;
+  int lo = (2 * slots + rows - 1) / rows;
+  lo = lo < 1 ? 1 : (lo > kGumbelMaxParts ? kGumbelMaxParts : lo);
+  const int hi = std::min(kGumbelMaxParts, 2 * lo);
+  int best = lo;
+  double best_fill = 0.0;
+  for (int p = lo; p <= hi; ++p) {
+    const int64_t ctas = static_cast<int64_t>(rows) * p;
+    const int64_t rounds = (ctas + slots - 1) / slots;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(rounds * slots);
+    if (fill > best_fill + 0.02) {
+      best = p;
+      best_fill = fill;
+    }
+  }
+  return best;
 }
 
 size_t gumbel_workspace_bytes(int B) {
@@ -457,10 +514,10 @@ size_t gumbel_workspace_bytes(int B) {
 
 cudaError_t launch_gumbel_draft(const float* q, uint64_t seed, int B, int G, int V, bool vec, int32_t* out,
                                 cudaStream_t stream) {
-  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  const PhiloxKeys ks = philox_keys(seed);
   const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(G)), block(kGumbelThreads);
-  if (vec) return launch_kernel(gumbel_draft_kernel<true>, grid, block, 0, stream, 0, q, k0, k1, G, V, out);
-  return launch_kernel(gumbel_draft_kernel<false>, grid, block, 0, stream, 0, q, k0, k1, G, V, out);
+  if (vec) return launch_kernel(gumbel_draft_kernel<true>, grid, block, 0, stream, 0, q, ks, G, V, out);
+  return launch_kernel(gumbel_draft_kernel<false>, grid, block, 0, stream, 0, q, ks, G, V, out);
 }
 
 }  // namespace specdec
