@@ -68,6 +68,21 @@ def test_all_rows_path_greedy_call(sd, hooks):
         assert np.array_equal(_np(out["tokens"])[b], o["tokens"])
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 1_048_576), ("fp32", 786_432)])
+def test_vocabulary_at_the_left_to_right_limit(sd, dtype, V):
+    """The largest vocabulary the left-to-right kernel takes (a full chunk table in both
+    members): it runs that kernel, and matches the oracle."""
+    rep = ParityReport(f"V={V} {dtype} (left-to-right limit)")
+    for seed in range(2):
+        x = workloads.make_chain_inputs(2, 2, V, dtype, seed=10 + seed, device=DEV, recipe="spikes", scale=2.0,
+                                        n_spikes=4, spike=8.0, noise=0.5, temps="const:1.0")
+        with sd.KernelTimer() as kt:
+            _check(sd, rep, x, workers=1)
+            launches = kt.read()
+        assert launches["chain_seq"][1] == 1 and launches["chain_stats"][1] == 0, launches
+    assert not rep.failures, rep.failures[:5]
+
+
 @pytest.mark.parametrize("dtype,V", [("bf16", 1_048_576 + 1024), ("fp32", 786_432 + 512)])
 def test_vocabulary_beyond_the_left_to_right_limit(sd, dtype, V):
     """One past the left-to-right kernel's chunk table: the all-rows kernels serve it."""
@@ -75,7 +90,10 @@ def test_vocabulary_beyond_the_left_to_right_limit(sd, dtype, V):
     for seed in range(2):
         x = workloads.make_chain_inputs(2, 2, V, dtype, seed=seed, device=DEV, recipe="spikes", scale=2.0,
                                         n_spikes=4, spike=8.0, noise=0.5, temps="const:1.0")
-        _check(sd, rep, x, workers=1)
+        with sd.KernelTimer() as kt:
+            _check(sd, rep, x, workers=1)
+            launches = kt.read()
+        assert launches["chain_seq"][1] == 0 and launches["chain_stats"][1] == 1, launches
     assert not rep.failures, rep.failures[:5]
 
 
