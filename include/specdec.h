@@ -273,7 +273,7 @@ int specdec_verify_tree_recursive(const void* logits, specdec_dtype ldt, const f
 /* ------------------------------------------------------------------------------------
  * Gumbel-coupled verification (Art of Guessing, "Gumbel coupling", Daliri et al.).
  *
- * The drafter and the target share the noise g_k at position k: the drafter proposed
+ * The drafter and the target use the same noise g_k at position k: the drafter proposed
  * x_k = argmax_i (log q_k(i) + g_k,i) (specdec_gumbel_draft below), the target samples
  * t_k = argmax_i (log p_k(i) + g_k,i) with p_k = softmax(logits[b, k, :] / T); the round keeps
  * x_0..x_{n-1} for the first n with x_n != t_n (n = g if none) and appends t_n.  The emitted

@@ -151,10 +151,9 @@ def verify_chain_sequence(logits, q, drafts, T: float, u, want_cdf: bool = False
       extra token y ~ (p_J - q_J)+ normalised, with q_gamma == 0 (bonus from p_gamma)
       emit x_0 .. x_{J-1}, y
 
-    The positions are evaluated left to right and evaluation stops at the first
-    rejection (SD 20.5, "A whole round of speculative sampling": the rule is applied to
-    the drafts from left to right and stops at the first rejection; the drafts after it
-    are discarded).  READING: only what is evaluated is validated -- row i, draft i,
+    The positions are evaluated in order and evaluation ends at the first rejected
+    draft (SD 20.5, "A whole round of speculative sampling": the drafts are tested one
+    after another and the round ends at the first one rejected, dropping the rest).  READING: only what is evaluated is validated -- row i, draft i,
     q_i(x_i) and u_i for i <= J, u_gamma and the q row of the draw -- and p_draft is NaN
     after J.
 
@@ -467,10 +466,10 @@ def verify_block(logits, q, drafts, T, u) -> dict:
 
 # ---------------------------------------------------------------------------------
 # Gumbel coupling (Art of Guessing, "Speculative sampling" -> the Gumbel-max trick and
-# "Gumbel coupling", Daliri et al.): the drafter and the target share the noise g_k at
+# "Gumbel coupling", Daliri et al.): the drafter and the target use the same noise g_k at
 # position k; the drafter proposes argmax(log q_k + g_k), the target samples
-# argmax(log p_k + g_k), and the round keeps the longest agreeing prefix plus the target's
-# token at the first disagreement.
+# argmax(log p_k + g_k), and the round keeps the drafts up to the first position where the
+# two differ, then emits the target's sample there.
 #
 # The noise is not an input: both sides generate it with Philox4x32-10 (Salmon, Moraes,
 # Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), written here from
@@ -627,7 +626,7 @@ def verify_greedy_sequence(logits, drafts) -> dict:
 # ---------------------------------------------------------------------------------------
 
 def tree_depths(parents) -> np.ndarray:
-    """depth(i) = number of ancestors of node i; children of the prefix have depth 0.
+    """depth(i) = number of ancestors of node i (a node whose parent is the prefix: 0).
 
     SD 20.5, "Token tree and tree attention".  Parents must satisfy par(i) in [-1, i).
     """
@@ -643,8 +642,9 @@ def tree_depths(parents) -> np.ndarray:
 def build_tree_mask(parents, prefix_len: int):
     """Tree-attention mask M [n, P+n] (bool) and position ids P + depth (int64).
 
-    SD 20.5, "Token tree and tree attention": node i sees every prefix position, itself
-    and its ancestors, nothing else; its position id is P + depth(i).  Plain ancestor
+    SD 20.5, "Token tree and tree attention": node i attends to all P prefix positions,
+    to its own ancestors and to itself, and to no other node; its position id is
+    P + depth(i).  Plain ancestor
     walk.  Returns (mask, position_ids, depth).
     """
     parents = [int(x) for x in parents]

@@ -1,9 +1,9 @@
 // Gumbel-coupled verification and the drafter's shared-noise sampler.
 //
-// Art of Guessing, "Gumbel coupling" (Daliri et al.): the drafter and the target share the
-// noise g_k at draft position k.  The drafter proposes x_k = argmax_i (log q_k(i) + g_k,i);
-// the target samples t_k = argmax_i (log p_k(i) + g_k,i); the round keeps the longest
-// prefix with x_k == t_k and appends the target's token at the first disagreement.
+// Art of Guessing, "Gumbel coupling" (Daliri et al.): the drafter and the target use the
+// same noise g_k at draft position k.  The drafter proposes x_k = argmax_i (log q_k(i) + g_k,i);
+// the target samples t_k = argmax_i (log p_k(i) + g_k,i); the round keeps the drafts while
+// x_k == t_k and emits t_k at the first position where they differ.
 // Verification is exact matching, and the emitted text is what the target alone samples
 // with that noise, whatever the drafter.
 //

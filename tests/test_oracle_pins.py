@@ -311,8 +311,8 @@ def test_status_flags_and_degenerate_cases():
 
 
 def test_positions_after_the_first_rejection_are_not_evaluated():
-    """SD 20.5, "A whole round of speculative sampling": the rule runs left to right and
-    stops at the first rejection; what lies after it is never looked at."""
+    """SD 20.5, "A whole round of speculative sampling": drafts are tested in order and
+    the round ends at the first rejected one, so later positions are never examined."""
     l = np.array([[0.0, 0.0], [np.nan, 0.0], [0.0, 0.0]])
     q = np.array([[1.0, 0.0], [0.5, 0.5]])
     r = so.verify_chain_sequence(l, q, [0, 99], 1.0, [0.9, 0.5, 0.25])
