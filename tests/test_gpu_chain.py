@@ -103,6 +103,8 @@ def test_chain_b512_v152064_full_rounds(sd):
     (3, 1, 1, "fp32"), (2, 2, 7, "bf16"), (5, 3, 1001, "fp32"), (4, 4, 1001, "bf16"),
     (2, 16, 4099, "bf16"), (3, 2, 16384 + 8, "bf16"), (2, 3, 3 * 8192 + 4, "fp32"),
     (1, 1, 8, "fp32"), (7, 5, 50000, "bf16"), (2, 255, 64, "fp32"),
+    (4, 31, 8192, "bf16"), (3, 31, 6144 + 4, "fp32"),  # the left-to-right kernel's longest chains
+    (300, 2, 1024, "bf16"),                              # more sequences than teams
 ])
 def test_chain_ragged_shapes(sd, B, gamma, V, dtype):
     rep = ParityReport(f"ragged B={B} g={gamma} V={V} {dtype}")
