@@ -114,6 +114,18 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
  */
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
 
+/* Workspace for host-resident logits: specdec_chain_workspace_bytes plus room for one
+ * device copy of a logits row per sequence (B * V * element size, rounded up to 256
+ * bytes).  Given a workspace at least this large, with logits in pinned host memory, the
+ * left-to-right kernel also writes each row it streams for a sequence's chain into that
+ * sequence's copy, and a draw from that row (the residual at a rejection, or the bonus
+ * row) reads the copy from device memory instead of reading the row a second time over
+ * the host link.  A smaller workspace (at least specdec_chain_workspace_bytes) gives the
+ * same results and reads drawn rows from the host again.  Device-resident logits, and
+ * greedy-only calls, never use the copy.  The same sizes serve
+ * specdec_verify_chain_varlen.  Returns 0 for invalid sizes or dtype. */
+size_t specdec_chain_host_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
+
 int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* draft_probs,
                          const int32_t* draft_tokens, const float* temperatures,
                          const float* uniforms, int B, int g, int V, int32_t* out_tokens,

@@ -72,6 +72,8 @@ def load_library():
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.specdec_chain_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.specdec_chain_workspace_bytes.restype = sz
+    lib.specdec_chain_host_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.specdec_chain_host_workspace_bytes.restype = sz
     lib.specdec_greedy_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.specdec_greedy_workspace_bytes.restype = sz
     lib.specdec_block_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -298,6 +300,10 @@ def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, 
         if with_p_draft:
             out["p_draft"] = torch.empty(B, g, dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if rows_on_host and logits.device.type == "cpu":
+        # room for the device copy of each sequence's latest row (drawn rows are then not
+        # read over the host link twice)
+        ws_entry = "specdec_chain_host_workspace_bytes"
     ws, wsb = _workspace(int(getattr(lib, ws_entry)(B, g, V, code)), dev, s.cuda_stream)
     fn = getattr(lib, entry) if isinstance(entry, str) else entry
 

@@ -318,16 +318,18 @@ enum : int { kTaskRow = 1, kTaskDraw = 2, kTaskDrawP = 3, kTaskAhead = 4 };
 
 // A task entry: 32 bytes, in the global rings and in a team's mailbox.
 //   e0 = (sequence b (-1: no more work), row | kind << 8 | warnings << 16, m, Z)
-//   e1 = (T, 0, 0, 0)
+//   e1 = (T, cached, 0, 0)
 // (m, Z) are the drawn row's maximum and normaliser for draw tasks; the warnings are
-// the sequence's status bits above the error byte, shifted down by 8.
+// the sequence's status bits above the error byte, shifted down by 8; `cached` (draw
+// tasks, host-resident logits) says that the drawn row's device copy is in place.
 struct Entry {
   int b, row, kind, warn;
   float m, Z, T;
+  int cached = 0;
 };
 __device__ __forceinline__ void pack_entry(const Entry& e, float4& e0, float4& e1) {
   e0 = make_float4(__int_as_float(e.b), __int_as_float(e.row | (e.kind << 8) | (e.warn << 16)), e.m, e.Z);
-  e1 = make_float4(e.T, 0.f, 0.f, 0.f);
+  e1 = make_float4(e.T, __int_as_float(e.cached), 0.f, 0.f);
 }
 __device__ __forceinline__ Entry unpack_entry(const float4& e0, const float4& e1) {
   Entry e;
@@ -339,6 +341,7 @@ __device__ __forceinline__ Entry unpack_entry(const float4& e0, const float4& e1
   e.m = e0.z;
   e.Z = e0.w;
   e.T = e1.x;
+  e.cached = __float_as_int(e1.y);
   return e;
 }
 
@@ -811,6 +814,8 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     Task t;
     t.kind = e.kind == kTaskAhead ? kTaskRow : e.kind;
     t.src = logits + (static_cast<int64_t>(e.b) * R + e.row) * row_bytes;
+    if constexpr (kHost)  // a drawn row whose device copy is in place: read it, not the host
+      if (t.kind != kTaskRow && e.cached) t.src = P.row_cache + static_cast<int64_t>(e.b) * row_bytes;
     t.q = (e.kind == kTaskDraw && e.row < gamma_of(e.b)) ? P.q + (static_cast<int64_t>(e.b) * P.gamma + e.row) * V
                                                           : nullptr;
     t.lo = (t.kind == kTaskRow) ? c0 : d0;
@@ -880,7 +885,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   int s_b = 0, s_J = 0, s_par = 0;
   long long s_base = 0, s_target = 0;
   float s_m = 0.f, s_c = 0.f, s_invZ = 1.f;
-  bool s_noq = true;
+  bool s_noq = true, s_cached = false;
 
   while (cur.b >= 0 && tm.ok) {
     const int par = static_cast<int>(t & 1u);
@@ -963,6 +968,10 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     } else if (tc.kind == kTaskRow) {
       float ml = -kInf, Zl = 0.f;
       int zl = INT_MAX;
+      // host-resident logits: this chain's own row also goes to the sequence's device copy,
+      // which a draw from this row then reads instead of the host (rows computed ahead for
+      // another team's chain are not copied)
+      const bool to_cache = kHost && P.row_cache != nullptr && kind == kTaskRow;
       for (int j = 0; j < tc.n && pp.ok; ++j) {
         if (!pp.wait()) {
           if (lane == 0) atomicOr(P.ws.error, 1u);
@@ -985,10 +994,22 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
         __syncwarp();
         pp.consume();
         refill();
+        if constexpr (kHost) {
+          if (to_cache) {
+            uint4* dst = reinterpret_cast<uint4*>(P.row_cache + static_cast<int64_t>(b) * row_bytes +
+                                                  static_cast<int64_t>(ch) * kSeqChunkBytes);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+              if (lane + 32 * v < nv) __stcg(dst + lane + 32 * v, w[v]);
+          }
+        }
         row_chunk<T>(w, nv, ch, greedy, c, lane, ml, Zl, zl);
         gather2();
       }
       gather2();
+      // the copy is visible device-wide before this row's summary leaves the member (every
+      // reader of the copy learns of the draw through that summary or after it)
+      if (to_cache) __threadfence();
       RowSum r;
       r.m = ml;
       r.Z = Zl;
@@ -1223,6 +1244,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
             e.m = rs.m;
             e.Z = rs.Z;
             e.T = Tc;
+            e.cached = (kHost && P.row_cache != nullptr && !ahead_row) ? 1 : 0;
             if (starts_gone) {
               // no sequence waits to start: this team draws now, while row J is in L2
               nxt_local = true;
@@ -1279,6 +1301,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
           s_c = c;
           s_invZ = 1.f / cur.Z;
           s_noq = kind == kTaskDrawP || tc.q == nullptr;
+          s_cached = kHost && cur.cached != 0;
         }
         done = drawn = true;
       }
@@ -1303,7 +1326,9 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     // finds the drawn token with its second warp meanwhile (the leader, in the first warp,
     // fetches the ticket).
     if (srch && gwarp == 1) {
-      const T* lrow = reinterpret_cast<const T*>(logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
+      const T* lrow = reinterpret_cast<const T*>(
+          s_cached ? P.row_cache + static_cast<int64_t>(s_b) * row_bytes
+                   : logits + (static_cast<int64_t>(s_b) * R + s_J) * row_bytes);
       const float* qrow = s_noq ? nullptr : P.q + (static_cast<int64_t>(s_b) * P.gamma + s_J) * V;
       const int y = local_search<T, kHost>(lrow, qrow, V, d0, d1 - d0, s_base, s_target, s_m, s_c, s_invZ, s_noq,
                                            gs.mass[s_par], lane);

@@ -178,6 +178,12 @@ bool chain_sizes_ok(int B, int g, int V) {
   return true;
 }
 
+// The device copy of each sequence's latest row that the left-to-right kernel keeps when
+// the logits sit in host memory (placed after the regular workspace).
+size_t chain_row_cache_bytes(int B, int V, specdec_dtype ldt) {
+  return round_up(static_cast<size_t>(B) * static_cast<size_t>(V) * elem_size(ldt));
+}
+
 int chain_common(const void* logits, specdec_dtype ldt, const float* q, const int32_t* drafts,
                  const float* temps, const float* u, int B, int g, int V, int32_t* out_tokens,
                  int32_t* out_J, float* out_p, int32_t* out_status, void* workspace,
@@ -204,7 +210,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
   // logits and q in pinned host memory: the left-to-right kernel reads the rows it needs
   // over the host link; pageable host memory is refused (the first check that asks the
   // CUDA runtime)
-  bool host_in = false;
+  bool host_in = false, logits_on_host = false;
   for (const void* p : {logits, greedy_only ? nullptr : static_cast<const void*>(q)}) {
     if (p == nullptr) continue;
     cudaPointerAttributes a{};
@@ -220,6 +226,7 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
     if (a.type == cudaMemoryTypeHost) {
       if (a.devicePointer != p) return fail(SPECDEC_ERR_UNSUPPORTED, "host memory not mapped at its own address");
       host_in = true;
+      logits_on_host |= p == logits;
     }
   }
   if (host_in && !(stream_path && (gammas || use_left_to_right()) && V <= seq_max_v(ldt)))
@@ -259,6 +266,11 @@ int chain_common(const void* logits, specdec_dtype ldt, const float* q, const in
     P.counter_bytes = counter_bytes;
     P.grid_stats = device_sm_count();
     P.host_inputs = host_in ? 1 : 0;
+    // host-resident logits and room for a device copy of each sequence's latest row: a
+    // drawn row is then read from device memory, not a second time over the host link
+    const size_t ws_base = chain_ws_bytes(B, g, V, ldt);
+    if (logits_on_host && !greedy_only && workspace_bytes >= ws_base + chain_row_cache_bytes(B, V, ldt))
+      P.row_cache = static_cast<char*>(workspace) + ws_base;
     P.drop_draws = test_hook(SPECDEC_HOOK_CHAIN_DROP_DRAWS) ? 1 : 0;
     const int wait_us = test_hook(SPECDEC_HOOK_QUEUE_WAIT_US);
     P.queue_wait_ns = wait_us > 0 ? static_cast<unsigned long long>(wait_us) * 1000ull : 1000000000ull;
@@ -369,6 +381,11 @@ extern "C" {
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
   if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return 0;
   return chain_ws_bytes(B, g, V, ldt);
+}
+
+size_t specdec_chain_host_workspace_bytes(int B, int g, int V, specdec_dtype ldt) {
+  if (!valid_dtype(ldt) || !chain_sizes_ok(B, g, V)) return 0;
+  return chain_ws_bytes(B, g, V, ldt) + chain_row_cache_bytes(B, V, ldt);
 }
 
 int specdec_verify_chain(const void* logits, specdec_dtype ldt, const float* draft_probs,

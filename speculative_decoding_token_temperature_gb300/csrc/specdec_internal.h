@@ -118,6 +118,8 @@ struct ChainParams {
   int seg;               // elements per segment
   int greedy_only;
   int host_inputs;       // left-to-right kernel: logits and q may sit in pinned host memory
+  char* row_cache;       // left-to-right kernel, host-resident logits: a device copy of each
+                        // sequence's latest row (B rows of V elements), or nullptr
   int drop_draws;        // left-to-right kernel, test hook: queued draws are never marked published
   unsigned long long queue_wait_ns;  // left-to-right kernel: bound on waits for queued work
   size_t counter_bytes;  // left-to-right kernel: the counter block at the workspace's start (cleared per call)

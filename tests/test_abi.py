@@ -54,6 +54,13 @@ def test_workspace_sizes(built_library):
     assert blk > a and blk % 256 == 0
     assert lib.specdec_block_workspace_bytes(0, 7, 10, sd.BF16) == 0
     assert lib.specdec_block_workspace_bytes(1, 7, 10, 9) == 0
+    # host-resident logits: room for one device copy of a row per sequence on top
+    for B_, g_, V_, code, es in ((256, 7, 128256, sd.BF16, 2), (3, 2, 1000, sd.F32, 4), (1, 1, 8, sd.BF16, 2)):
+        base = lib.specdec_chain_workspace_bytes(B_, g_, V_, code)
+        extra = -(-(B_ * V_ * es) // 256) * 256
+        assert lib.specdec_chain_host_workspace_bytes(B_, g_, V_, code) == base + extra
+    assert lib.specdec_chain_host_workspace_bytes(0, 7, 10, sd.BF16) == 0
+    assert lib.specdec_chain_host_workspace_bytes(1, 7, 10, 9) == 0
 
 
 def _fake(n=64):

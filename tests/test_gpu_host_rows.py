@@ -112,3 +112,61 @@ def test_pageable_host_rows_are_refused(sd):
                                   None, None, p(ws.data_ptr()), ctypes.c_size_t(ws.numel()), None)
     assert rc == 1  # SPECDEC_ERR_INVALID_ARG
     assert b"pinned" in lib.specdec_last_error()
+
+
+def _abi_chain(sd, x, ws_bytes):
+    """specdec_verify_chain through the C ABI with a workspace of the given size."""
+    lib = sd.load_library()
+    B, g1, V = x["logits"].shape
+    g = g1 - 1
+    code = sd.BF16 if x["logits"].dtype == torch.bfloat16 else sd.F32
+    ws = torch.empty(int(ws_bytes), dtype=torch.uint8, device=DEV)
+    out = {"tokens": torch.full((B, g1), -9, dtype=torch.int32, device=DEV),
+           "num_accepted": torch.full((B,), -9, dtype=torch.int32, device=DEV),
+           "p_draft": torch.full((B, g), -9.0, dtype=torch.float32, device=DEV),
+           "status": torch.full((B,), -9, dtype=torch.int32, device=DEV)}
+    p = ctypes.c_void_p
+    d = {k: (v if v.device.type == "cpu" else v.to(DEV)) for k, v in x.items()}
+    for k in ("draft_tokens", "temperatures", "uniforms"):
+        d[k] = x[k].to(DEV)
+    rc = lib.specdec_verify_chain(p(d["logits"].data_ptr()), code, p(d["draft_probs"].data_ptr()),
+                                  p(d["draft_tokens"].data_ptr()), p(d["temperatures"].data_ptr()),
+                                  p(d["uniforms"].data_ptr()), B, g, V, p(out["tokens"].data_ptr()),
+                                  p(out["num_accepted"].data_ptr()), p(out["p_draft"].data_ptr()),
+                                  p(out["status"].data_ptr()), p(ws.data_ptr()), ctypes.c_size_t(ws.numel()),
+                                  p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, lib.specdec_last_error()
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("case", [
+    ("chain_b256_v128256", 0), ("chain_b256_v128256", 1), ("chain_b256_v128256_s075", 0),
+    ("chain_b64_v32000", 3), (300, 3, 4096, "bf16"), (9, 7, 50000, "fp32"), (4, 31, 8192, "bf16"),
+])
+def test_host_rows_device_copy_same_bits(sd, case):
+    """With host logits and the larger workspace (specdec_chain_host_workspace_bytes) the
+    kernel keeps a device copy of each sequence's latest row and draws read it; with the
+    plain workspace they read the host row again.  Both give the device-input bits, for
+    queued and immediate draws, rows computed ahead and mixed greedy/sampled sequences."""
+    lib = sd.load_library()
+    if isinstance(case[0], str):
+        x = {k: v.cpu() for k, v in workloads.chain_workload(case[0], case[1], DEV).items()}
+    else:
+        B, g, V, dt = case
+        x = workloads.make_chain_inputs(B, g, V, dt, seed=5, device=DEV, recipe="spikes", scale=2.0,
+                                        n_spikes=3, spike=4.0, noise=0.6, temps="uniform:0.0:1.5")
+        x = {k: v.cpu() for k, v in x.items()}
+    B, g1, V = x["logits"].shape
+    code = sd.BF16 if x["logits"].dtype == torch.bfloat16 else sd.F32
+    small = lib.specdec_chain_workspace_bytes(B, g1 - 1, V, code)
+    big = lib.specdec_chain_host_workspace_bytes(B, g1 - 1, V, code)
+    assert big > small
+    ref = _abi_chain(sd, {k: v.to(DEV) for k, v in x.items()}, small)
+    h = _pinned(x)
+    _same(ref, _abi_chain(sd, h, big))    # device copy of the drawn rows
+    _same(ref, _abi_chain(sd, h, small))  # drawn rows read from the host again
+    # logits on the host with q on the device (the copy is used), and q alone on the host
+    # (it is not: nothing of the logits sits on the host)
+    _same(ref, _abi_chain(sd, {**h, "draft_probs": x["draft_probs"].to(DEV)}, big))
+    _same(ref, _abi_chain(sd, {**h, "logits": x["logits"].to(DEV)}, big))
