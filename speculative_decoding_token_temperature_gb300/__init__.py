@@ -206,16 +206,23 @@ def chain_workspace_bytes(B: int, gamma: int, V: int, dtype=torch.bfloat16) -> i
 
 
 class _HostRoundTrip:
-    """Copies host inputs to the device and device outputs back (argument marshalling)."""
+    """Copies host inputs to the device and device outputs back (argument marshalling).
 
-    def __init__(self, tensors):
+    Every copy runs on the stream the library call runs on (the caller's `stream`, else the
+    device's current stream), so that the inputs land before the kernels read them and the
+    outputs are read after the kernels wrote them, whichever stream the caller chose."""
+
+    def __init__(self, tensors, stream=None):
         self.on_host = tensors[0].device.type == "cpu"
         self.device = torch.device("cuda", torch.cuda.current_device()) if self.on_host else tensors[0].device
+        self.stream = stream if stream is not None else (
+            torch.cuda.current_stream(self.device) if self.on_host else None)
 
     def to_device(self, t):
         if t is None or not self.on_host:
             return t
-        return t.to(self.device, non_blocking=True)
+        with torch.cuda.stream(self.stream):
+            return t.to(self.device, non_blocking=True)
 
     def rows(self, t):
         """The logits and draft-probability rows of the chain calls: pinned host tensors stay
@@ -223,12 +230,20 @@ class _HostRoundTrip:
         copied like every other input."""
         if t is None or not self.on_host or (t.is_pinned() and t.is_contiguous()):
             return t
-        return t.to(self.device, non_blocking=True)
+        return self.to_device(t)
 
-    def to_host(self, t):
-        if t is None or not self.on_host:
-            return t
-        return t.to("cpu", non_blocking=False)
+    def outputs(self, out):
+        """The call's outputs (a tensor or a dict of tensors): on the host, for host inputs,
+        copied on the call's stream and waited for once."""
+        if not self.on_host:
+            return out
+        with torch.cuda.stream(self.stream):
+            if isinstance(out, dict):
+                res = {k: (None if v is None else v.to("cpu", non_blocking=True)) for k, v in out.items()}
+            else:
+                res = out.to("cpu", non_blocking=True)
+        self.stream.synchronize()
+        return res
 
 
 def verify_chain(logits, draft_probs, draft_tokens, temperatures, uniforms, *, out=None,
@@ -251,7 +266,7 @@ def verify_chain_varlen(logits, draft_probs, draft_tokens, temperatures, uniform
     """Chain verification of the first gammas[b] drafts of each sequence
     (specdec_verify_chain_varlen); gammas [B] int32 in [0, g].  Results as verify_chain."""
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     gammas = rt.to_device(gammas)
     B = logits.shape[0]
     _need(gammas, "gammas", torch.int32, (B,), gammas.device)
@@ -276,7 +291,7 @@ def verify_block(logits, draft_probs, draft_tokens, temperatures, uniforms, *, o
 def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, temperatures, uniforms,
                   out, with_p_draft, stream, rows_on_host: bool = False) -> dict:
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     rows = rt.rows if rows_on_host else rt.to_device
     logits, draft_probs = rows(logits), rows(draft_probs)
     draft_tokens, temperatures, uniforms = (rt.to_device(t) for t in (draft_tokens, temperatures, uniforms))
@@ -320,13 +335,13 @@ def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, 
         # left-to-right kernel): copy them like the other inputs
         rc = call(rt.to_device(logits), rt.to_device(draft_probs))
     _check(rc, entry if isinstance(entry, str) else "specdec_verify_chain_varlen")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 def verify_greedy(logits, draft_tokens, *, out=None, stream=None) -> dict:
     """Greedy verification (specdec_verify_greedy): tokens, num_accepted, status."""
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     logits, draft_tokens = rt.rows(logits), rt.to_device(draft_tokens)
     B, g1, V = logits.shape
     g = g1 - 1
@@ -352,7 +367,7 @@ def verify_greedy(logits, draft_tokens, *, out=None, stream=None) -> dict:
     if rc == ERR_UNSUPPORTED and logits.device.type == "cpu":  # rows the kernel cannot read in place
         rc = call(rt.to_device(logits))
     _check(rc, "specdec_verify_greedy")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth: int, *,
@@ -360,7 +375,7 @@ def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth:
     """Medusa tree walk (specdec_verify_tree): tokens [B, D+1], path [B, D],
     num_accepted [B], status [B]."""
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     logits, node_tokens, parents, temperatures, uniforms = (
         rt.to_device(t) for t in (logits, node_tokens, parents, temperatures, uniforms))
     B, n1, V = logits.shape
@@ -388,7 +403,7 @@ def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth:
                                  _ptr(out.get("status")), _ptr(ws), wsb,
                                  ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_tree")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperatures, uniforms, max_depth: int, *,
@@ -402,7 +417,7 @@ def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperature
     (SPECDEC_TREE_WITHOUT_REPLACEMENT).  Returns tokens [B, D+1], path [B, D],
     num_accepted [B], status [B]."""
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     logits, draft_probs, node_tokens, parents, temperatures, uniforms = (
         rt.to_device(t) for t in (logits, draft_probs, node_tokens, parents, temperatures, uniforms))
     B, n1, V = logits.shape
@@ -430,14 +445,14 @@ def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperature
                                            _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["num_accepted"]),
                                            _ptr(out.get("status")), ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_tree_recursive")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 def verify_gumbel(logits, draft_tokens, temperatures, seed: int, *, out=None, stream=None) -> dict:
     """Gumbel-coupled verification (specdec_verify_gumbel): tokens [B, g+1], num_accepted
     [B], status [B].  The noise is Philox4x32-10 keyed by `seed` (0 <= seed < 2^64)."""
     lib = load_library()
-    rt = _HostRoundTrip([logits])
+    rt = _HostRoundTrip([logits], stream)
     logits, draft_tokens, temperatures = (rt.to_device(t) for t in (logits, draft_tokens, temperatures))
     B, g1, V = logits.shape
     g = g1 - 1
@@ -456,13 +471,13 @@ def verify_gumbel(logits, draft_tokens, temperatures, seed: int, *, out=None, st
                                    _ptr(out["tokens"]), _ptr(out["num_accepted"]), _ptr(out.get("status")),
                                    _ptr(ws), wsb, ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_verify_gumbel")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 def gumbel_draft(draft_probs, seed: int, *, out=None, stream=None):
     """The drafter's shared-noise sampler (specdec_gumbel_draft): draft tokens [B, g]."""
     lib = load_library()
-    rt = _HostRoundTrip([draft_probs])
+    rt = _HostRoundTrip([draft_probs], stream)
     draft_probs = rt.to_device(draft_probs)
     B, g, V = draft_probs.shape
     dev = draft_probs.device
@@ -472,7 +487,7 @@ def gumbel_draft(draft_probs, seed: int, *, out=None, stream=None):
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     rc = lib.specdec_gumbel_draft(_ptr(draft_probs), int(seed), B, g, V, _ptr(out), ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_gumbel_draft")
-    return rt.to_host(out)
+    return rt.outputs(out)
 
 
 def gumbel_noise(seed: int, B: int, rows: int, V: int, device=None, stream=None):
@@ -524,7 +539,7 @@ def build_tree_mask(parents, prefix_len: int, *, stream=None) -> dict:
     """Tree-attention mask [N, P+N] uint8, position ids [N] int64, depth [N] int32 and a
     one-element status (specdec_build_tree_mask)."""
     lib = load_library()
-    rt = _HostRoundTrip([parents])
+    rt = _HostRoundTrip([parents], stream)
     parents = rt.to_device(parents)
     if parents.dim() != 1 or parents.dtype != torch.int32 or not parents.is_contiguous():
         raise ValueError("parents must be a contiguous int32 vector")
@@ -541,7 +556,7 @@ def build_tree_mask(parents, prefix_len: int, *, stream=None) -> dict:
                                      _ptr(out["position_ids"]), _ptr(out["depth"]),
                                      _ptr(out["status"]), ctypes.c_void_p(s.cuda_stream))
     _check(rc, "specdec_build_tree_mask")
-    return {k: rt.to_host(v) for k, v in out.items()}
+    return rt.outputs(out)
 
 
 class KernelTimer:

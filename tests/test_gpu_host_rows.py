@@ -170,3 +170,21 @@ def test_host_rows_device_copy_same_bits(sd, case):
     # (it is not: nothing of the logits sits on the host)
     _same(ref, _abi_chain(sd, {**h, "draft_probs": x["draft_probs"].to(DEV)}, big))
     _same(ref, _abi_chain(sd, {**h, "logits": x["logits"].to(DEV)}, big))
+
+
+def test_host_inputs_on_the_callers_stream(sd):
+    """Host inputs with a `stream=` other than the current one: the binding's copies run on
+    that stream, so a stream kept busy before the call still sees the inputs land before
+    the kernel and the outputs read after it (a clock spin of a few ms holds it back)."""
+    x = workloads.chain_workload("chain_b64_v32000", 5, DEV)
+    ref = sd.verify_chain(*(x[k] for k in KEYS))
+    ref_g = sd.verify_greedy(x["logits"], x["draft_tokens"])
+    side = torch.cuda.Stream()
+    for h in ({k: v.cpu() for k, v in x.items()}, _pinned(x)):  # copied rows, rows read in place
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(20_000_000)
+        _same(ref, sd.verify_chain(*(h[k] for k in KEYS), stream=side))
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(20_000_000)
+        _same(ref_g, sd.verify_greedy(h["logits"], h["draft_tokens"], stream=side))
+    torch.cuda.synchronize()
