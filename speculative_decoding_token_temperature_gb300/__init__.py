@@ -9,6 +9,7 @@ calling without the compiled library raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from pathlib import Path
 
@@ -217,12 +218,23 @@ class _HostRoundTrip:
         self.device = torch.device("cuda", torch.cuda.current_device()) if self.on_host else tensors[0].device
         self.stream = stream if stream is not None else (
             torch.cuda.current_stream(self.device) if self.on_host else None)
+        # torch copies go to the current stream: switch only for a caller's other stream
+        self.switch = self.on_host and stream is not None and stream != torch.cuda.current_stream(self.device)
+
+    def _on_stream(self):
+        return torch.cuda.stream(self.stream) if self.switch else contextlib.nullcontext()
 
     def to_device(self, t):
         if t is None or not self.on_host:
             return t
-        with torch.cuda.stream(self.stream):
+        with self._on_stream():
             return t.to(self.device, non_blocking=True)
+
+    def to_device_all(self, *ts):
+        if not self.on_host:
+            return ts
+        with self._on_stream():
+            return tuple(None if t is None else t.to(self.device, non_blocking=True) for t in ts)
 
     def rows(self, t):
         """The logits and draft-probability rows of the chain calls: pinned host tensors stay
@@ -237,7 +249,7 @@ class _HostRoundTrip:
         copied on the call's stream and waited for once."""
         if not self.on_host:
             return out
-        with torch.cuda.stream(self.stream):
+        with self._on_stream():
             if isinstance(out, dict):
                 res = {k: (None if v is None else v.to("cpu", non_blocking=True)) for k, v in out.items()}
             else:
@@ -294,7 +306,7 @@ def _verify_round(entry: str, ws_entry: str, logits, draft_probs, draft_tokens, 
     rt = _HostRoundTrip([logits], stream)
     rows = rt.rows if rows_on_host else rt.to_device
     logits, draft_probs = rows(logits), rows(draft_probs)
-    draft_tokens, temperatures, uniforms = (rt.to_device(t) for t in (draft_tokens, temperatures, uniforms))
+    draft_tokens, temperatures, uniforms = rt.to_device_all(draft_tokens, temperatures, uniforms)
     if logits.dim() != 3:
         raise ValueError("logits must be [B, g+1, V]")
     B, g1, V = logits.shape
@@ -376,8 +388,8 @@ def verify_tree(logits, node_tokens, parents, temperatures, uniforms, max_depth:
     num_accepted [B], status [B]."""
     lib = load_library()
     rt = _HostRoundTrip([logits], stream)
-    logits, node_tokens, parents, temperatures, uniforms = (
-        rt.to_device(t) for t in (logits, node_tokens, parents, temperatures, uniforms))
+    logits, node_tokens, parents, temperatures, uniforms = rt.to_device_all(
+        logits, node_tokens, parents, temperatures, uniforms)
     B, n1, V = logits.shape
     N = n1 - 1
     D = int(max_depth)
@@ -418,8 +430,8 @@ def verify_tree_recursive(logits, draft_probs, node_tokens, parents, temperature
     num_accepted [B], status [B]."""
     lib = load_library()
     rt = _HostRoundTrip([logits], stream)
-    logits, draft_probs, node_tokens, parents, temperatures, uniforms = (
-        rt.to_device(t) for t in (logits, draft_probs, node_tokens, parents, temperatures, uniforms))
+    logits, draft_probs, node_tokens, parents, temperatures, uniforms = rt.to_device_all(
+        logits, draft_probs, node_tokens, parents, temperatures, uniforms)
     B, n1, V = logits.shape
     N = n1 - 1
     D = int(max_depth)
@@ -453,7 +465,7 @@ def verify_gumbel(logits, draft_tokens, temperatures, seed: int, *, out=None, st
     [B], status [B].  The noise is Philox4x32-10 keyed by `seed` (0 <= seed < 2^64)."""
     lib = load_library()
     rt = _HostRoundTrip([logits], stream)
-    logits, draft_tokens, temperatures = (rt.to_device(t) for t in (logits, draft_tokens, temperatures))
+    logits, draft_tokens, temperatures = rt.to_device_all(logits, draft_tokens, temperatures)
     B, g1, V = logits.shape
     g = g1 - 1
     dev = logits.device
