@@ -370,16 +370,20 @@ struct Queue {
   int* ready_draws;
   float4* ring_draws;
   int B, cap;
-  unsigned first;  // sequences 0..first-1 start without a ticket (team t starts sequence t)
 };
 constexpr int kDrawTag = 1 << 30;
 
 // A ticket for the team's next task.  `pre` is a start ticket the leader already took
-// (UINT_MAX: none); start ticket i is sequence first + i.  Once a start ticket comes back
-// past the last sequence, the team (starts_left false) takes only draw tickets.
+// (UINT_MAX: none).  Once a start ticket comes back past the last sequence, the team
+// (starts_left false) takes only draw tickets.
+//
+// Every sequence, the first ones too, is started through a ticket, by whichever team takes
+// it: part of the grid may not be resident while other kernels hold SMs, and a sequence
+// tied to a team that is not yet running would hold back every team that waits for the
+// call to end.  So no team ever waits on a team that has not started.
 __device__ __forceinline__ int take_ticket(const Queue& q, unsigned pre, bool& starts_left) {
   if (starts_left) {
-    const unsigned s = (pre != UINT_MAX ? pre : atomicAdd(q.start_ticket, 1u)) + q.first;
+    const unsigned s = pre != UINT_MAX ? pre : atomicAdd(q.start_ticket, 1u);
     if (s < static_cast<unsigned>(q.B)) return static_cast<int>(s);
     starts_left = false;
   }
@@ -804,9 +808,6 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
   qu.ring_draws = P.ws.ring;
   qu.B = P.B;
   qu.cap = P.ws.ring_cap;
-  const int nteams = static_cast<int>(gridDim.x / kC) * kSeqGroups;
-  const int team = static_cast<int>(blockIdx.x / kC) * kSeqGroups + group;
-  qu.first = static_cast<unsigned>(min(nteams, P.B));
 
   // drafts to verify for sequence b: gamma, or its own count (the bonus row is row gb)
   auto gamma_of = [&](int b) { return P.gammas ? __ldg(P.gammas + b) : P.gamma; };
@@ -860,20 +861,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
     return e;
   };
 
-  // The first task: team t starts sequence t without a ticket or a hand-over (every
-  // thread forms the entry), the other teams ask the queues.
-  Entry cur;
-  if (team < P.B) {
-    cur.b = team;
-    cur.row = 0;
-    cur.kind = kTaskRow;
-    cur.warn = 0;
-    cur.m = 0.f;
-    cur.Z = 1.f;
-    cur.T = P.greedy_only ? 0.f : __ldg(P.temps + team);
-  } else {
-    cur = take_box();
-  }
+  Entry cur = take_box();
   uint32_t t = 0;  // tasks done by this team
   // rows ahead_lo..ahead_hi of the team's current chain went to teams that waited for work
   int ahead_lo = INT_MAX, ahead_hi = -1;
@@ -1028,7 +1016,7 @@ __global__ void __launch_bounds__(kSeqWarps * 32, 1) chain_seq_kernel(const Chai
       // the leader's view of the queues: teams waiting for work, and whether start tickets
       // may remain (bit 30)
       const int idle = static_cast<int>(w_dt - w_pd);
-      const bool starts_remain = leader && w_st + qu.first < static_cast<unsigned>(P.B);
+      const bool starts_remain = leader && w_st < static_cast<unsigned>(P.B);
       const int qv = min(max(idle, 0), (1 << 30) - 1) | (starts_remain ? (1 << 30) : 0);
       // bit 31: a copy wait of this member gave up (its summary is incomplete)
       const bool lost = group_any(group, !pp.ok);

@@ -118,3 +118,26 @@ def test_wait_that_gives_up_marks_unfinished_sequences(sd):
     rep2 = ParityReport("after the hook")
     _check(sd, rep2, x)
     assert not rep2.failures, rep2.failures[:5]
+
+
+def test_launch_beside_kernels_that_hold_sms(sd):
+    """Kernels on other streams hold SMs for longer than the queue waits' bound (48 bounded
+    clock spins of about 0.5 s, one CTA each, the bound shortened to 200 ms by the test
+    hook), so part of the left-to-right launch cannot be resident until they end.  The
+    teams that are resident must finish every sequence without waiting on the others: the
+    outputs equal those of the call on an idle GPU, with no sequence timed out."""
+    x = workloads.chain_workload("chain_b256_v128256", 1, DEV)
+    ref = sd.verify_chain(*(x[k] for k in KEYS))
+    torch.cuda.synchronize()
+    sides = [torch.cuda.Stream() for _ in range(48)]
+    with sd.test_hooks(queue_wait_us=200_000):
+        for sdv in sides:
+            with torch.cuda.stream(sdv):
+                torch.cuda._sleep(1_000_000_000)  # ~0.5 s of clock cycles
+        out = sd.verify_chain(*(x[k] for k in KEYS))
+        torch.cuda.synchronize()
+    st = _np(out["status"]).astype(np.int64)
+    assert not ((st & 0xFF) == sd.STATUS_TIMEOUT).any(), int(((st & 0xFF) == sd.STATUS_TIMEOUT).sum())
+    for k in ref:
+        a, b = _np(ref[k]), _np(out[k])
+        assert np.array_equal(np.nan_to_num(a, nan=-7.0), np.nan_to_num(b, nan=-7.0)), k
