@@ -110,7 +110,10 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
  * for specdec_verify_greedy and specdec_verify_chain_varlen.
  * Bounded waits: the left-to-right kernel's waits on its queues and copies give up after a
  * bound (one second); a sequence the kernel could not finish then comes back with
- * SPECDEC_STATUS_TIMEOUT, num_accepted -1 and tokens -1 (out_p_draft NaN).
+ * SPECDEC_STATUS_TIMEOUT, num_accepted -1 and tokens -1 (out_p_draft NaN).  The kernel
+ * does not need its whole grid resident at once: while kernels on other streams hold SMs,
+ * the part that is running takes every sequence in turn, and no running part waits on one
+ * that has not started, so sharing the GPU slows a call but does not time it out.
  */
 size_t specdec_chain_workspace_bytes(int B, int g, int V, specdec_dtype ldt);
 
