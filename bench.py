@@ -56,17 +56,17 @@ FALLBACK_HBM_GBS = 6800.0
 # files (KERNEL_SOURCES) it was taken on; reported only for that workload and rule, and
 # as null once the sources differ.
 NCU_TRAFFIC = {
-    # all-rows chain kernels (the test hook): 525.37 MB read + 4.48 MB written
-    "chain_stats": {"bytes": 529_844_736, "src_sha": "94193918dae374cb", "workload": "chain_b256_v128256", "rule": "chain"},
-    # left-to-right chain kernel: 311.55 MB read + 5.49 MB written (batch seed 0)
-    "chain_seq": {"bytes": 317_042_944, "src_sha": "e34faa930c369412", "workload": "chain_b256_v128256", "rule": "chain"},
-    # one-launch block kernel: 1446.09 MB read + 4.72 MB written (batch seed 0)
-    "block_fused": {"bytes": 1_450_804_480, "src_sha": "6b3ef2c8d20866f8", "workload": "chain_b256_v128256",
+    # all-rows chain kernels (the test hook): 525.37 MB read + 4.59 MB written
+    "chain_stats": {"bytes": 529_954_816, "src_sha": "39194e10996fabbe", "workload": "chain_b256_v128256", "rule": "chain"},
+    # left-to-right chain kernel: 310.02 MB read + 5.20 MB written (batch seed 0)
+    "chain_seq": {"bytes": 315_212_288, "src_sha": "130ed97f2e6a85c6", "workload": "chain_b256_v128256", "rule": "chain"},
+    # one-launch block kernel: 1445.90 MB read + 4.92 MB written (batch seed 0)
+    "block_fused": {"bytes": 1_450_814_720, "src_sha": "baf5f641c6f7d206", "workload": "chain_b256_v128256",
                     "rule": "block"},
     # Medusa walk on a cluster: 2.30 MB read, 0 written (batch seed 0)
-    "tree_walk": {"bytes": 2_304_256, "src_sha": "2829f64e6a972a75", "workload": "tree_b32_n64_v32000", "rule": "tree"},
+    "tree_walk": {"bytes": 2_304_000, "src_sha": "247e250351458bee", "workload": "tree_b32_n64_v32000", "rule": "tree"},
     # recursive rejection on a cluster: 17.88 MB read, 0 written (batch seed 0)
-    "tree_rr": {"bytes": 17_883_648, "src_sha": "51a76a1993c3b0a7", "workload": "tree_rr_b32_n64_v32000",
+    "tree_rr": {"bytes": 17_883_648, "src_sha": "3bd0966d0b64712e", "workload": "tree_rr_b32_n64_v32000",
                 "rule": "tree_recursive"},
 }
 

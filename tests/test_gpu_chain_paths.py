@@ -141,3 +141,20 @@ def test_launch_beside_kernels_that_hold_sms(sd):
     for k in ref:
         a, b = _np(ref[k]), _np(out[k])
         assert np.array_equal(np.nan_to_num(a, nan=-7.0), np.nan_to_num(b, nan=-7.0)), k
+
+
+def test_two_calls_in_flight_on_two_streams(sd):
+    """Two B=256 calls launched back to back on two streams (each with its own workspace)
+    compete for SMs; each must equal the same call made alone."""
+    xs = [workloads.chain_workload("chain_b256_v128256", r, DEV) for r in (0, 2)]
+    refs = [sd.verify_chain(*(x[k] for k in KEYS)) for x in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.current_stream().synchronize()
+    for rep in range(3):
+        outs = [sd.verify_chain(*(x[k] for k in KEYS), stream=s) for x, s in zip(xs, streams)]
+        torch.cuda.synchronize()
+        for ref, out in zip(refs, outs):
+            for k in ref:
+                a, b = _np(ref[k]), _np(out[k])
+                assert np.array_equal(np.nan_to_num(a, nan=-7.0), np.nan_to_num(b, nan=-7.0)), (rep, k)
