@@ -90,3 +90,24 @@ def test_random_sweep_greedy(sd):
             o = so.verify_greedy_sequence(L[b], d[b])
             assert int(J[b]) == o["J"] and int(st[b]) == o["status"], (c, b)
             assert np.array_equal(toks[b], o["tokens"]), (c, b)
+
+
+def test_random_sweep_gumbel(sd):
+    """Gumbel coupling over the same kind of random cases (the drafts from the oracle's
+    shared-noise drafter, so that long agreeing prefixes occur), against the oracle's race."""
+    from test_gpu_gumbel import Report as GumbelReport, check_rounds, oracle_drafts
+    rep = GumbelReport("random sweep, gumbel")
+    for i, c in enumerate(_cases(15, 12)):
+        B = max(1, min(c["B"], 2_000_000 // ((c["gamma"] + 1) * c["V"])))
+        c = dict(c, B=B)
+        x = _inputs(c)
+        seed = c["seed"] % (2**40)
+        od = oracle_drafts(_np(x["draft_probs"]), seed, range(B))
+        drafts = torch.tensor(np.stack([od[b]["drafts"] for b in range(B)]), dtype=torch.int32, device=DEV)
+        out = sd.verify_gumbel(x["logits"], drafts, x["temperatures"], seed)
+        torch.cuda.synchronize()
+        n0 = len(rep.failures)
+        check_rounds(rep, _np(x["logits"]), {b: od[b]["drafts"] for b in range(B)}, _np(x["temperatures"]), seed,
+                     out, range(B))
+        assert len(rep.failures) == n0, (i, {k: c[k] for k in ("B", "gamma", "V", "dtype")}, rep.failures[n0:n0 + 3])
+    rep.finish()
