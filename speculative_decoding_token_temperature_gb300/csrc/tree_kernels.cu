@@ -184,40 +184,56 @@ cudaError_t launch_walk_t(const TreeParams& P, cudaStream_t stream) {
   return launch_kernel(tree_walk_kernel<T, VEC, kTreeThreads>, dim3(P.B), dim3(kTreeThreads), 0, stream, 0, P);
 }
 
-__global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restrict__ parents, int N,
-                                                        int P, uint8_t* __restrict__ mask,
-                                                        int64_t* __restrict__ pos,
-                                                        int32_t* __restrict__ depth,
-                                                        int32_t* __restrict__ status) {
+// Bytes 0..n-1 of a little-endian 8-byte word set to 1 (0 <= n <= 8).
+__device__ __forceinline__ unsigned long long mask_ones(int n) {
+  return n >= 8 ? 0x0101010101010101ull : (0x0101010101010101ull & ((1ull << (8 * n)) - 1ull));
+}
+
+// One warp per node, i.e. per mask row: the row is written as 16-byte words (prefix columns
+// 1, node columns 0; the row's unaligned ends byte by byte), then the warp's first lane
+// walks the node's ancestor chain once, setting the node's own column and each ancestor's
+// to 1 and counting the depth.  A row costs one pass of coalesced stores plus depth + 1
+// byte stores, instead of an ancestor walk per byte.
+constexpr int kMaskWarps = 8;
+__global__ void __launch_bounds__(kMaskWarps * 32) tree_mask_kernel(const int32_t* __restrict__ parents, int N,
+                                                                   int P, uint8_t* __restrict__ mask,
+                                                                   int64_t* __restrict__ pos,
+                                                                   int32_t* __restrict__ depth,
+                                                                   int32_t* __restrict__ status) {
   __shared__ int sh_i[32];
+  const int lane = threadIdx.x & 31;
   const int64_t W = static_cast<int64_t>(P) + N;
-  const int64_t total = W * N;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
-    const int i = static_cast<int>(e / W);
-    const int64_t j = e - static_cast<int64_t>(i) * W;
-    uint8_t v = 0;
-    if (j < P) {
-      v = 1;
-    } else {
-      const int jj = static_cast<int>(j - P);
-      int a = i, steps = 0;
-      while (a >= 0 && steps <= N) {  // walk i's ancestors (bounded even for bad parents)
-        if (a == jj) { v = 1; break; }
-        const int pa = __ldg(parents + a);
-        if (!(pa >= -1 && pa < a)) break;
-        a = pa;
-        ++steps;
-      }
+  const int nwarps = static_cast<int>(gridDim.x) * kMaskWarps;
+  for (int i = static_cast<int>(blockIdx.x) * kMaskWarps + static_cast<int>(threadIdx.x >> 5); i < N; i += nwarps) {
+    uint8_t* row = mask + static_cast<int64_t>(i) * W;
+    const int64_t head = min(W, static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u));
+    const int64_t nvec = (W - head) / 16;
+    const int64_t tail = head + nvec * 16;
+    for (int64_t c = lane; c < head; c += 32) row[c] = c < P ? 1 : 0;
+    uint4* vrow = reinterpret_cast<uint4*>(row + head);
+    for (int64_t k = lane; k < nvec; k += 32) {
+      const int64_t c0 = head + 16 * k;  // the word's first column
+      const int n1 = static_cast<int>(min(static_cast<int64_t>(16), max(static_cast<int64_t>(0), P - c0)));
+      const unsigned long long lo = mask_ones(min(n1, 8)), hi = mask_ones(max(n1 - 8, 0));
+      vrow[k] = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(hi),
+                           static_cast<uint32_t>(hi >> 32));
     }
-    mask[e] = v;
-  }
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
-    int dd = 0, a = __ldg(parents + i), steps = 0;
-    int prev = static_cast<int>(i);
-    while (a >= 0 && a < prev && steps < N) { ++dd; prev = a; a = __ldg(parents + a); ++steps; }
-    pos[i] = static_cast<int64_t>(P) + dd;
-    if (depth) depth[i] = dd;
+    for (int64_t c = tail + lane; c < W; c += 32) row[c] = c < P ? 1 : 0;
+    __syncwarp();  // (orders the words before the ancestor bytes written over them)
+    if (lane == 0) {
+      // the chain climbs strictly (parents[a] < a), so it ends within N steps even for a
+      // bad tree (whose outputs are unspecified; its status says so)
+      int a = i, d = 0, pa = __ldg(parents + i);
+      row[P + i] = 1;
+      while (pa >= 0 && pa < a) {
+        row[P + pa] = 1;
+        a = pa;
+        pa = __ldg(parents + a);
+        ++d;
+      }
+      pos[i] = static_cast<int64_t>(P) + d;
+      if (depth) depth[i] = d;
+    }
   }
   if (blockIdx.x == 0) {
     int bad = 0;
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restric
       const int pa = __ldg(parents + i);
       if (!(pa >= -1 && pa < i)) bad = SPECDEC_STATUS_BAD_TREE;
     }
-    bad = Block<256>::or_int(bad, sh_i);
+    bad = Block<kMaskWarps * 32>::or_int(bad, sh_i);
     if (threadIdx.x == 0) *status = bad;
   }
 }
@@ -246,11 +262,12 @@ cudaError_t launch_tree_walk(const TreeParams& P, specdec_dtype ldt, bool vector
 
 cudaError_t launch_tree_mask(const int32_t* parents, int N, int prefix_len, uint8_t* mask,
                              int64_t* pos, int32_t* depth, int32_t* status, cudaStream_t stream) {
-  const int64_t total = (static_cast<int64_t>(prefix_len) + N) * N;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  // one warp per row, at most eight 256-thread blocks per SM at once
+  int64_t blocks = (static_cast<int64_t>(N) + kMaskWarps - 1) / kMaskWarps;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_kernel(tree_mask_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 0,
+  return launch_kernel(tree_mask_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMaskWarps * 32), 0, stream, 0,
                        parents, N, prefix_len, mask, pos, depth, status);
 }
 

@@ -256,3 +256,33 @@ def test_mask_matches_oracle(sd, which):
 def test_mask_bad_parents(sd):
     r = sd.build_tree_mask(torch.tensor([-1, 0, 5, 1], dtype=torch.int32, device=DEV), 2)
     assert int(r["status"][0]) == so.STATUS_BAD_TREE
+
+
+@pytest.mark.parametrize("P", [0, 1, 15, 16, 33, 100])
+@pytest.mark.parametrize("offset", [0, 1, 7])
+def test_mask_rows_of_every_alignment(sd, P, offset):
+    """Rows of P + N bytes start at every offset modulo 16, and the mask itself may start
+    off a 16-byte boundary (a byte offset into a larger buffer, through the C ABI): the
+    kernel's word stores and byte ends must give the oracle's mask exactly."""
+    import ctypes
+    rng = np.random.default_rng(P * 10 + offset)
+    lib = sd.load_library()
+    for N in (1, 2, 5, 37, 130):
+        parents = [-1] + [int(rng.integers(-1, i)) for i in range(1, N)]
+        par = torch.tensor(parents, dtype=torch.int32, device=DEV)
+        W = P + N
+        buf = torch.full((offset + W * N + 64,), 7, dtype=torch.uint8, device=DEV)
+        pos = torch.empty(N, dtype=torch.int64, device=DEV)
+        dep = torch.empty(N, dtype=torch.int32, device=DEV)
+        st = torch.empty(1, dtype=torch.int32, device=DEV)
+        p = ctypes.c_void_p
+        rc = lib.specdec_build_tree_mask(p(par.data_ptr()), N, P, p(buf.data_ptr() + offset), p(pos.data_ptr()),
+                                         p(dep.data_ptr()), p(st.data_ptr()), p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+        torch.cuda.synchronize()
+        mask, opos, odep = so.build_tree_mask(parents, P)
+        got = _np(buf)
+        assert (got[:offset] == 7).all() and (got[offset + W * N:] == 7).all(), (N, "writes outside the mask")
+        assert np.array_equal(got[offset:offset + W * N].reshape(N, W).astype(bool), mask), (N, P, offset)
+        assert set(np.unique(got[offset:offset + W * N])) <= {0, 1}
+        assert np.array_equal(_np(pos), opos) and np.array_equal(_np(dep), odep) and int(st[0]) == 0
