@@ -163,3 +163,24 @@ def test_test_hooks_are_validated_and_default_to_production(built_library):
         assert lib.specdec_get_test_hook(sd.HOOK_QUEUE_WAIT_US) == 250
     assert lib.specdec_get_test_hook(sd.HOOK_TREE_CLUSTER) == 0
     assert lib.specdec_get_test_hook(sd.HOOK_QUEUE_WAIT_US) == 0
+
+
+def test_header_compiles_as_c_and_cpp(tmp_path):
+    """include/specdec.h is plain C: a C99 and a C++17 translation unit that include it and
+    name every entry point compile without a warning (no GPU, no CUDA headers needed)."""
+    import re
+    import shutil
+    import subprocess
+    hdr = ROOT / "include" / "specdec.h"
+    names = sorted(set(re.findall(r"^(?:int|size_t|const char\s*\*)\s*(specdec_\w+)\(", hdr.read_text(), re.M)))
+    assert len(names) > 20, names
+    body = '#include "specdec.h"\ntypedef void (*fn_t)(void);\nint main(void) {\n  fn_t p[] = {'
+    body += ", ".join(f"(fn_t){n}" for n in names) + "};\n  return p[0] == 0;\n}\n"
+    for compiler, flags, suffix in (("gcc", ["-std=c99", "-pedantic"], ".c"), ("g++", ["-std=c++17"], ".cpp")):
+        if shutil.which(compiler) is None:
+            pytest.skip(f"{compiler} not found")
+        src = tmp_path / ("probe" + suffix)
+        src.write_text(body)
+        r = subprocess.run([compiler, *flags, "-Wall", "-Wextra", "-Werror", f"-I{ROOT / 'include'}", "-c", str(src),
+                            "-o", str(tmp_path / "probe.o")], capture_output=True, text=True)
+        assert r.returncode == 0, (compiler, r.stderr[-2000:])
